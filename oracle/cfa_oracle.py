@@ -1,0 +1,167 @@
+"""ctypes wrapper around the fp64 C oracle in ``cfa_oracle.c``.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this module. The product path (the
+CUDA library and its binding) never imports it and fails loudly when its own
+extension is missing instead of falling back here.
+
+Cited page: "ClusterFusion框架解析：LLM推理优化的集群通信革命" (ClusterFusion
+framework analysis), written [CF §n]. The arithmetic lives in the C file;
+this module only moves arrays across the boundary.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cfa_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libcfa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP when the compiler has it)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.cfa_oracle_decode_step.restype = ctypes.c_int
+            lib.cfa_oracle_decode_step.argtypes = (
+                [ctypes.c_int] * 6 + [_u16p] * 5 + [_dp] * 4 + [ctypes.c_int])
+            lib.cfa_oracle_attention.restype = None
+            lib.cfa_oracle_attention.argtypes = [
+                ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, ctypes.c_double, _dp]
+            lib.cfa_oracle_split_partial.restype = None
+            lib.cfa_oracle_split_partial.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, _dp, _dp,
+                ctypes.c_double, _dp, _dp, _dp]
+            lib.cfa_oracle_split_combine.restype = None
+            lib.cfa_oracle_split_combine.argtypes = [
+                ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp]
+            lib.cfa_oracle_widen_bf16.restype = None
+            lib.cfa_oracle_widen_bf16.argtypes = [_u16p, _dp, ctypes.c_long]
+            lib.cfa_oracle_threads.restype = ctypes.c_int
+            lib.cfa_oracle_threads.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+def _bits(a) -> np.ndarray:
+    """bf16 data as a contiguous uint16 array of bit patterns.
+
+    Accepts a numpy uint16 array or a CPU torch bf16 tensor.
+    """
+    if isinstance(a, np.ndarray):
+        if a.dtype != np.uint16:
+            raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+        return np.ascontiguousarray(a)
+    import torch  # only for tensor inputs
+    if a.dtype != torch.bfloat16:
+        raise TypeError("oracle inputs must be bf16")
+    return a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def widen(bits) -> np.ndarray:
+    """Exact bf16 -> float64 widening of a bit-pattern array."""
+    b = _bits(bits)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().cfa_oracle_widen_bf16(b.ctypes.data_as(_u16p),
+                                  out.ctypes.data_as(_dp), b.size)
+    return out
+
+
+def threads_used(n: int) -> int:
+    return int(_load().cfa_oracle_threads(int(n)))
+
+
+def decode_step(x, W_qkv, W_o, k_cache, v_cache, ctx_len: int, nthreads: int = 1):
+    """fp64 result of one decode step [CF §1.1, §3.2, §5.1].
+
+    x [B, H], W_qkv [H, 3H], W_o [H, H], caches [B, nh, max_ctx, d] (bf16).
+    Returns dict(out [B, H], k_new [B, nh, d], v_new [B, nh, d],
+    attn [B, nh, d]) as float64 arrays.
+    """
+    xb, wq, wo, kc, vc = (_bits(t) for t in (x, W_qkv, W_o, k_cache, v_cache))
+    B, H = xb.shape
+    _, nh, max_ctx, d = kc.shape
+    if wq.shape != (H, 3 * H) or wo.shape != (H, H) or vc.shape != kc.shape \
+            or kc.shape[0] != B or nh * d != H:
+        raise ValueError("inconsistent shapes")
+    out = np.empty((B, H), np.float64)
+    k_new = np.empty((B, nh, d), np.float64)
+    v_new = np.empty((B, nh, d), np.float64)
+    attn = np.empty((B, nh, d), np.float64)
+    rc = _load().cfa_oracle_decode_step(
+        B, H, nh, d, max_ctx, int(ctx_len),
+        xb.ctypes.data_as(_u16p), wq.ctypes.data_as(_u16p), wo.ctypes.data_as(_u16p),
+        kc.ctypes.data_as(_u16p), vc.ctypes.data_as(_u16p),
+        out.ctypes.data_as(_dp), k_new.ctypes.data_as(_dp),
+        v_new.ctypes.data_as(_dp), attn.ctypes.data_as(_dp), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return {"out": out, "k_new": k_new, "v_new": v_new, "attn": attn}
+
+
+def attention(q, K, V, scale: float) -> np.ndarray:
+    """Monolithic single-query softmax attention in fp64 [CF §1.1]."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    T, d = K.shape
+    a = np.empty(d, np.float64)
+    _load().cfa_oracle_attention(T, d, q.ctypes.data_as(_dp), K.ctypes.data_as(_dp),
+                                 V.ctypes.data_as(_dp), float(scale),
+                                 a.ctypes.data_as(_dp))
+    return a
+
+
+def split_partial(q, K, V, t0: int, t1: int, scale: float):
+    """(m, l, o) of keys [t0, t1) [CF §3.2]."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    d = K.shape[1]
+    m = ctypes.c_double()
+    l = ctypes.c_double()
+    o = np.empty(d, np.float64)
+    _load().cfa_oracle_split_partial(int(t0), int(t1), d, q.ctypes.data_as(_dp),
+                                     K.ctypes.data_as(_dp), V.ctypes.data_as(_dp),
+                                     float(scale), ctypes.byref(m), ctypes.byref(l),
+                                     o.ctypes.data_as(_dp))
+    return m.value, l.value, o
+
+
+def split_combine(m, l, o) -> np.ndarray:
+    """Two-step max-then-sum combine of split partials [CF §3.1.1, §3.2]."""
+    m, l, o = _f64(m), _f64(l), _f64(o)
+    n, d = o.shape
+    a = np.empty(d, np.float64)
+    _load().cfa_oracle_split_combine(n, d, m.ctypes.data_as(_dp), l.ctypes.data_as(_dp),
+                                     o.ctypes.data_as(_dp), a.ctypes.data_as(_dp))
+    return a

@@ -1,0 +1,131 @@
+"""Workload shapes and seeded synthetic inputs.
+
+This module holds no arithmetic of the method: it only names the shapes and
+draws seeded random bf16 tensors. Both the CUDA path (tests, bench, smoke) and
+the fp64 oracle are fed from here, so the two sides see the same inputs.
+
+Every workload is synthetic (no dataset, no trained weights):
+x ~ N(0, 1), W_qkv and W_o ~ N(0, 0.02), cached K and V ~ N(0, 1), all rounded
+to bf16. The long-context workload additionally multiplies 5% of the cached
+key rows of every (batch, head) by 4, at positions drawn without replacement.
+Cache rows at positions >= ctx_len are never part of the computation; they can
+be filled with NaN so that a stray read shows up in the result.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional
+
+import torch
+
+
+def _round_up(v: int, m: int) -> int:
+    return (v + m - 1) // m * m
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    hidden: int
+    n_heads: int
+    head_dim: int
+    ctx_len: int
+    max_ctx: int
+    spiky_frac: float = 0.0
+    spiky_scale: float = 1.0
+    description: str = ""
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Bytes the step must move from HBM: both weights plus the cached K/V
+        rows that are read (the appended row, x and out are not counted)."""
+        H = self.hidden
+        return (2 * H * 3 * H + 2 * H * H
+                + self.B * 2 * self.n_heads * self.ctx_len * self.head_dim * 2)
+
+    @property
+    def flops(self) -> int:
+        H, B = self.hidden, self.B
+        T = self.ctx_len + 1
+        return (2 * B * H * 3 * H + 2 * B * H * H
+                + B * self.n_heads * T * self.head_dim * 4)
+
+    def as_config(self) -> Dict[str, object]:
+        return {"workload": self.name, "B": self.B, "hidden": self.hidden,
+                "n_heads": self.n_heads, "head_dim": self.head_dim,
+                "ctx_len": self.ctx_len, "max_ctx": self.max_ctx}
+
+
+def _wl(name, B, H, nh, d, L, desc, spiky_frac=0.0, spiky_scale=1.0, max_ctx=None):
+    return Workload(name, B, H, nh, d, L,
+                    max_ctx if max_ctx is not None else _round_up(L + 1, 64),
+                    spiky_frac, spiky_scale, desc)
+
+
+WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
+    _wl("tiny", 1, 256, 2, 128, 64,
+        "tiny block: B=1, hidden 256, 2 heads x 128, ctx_len 64", max_ctx=128),
+    _wl("llama7b_b1_ctx1k", 1, 4096, 32, 128, 1024,
+        "Llama2-7B-shaped block, B=1, ctx_len 1024"),
+    _wl("llama7b_b1_ctx4k", 1, 4096, 32, 128, 4096,
+        "Llama2-7B-shaped block, B=1, ctx_len 4096"),
+    _wl("llama7b_b16_ctx4k", 16, 4096, 32, 128, 4096,
+        "Llama2-7B-shaped block, B=16, ctx_len 4096, per-sequence caches"),
+    _wl("llama7b_b1_ctx16k_spiky", 1, 4096, 32, 128, 16384,
+        "Llama2-7B-shaped block, B=1, ctx_len 16384, 5% of keys x4",
+        spiky_frac=0.05, spiky_scale=4.0),
+    _wl("hd64_b8_ctx2k", 8, 4096, 64, 64, 2048,
+        "hidden 4096, 64 heads x 64, B=8, ctx_len 2048"),
+]}
+
+
+def custom(B: int, hidden: int, n_heads: int, head_dim: int, ctx_len: int,
+           max_ctx: Optional[int] = None, name: str = "custom",
+           spiky_frac: float = 0.0, spiky_scale: float = 1.0) -> Workload:
+    return _wl(name, B, hidden, n_heads, head_dim, ctx_len,
+               f"{name}: B={B}, hidden {hidden}, {n_heads}x{head_dim}, ctx_len {ctx_len}",
+               spiky_frac, spiky_scale, max_ctx)
+
+
+def _gen(device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, std: float, device, seed: int) -> torch.Tensor:
+    t = torch.randn(*shape, generator=_gen(device, seed), device=device,
+                    dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(torch.bfloat16)
+
+
+def make_inputs(wl: Workload, seed: int = 0, device="cpu",
+                poison_tail: bool = False) -> Dict[str, torch.Tensor]:
+    """Seeded bf16 inputs of workload ``wl`` on ``device``.
+
+    Each tensor has its own sub-seed, so a tensor does not depend on which
+    other tensors were drawn. ``poison_tail`` fills cache rows at positions
+    >= ctx_len with NaN.
+    """
+    device = torch.device(device)
+    B, H, nh, d, L, mc = wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.ctx_len, wl.max_ctx
+    s = 1000003 * (seed + 1)
+    x = _normal((B, H), 1.0, device, s + 1)
+    W_qkv = _normal((H, 3 * H), 0.02, device, s + 2)
+    W_o = _normal((H, H), 0.02, device, s + 3)
+    k_cache = _normal((B, nh, mc, d), 1.0, device, s + 4)
+    v_cache = _normal((B, nh, mc, d), 1.0, device, s + 5)
+    if wl.spiky_frac > 0.0 and L > 0:
+        n_spiky = max(1, int(round(wl.spiky_frac * L)))
+        g = _gen("cpu", s + 6)
+        for b in range(B):
+            for h in range(nh):
+                pos = torch.randperm(L, generator=g)[:n_spiky].to(device)
+                k_cache[b, h, pos] = k_cache[b, h, pos] * wl.spiky_scale
+    if poison_tail and L < mc:
+        k_cache[:, :, L:, :] = float("nan")
+        v_cache[:, :, L:, :] = float("nan")
+    return {"x": x, "W_qkv": W_qkv, "W_o": W_o, "k_cache": k_cache, "v_cache": v_cache}
