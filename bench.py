@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused decode-attention step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--cluster-size C] [--stages S]
+
+Prints ONE JSON line (rank 0). A step is one fused decode step (QKV projection,
+KV append, attention, output projection) of the workload over one batch; the
+default workload is the Llama2-7B-shaped block at B=1, ctx_len 4096.
+
+value    = achieved HBM GB/s over the step's algorithmic bytes (both weights +
+           the K/V cache rows read), summed over ranks: total bytes / max
+           over ranks of the timed region.
+e2e      = the same metric through the host-buffer C-ABI entry point
+           (cfa_decode_step_host): every step copies x host->device, runs the
+           kernel, copies out device->host and synchronizes.
+roofline = the fused kernel (the only kernel of a step) against the measured
+           HBM copy bandwidth.
+cpu_baseline / --impl reference = the fp64 CPU oracle on the host cores.
+
+Inputs live in three rotating copies (each larger than the 129 MB L2), so no
+step reads what the previous step left in L2. Multi-GPU runs are independent
+replicas (the step has no exchange between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused decode-attn step latency (µs) and achieved HBM GB/s vs GB300 peak"
+DEFAULT_WORKLOAD = "llama7b_b1_ctx4k"
+FALLBACK_HBM_GBS = 6800.0
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+# ------------------------------------------------------------ host helpers
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cluster-size", type=int, default=None)
+    ap.add_argument("--stages", type=int, default=None)
+    ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--preload-seconds", type=float, default=1.0,
+                    help="untimed load before the timed region, for clock samples")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate_max(value: float, world: int, device=None) -> float:
+    """Max of `value` over ranks (identity without a process group)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Units all ranks processed / max-over-ranks time, in GB/s."""
+    return bytes_per_step * steps * world / max_seconds / 1e9
+
+
+def percentile(xs, q):
+    xs = sorted(xs)
+    if not xs:
+        return float("nan")
+    k = (len(xs) - 1) * q
+    lo, hi = math.floor(k), math.ceil(k)
+    return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    """Digest of the CUDA sources; ncu traffic figures are tied to it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "out_proj_block_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, cluster_size: int):
+    """DRAM bytes per launch from a committed ncu summary of the same kernel
+    sources, workload and cluster size, or None."""
+    pat = re.compile(r"^traffic_bytes_per_launch:\s*(\d+)\s+workload=(\S+)\s+cluster_size=(\d+)"
+                     r"\s+source_digest=(\w+)", re.M)
+    digest = kernel_source_digest()
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for m in pat.finditer(f.read()):
+                if m.group(2) == workload and int(m.group(3)) == cluster_size and m.group(4) == digest:
+                    return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines):
+    """Median SM clock, max clock and the throttle reasons seen in the samples."""
+    sm, smax, reasons, power = [], [], set(), []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+            power.append(float(parts[3]))
+        except ValueError:
+            continue
+        for name, val in zip(REASON_NAMES, parts[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+            "reasons": sorted(reasons), "samples": len(sm),
+            "power_w_max": max(power) if power else None}
+
+
+def oracle_baseline(wl, cpu_inputs, budget_s: float, max_reps: int = 50):
+    """The fp64 oracle, as it is, on all host cores: full decode steps of the
+    workload, repeated until the time budget is spent (at least one)."""
+    from oracle import cfa_oracle
+    cores = os.cpu_count() or 1
+    used = cfa_oracle.threads_used(cores)
+    times, ref = [], None
+    t_start = time.perf_counter()
+    while len(times) < max_reps:
+        t0 = time.perf_counter()
+        ref = cfa_oracle.decode_step(cpu_inputs["x"], cpu_inputs["W_qkv"], cpu_inputs["W_o"],
+                                     cpu_inputs["k_cache"], cpu_inputs["v_cache"],
+                                     wl.ctx_len, nthreads=used)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    step_s = statistics.median(times)
+    return {"value": wl.algorithmic_bytes / step_s / 1e9, "unit": "GB/s", "cores": used,
+            "kind": "oracle",
+            "sample": f"{len(times)} full fp64 decode steps of {wl.name} "
+                      f"(median {step_s * 1e3:.1f} ms per step)",
+            "step_ms": step_s * 1e3}, ref
+
+
+# --------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from out_proj_block_gb300 import workloads
+    from oracle import cfa_oracle
+    cfa_oracle.build()
+    wl = workloads.WORKLOADS[args.workload]
+    t = workloads.make_inputs(wl, seed=0, device="cpu")
+    cores = os.cpu_count() or 1
+    used = cfa_oracle.threads_used(cores)
+    run = lambda: cfa_oracle.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"],
+                                         t["v_cache"], wl.ctx_len, nthreads=used)
+    for _ in range(max(args.warmup, 0)):
+        run()
+    times = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - s)
+    total = time.perf_counter() - t0
+    value = wl.algorithmic_bytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wl.as_config(), l2="host run; no GPU L2 involved"),
+        "latency_us": {"p50": percentile(times, 0.5) * 1e6, "p10": percentile(times, 0.1) * 1e6,
+                       "p90": percentile(times, 0.9) * 1e6},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": f"{args.steps} full fp64 decode steps of {wl.name}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    del torch
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from out_proj_block_gb300 import build as cuda_build
+    if rank == 0 or world == 1:
+        cuda_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from out_proj_block_gb300 import cfa, workloads
+
+    wl = workloads.WORKLOADS[args.workload]
+    B, H = wl.B, wl.hidden
+    copies = [workloads.make_inputs(wl, seed=i, device=dev) for i in range(max(args.copies, 1))]
+    outs = [torch.empty(B, H, dtype=torch.bfloat16, device=dev) for _ in copies]
+    plan = cfa.Plan(B, H, wl.n_heads, wl.head_dim, wl.max_ctx,
+                    cluster_size=args.cluster_size, stages=args.stages)
+    desc = plan.describe()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        c = copies[i % len(copies)]
+        plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
+                         wl.ctx_len, outs[i % len(copies)], stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    st = plan.status()
+    if st != cfa.CFA_OK:
+        raise RuntimeError(f"device status after warm-up: {cfa.cfa_status_string(st)}")
+
+    sampler = ClockSampler(local).start()
+    t_end = time.perf_counter() + args.preload_seconds
+    i = 0
+    while time.perf_counter() < t_end:  # untimed load so clocks settle and get sampled
+        for _ in range(64):
+            step(i)
+            i += 1
+        torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for k in range(K):
+        step(k)
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(K)]
+    total_s = ev[0].elapsed_time(ev[K]) / 1e3
+    st = plan.status()
+    if st != cfa.CFA_OK:
+        raise RuntimeError(f"device status after timing: {cfa.cfa_status_string(st)}")
+    max_total_s = aggregate_max(total_s, world, dev)
+    value = whole_job_gbs(wl.algorithmic_bytes, K, world, max_total_s)
+    mean_step_s = total_s / K
+    achieved = wl.algorithmic_bytes / mean_step_s / 1e9
+
+    # CUDA-graph replay of the same steps (launch overhead removed)
+    graph_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(dev)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            with torch.cuda.graph(g, stream=s2):
+                for k in range(len(copies)):
+                    c = copies[k]
+                    plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
+                                     wl.ctx_len, outs[k], s2)
+        stream.wait_stream(s2)
+        reps = max(1, K // len(copies))
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = e0.elapsed_time(e1) * 1e3 / (reps * len(copies))
+    except Exception as exc:  # graph capture is an extra measurement, not the headline
+        graph_us = f"unavailable: {type(exc).__name__}: {exc}"
+
+    # end-to-end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        x_host = [c["x"].cpu().pin_memory() for c in copies]
+        out_host = [torch.empty(B, H, dtype=torch.bfloat16).pin_memory() for _ in copies]
+
+        def host_step(k):
+            c = copies[k % len(copies)]
+            plan.decode_step_host(x_host[k % len(copies)], c["W_qkv"], c["W_o"], c["k_cache"],
+                                  c["v_cache"], wl.ctx_len, out_host[k % len(copies)], stream)
+
+        for k in range(max(args.warmup, 3)):
+            host_step(k)
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for k in range(K):
+            host_step(k)
+        e2e_s = aggregate_max(time.perf_counter() - t0, world, dev)
+        e2e = {"value": whole_job_gbs(wl.algorithmic_bytes, K, world, e2e_s), "unit": "GB/s",
+               "h2d_bytes_per_step": int(x_host[0].numel() * 2),
+               "d2h_bytes_per_step": int(out_host[0].numel() * 2),
+               "ms_per_step": e2e_s / K * 1e3}
+
+    peak, peak_kind = measured_peaks()
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+            "traffic": recorded_traffic(wl.name, plan.cluster_size),
+            "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+            "kernel": "cfa::fused_decode_kernel"}
+
+    cpu_base, parity = None, None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_inputs = {k: v.cpu() for k, v in copies[0].items()}
+        cpu_base, ref = oracle_baseline(wl, cpu_inputs, args.cpu_seconds)
+        step(0)  # recompute copy 0 so its output matches the oracle's inputs
+        torch.cuda.synchronize(dev)
+        got = outs[0].float().cpu().numpy()
+        parity = {"out_rel_l2": float(np.linalg.norm(got - ref["out"]) / np.linalg.norm(ref["out"])),
+                  "out_max_abs": float(np.abs(got - ref["out"]).max())}
+
+    plan.close()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": max_total_s / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(wl.as_config(), cluster_size=desc["cluster_size"],
+                       stages=desc["stages"], grid=desc["grid"],
+                       l2=f"{len(copies)} rotating input copies of "
+                          f"{wl.algorithmic_bytes / 1e6:.0f} MB each (> 129 MB L2)",
+                       parallelism=f"replicas x{world}"),
+        "latency_us": {"mean": mean_step_s * 1e6, "p10": percentile(step_ms, 0.1) * 1e3,
+                       "p50": percentile(step_ms, 0.5) * 1e3, "p90": percentile(step_ms, 0.9) * 1e3},
+        "graph_latency_us": graph_us,
+        "roofline": roof,
+        "cpu_baseline": cpu_base,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": K,
+        "parity": parity,
+        "plan": desc,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

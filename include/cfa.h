@@ -1,0 +1,169 @@
+/*
+ * cfa.h -- C ABI of the cluster-fused decode-attention library (libcfa.so).
+ *
+ * One call runs one decode step of a decoder attention block for a batch of
+ * B sequences on one GPU, in a single kernel launch:
+ *
+ *   1. QKV projection of the new token      qkv[b] = x[b] . W_qkv
+ *   2. KV append                            k_cache[b,h,ctx_len] = k[b,h]
+ *                                           v_cache[b,h,ctx_len] = v[b,h]
+ *   3. single-query attention with a max-subtracted softmax over the
+ *      ctx_len cached keys plus the new one (scale 1/sqrt(head_dim))
+ *   4. output projection                    out[b] = concat_h(attn[b,h]) . W_o
+ *
+ * This is the decoder block of the page "ClusterFusion框架解析：LLM推理优化的集群
+ * 通信革命" (ClusterFusion framework analysis): the three stages of its §1.1,
+ * fused the way its §3.2 describes (one thread-block cluster per head, the
+ * cluster's blocks splitting head_dim and the KV length, q/k/v shared by a
+ * cluster gather and the softmax statistics and partial outputs combined by
+ * cluster reductions over distributed shared memory, §3.1). The page merges
+ * its partial output projections with atomicAdd; this library merges them in
+ * a fixed head order instead, so results are bitwise reproducible.
+ *
+ * Conventions shared by every call:
+ *   - All tensors are bf16 (IEEE binary32 with the low 16 bits dropped),
+ *     dense, row-major, and live in device memory owned by the caller. All
+ *     arithmetic accumulates in fp32. Results are rounded to bf16 with
+ *     round-to-nearest-even.
+ *   - Weights are [in, out] and applied as x . W (the page's
+ *     torch.mm(hidden_states, W_qkv) form, §1.1):
+ *       W_qkv [hidden, 3*hidden]: columns [0,H) are Q, [H,2H) K, [2H,3H) V;
+ *                                 head h owns columns [h*d, (h+1)*d) of each.
+ *       W_o   [hidden, hidden]:   row block [h*d, (h+1)*d) multiplies head h.
+ *   - Caches are [B, n_heads, max_ctx, head_dim]. Positions [0, ctx_len) are
+ *     read; position ctx_len is written; all other positions are neither read
+ *     nor written.
+ *   - Every device pointer must be 16-byte aligned. `out` must not overlap an
+ *     input. ctx_len is shared by all B sequences.
+ *   - Calls are asynchronous on the given CUDA stream (NULL = legacy default
+ *     stream) unless stated otherwise. A plan owns a small device workspace,
+ *     so one plan must not run concurrently on two streams; use one plan per
+ *     stream.
+ *   - Functions that return cfa_status never abort the process. Host-side
+ *     argument checks happen before anything is launched; an error leaves
+ *     every buffer untouched.
+ *
+ * Supported shapes: hidden == n_heads * head_dim, head_dim in {64, 128},
+ * 1 <= B <= 16, hidden a multiple of 64, 1 <= max_ctx <= 1<<22. Other shapes
+ * return CFA_ERR_UNSUPPORTED.
+ */
+#ifndef CFA_H
+#define CFA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct cfa_plan cfa_plan; /* opaque */
+
+typedef enum cfa_status {
+    CFA_OK = 0,
+    CFA_ERR_INVALID_ARG = 1, /* NULL plan or pointer, ctx_len out of range, ... */
+    CFA_ERR_UNSUPPORTED = 2, /* a shape or cluster size this build does not run */
+    CFA_ERR_CUDA = 3,        /* a CUDA runtime call failed (no device, launch, ...) */
+    CFA_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see cfa_plan_status) */
+    CFA_ERR_ALIGNMENT = 5    /* a pointer is not 16-byte aligned */
+} cfa_status;
+
+/*
+ * Create a plan for batch B, hidden size `hidden` = n_heads * head_dim and a
+ * cache capacity of max_ctx positions, on the current CUDA device.
+ * Chooses the cluster size (blocks per head) and the pipeline depth, sets the
+ * kernel attributes, and allocates the plan's workspace (fp32 per-head
+ * output-projection partials [n_heads, B, hidden], per-column-chunk arrival
+ * counters, a status word, and device staging for cfa_decode_step_host).
+ * Returns NULL on failure; cfa_last_error() then says why.
+ */
+cfa_plan *cfa_plan_create(int B, int hidden, int n_heads, int head_dim, int max_ctx);
+
+/* Release the plan and its workspace. Synchronizes the device first. NULL is a no-op. */
+void cfa_plan_destroy(cfa_plan *plan);
+
+/*
+ * One decode step (steps 1-4 above), launched on `stream` (a cudaStream_t).
+ *   x       bf16 [B, hidden]               read
+ *   W_qkv   bf16 [hidden, 3*hidden]        read
+ *   W_o     bf16 [hidden, hidden]          read
+ *   k_cache bf16 [B, n_heads, max_ctx, head_dim]  rows [0,ctx_len) read, row ctx_len written
+ *   v_cache bf16 [B, n_heads, max_ctx, head_dim]  same
+ *   ctx_len number of cached positions before this token, 0 <= ctx_len < max_ctx
+ *   out     bf16 [B, hidden]               written
+ * Re-running a step with the same ctx_len rewrites the same cache row with
+ * the same value, so a step is idempotent.
+ * Errors: CFA_ERR_INVALID_ARG (NULL pointer, ctx_len out of range),
+ * CFA_ERR_ALIGNMENT, CFA_ERR_CUDA (launch failure). Faults raised while the
+ * kernel runs surface at the next synchronizing call, as with any CUDA kernel.
+ */
+cfa_status cfa_decode_step(cfa_plan *plan, const void *x, const void *W_qkv,
+                           const void *W_o, void *k_cache, void *v_cache,
+                           int ctx_len, void *out, void *stream);
+
+/*
+ * The same step for a caller whose token activations live in host memory:
+ * copies x_host (bf16 [B, hidden]) to the plan's device staging buffer,
+ * runs cfa_decode_step on `stream`, copies the result back to out_host
+ * (bf16 [B, hidden]) and synchronizes `stream` before returning. Weights and
+ * caches stay device pointers. Host buffers should be pinned
+ * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously;
+ * pageable memory works but is slower. Errors as cfa_decode_step.
+ */
+cfa_status cfa_decode_step_host(cfa_plan *plan, const void *x_host, const void *W_qkv,
+                                const void *W_o, void *k_cache, void *v_cache,
+                                int ctx_len, void *out_host, void *stream);
+
+/*
+ * Override the cluster size (thread blocks per head): 1, 2, 4, 8 or 16.
+ * CFA_ERR_UNSUPPORTED if the shape does not split evenly at that size, the
+ * device cannot co-schedule such a cluster, or its shared memory does not fit.
+ * The plan is unchanged on error.
+ */
+cfa_status cfa_plan_set_cluster_size(cfa_plan *plan, int cluster_size);
+
+/*
+ * Override the pipeline depth (number of 16 KB shared-memory stages per
+ * block); 0 restores the automatic choice. CFA_ERR_UNSUPPORTED if the shared
+ * memory does not fit or the depth is outside [2, 64]. The plan is unchanged
+ * on error.
+ */
+cfa_status cfa_plan_set_stages(cfa_plan *plan, int stages);
+
+/* Current cluster size of the plan, or -1 for NULL. */
+int cfa_plan_cluster_size(const cfa_plan *plan);
+
+/*
+ * Write a one-line JSON description of the plan (shape, cluster size, grid,
+ * block, shared memory per block, pipeline stages, stage bytes, co-resident
+ * clusters) into buf (NUL-terminated, truncated to len). CFA_ERR_INVALID_ARG
+ * for NULL arguments.
+ */
+cfa_status cfa_plan_describe(const cfa_plan *plan, char *buf, int len);
+
+/*
+ * Device-side status of the plan: synchronizes the device, reads and clears
+ * the status word the kernels set when a bounded wait gives up. CFA_OK when
+ * nothing happened, CFA_ERR_TIMEOUT after a timed-out wait, CFA_ERR_CUDA if
+ * the read itself fails.
+ */
+cfa_status cfa_plan_status(cfa_plan *plan);
+
+/* Status of the last failed call on this thread (plan creation included). */
+cfa_status cfa_last_error(void);
+
+/* Static, human-readable name of a status code. */
+const char *cfa_status_string(cfa_status status);
+
+/*
+ * Self-test of the bounded-wait mechanism every in-kernel wait uses: launches
+ * one block that waits on a shared-memory barrier nothing ever arrives on,
+ * giving up after limit_us microseconds, then reports through a status word.
+ * Synchronizes `stream`. Returns CFA_ERR_TIMEOUT when the wait gave up as it
+ * must, CFA_OK if it (wrongly) completed, CFA_ERR_CUDA on a CUDA error.
+ * limit_us must be in [1, 1<<20]. No GPU fault or hang is involved.
+ */
+cfa_status cfa_selftest_wait_timeout(int limit_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CFA_H */

@@ -1,0 +1,512 @@
+// cfa_api.cu -- host side of the C ABI declared in include/cfa.h: plan
+// creation and validation, shared-memory layout, tensor-map encoding and the
+// cluster launch of the fused kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "cfa.h"
+#include "cfa_internal.h"
+
+namespace cfa {
+const void *fused_kernel_d128(int maxb);
+const void *fused_kernel_d64(int maxb);
+const void *selftest_wait_kernel_ptr();
+}  // namespace cfa
+
+using cfa::KernelParams;
+
+namespace {
+
+thread_local cfa_status g_last_error = CFA_OK;
+
+cfa_status fail(cfa_status s) {
+    g_last_error = s;
+    return s;
+}
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxStages = 12;
+constexpr int kMinStages = 2;
+
+int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct cfa_plan {
+    int B = 0, H = 0, nh = 0, D = 0, max_ctx = 0;
+    int device = -1, num_sms = 0, smem_per_sm = 0, smem_optin = 0, smem_reserved = 0;
+    int C = 0;
+    int stages_override = 0;      // 0 = choose automatically
+    KernelParams kp{};            // everything but the per-call pointers
+    int smem_bytes = 0;
+    int coresident_clusters = 0;
+    const void *kernel = nullptr;
+    // workspace
+    float *partials = nullptr;    // [nh][B][H]
+    unsigned *words = nullptr;    // [0, kMaxCluster) counters, [kMaxCluster] status
+    uint16_t *x_stage = nullptr;  // [B][H] for cfa_decode_step_host
+    uint16_t *out_stage = nullptr;
+    // cached tensor maps
+    CUtensorMap tm_wqkv;  // 64-byte aligned by its own declaration
+    CUtensorMap tm_wo;
+    const void *tm_wqkv_src = nullptr;
+    const void *tm_wo_src = nullptr;
+    int tm_wqkv_rows = 0;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Row-major bf16 matrix [rows][cols]; boxes of box_rows x box_cols elements.
+cfa_status encode_2d(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t rows,
+                     uint32_t box_cols, uint32_t box_rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return CFA_ERR_CUDA;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), gdim,
+                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? CFA_OK : CFA_ERR_CUDA;
+}
+
+const void *kernel_for(int D, int maxb) {
+    return D == 128 ? cfa::fused_kernel_d128(maxb) : cfa::fused_kernel_d64(maxb);
+}
+
+// Work split, shared-memory layout and pipeline depth for cluster size C.
+// Pure host arithmetic; no CUDA calls.
+cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelParams *kp,
+                       int *smem_out, int *maxb_out) {
+    const int D = pl->D, B = pl->B, H = pl->H;
+    if (C != 1 && C != 2 && C != 4 && C != 8 && C != 16) return CFA_ERR_UNSUPPORTED;
+    const int G = D / cfa::kTileCols;  // 64-column groups per head block
+    if (C < G) return CFA_ERR_UNSUPPORTED;
+    const int RG = C / G;
+    if (H % RG) return CFA_ERR_UNSUPPORTED;
+    const int R = H / RG;
+    int TRA = 128;
+    while (TRA > 8 && R % TRA) TRA >>= 1;
+    if (R % TRA || TRA < cfa::kComputeWarps) return CFA_ERR_UNSUPPORTED;
+    if (H % C) return CFA_ERR_UNSUPPORTED;
+    const int ncols = H / C;
+    if (ncols % cfa::kTileCols) return CFA_ERR_UNSUPPORTED;
+    int maxb = 1;
+    while (maxb < B) maxb <<= 1;
+
+    const int xstage = B * TRA * 2;
+    const int nstate = cfa::kComputeWarps * (256 / D);
+    const int qkv_recv = C * B * 3 * cfa::kTileCols * 4;
+    const int sm_recv = C * B * (D + 4) * 4;
+    const int qkv_full = B * 3 * D * 4;
+    const int attn = B * D * 4;
+    const int scratch = std::max(cfa::kComputeWarps * B * cfa::kTileCols * 4,
+                                 (nstate * D + 2 * nstate) * 4);
+    const int fixed = align_up(qkv_recv, 128) + align_up(sm_recv, 128) +
+                      align_up(qkv_full, 128) + align_up(attn, 128) + align_up(scratch, 128) +
+                      128 /* barriers and flags, per stage added below */;
+    const int per_stage = cfa::kStageBytes + xstage + 16;
+
+    const int grid = pl->nh * C;
+    int per_sm = (grid + pl->num_sms - 1) / std::max(pl->num_sms, 1);
+    per_sm = std::min(std::max(per_sm, 1), 4);
+    int NS = 0;
+    for (; per_sm >= 1 && NS < kMinStages; --per_sm) {
+        const int budget =
+            std::min(pl->smem_optin, pl->smem_per_sm / per_sm - pl->smem_reserved);
+        NS = std::min(kMaxStages, (budget - fixed) / per_stage);
+    }
+    if (stages_override > 0) NS = stages_override;
+    if (NS < kMinStages || NS > 64) return CFA_ERR_UNSUPPORTED;
+
+    int off = NS * cfa::kStageBytes;
+    KernelParams k{};
+    k.off_xring = off;
+    off = align_up(off + NS * xstage, 128);
+    k.off_qkv_recv = off;
+    off = align_up(off + qkv_recv, 128);
+    k.off_sm_recv = off;
+    off = align_up(off + sm_recv, 128);
+    k.off_qkv_full = off;
+    off = align_up(off + qkv_full, 128);
+    k.off_attn = off;
+    off = align_up(off + attn, 128);
+    k.off_scratch = off;
+    off = align_up(off + scratch, 128);
+    k.off_bars = off;
+    off += (2 * NS + 2) * 8 + 16;
+    if (off > pl->smem_optin) return CFA_ERR_UNSUPPORTED;
+
+    k.B = B;
+    k.H = H;
+    k.nh = pl->nh;
+    k.max_ctx = pl->max_ctx;
+    k.C = C;
+    k.G = G;
+    k.RG = RG;
+    k.R = R;
+    k.TRA = TRA;
+    k.nA = R / TRA;
+    k.ncols = ncols;
+    k.nstages = NS;
+    k.timeout_ns = kDefaultTimeoutNs;
+    k.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    *kp = k;
+    *smem_out = off;
+    *maxb_out = maxb;
+    return CFA_OK;
+}
+
+cudaLaunchConfig_t launch_config(const cfa_plan *pl, const KernelParams &kp, int smem,
+                                 cudaStream_t stream, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl->nh * kp.C, 1, 1);
+    cfg.blockDim = dim3(cfa::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kp.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Apply cluster size C to the plan if the device can run it.
+cfa_status configure(cfa_plan *pl, int C, int stages_override) {
+    KernelParams kp;
+    int smem = 0, maxb = 1;
+    cfa_status st = make_layout(pl, C, stages_override, &kp, &smem, &maxb);
+    if (st != CFA_OK) return st;
+    const void *kernel = kernel_for(pl->D, maxb);
+    if (!kernel) return CFA_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pl->smem_optin) != cudaSuccess ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return CFA_ERR_CUDA;
+    }
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config(pl, kp, smem, nullptr, attr);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return CFA_ERR_UNSUPPORTED;
+    }
+    if (clusters < 1) return CFA_ERR_UNSUPPORTED;
+    pl->C = C;
+    pl->kp = kp;
+    pl->smem_bytes = smem;
+    pl->kernel = kernel;
+    pl->coresident_clusters = clusters;
+    pl->tm_wqkv_src = nullptr;  // the projection box height may have changed
+    return CFA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+void free_workspace(cfa_plan *pl) {
+    if (pl->partials) cudaFree(pl->partials);
+    if (pl->words) cudaFree(pl->words);
+    if (pl->x_stage) cudaFree(pl->x_stage);
+    if (pl->out_stage) cudaFree(pl->out_stage);
+    pl->partials = nullptr;
+    pl->words = nullptr;
+    pl->x_stage = pl->out_stage = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *cfa_status_string(cfa_status s) {
+    switch (s) {
+        case CFA_OK: return "CFA_OK";
+        case CFA_ERR_INVALID_ARG: return "CFA_ERR_INVALID_ARG";
+        case CFA_ERR_UNSUPPORTED: return "CFA_ERR_UNSUPPORTED";
+        case CFA_ERR_CUDA: return "CFA_ERR_CUDA";
+        case CFA_ERR_TIMEOUT: return "CFA_ERR_TIMEOUT";
+        case CFA_ERR_ALIGNMENT: return "CFA_ERR_ALIGNMENT";
+    }
+    return "CFA_ERR_UNKNOWN";
+}
+
+cfa_status cfa_last_error(void) { return g_last_error; }
+
+cfa_plan *cfa_plan_create(int B, int hidden, int n_heads, int head_dim, int max_ctx) {
+    if (B < 1 || hidden < 1 || n_heads < 1 || head_dim < 1 || max_ctx < 1 ||
+        static_cast<long long>(n_heads) * head_dim != hidden) {
+        fail(CFA_ERR_INVALID_ARG);
+        return nullptr;
+    }
+    if ((head_dim != 64 && head_dim != 128) || B > 16 || hidden % 64 != 0 ||
+        max_ctx > (1 << 22) || hidden > (1 << 16)) {
+        fail(CFA_ERR_UNSUPPORTED);
+        return nullptr;
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    int major = 0, minor = 0, sms = 0, per_sm = 0, optin = 0, reserved = 0, cluster_ok = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&cluster_ok, cudaDevAttrClusterLaunch, dev) != cudaSuccess) {
+        cudaGetLastError();
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    if (major != 10 || minor != 3 || !cluster_ok) {  // the library is built for sm_103a only
+        fail(CFA_ERR_UNSUPPORTED);
+        return nullptr;
+    }
+    cfa_plan *pl = new (std::nothrow) cfa_plan();
+    if (!pl) {
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    pl->B = B;
+    pl->H = hidden;
+    pl->nh = n_heads;
+    pl->D = head_dim;
+    pl->max_ctx = max_ctx;
+    pl->device = dev;
+    pl->num_sms = sms;
+    pl->smem_per_sm = per_sm;
+    pl->smem_optin = optin;
+    pl->smem_reserved = reserved;
+
+    const size_t part_bytes = sizeof(float) * static_cast<size_t>(n_heads) * B * hidden;
+    const size_t act_bytes = 2u * static_cast<size_t>(B) * hidden;
+    if (cudaMalloc(&pl->partials, part_bytes) != cudaSuccess ||
+        cudaMalloc(&pl->words, sizeof(unsigned) * (cfa::kMaxCluster + 16)) != cudaSuccess ||
+        cudaMalloc(&pl->x_stage, act_bytes) != cudaSuccess ||
+        cudaMalloc(&pl->out_stage, act_bytes) != cudaSuccess ||
+        cudaMemset(pl->words, 0, sizeof(unsigned) * (cfa::kMaxCluster + 16)) != cudaSuccess) {
+        cudaGetLastError();
+        free_workspace(pl);
+        delete pl;
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+
+    // Default cluster size: the smallest that gives at least one block per SM,
+    // else the largest that fits this shape.
+    const int candidates[5] = {1, 2, 4, 8, 16};
+    int chosen = 0;
+    for (int C : candidates) {
+        if (n_heads * C < sms) continue;
+        if (configure(pl, C, 0) == CFA_OK) {
+            chosen = C;
+            break;
+        }
+    }
+    if (!chosen) {
+        for (int i = 4; i >= 0 && !chosen; --i)
+            if (configure(pl, candidates[i], 0) == CFA_OK) chosen = candidates[i];
+    }
+    if (!chosen) {
+        free_workspace(pl);
+        delete pl;
+        fail(CFA_ERR_UNSUPPORTED);
+        return nullptr;
+    }
+    return pl;
+}
+
+void cfa_plan_destroy(cfa_plan *pl) {
+    if (!pl) return;
+    cudaDeviceSynchronize();
+    free_workspace(pl);
+    delete pl;
+}
+
+cfa_status cfa_plan_set_cluster_size(cfa_plan *pl, int C) {
+    if (!pl) return fail(CFA_ERR_INVALID_ARG);
+    const cfa_status st = configure(pl, C, pl->stages_override);
+    return st == CFA_OK ? CFA_OK : fail(st);  // on error the plan is unchanged
+}
+
+cfa_status cfa_plan_set_stages(cfa_plan *pl, int stages) {
+    if (!pl || stages < 0) return fail(CFA_ERR_INVALID_ARG);
+    const cfa_status st = configure(pl, pl->C, stages);
+    if (st != CFA_OK) return fail(st);  // on error the plan is unchanged
+    pl->stages_override = stages;
+    return CFA_OK;
+}
+
+int cfa_plan_cluster_size(const cfa_plan *pl) { return pl ? pl->C : -1; }
+
+cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
+    if (!pl || !buf || len < 1) return fail(CFA_ERR_INVALID_ARG);
+    const KernelParams &k = pl->kp;
+    std::snprintf(buf, static_cast<size_t>(len),
+                  "{\"B\": %d, \"hidden\": %d, \"n_heads\": %d, \"head_dim\": %d, "
+                  "\"max_ctx\": %d, \"cluster_size\": %d, \"grid\": %d, \"block\": %d, "
+                  "\"smem_bytes\": %d, \"stages\": %d, \"stage_bytes\": %d, "
+                  "\"proj_rows_per_block\": %d, \"proj_tile_rows\": %d, "
+                  "\"out_cols_per_block\": %d, \"coresident_clusters\": %d, \"num_sms\": %d}",
+                  pl->B, pl->H, pl->nh, pl->D, pl->max_ctx, pl->C, pl->nh * pl->C,
+                  cfa::kThreads, pl->smem_bytes, k.nstages, cfa::kStageBytes, k.R, k.TRA,
+                  k.ncols, pl->coresident_clusters, pl->num_sms);
+    return CFA_OK;
+}
+
+cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const void *W_o,
+                           void *k_cache, void *v_cache, int ctx_len, void *out,
+                           void *stream) {
+    if (!pl || !x || !W_qkv || !W_o || !k_cache || !v_cache || !out)
+        return fail(CFA_ERR_INVALID_ARG);
+    if (ctx_len < 0 || ctx_len >= pl->max_ctx) return fail(CFA_ERR_INVALID_ARG);
+    if (!aligned16(x) || !aligned16(W_qkv) || !aligned16(W_o) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || !aligned16(out))
+        return fail(CFA_ERR_ALIGNMENT);
+    const size_t H = static_cast<size_t>(pl->H);
+    const size_t act = 2 * H * pl->B;
+    const size_t cache = 2 * static_cast<size_t>(pl->B) * pl->nh * pl->max_ctx * pl->D;
+    if (overlaps(out, act, x, act) || overlaps(out, act, W_qkv, 2 * H * 3 * H) ||
+        overlaps(out, act, W_o, 2 * H * H) || overlaps(out, act, k_cache, cache) ||
+        overlaps(out, act, v_cache, cache))
+        return fail(CFA_ERR_INVALID_ARG);
+
+    if (pl->tm_wqkv_src != W_qkv || pl->tm_wqkv_rows != pl->kp.TRA) {
+        if (encode_2d(&pl->tm_wqkv, W_qkv, 3 * H, H, cfa::kTileCols,
+                      static_cast<uint32_t>(pl->kp.TRA)) != CFA_OK) {
+            pl->tm_wqkv_src = nullptr;
+            return fail(CFA_ERR_CUDA);
+        }
+        pl->tm_wqkv_src = W_qkv;
+        pl->tm_wqkv_rows = pl->kp.TRA;
+    }
+    if (pl->tm_wo_src != W_o) {
+        if (encode_2d(&pl->tm_wo, W_o, H, H, cfa::kTileCols, static_cast<uint32_t>(pl->D)) !=
+            CFA_OK) {
+            pl->tm_wo_src = nullptr;
+            return fail(CFA_ERR_CUDA);
+        }
+        pl->tm_wo_src = W_o;
+    }
+
+    KernelParams kp = pl->kp;
+    kp.x = static_cast<const uint16_t *>(x);
+    kp.k_cache = static_cast<uint16_t *>(k_cache);
+    kp.v_cache = static_cast<uint16_t *>(v_cache);
+    kp.out = static_cast<uint16_t *>(out);
+    kp.partials = pl->partials;
+    kp.counters = pl->words;
+    kp.status = pl->words + cfa::kMaxCluster;
+    kp.ctx_len = ctx_len;
+
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg =
+        launch_config(pl, kp, pl->smem_bytes, static_cast<cudaStream_t>(stream), attr);
+    void *args[3] = {&pl->tm_wqkv, &pl->tm_wo, &kp};
+    if (cudaLaunchKernelExC(&cfg, pl->kernel, args) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    return CFA_OK;
+}
+
+cfa_status cfa_decode_step_host(cfa_plan *pl, const void *x_host, const void *W_qkv,
+                                const void *W_o, void *k_cache, void *v_cache, int ctx_len,
+                                void *out_host, void *stream) {
+    if (!pl || !x_host || !out_host) return fail(CFA_ERR_INVALID_ARG);
+    if (ctx_len < 0 || ctx_len >= pl->max_ctx) return fail(CFA_ERR_INVALID_ARG);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t act = 2u * static_cast<size_t>(pl->B) * pl->H;
+    if (cudaMemcpyAsync(pl->x_stage, x_host, act, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    const cfa_status st =
+        cfa_decode_step(pl, pl->x_stage, W_qkv, W_o, k_cache, v_cache, ctx_len, pl->out_stage, s);
+    if (st != CFA_OK) return st;
+    if (cudaMemcpyAsync(out_host, pl->out_stage, act, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    return CFA_OK;
+}
+
+cfa_status cfa_plan_status(cfa_plan *pl) {
+    if (!pl) return fail(CFA_ERR_INVALID_ARG);
+    unsigned word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, pl->words + cfa::kMaxCluster, sizeof word, cudaMemcpyDeviceToHost) !=
+            cudaSuccess ||
+        cudaMemset(pl->words + cfa::kMaxCluster, 0, sizeof word) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    if (word & cfa::kStatusTimeoutBit) return fail(CFA_ERR_TIMEOUT);
+    return CFA_OK;
+}
+
+cfa_status cfa_selftest_wait_timeout(int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > (1 << 20)) return fail(CFA_ERR_INVALID_ARG);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned *word = nullptr;
+    unsigned host = 0;
+    if (cudaMalloc(&word, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    unsigned long long ns = static_cast<unsigned long long>(limit_us) * 1000ull;
+    void *args[2] = {&word, &ns};
+    cudaError_t e = cudaMemsetAsync(word, 0, sizeof(unsigned), s);
+    if (e == cudaSuccess)
+        e = cudaLaunchKernel(cfa::selftest_wait_kernel_ptr(), dim3(1), dim3(32), args, 0, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&host, word, sizeof host, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(word);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    return (host & cfa::kStatusTimeoutBit) ? CFA_ERR_TIMEOUT : CFA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// cfa_internal.h -- launch parameters shared by the host side and the fused
+// kernel. Not part of the public ABI (that is include/cfa.h).
+#pragma once
+
+#include <cstdint>
+
+namespace cfa {
+
+constexpr int kComputeWarps = 8;                   // warps doing arithmetic
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kThreads = kComputeThreads + 32;     // + one load-issuing warp
+constexpr int kStageBytes = 16384;                 // one pipeline stage
+constexpr int kTileCols = 64;                      // weight tile width (128 bytes of bf16)
+constexpr int kMaxCluster = 16;
+
+// Status word bits, written by kernels and read by cfa_plan_status.
+constexpr unsigned kStatusTimeoutBit = 1u;
+constexpr unsigned kStatusSiteShift = 8;  // site code of the first timeout
+
+// Site codes recorded with a timeout in the status word.
+enum WaitSite : unsigned {
+    kSiteStageFull = 1,
+    kSiteStageEmpty = 2,
+    kSiteQkvExchange = 3,
+    kSiteSoftmaxExchange = 4,
+    kSiteSelftest = 15,
+};
+
+struct KernelParams {
+    const uint16_t *x;     // [B][H] bf16
+    uint16_t *k_cache;     // [B][nh][max_ctx][D] bf16
+    uint16_t *v_cache;
+    uint16_t *out;         // [B][H] bf16
+    float *partials;       // [nh][B][H] fp32 per-head output-projection partials
+    unsigned *counters;    // [C] arrivals per output-column chunk
+    unsigned *status;      // device status word
+    int B, H, nh, max_ctx, ctx_len;
+    int C;                 // blocks per cluster (= per head)
+    int G;                 // column groups of 64 inside one head's Q/K/V block: D/64 or fewer
+    int RG;                // row groups of the hidden dimension: C / G
+    int R;                 // hidden rows per block in the projection: H / RG
+    int TRA;               // rows per projection tile
+    int nA;                // projection tiles per Q/K/V block: R / TRA
+    int ncols;             // output columns per block in the out-projection: H / C
+    int nstages;           // pipeline depth
+    int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_scratch, off_bars;
+    unsigned long long timeout_ns;
+    float qscale;          // log2(e) / sqrt(D)
+};
+
+}  // namespace cfa

@@ -1,0 +1,217 @@
+"""GPU parity: the fused CUDA kernel against the fp64 oracle, through the C ABI.
+
+Tolerance (both for `out` and for the appended K/V rows, each compared with
+the oracle's unrounded fp64 values): relative L2 error <= 5e-3 and max abs
+error <= 3e-2. Cache rows other than row ctx_len must be bit-identical after
+the call; rows past ctx_len are NaN-poisoned, so a stray read would also show
+up as a non-finite output.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from out_proj_block_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 5e-3
+MAX_ABS = 3e-2
+NTHREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def cfa():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from out_proj_block_gb300 import build
+    build.build()
+    from out_proj_block_gb300 import cfa as mod
+    return mod
+
+
+def rel_l2(got, ref):
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def check_close(name, got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    e_rel = rel_l2(got, ref)
+    e_abs = float(np.abs(got - ref).max())
+    assert e_rel <= REL_L2 and e_abs <= MAX_ABS, (
+        f"{name}: rel L2 {e_rel:.3e} (<= {REL_L2}), max abs {e_abs:.3e} (<= {MAX_ABS})")
+    return e_rel, e_abs
+
+
+def run_and_check(cfa, oracle, wl, seed=1, C=None, stages=None, check_untouched=True):
+    t = workloads.make_inputs(wl, seed=seed, device="cuda", poison_tail=True)
+    k_before = t["k_cache"].clone() if check_untouched else None
+    v_before = t["v_cache"].clone() if check_untouched else None
+    cpu = {k: v.cpu() for k, v in t.items()}
+    L = wl.ctx_len
+    out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx,
+                  cluster_size=C, stages=stages) as plan:
+        plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], L, out)
+        torch.cuda.synchronize()
+        assert plan.status() == cfa.CFA_OK
+        used_C = plan.cluster_size
+    ref = oracle.decode_step(cpu["x"], cpu["W_qkv"], cpu["W_o"], cpu["k_cache"],
+                             cpu["v_cache"], L, nthreads=NTHREADS)
+    got = out.float().cpu().numpy()
+    errs = {"out": check_close("out", got, ref["out"])}
+    k_row = t["k_cache"][:, :, L].float().cpu().numpy()
+    v_row = t["v_cache"][:, :, L].float().cpu().numpy()
+    errs["k_new"] = check_close("k_new", k_row, ref["k_new"])
+    errs["v_new"] = check_close("v_new", v_row, ref["v_new"])
+    if check_untouched:
+        for name, before, after in (("k", k_before, t["k_cache"]), ("v", v_before, t["v_cache"])):
+            b = before.view(torch.int16).clone()
+            a = after.view(torch.int16).clone()
+            b[:, :, L] = 0
+            a[:, :, L] = 0
+            assert torch.equal(a, b), f"{name}_cache changed outside row ctx_len"
+    return errs, used_C, out
+
+
+# ------------------------------------------------ the benchmark configurations
+
+
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_workload_default_plan(cfa, oracle, name):
+    errs, C, _ = run_and_check(cfa, oracle, workloads.WORKLOADS[name], seed=1)
+    print(f"{name}: C={C} out rel {errs['out'][0]:.2e} abs {errs['out'][1]:.2e}")
+
+
+# --------------------------------------------- every cluster size, ragged tails
+
+
+@pytest.mark.parametrize("C", [2, 4, 8, 16])
+@pytest.mark.parametrize("B", [1, 3])
+def test_cluster_sizes_head_dim_128(cfa, oracle, C, B):
+    # ctx 301: 301 = 7 * 43, ragged against every split and against 32-row tiles
+    wl = workloads.custom(B, 1024, 8, 128, 301, max_ctx=320)
+    run_and_check(cfa, oracle, wl, seed=2 + C, C=C)
+
+
+@pytest.mark.parametrize("C", [1, 2, 4, 8, 16])
+def test_cluster_sizes_head_dim_64(cfa, oracle, C):
+    wl = workloads.custom(2, 1024, 16, 64, 77, max_ctx=128)
+    run_and_check(cfa, oracle, wl, seed=3 + C, C=C)
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+@pytest.mark.parametrize("L", [0, 1, 3, 7, 63, 64, 65])
+def test_short_contexts(cfa, oracle, L):
+    """ctx_len = 0 (only the new token), ctx_len + 1 < cluster size (empty
+    splits), and tile boundaries."""
+    wl = workloads.custom(1, 512, 4, 128, L, max_ctx=96)
+    run_and_check(cfa, oracle, wl, seed=10 + L, C=8)
+
+
+def test_last_cache_row(cfa, oracle):
+    """ctx_len = max_ctx - 1 writes the final row of the cache."""
+    wl = workloads.custom(2, 512, 4, 128, 127, max_ctx=128)
+    run_and_check(cfa, oracle, wl, seed=20, C=4)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 5, 8, 9, 16])
+def test_batch_sizes(cfa, oracle, B):
+    wl = workloads.custom(B, 512, 4, 128, 150, max_ctx=192)
+    run_and_check(cfa, oracle, wl, seed=30 + B, C=4)
+
+
+@pytest.mark.parametrize("stages", [2, 3, 5])
+def test_shallow_pipelines(cfa, oracle, stages):
+    """Few stages force many ring wrap-arounds and phase changes mid-ring."""
+    wl = workloads.custom(2, 1024, 8, 128, 500, max_ctx=512)
+    run_and_check(cfa, oracle, wl, seed=40 + stages, C=4, stages=stages)
+
+
+def test_spiky_keys_long_tile_count(cfa, oracle):
+    wl = workloads.custom(1, 1024, 8, 128, 3000, max_ctx=3008, spiky_frac=0.05,
+                          spiky_scale=4.0)
+    run_and_check(cfa, oracle, wl, seed=50, C=2)
+
+
+# ------------------------------------------------------ determinism and reuse
+
+
+def test_deterministic_and_idempotent(cfa):
+    wl = workloads.WORKLOADS["llama7b_b1_ctx1k"]
+    t = workloads.make_inputs(wl, seed=5, device="cuda")
+    outs, caches = [], []
+    with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx) as plan:
+        for _ in range(3):
+            out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+            plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"],
+                             wl.ctx_len, out)
+            torch.cuda.synchronize()
+            outs.append(out.view(torch.int16).clone())
+            caches.append(t["k_cache"][:, :, wl.ctx_len].view(torch.int16).clone())
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    assert all(torch.equal(caches[0], c) for c in caches[1:])
+
+
+def test_cluster_size_does_not_change_result_beyond_rounding(cfa):
+    wl = workloads.custom(1, 2048, 16, 128, 700, max_ctx=768)
+    t = workloads.make_inputs(wl, seed=6, device="cuda")
+    res = {}
+    for C in (2, 4, 8, 16):
+        out = torch.empty(1, wl.hidden, dtype=torch.bfloat16, device="cuda")
+        with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx, cluster_size=C) as p:
+            p.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"],
+                          wl.ctx_len, out)
+        res[C] = out.float().cpu().numpy()
+    for C in (4, 8, 16):
+        assert rel_l2(res[C], res[2]) < 5e-3
+
+
+def test_host_entry_point_matches_device(cfa):
+    wl = workloads.custom(3, 1024, 8, 128, 200, max_ctx=256)
+    t = workloads.make_inputs(wl, seed=7, device="cuda")
+    out_dev = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    x_host = t["x"].cpu().pin_memory()
+    out_host = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16).pin_memory()
+    with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx) as plan:
+        plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"],
+                         wl.ctx_len, out_dev)
+        plan.decode_step_host(x_host, t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"],
+                              wl.ctx_len, out_host)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host.view(torch.int16), out_dev.cpu().view(torch.int16))
+
+
+# ------------------------------------------------------------- error handling
+
+
+def test_runtime_argument_errors(cfa):
+    wl = workloads.custom(1, 512, 4, 128, 10, max_ctx=64)
+    t = workloads.make_inputs(wl, seed=8, device="cuda")
+    out = torch.zeros(1, 512, dtype=torch.bfloat16, device="cuda")
+    with cfa.Plan(1, 512, 4, 128, 64) as plan:
+        h = plan.handle
+        args = [t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"]]
+        assert cfa.cfa_decode_step(h, *args, 64, out) == cfa.CFA_ERR_INVALID_ARG
+        assert cfa.cfa_decode_step(h, *args, -1, out) == cfa.CFA_ERR_INVALID_ARG
+        assert cfa.cfa_decode_step(h, t["x"].data_ptr() + 2, *args[1:], 10, out) == \
+            cfa.CFA_ERR_ALIGNMENT
+        assert cfa.cfa_decode_step(h, *args, 10, t["x"]) == cfa.CFA_ERR_INVALID_ARG  # aliasing
+        assert cfa.cfa_plan_set_cluster_size(h, 3) == cfa.CFA_ERR_UNSUPPORTED
+        assert cfa.cfa_plan_set_cluster_size(h, 1) == cfa.CFA_ERR_UNSUPPORTED  # d=128 needs >= 2
+        assert cfa.cfa_plan_set_stages(h, 1) == cfa.CFA_ERR_UNSUPPORTED
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(out) == 0  # nothing was launched
+        assert plan.status() == cfa.CFA_OK
+
+
+def test_bounded_wait_times_out_cleanly(cfa):
+    """A wait on a barrier nothing arrives on gives up and reports a status;
+    the context stays usable afterwards."""
+    assert cfa.cfa_selftest_wait_timeout(2000) == cfa.CFA_ERR_TIMEOUT
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum().item()) == 4.0
