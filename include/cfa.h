@@ -90,6 +90,13 @@ void cfa_plan_destroy(cfa_plan *plan);
  *   out     bf16 [B, hidden]               written
  * Re-running a step with the same ctx_len rewrites the same cache row with
  * the same value, so a step is idempotent.
+ * Launch overlap (on by default, see cfa_plan_set_overlap): the step is
+ * launched with programmatic stream serialization, so it may be scheduled
+ * while the previous kernel on the stream is still running. Before that
+ * kernel has finished it only initialises shared memory and prefetches
+ * weight tiles; x and the caches are read, and every buffer is written, only
+ * afterwards. The weights must therefore not be written by kernels still in
+ * flight on the stream.
  * Errors: CFA_ERR_INVALID_ARG (NULL pointer, ctx_len out of range),
  * CFA_ERR_ALIGNMENT, CFA_ERR_CUDA (launch failure). Faults raised while the
  * kernel runs surface at the next synchronizing call, as with any CUDA kernel.
@@ -126,6 +133,14 @@ cfa_status cfa_plan_set_cluster_size(cfa_plan *plan, int cluster_size);
  * on error.
  */
 cfa_status cfa_plan_set_stages(cfa_plan *plan, int stages);
+
+/*
+ * Enable (1, the default) or disable (0) launch overlap for the following
+ * steps. With overlap on, a step's prologue and first weight loads run under
+ * the tail of the previous kernel in the stream (see cfa_decode_step); with
+ * it off, the step starts only after that kernel has finished.
+ */
+cfa_status cfa_plan_set_overlap(cfa_plan *plan, int enable);
 
 /* Current cluster size of the plan, or -1 for NULL. */
 int cfa_plan_cluster_size(const cfa_plan *plan);

@@ -40,6 +40,8 @@ _lib.cfa_plan_set_cluster_size.restype = _i
 _lib.cfa_plan_set_cluster_size.argtypes = [_vp, _i]
 _lib.cfa_plan_set_stages.restype = _i
 _lib.cfa_plan_set_stages.argtypes = [_vp, _i]
+_lib.cfa_plan_set_overlap.restype = _i
+_lib.cfa_plan_set_overlap.argtypes = [_vp, _i]
 _lib.cfa_plan_cluster_size.restype = _i
 _lib.cfa_plan_cluster_size.argtypes = [_vp]
 _lib.cfa_plan_describe.restype = _i
@@ -62,7 +64,8 @@ CFA_ERR_ALIGNMENT = 5
 
 EXPORTED_SYMBOLS = (
     "cfa_plan_create", "cfa_plan_destroy", "cfa_decode_step", "cfa_decode_step_host",
-    "cfa_plan_set_cluster_size", "cfa_plan_set_stages", "cfa_plan_cluster_size",
+    "cfa_plan_set_cluster_size", "cfa_plan_set_stages", "cfa_plan_set_overlap",
+    "cfa_plan_cluster_size",
     "cfa_plan_describe", "cfa_plan_status", "cfa_last_error", "cfa_status_string",
     "cfa_selftest_wait_timeout",
 )
@@ -132,6 +135,10 @@ def cfa_plan_set_stages(plan, stages: int) -> int:
     return int(_lib.cfa_plan_set_stages(plan, int(stages)))
 
 
+def cfa_plan_set_overlap(plan, enable: bool) -> int:
+    return int(_lib.cfa_plan_set_overlap(plan, 1 if enable else 0))
+
+
 def cfa_plan_cluster_size(plan) -> int:
     return int(_lib.cfa_plan_cluster_size(plan))
 
@@ -159,7 +166,8 @@ class Plan:
     """Owns a cfa_plan; checks tensors and launches decode steps."""
 
     def __init__(self, B: int, hidden: int, n_heads: int, head_dim: int, max_ctx: int,
-                 cluster_size: Optional[int] = None, stages: Optional[int] = None):
+                 cluster_size: Optional[int] = None, stages: Optional[int] = None,
+                 overlap: Optional[bool] = None):
         self.B, self.hidden, self.n_heads, self.head_dim, self.max_ctx = (
             B, hidden, n_heads, head_dim, max_ctx)
         self.handle = cfa_plan_create(B, hidden, n_heads, head_dim, max_ctx)
@@ -168,6 +176,8 @@ class Plan:
                 self.set_cluster_size(cluster_size)
             if stages is not None:
                 self.set_stages(stages)
+            if overlap is not None:
+                self.set_overlap(overlap)
         except Exception:
             self.close()
             raise
@@ -202,6 +212,11 @@ class Plan:
         st = cfa_plan_set_stages(self.handle, n)
         if st != CFA_OK:
             raise CfaError(st, f"stages {n}")
+
+    def set_overlap(self, enable: bool) -> None:
+        st = cfa_plan_set_overlap(self.handle, enable)
+        if st != CFA_OK:
+            raise CfaError(st, "overlap")
 
     def describe(self) -> dict:
         return cfa_plan_describe(self.handle)

@@ -45,13 +45,14 @@ struct cfa_plan {
     int device = -1, num_sms = 0, smem_per_sm = 0, smem_optin = 0, smem_reserved = 0;
     int C = 0;
     int stages_override = 0;      // 0 = choose automatically
+    bool overlap = true;          // programmatic dependent launch
     KernelParams kp{};            // everything but the per-call pointers
     int smem_bytes = 0;
     int coresident_clusters = 0;
     const void *kernel = nullptr;
     // workspace
     float *partials = nullptr;    // [nh][B][H]
-    unsigned *words = nullptr;    // [0, kMaxCluster) counters, [kMaxCluster] status
+    unsigned *words = nullptr;    // [0, kMaxCluster) chunk counters, [kMaxCluster] status
     uint16_t *x_stage = nullptr;  // [B][H] for cfa_decode_step_host
     uint16_t *out_stage = nullptr;
     // cached tensor maps
@@ -120,13 +121,12 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     while (maxb < B) maxb <<= 1;
 
     const int xstage = B * TRA * 2;
-    const int nstate = cfa::kComputeWarps * (256 / D);
     const int qkv_recv = C * B * 3 * cfa::kTileCols * 4;
     const int sm_recv = C * B * (D + 4) * 4;
-    const int qkv_full = B * 3 * D * 4;
+    const int qkv_full = B * (3 * D + 1) * 4;
     const int attn = B * D * 4;
     const int scratch = std::max(cfa::kComputeWarps * B * cfa::kTileCols * 4,
-                                 (nstate * D + 2 * nstate) * 4);
+                                 (cfa::kComputeWarps * D + 2 * cfa::kComputeWarps) * 4);
     const int fixed = align_up(qkv_recv, 128) + align_up(sm_recv, 128) +
                       align_up(qkv_full, 128) + align_up(attn, 128) + align_up(scratch, 128) +
                       128 /* barriers and flags, per stage added below */;
@@ -159,7 +159,7 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.off_scratch = off;
     off = align_up(off + scratch, 128);
     k.off_bars = off;
-    off += (2 * NS + 2) * 8 + 16;
+    off += (2 * NS + 4) * 8 + 16;
     if (off > pl->smem_optin) return CFA_ERR_UNSUPPORTED;
 
     k.B = B;
@@ -376,6 +376,12 @@ cfa_status cfa_plan_set_stages(cfa_plan *pl, int stages) {
     return CFA_OK;
 }
 
+cfa_status cfa_plan_set_overlap(cfa_plan *pl, int enable) {
+    if (!pl) return fail(CFA_ERR_INVALID_ARG);
+    pl->overlap = enable != 0;
+    return CFA_OK;
+}
+
 int cfa_plan_cluster_size(const cfa_plan *pl) { return pl ? pl->C : -1; }
 
 cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
@@ -386,10 +392,11 @@ cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
                   "\"max_ctx\": %d, \"cluster_size\": %d, \"grid\": %d, \"block\": %d, "
                   "\"smem_bytes\": %d, \"stages\": %d, \"stage_bytes\": %d, "
                   "\"proj_rows_per_block\": %d, \"proj_tile_rows\": %d, "
-                  "\"out_cols_per_block\": %d, \"coresident_clusters\": %d, \"num_sms\": %d}",
+                  "\"out_cols_per_block\": %d, \"coresident_clusters\": %d, \"num_sms\": %d, "
+                  "\"overlap\": %d}",
                   pl->B, pl->H, pl->nh, pl->D, pl->max_ctx, pl->C, pl->nh * pl->C,
                   cfa::kThreads, pl->smem_bytes, k.nstages, cfa::kStageBytes, k.R, k.TRA,
-                  k.ncols, pl->coresident_clusters, pl->num_sms);
+                  k.ncols, pl->coresident_clusters, pl->num_sms, pl->overlap ? 1 : 0);
     return CFA_OK;
 }
 
@@ -438,9 +445,14 @@ cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const
     kp.status = pl->words + cfa::kMaxCluster;
     kp.ctx_len = ctx_len;
 
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
         launch_config(pl, kp, pl->smem_bytes, static_cast<cudaStream_t>(stream), attr);
+    if (pl->overlap) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     void *args[3] = {&pl->tm_wqkv, &pl->tm_wo, &kp};
     if (cudaLaunchKernelExC(&cfg, pl->kernel, args) != cudaSuccess) {
         cudaGetLastError();

@@ -37,10 +37,29 @@ __device__ __forceinline__ void cluster_sync_all() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split form of the same barrier: arrive early, wait later. Every thread must
+// wait before it arrives again.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Named barrier 1 over the first `nthreads` threads (the compute warps).
 template <int NTHREADS>
 __device__ __forceinline__ void compute_bar() {
     asm volatile("bar.sync 1, %0;" :: "n"(NTHREADS) : "memory");
+}
+
+// Programmatic dependent launch: wait until the previous kernel in the stream
+// has finished and its writes are visible (a no-op without a prerequisite
+// grid), and allow the next kernel to be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -150,6 +169,16 @@ __device__ __forceinline__ void push_16B(uint32_t remote_addr, float4 v, uint32_
         :: "r"(remote_addr), "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)),
            "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w)), "r"(remote_bar)
         : "memory");
+}
+
+// ------------------------------------------------------ global atomics
+
+// Fetch-and-add with acquire-release semantics at GPU scope.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *addr, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
 }
 
 // ---------------------------------------------------------------- bf16 bits

@@ -21,8 +21,9 @@ constexpr unsigned kStatusSiteShift = 8;  // site code of the first timeout
 enum WaitSite : unsigned {
     kSiteStageFull = 1,
     kSiteStageEmpty = 2,
-    kSiteQkvExchange = 3,
+    kSiteQExchange = 3,
     kSiteSoftmaxExchange = 4,
+    kSiteKvExchange = 5,
     kSiteSelftest = 15,
 };
 

@@ -16,28 +16,34 @@
 //  A  Deferred QKV projection [CF §3.2, §5.1]: the block owns one 64-column
 //     group g of head h's Q, K and V column blocks ("split head_dim") and one
 //     row group rg of the hidden dimension; it multiplies its rows of x by
-//     its weight tile into partial q/k/v sums.
+//     its weight tiles into partial q/k/v sums.
 //  X1 Cluster gather/reduce of q, k, v [CF §3.1.2]: every block pushes its
 //     partials into every other block's shared memory (st.async with
-//     transaction counting on the receiver's mbarrier). Each block then sums
-//     the row-group partials in rank order and concatenates the column
-//     groups, so all blocks hold identical q, k_new, v_new. k_new and v_new
-//     are rounded to bf16; rank 0 appends them to the caches.
+//     transaction counting on the receiver's mbarrier). The q partials leave
+//     as soon as the Q section is done, so the exchange overlaps the K and V
+//     sections; the k/v partials leave after the V section and their exchange
+//     overlaps attention. Each block sums the row-group partials in rank
+//     order and concatenates the column groups, so all blocks hold identical
+//     q, k_new, v_new. k_new and v_new are rounded to bf16; rank 0 appends
+//     them to the caches.
 //  B  Split-KV attention [CF §3.2]: the block owns cached positions
-//     [L*r/C, L*(r+1)/C); the last rank also owns the new token, attended
-//     from its on-chip copy. Each half- or quarter-warp keeps an online
-//     softmax state (m, l, o) in base-2 units; the states are merged per
-//     batch row at the end.
+//     [L*r/C, L*(r+1)/C). Each warp keeps an online-softmax state in base-2
+//     units with one running max for the whole warp (rescaled once per step,
+//     only when the max grows); the states are merged per batch row at the
+//     end.
 //  X2 ClusterReduce of the softmax statistics [CF §3.1.1, §3.2]: every block
-//     pushes (m_r, l_r, o_r) to every other; each block takes m = max m_r and
-//     sums the rescaled l_r and o_r in rank order, so all hold identical
-//     attn = o / l.
+//     pushes (m_r, l_r, o_r) to every other; each block takes the max over
+//     them and over the new token's score, then sums the rescaled l_r, o_r
+//     and the new token's (1, v_new) in a fixed order, so all blocks hold
+//     identical attn = o / l. The new token is thus one more split of the
+//     softmax, attended from its on-chip bf16-rounded copy.
 //  C  Output projection [CF §3.2]: the block owns H/C output columns and
 //     multiplies attn (head h's d rows of W_o) into fp32 partials, written to
 //     a per-head workspace row.
 //  D  Cross-head merge: instead of the page's atomicAdd merge [CF §3.2], the
-//     last block to finish a column chunk (a release/acquire counter) sums
-//     the n_heads partials in head order and writes bf16 out. Deterministic.
+//     last of the n_heads blocks to finish a column chunk (a release/acquire
+//     counter) sums the n_heads partials in head order and writes bf16 out.
+//     Deterministic.
 #pragma once
 
 #include <cuda.h>
@@ -48,19 +54,7 @@
 
 namespace cfa {
 
-__device__ __forceinline__ float dot8_bf16(const float (&q)[8], uint4 k) {
-    float s = q[0] * bf16_lo(k.x);
-    s = fmaf(q[1], bf16_hi(k.x), s);
-    s = fmaf(q[2], bf16_lo(k.y), s);
-    s = fmaf(q[3], bf16_hi(k.y), s);
-    s = fmaf(q[4], bf16_lo(k.z), s);
-    s = fmaf(q[5], bf16_hi(k.z), s);
-    s = fmaf(q[6], bf16_lo(k.w), s);
-    s = fmaf(q[7], bf16_hi(k.w), s);
-    return s;
-}
-
-__device__ __forceinline__ void unpack8_bf16(uint4 v, float (&f)[8]) {
+__device__ __forceinline__ void unpack8_bf16(uint4 v, float *f) {
     f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
     f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
     f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
@@ -73,19 +67,124 @@ __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
     return lo | (hi << 16);
 }
 
+// CPL consecutive bf16 weights from shared memory, widened to fp32.
+template <int CPL>
+__device__ __forceinline__ void load_weights(const uint8_t *p, float (&w)[CPL]) {
+    if constexpr (CPL == 8) {
+        unpack8_bf16(*reinterpret_cast<const uint4 *>(p), w);
+    } else if constexpr (CPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
+    } else {
+        const uint32_t v = *reinterpret_cast<const uint32_t *>(p);
+        w[0] = bf16_lo(v); w[1] = bf16_hi(v);
+    }
+}
+
+__device__ __forceinline__ float load_input(const uint16_t *p) { return bf16_bits(*p); }
+__device__ __forceinline__ float load_input(const float *p) { return *p; }
+
+// Position in the stage ring: stage index and the parity of the current pass.
+struct RingCursor {
+    int stage = 0;
+    uint32_t phase = 0;
+    bool wrapped = false;  // every stage has been filled at least once
+    __device__ __forceinline__ void advance(int ns) {
+        if (++stage == ns) {
+            stage = 0;
+            phase ^= 1u;
+            wrapped = true;
+        }
+    }
+};
+
+// Columns each lane owns in a 64-column weight tile: wide vectors for small
+// batches, narrow ones when the per-lane accumulators would not fit.
+template <int MAXB>
+struct GemvShape {
+    static constexpr int CPL = MAXB <= 2 ? 8 : (MAXB <= 4 ? 4 : 2);  // columns per lane
+    static constexpr int LPR = kTileCols / CPL;                      // lanes per tile row
+    static constexpr int RPI = 32 / LPR;                             // rows per warp access
+};
+
+// acc[b][c] += sum over this warp's rows of in[b][row] * W[row][cg*CPL + c].
+// Rows [warp*rpw, (warp+1)*rpw) of the tile belong to this warp; the lane
+// takes every RPI-th of them. The tile is [rows][64] bf16 (128-byte rows).
+template <int MAXB, typename InT>
+__device__ __forceinline__ void gemv_tile(const uint8_t *tile, int rpw, const InT *in,
+                                          int in_stride, int B, int warp, int lane,
+                                          float (&acc)[MAXB][GemvShape<MAXB>::CPL]) {
+    using S = GemvShape<MAXB>;
+    const int cg = lane % S::LPR, rq = lane / S::LPR;
+    const int r0 = warp * rpw;
+#pragma unroll 4
+    for (int j = rq; j < rpw; j += S::RPI) {
+        const int row = r0 + j;
+        float w[S::CPL];
+        load_weights<S::CPL>(tile + row * (kTileCols * 2) + cg * (S::CPL * 2), w);
+#pragma unroll
+        for (int b = 0; b < MAXB; ++b) {
+            if (b < B) {
+                const float xv = load_input(in + b * in_stride + row);
+#pragma unroll
+                for (int c = 0; c < S::CPL; ++c) acc[b][c] = fmaf(xv, w[c], acc[b][c]);
+            }
+        }
+    }
+}
+
+// Sums the per-lane partials of all compute warps into dst[b*dst_stride + c]
+// (c < 64) in a fixed order. Uses `scratch` ([8][B][64] floats) and two
+// compute-warp barriers.
+template <int MAXB>
+__device__ __forceinline__ void gemv_reduce(float (&acc)[MAXB][GemvShape<MAXB>::CPL], int B,
+                                            int warp, int lane, int tid, float *scratch,
+                                            float *dst, int dst_stride) {
+    using S = GemvShape<MAXB>;
+    const int cg = lane % S::LPR, rq = lane / S::LPR;
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) {
+#pragma unroll
+        for (int c = 0; c < S::CPL; ++c) {
+#pragma unroll
+            for (int off = S::LPR; off < 32; off <<= 1)
+                acc[b][c] += __shfl_xor_sync(0xffffffffu, acc[b][c], off);
+        }
+    }
+    if (rq == 0) {
+#pragma unroll
+        for (int b = 0; b < MAXB; ++b)
+            if (b < B) {
+#pragma unroll
+                for (int c = 0; c < S::CPL; ++c)
+                    scratch[(warp * B + b) * kTileCols + cg * S::CPL + c] = acc[b][c];
+            }
+    }
+    compute_bar<kComputeThreads>();
+    for (int idx = tid; idx < B * kTileCols; idx += kComputeThreads) {
+        const int b = idx / kTileCols, c = idx % kTileCols;
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) sum += scratch[(w * B + b) * kTileCols + c];
+        dst[b * dst_stride + c] = sum;
+    }
+    compute_bar<kComputeThreads>();
+}
+
 template <int D, int MAXB>
 __global__ void __launch_bounds__(kThreads, 2)
 fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     const __grid_constant__ CUtensorMap tm_wo,
                     const KernelParams p) {
     static_assert(D == 64 || D == 128, "head_dim must be 64 or 128");
-    constexpr int TK = kStageBytes / (4 * D);            // cache rows per K (or V) tile
-    constexpr int LPR = D / 8;                           // lanes per cache row (16 B each)
-    constexpr int RPW = 32 / LPR;                        // rows a warp covers per step
-    constexpr int NSTATE = kComputeWarps * RPW;          // online-softmax states per block
-    constexpr int KV_STEPS = TK / (kComputeWarps * RPW); // steps per warp per tile
-    constexpr int SMW = D + 4;                           // floats per softmax record
-    static_assert(KV_STEPS * kComputeWarps * RPW == TK, "tile rows must split evenly");
+    using GS = GemvShape<MAXB>;
+    constexpr int TK = kStageBytes / (4 * D);     // cache rows per K (or V) tile
+    constexpr int NV = D / 64;                    // 16-byte vectors per lane per cache row
+    constexpr int DPL = 8 * NV;                   // head dims per lane
+    constexpr int KV_RPS = 4;                     // cache rows per warp step (8 lanes each)
+    constexpr int KV_STEPS = TK / (kComputeWarps * KV_RPS);
+    constexpr int SMW = D + 4;                    // floats per softmax record
+    static_assert(KV_STEPS * kComputeWarps * KV_RPS == TK, "tile rows must split evenly");
 
     extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -102,9 +201,10 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
 
     const uint32_t bar_full0 = smem_addr(smem + p.off_bars);
     const uint32_t bar_empty0 = bar_full0 + 8u * NS;
-    const uint32_t bar_qkv = bar_full0 + 16u * NS;
-    const uint32_t bar_sm = bar_qkv + 8u;
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 16);
+    const uint32_t bar_q = bar_full0 + 16u * NS;   // q partials from every peer
+    const uint32_t bar_kv = bar_q + 8u;             // k/v partials from every peer
+    const uint32_t bar_sm = bar_q + 16u;            // softmax statistics from every peer
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 32);
     volatile int *timed_out = flags;      // set by the first wait that gives up
     volatile int *is_last = flags + 1;    // this block merges its column chunk
 
@@ -123,16 +223,24 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             mbar_init(bar_full0 + 8u * s, 1);
             mbar_init(bar_empty0 + 8u * s, kComputeWarps);
         }
-        mbar_init(bar_qkv, 1);
+        mbar_init(bar_q, 1);
+        mbar_init(bar_kv, 1);
         mbar_init(bar_sm, 1);
         *timed_out = 0;
         *is_last = 0;
         fence_mbar_init();
         // Each exchange barrier completes once every peer's bytes have landed.
-        mbar_arrive_expect_tx(bar_qkv, static_cast<uint32_t>((C - 1) * qkv_payload * 4));
+        mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>((C - 1) * B * kTileCols * 4));
+        mbar_arrive_expect_tx(bar_kv, static_cast<uint32_t>((C - 1) * B * 2 * kTileCols * 4));
         mbar_arrive_expect_tx(bar_sm, static_cast<uint32_t>((C - 1) * sm_payload * 4));
     }
-    cluster_sync_all();  // barriers initialised everywhere before any push
+    __syncthreads();
+    // The next kernel in the stream may be scheduled now; it waits for this
+    // one to finish before touching anything this one writes.
+    grid_dependents_launch();
+    // Announce this block's barriers to the cluster; the matching wait comes
+    // right before the first push, so loading starts without a cluster round trip.
+    cluster_arrive();
 
     if (warp == kComputeWarps) {
         // ------------------------------------------------------------ load warp
@@ -140,33 +248,50 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             const uint32_t ring = smem_addr(smem);
             const uint32_t xring = smem_addr(smem + p.off_xring);
             const int xstage = B * p.TRA * 2;
-            uint32_t it = 0;
-            auto acquire = [&](uint32_t i) -> int {
-                const int s = static_cast<int>(i % NS);
-                if (i >= static_cast<uint32_t>(NS))
-                    mbar_wait_bounded<false>(bar_empty0 + 8u * s, ((i / NS) - 1) & 1u,
+            RingCursor cur;
+            auto acquire = [&]() -> int {
+                if (cur.wrapped)
+                    mbar_wait_bounded<false>(bar_empty0 + 8u * cur.stage, cur.phase ^ 1u,
                                              p.timeout_ns, timed_out, p.status, kSiteStageEmpty);
-                return s;
+                return cur.stage;
             };
-            // A: weight tiles [TRA rows x 64 cols] of Q, K, V plus the matching x rows
-            for (int sec = 0; sec < 3; ++sec) {
-                for (int t = 0; t < p.nA; ++t, ++it) {
-                    const int s = acquire(it);
-                    const uint32_t full = bar_full0 + 8u * s;
-                    const int row = rg * p.R + t * p.TRA;
-                    mbar_arrive_expect_tx(full, p.TRA * kTileCols * 2 + xstage);
-                    tma_load_2d(ring + s * kStageBytes, &tm_wqkv,
-                                sec * H + h * D + g * kTileCols, row, full);
-                    for (int b = 0; b < B; ++b)
-                        bulk_load_1d(xring + s * xstage + b * p.TRA * 2,
-                                     p.x + static_cast<size_t>(b) * H + row, p.TRA * 2, full);
-                }
+            // A: weight tiles [TRA rows x 64 cols] of Q, K, V plus the matching x
+            // rows. Weights do not depend on earlier kernels in the stream, so
+            // the first ring of weight tiles is requested before waiting for
+            // them; x (an earlier kernel's output) only after.
+            const int n_a = 3 * p.nA;
+            const int n_pre = min(NS, n_a);
+            auto issue_w = [&](int i, int s) {
+                const int sec = i / p.nA, t = i % p.nA;
+                tma_load_2d(ring + s * kStageBytes, &tm_wqkv, sec * H + h * D + g * kTileCols,
+                            rg * p.R + t * p.TRA, bar_full0 + 8u * s);
+            };
+            auto issue_x = [&](int i, int s) {
+                const int row = rg * p.R + (i % p.nA) * p.TRA;
+                for (int b = 0; b < B; ++b)
+                    bulk_load_1d(xring + s * xstage + b * p.TRA * 2,
+                                 p.x + static_cast<size_t>(b) * H + row, p.TRA * 2,
+                                 bar_full0 + 8u * s);
+            };
+            for (int i = 0; i < n_pre; ++i) {
+                mbar_arrive_expect_tx(bar_full0 + 8u * i, p.TRA * kTileCols * 2 + xstage);
+                issue_w(i, i);
+            }
+            grid_dependency_wait();
+            for (int i = 0; i < n_pre; ++i) issue_x(i, i);
+            for (int i = 0; i < n_pre; ++i) cur.advance(NS);
+            for (int i = n_pre; i < n_a; ++i) {
+                const int s = acquire();
+                mbar_arrive_expect_tx(bar_full0 + 8u * s, p.TRA * kTileCols * 2 + xstage);
+                issue_w(i, s);
+                issue_x(i, s);
+                cur.advance(NS);
             }
             // B: contiguous runs of cached K and V rows
             for (int b = 0; b < B; ++b) {
                 const size_t base = (static_cast<size_t>(b) * p.nh + h) * p.max_ctx * D;
-                for (int t = 0; t < n_kv_tiles; ++t, ++it) {
-                    const int s = acquire(it);
+                for (int t = 0; t < n_kv_tiles; ++t) {
+                    const int s = acquire();
                     const uint32_t full = bar_full0 + 8u * s;
                     const int t0 = kv_s + t * TK;
                     const int n = min(TK, kv_e - t0);
@@ -176,199 +301,206 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                  bytes, full);
                     bulk_load_1d(ring + s * kStageBytes + TK * D * 2,
                                  p.v_cache + base + static_cast<size_t>(t0) * D, bytes, full);
+                    cur.advance(NS);
                 }
             }
             // C: W_o tiles [D rows x 64 cols] of this block's output columns
-            for (int ct = 0; ct < n_out_tiles; ++ct, ++it) {
-                const int s = acquire(it);
+            for (int ct = 0; ct < n_out_tiles; ++ct) {
+                const int s = acquire();
                 const uint32_t full = bar_full0 + 8u * s;
                 mbar_arrive_expect_tx(full, D * kTileCols * 2);
                 tma_load_2d(ring + s * kStageBytes, &tm_wo, col0 + ct * kTileCols, h * D, full);
+                cur.advance(NS);
             }
             // Drain: the block may not exit with its own copies still in flight.
-            const uint32_t issued = it;
-            for (int s = 0; s < NS && static_cast<uint32_t>(s) < issued; ++s) {
-                const uint32_t last = s + NS * ((issued - 1 - s) / NS);
+            // Stages before the cursor were last filled in the current pass,
+            // the others in the previous one (if the ring ever wrapped).
+            for (int s = 0; s < NS; ++s) {
+                if (s >= cur.stage && !cur.wrapped) break;
                 volatile int ignore = 0;
-                mbar_wait_bounded<false>(bar_full0 + 8u * s, (last / NS) & 1u, p.timeout_ns,
-                                         &ignore, p.status, kSiteStageFull);
+                mbar_wait_bounded<false>(bar_full0 + 8u * s, s < cur.stage ? cur.phase : cur.phase ^ 1u,
+                                         p.timeout_ns, &ignore, p.status, kSiteStageFull);
             }
+        } else {
+            grid_dependency_wait();
         }
         __syncwarp();
+        cluster_wait();
     } else {
         // --------------------------------------------------------- compute warps
         const uint8_t *ring = smem;
         const uint16_t *xring = reinterpret_cast<const uint16_t *>(smem + p.off_xring);
         float *qkv_recv = reinterpret_cast<float *>(smem + p.off_qkv_recv);  // [C][B][3][64]
         float *sm_recv = reinterpret_cast<float *>(smem + p.off_sm_recv);    // [C][B][SMW]
-        float *qkv_full = reinterpret_cast<float *>(smem + p.off_qkv_full);  // [B][3][D]
+        float *qkv_full = reinterpret_cast<float *>(smem + p.off_qkv_full);  // [B][3][D], then s_new [B]
         float *attn = reinterpret_cast<float *>(smem + p.off_attn);          // [B][D]
         float *scratch = reinterpret_cast<float *>(smem + p.off_scratch);
-        uint32_t it = 0;
-        auto wait_full = [&](uint32_t i) -> int {
-            const int s = static_cast<int>(i % NS);
-            mbar_wait_bounded<false>(bar_full0 + 8u * s, (i / NS) & 1u, p.timeout_ns, timed_out,
+        grid_dependency_wait();  // no dependent read or global write before this
+        RingCursor cur;
+        auto wait_full = [&]() -> int {
+            mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out,
                                      p.status, kSiteStageFull);
-            return s;
+            return cur.stage;
         };
         auto release = [&](int s) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty0 + 8u * s);
+            cur.advance(NS);
         };
 
-        // ---- A: partial QKV projection ----------------------------------
+        // ---- A: partial QKV projection; partials leave as soon as they exist --
         float *my_qkv = qkv_recv + static_cast<size_t>(r) * qkv_payload;
+        const uint32_t my_qkv_addr = smem_addr(my_qkv);
+        // Push sections [sec0, sec0 + nsec) of every batch row to every peer.
+        auto push_sections = [&](int sec0, int nsec, uint32_t bar) {
+            const int per_b = nsec * (kTileCols / 4);  // 16-byte chunks per batch row
+            const int chunks = B * per_b;
+            for (int idx = tid; idx < (C - 1) * chunks; idx += kComputeThreads) {
+                const int pi = idx / chunks, c = idx % chunks;
+                const int peer = pi < r ? pi : pi + 1;
+                const int off = ((c / per_b) * 3 + sec0) * kTileCols + 4 * (c % per_b);
+                const float4 v = *reinterpret_cast<const float4 *>(my_qkv + off);
+                push_16B(map_to_rank(my_qkv_addr + 4u * off, peer), v, map_to_rank(bar, peer));
+            }
+        };
         {
             const int xstage = B * p.TRA;
             const int rpw = p.TRA / kComputeWarps;
             for (int sec = 0; sec < 3; ++sec) {
-                float acc[MAXB][2];
-#pragma unroll
-                for (int b = 0; b < MAXB; ++b) acc[b][0] = acc[b][1] = 0.f;
-                for (int t = 0; t < p.nA; ++t, ++it) {
-                    const int s = wait_full(it);
-                    const uint32_t *W = reinterpret_cast<const uint32_t *>(ring + s * kStageBytes);
-                    const uint16_t *X = xring + s * xstage;
-                    const int r0 = warp * rpw;
-#pragma unroll 4
-                    for (int i = 0; i < rpw; ++i) {
-                        const int row = r0 + i;
-                        const uint32_t w2 = W[row * 32 + lane];
-                        const float w0 = bf16_lo(w2), w1 = bf16_hi(w2);
-#pragma unroll
-                        for (int b = 0; b < MAXB; ++b) {
-                            if (b < B) {
-                                const float xv = bf16_bits(X[b * p.TRA + row]);
-                                acc[b][0] = fmaf(xv, w0, acc[b][0]);
-                                acc[b][1] = fmaf(xv, w1, acc[b][1]);
-                            }
-                        }
-                    }
-                    release(s);
-                }
-                float2 *scr2 = reinterpret_cast<float2 *>(scratch);
+                float acc[MAXB][GS::CPL];
 #pragma unroll
                 for (int b = 0; b < MAXB; ++b)
-                    if (b < B) scr2[(warp * B + b) * 32 + lane] = make_float2(acc[b][0], acc[b][1]);
-                compute_bar<kComputeThreads>();
-                for (int idx = tid; idx < B * kTileCols; idx += kComputeThreads) {
-                    const int b = idx / kTileCols, c = idx % kTileCols;
-                    float sum = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kComputeWarps; ++w) sum += scratch[(w * B + b) * kTileCols + c];
-                    my_qkv[(b * 3 + sec) * kTileCols + c] = sum;
+                    for (int c = 0; c < GS::CPL; ++c) acc[b][c] = 0.f;
+                for (int t = 0; t < p.nA; ++t) {
+                    const int s = wait_full();
+                    gemv_tile<MAXB>(ring + s * kStageBytes, rpw, xring + s * xstage, p.TRA, B,
+                                    warp, lane, acc);
+                    release(s);
                 }
-                compute_bar<kComputeThreads>();
-            }
-        }
-
-        // ---- X1: gather q/k/v partials across the cluster ----------------
-        {
-            const int chunks = qkv_payload / 4;
-            const uint32_t my_addr = smem_addr(my_qkv);
-            for (int idx = tid; idx < (C - 1) * chunks; idx += kComputeThreads) {
-                const int pi = idx / chunks, c = idx % chunks;
-                const int peer = pi < r ? pi : pi + 1;
-                const float4 v = reinterpret_cast<const float4 *>(my_qkv)[c];
-                push_16B(map_to_rank(my_addr + 16u * c, peer), v, map_to_rank(bar_qkv, peer));
-            }
-            mbar_wait_bounded<true>(bar_qkv, 0, p.timeout_ns, timed_out, p.status,
-                                    kSiteQkvExchange);
-            for (int idx = tid; idx < B * 3 * D; idx += kComputeThreads) {
-                const int b = idx / (3 * D), rem = idx % (3 * D);
-                const int sec = rem / D, j = rem % D;
-                const int gg = j / kTileCols, c = j % kTileCols;
-                float sum = 0.f;
-                for (int q = 0; q < p.RG; ++q)
-                    sum += qkv_recv[static_cast<size_t>(q * p.G + gg) * qkv_payload +
-                                    (b * 3 + sec) * kTileCols + c];
+                gemv_reduce<MAXB>(acc, B, warp, lane, tid, scratch, my_qkv + sec * kTileCols,
+                                  3 * kTileCols);
                 if (sec == 0) {
-                    qkv_full[idx] = sum * p.qscale;
-                } else {
-                    const __nv_bfloat16 hb = __float2bfloat16_rn(sum);
-                    qkv_full[idx] = __bfloat162float(hb);
-                    if (r == 0) {
-                        uint16_t *cache = sec == 1 ? p.k_cache : p.v_cache;
-                        cache[((static_cast<size_t>(b) * p.nh + h) * p.max_ctx + L) * D + j] =
-                            __bfloat16_as_ushort(hb);
-                    }
+                    cluster_wait();  // every peer's barriers are initialised
+                    push_sections(0, 1, bar_q);  // the q exchange overlaps the K and V sections
                 }
             }
-            compute_bar<kComputeThreads>();
+            push_sections(1, 2, bar_kv);  // the k/v exchange overlaps attention
         }
 
-        // ---- B: split-KV attention with per-lane-group online softmax ----
+        // ---- X1 (q): sum the row-group partials, concatenate column groups --
+        mbar_wait_bounded<true>(bar_q, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
+        for (int idx = tid; idx < B * D; idx += kComputeThreads) {
+            const int b = idx / D, j = idx % D;
+            const int gg = j / kTileCols, c = j % kTileCols;
+            float sum = 0.f;
+            for (int q = 0; q < p.RG; ++q)
+                sum += qkv_recv[static_cast<size_t>(q * p.G + gg) * qkv_payload + (b * 3) * kTileCols + c];
+            qkv_full[b * 3 * D + j] = sum * p.qscale;
+        }
+        compute_bar<kComputeThreads>();
+
+        // ---- B: split-KV attention over cached rows, one state per warp -----
         float *my_sm = sm_recv + static_cast<size_t>(r) * sm_payload;
         {
-            const int sub = lane / LPR, li = lane % LPR;
-            float *st_o = scratch;                 // [NSTATE][D]
-            float *st_m = scratch + NSTATE * D;    // [NSTATE]
-            float *st_l = st_m + NSTATE;           // [NSTATE]
+            // lane = 8 * rq + li: cache row rq of each 4-row step; 16-byte
+            // vectors li and li + 8 of that row, i.e. dims [8li, 8li+8) and
+            // [64 + 8li, 64 + 8li + 8) (the second only when D = 128).
+            const int rq = lane >> 3, li = lane & 7;
+            float *st_o = scratch;                          // [8][D]
+            float *st_m = scratch + kComputeWarps * D;      // [8]
+            float *st_l = st_m + kComputeWarps;             // [8]
             for (int b = 0; b < B; ++b) {
                 const float *qb = qkv_full + static_cast<size_t>(b) * 3 * D;
-                float q8[8];
+                float q[DPL], o[DPL];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) q8[k] = qb[8 * li + k];
-                float m = -INFINITY, l = 0.f, o[8];
+                for (int v = 0; v < NV; ++v)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) o[k] = 0.f;
-                if (r == C - 1 && warp == 0) {
-                    // position L: the new token, from the on-chip bf16-rounded copy
-                    float sc = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) sc = fmaf(q8[k], qb[D + 8 * li + k], sc);
-#pragma unroll
-                    for (int off = LPR / 2; off > 0; off >>= 1)
-                        sc += __shfl_xor_sync(0xffffffffu, sc, off);
-                    if (sub == 0) {
-                        m = sc;
-                        l = 1.f;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) o[k] = qb[2 * D + 8 * li + k];
+                    for (int k = 0; k < 8; ++k) {
+                        q[8 * v + k] = qb[64 * v + 8 * li + k];
+                        o[8 * v + k] = 0.f;
                     }
-                }
-                for (int t = 0; t < n_kv_tiles; ++t, ++it) {
-                    const int s = wait_full(it);
+                float m = -INFINITY, l = 0.f;   // m is the same in every lane of the warp
+                for (int t = 0; t < n_kv_tiles; ++t) {
+                    const int s = wait_full();
                     const int nrows = min(TK, kv_e - kv_s - t * TK);
                     const uint4 *Kt = reinterpret_cast<const uint4 *>(ring + s * kStageBytes);
                     const uint4 *Vt = reinterpret_cast<const uint4 *>(ring + s * kStageBytes + TK * D * 2);
 #pragma unroll
                     for (int j = 0; j < KV_STEPS; ++j) {
-                        const int row = warp * (TK / kComputeWarps) + j * RPW + sub;
-                        float sc = dot8_bf16(q8, Kt[row * LPR + li]);
+                        const int row = (warp * KV_STEPS + j) * KV_RPS + rq;
+                        const bool valid = row < nrows;
+                        uint4 kr[NV];
 #pragma unroll
-                        for (int off = LPR / 2; off > 0; off >>= 1)
-                            sc += __shfl_xor_sync(0xffffffffu, sc, off);
-                        if (row < nrows) {
-                            const float mn = fmaxf(m, sc);
-                            const float cf = exp2f(m - mn);
-                            const float pw = exp2f(sc - mn);
-                            float v[8];
-                            unpack8_bf16(Vt[row * LPR + li], v);
-                            l = fmaf(l, cf, pw);
+                        for (int v = 0; v < NV; ++v) kr[v] = Kt[row * (D / 8) + 8 * v + li];
+                        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) o[k] = fmaf(pw, v[k], o[k] * cf);
-                            m = mn;
+                        for (int v = 0; v < NV; ++v) {
+                            float kf[8];
+                            unpack8_bf16(kr[v], kf);
+#pragma unroll
+                            for (int k = 0; k < 8; k += 2) {
+                                s0 = fmaf(q[8 * v + k], kf[k], s0);
+                                s1 = fmaf(q[8 * v + k + 1], kf[k + 1], s1);
+                            }
+                        }
+                        float sc = s0 + s1;
+                        sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+                        sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+                        sc += __shfl_xor_sync(0xffffffffu, sc, 4);
+                        sc = valid ? sc : -INFINITY;
+                        float tmax = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
+                        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+                        if (tmax > m) {  // warp-uniform: rescale only when the max grows
+                            const float cf = exp2f(m - tmax);
+                            l *= cf;
+#pragma unroll
+                            for (int k = 0; k < DPL; ++k) o[k] *= cf;
+                            m = tmax;
+                        }
+                        if (valid) {
+                            const float pw = exp2f(sc - m);
+                            l += pw;
+#pragma unroll
+                            for (int v = 0; v < NV; ++v) {
+                                float vf[8];
+                                unpack8_bf16(Vt[row * (D / 8) + 8 * v + li], vf);
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) o[8 * v + k] = fmaf(pw, vf[k], o[8 * v + k]);
+                            }
                         }
                     }
                     release(s);
                 }
-                // merge the block's NSTATE states for batch row b
-                const int sid = warp * RPW + sub;
+                // the warp's four row groups share m: add their l and o
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) st_o[sid * D + 8 * li + k] = o[k];
-                if (li == 0) {
-                    st_m[sid] = m;
-                    st_l[sid] = l;
+                for (int k = 0; k < DPL; ++k) {
+                    o[k] += __shfl_xor_sync(0xffffffffu, o[k], 8);
+                    o[k] += __shfl_xor_sync(0xffffffffu, o[k], 16);
+                }
+                if (rq == 0) {
+#pragma unroll
+                    for (int v = 0; v < NV; ++v)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) st_o[warp * D + 64 * v + 8 * li + k] = o[8 * v + k];
+                    if (li == 0) {
+                        st_m[warp] = m;
+                        st_l[warp] = l;
+                    }
                 }
                 compute_bar<kComputeThreads>();
+                // merge the 8 warp states of batch row b (fixed order)
                 for (int t = tid; t <= D; t += kComputeThreads) {
                     float M = -INFINITY;
-                    for (int q = 0; q < NSTATE; ++q) M = fmaxf(M, st_m[q]);
+#pragma unroll
+                    for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, st_m[w]);
                     float acc = 0.f;
-                    for (int q = 0; q < NSTATE; ++q) {
-                        const float f = st_m[q] == -INFINITY ? 0.f : exp2f(st_m[q] - M);
-                        acc = fmaf(t < D ? st_o[q * D + t] : st_l[q], f, acc);
+#pragma unroll
+                    for (int w = 0; w < kComputeWarps; ++w) {
+                        const float f = st_m[w] == -INFINITY ? 0.f : exp2f(st_m[w] - M);
+                        acc = fmaf(t < D ? st_o[w * D + t] : st_l[w], f, acc);
                     }
                     if (t < D) {
                         my_sm[b * SMW + 4 + t] = acc;
@@ -383,7 +515,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             }
         }
 
-        // ---- X2: ClusterReduce(max) then ClusterReduce(sum) ---------------
+        // ---- X2 push: this block's softmax statistics to every peer ---------
         {
             const int chunks = sm_payload / 4;
             const uint32_t my_addr = smem_addr(my_sm);
@@ -393,97 +525,109 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 const float4 v = reinterpret_cast<const float4 *>(my_sm)[c];
                 push_16B(map_to_rank(my_addr + 16u * c, peer), v, map_to_rank(bar_sm, peer));
             }
-            mbar_wait_bounded<true>(bar_sm, 0, p.timeout_ns, timed_out, p.status,
-                                    kSiteSoftmaxExchange);
-            for (int idx = tid; idx < B * D; idx += kComputeThreads) {
-                const int b = idx / D, t = idx % D;
-                float M = -INFINITY;
-                for (int q = 0; q < C; ++q)
-                    M = fmaxf(M, sm_recv[static_cast<size_t>(q) * sm_payload + b * SMW]);
-                float num = 0.f, den = 0.f;
-                for (int q = 0; q < C; ++q) {
-                    const float *rec = sm_recv + static_cast<size_t>(q) * sm_payload + b * SMW;
-                    const float f = rec[0] == -INFINITY ? 0.f : exp2f(rec[0] - M);
-                    num = fmaf(rec[4 + t], f, num);
-                    den = fmaf(rec[1], f, den);
-                }
-                attn[idx] = num / den;
-            }
-            compute_bar<kComputeThreads>();
         }
 
-        // ---- C: output projection of this block's column chunk ------------
+        // ---- X1 (k, v) while X2 is in flight: k_new, v_new, cache append and
+        //      the new token's score; the new token is one more split of the
+        //      softmax, attended from its on-chip bf16-rounded copy.
+        mbar_wait_bounded<true>(bar_kv, 0, p.timeout_ns, timed_out, p.status, kSiteKvExchange);
+        for (int idx = tid; idx < B * 2 * D; idx += kComputeThreads) {
+            const int b = idx / (2 * D), rem = idx % (2 * D);
+            const int sec = 1 + rem / D, j = rem % D;
+            const int gg = j / kTileCols, c = j % kTileCols;
+            float sum = 0.f;
+            for (int q = 0; q < p.RG; ++q)
+                sum += qkv_recv[static_cast<size_t>(q * p.G + gg) * qkv_payload +
+                                (b * 3 + sec) * kTileCols + c];
+            const __nv_bfloat16 hb = __float2bfloat16_rn(sum);
+            qkv_full[(b * 3 + sec) * D + j] = __bfloat162float(hb);
+            if (r == 0) {
+                uint16_t *cache = sec == 1 ? p.k_cache : p.v_cache;
+                cache[((static_cast<size_t>(b) * p.nh + h) * p.max_ctx + L) * D + j] =
+                    __bfloat16_as_ushort(hb);
+            }
+        }
+        compute_bar<kComputeThreads>();
+        float *s_new = qkv_full + static_cast<size_t>(B) * 3 * D;  // [B]
+        for (int b = warp; b < B; b += kComputeWarps) {
+            const float *qb = qkv_full + static_cast<size_t>(b) * 3 * D;
+            float sc = 0.f;
+            for (int j = lane; j < D; j += 32) sc = fmaf(qb[j], qb[D + j], sc);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+            if (lane == 0) s_new[b] = sc;
+        }
+        compute_bar<kComputeThreads>();
+
+        // ---- X2 combine: ClusterReduce(max) then ClusterReduce(sum) --------
+        mbar_wait_bounded<true>(bar_sm, 0, p.timeout_ns, timed_out, p.status, kSiteSoftmaxExchange);
+        for (int idx = tid; idx < B * D; idx += kComputeThreads) {
+            const int b = idx / D, t = idx % D;
+            float M = s_new[b];
+            for (int q = 0; q < C; ++q)
+                M = fmaxf(M, sm_recv[static_cast<size_t>(q) * sm_payload + b * SMW]);
+            const float fn = exp2f(s_new[b] - M);
+            float num = qkv_full[(b * 3 + 2) * D + t] * fn, den = fn;
+            for (int q = 0; q < C; ++q) {
+                const float *rec = sm_recv + static_cast<size_t>(q) * sm_payload + b * SMW;
+                const float f = rec[0] == -INFINITY ? 0.f : exp2f(rec[0] - M);
+                num = fmaf(rec[4 + t], f, num);
+                den = fmaf(rec[1], f, den);
+            }
+            attn[idx] = num / den;
+        }
+        compute_bar<kComputeThreads>();
+
+        // ---- C: output projection of this block's column chunk --------------
         {
-            constexpr int rpw = D / kComputeWarps;
-            float2 *scr2 = reinterpret_cast<float2 *>(scratch);
-            for (int ct = 0; ct < n_out_tiles; ++ct, ++it) {
-                const int s = wait_full(it);
-                const uint32_t *W = reinterpret_cast<const uint32_t *>(ring + s * kStageBytes);
-                float acc[MAXB][2];
-#pragma unroll
-                for (int b = 0; b < MAXB; ++b) acc[b][0] = acc[b][1] = 0.f;
-                const int r0 = warp * rpw;
-#pragma unroll 4
-                for (int i = 0; i < rpw; ++i) {
-                    const int row = r0 + i;
-                    const uint32_t w2 = W[row * 32 + lane];
-                    const float w0 = bf16_lo(w2), w1 = bf16_hi(w2);
-#pragma unroll
-                    for (int b = 0; b < MAXB; ++b) {
-                        if (b < B) {
-                            const float av = attn[b * D + row];
-                            acc[b][0] = fmaf(av, w0, acc[b][0]);
-                            acc[b][1] = fmaf(av, w1, acc[b][1]);
-                        }
-                    }
-                }
-                release(s);
+            const int rpw = D / kComputeWarps;
+            const size_t head_stride = static_cast<size_t>(B) * H;
+            for (int ct = 0; ct < n_out_tiles; ++ct) {
+                const int s = wait_full();
+                float acc[MAXB][GS::CPL];
 #pragma unroll
                 for (int b = 0; b < MAXB; ++b)
-                    if (b < B) scr2[(warp * B + b) * 32 + lane] = make_float2(acc[b][0], acc[b][1]);
-                compute_bar<kComputeThreads>();
-                for (int idx = tid; idx < B * kTileCols; idx += kComputeThreads) {
-                    const int b = idx / kTileCols, c = idx % kTileCols;
-                    float sum = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kComputeWarps; ++w) sum += scratch[(w * B + b) * kTileCols + c];
-                    p.partials[(static_cast<size_t>(h) * B + b) * H + col0 + ct * kTileCols + c] = sum;
-                }
-                compute_bar<kComputeThreads>();
+                    for (int c = 0; c < GS::CPL; ++c) acc[b][c] = 0.f;
+                gemv_tile<MAXB>(ring + s * kStageBytes, rpw, attn, D, B, warp, lane, acc);
+                release(s);
+                gemv_reduce<MAXB>(acc, B, warp, lane, tid, scratch,
+                                  p.partials + static_cast<size_t>(h) * head_stride + col0 +
+                                      ct * kTileCols,
+                                  H);
             }
-        }
 
-        // ---- D: deterministic cross-head merge ---------------------------
-        __threadfence();
-        compute_bar<kComputeThreads>();
-        if (tid == 0) {
-            const unsigned prev = atomicAdd(p.counters + r, 1u);
-            *is_last = (prev == static_cast<unsigned>(p.nh - 1)) ? 1 : 0;
-        }
-        compute_bar<kComputeThreads>();
-        if (*is_last) {
-            __threadfence();
-            const int n4 = p.ncols / 4;
-            for (int idx = tid; idx < B * n4; idx += kComputeThreads) {
-                const int b = idx / n4;
-                const int c = col0 + 4 * (idx % n4);
-                const float *src = p.partials + static_cast<size_t>(b) * H + c;
-                const size_t head_stride = static_cast<size_t>(B) * H;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int hh = 0; hh < p.nh; ++hh) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + hh * head_stride));
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
-                uint2 packed;
-                packed.x = pack2_bf16(acc.x, acc.y);
-                packed.y = pack2_bf16(acc.z, acc.w);
-                *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+            // ---- D: the last head to finish this chunk merges it ------------
+            // gemv_reduce ended with a barrier after this block's last partial
+            // store, so one thread's release covers the whole block's stores.
+            if (tid == 0) {
+                const unsigned prev = atomic_add_acq_rel_gpu(p.counters + r, 1u);
+                const bool last = prev == static_cast<unsigned>(p.nh - 1);
+                if (last) p.counters[r] = 0u;  // ready for the next launch
+                *is_last = last ? 1 : 0;
             }
-            if (tid == 0) p.counters[r] = 0u;  // ready for the next launch
+            compute_bar<kComputeThreads>();
+            if (*is_last) {
+                const int n4 = p.ncols / 4;
+                for (int idx = tid; idx < B * n4; idx += kComputeThreads) {
+                    const int b = idx / n4;
+                    const int c = col0 + 4 * (idx % n4);
+                    const float *src = p.partials + static_cast<size_t>(b) * H + c;
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 16
+                    for (int hh = 0; hh < p.nh; ++hh) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + hh * head_stride));
+                        sum.x += v.x;
+                        sum.y += v.y;
+                        sum.z += v.z;
+                        sum.w += v.w;
+                    }
+                    uint2 packed;
+                    packed.x = pack2_bf16(sum.x, sum.y);
+                    packed.y = pack2_bf16(sum.z, sum.w);
+                    *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+                }
+            }
         }
     }
     cluster_sync_all();  // no block leaves while a peer may still touch its shared memory

@@ -68,6 +68,7 @@ def test_null_plan_is_rejected(lib):
     assert lib._lib.cfa_decode_step_host(None, 16, 16, 16, 16, 16, 0, 16, None) == lib.CFA_ERR_INVALID_ARG
     assert lib._lib.cfa_plan_set_cluster_size(None, 2) == lib.CFA_ERR_INVALID_ARG
     assert lib._lib.cfa_plan_set_stages(None, 2) == lib.CFA_ERR_INVALID_ARG
+    assert lib._lib.cfa_plan_set_overlap(None, 1) == lib.CFA_ERR_INVALID_ARG
     assert lib._lib.cfa_plan_cluster_size(None) == -1
     assert lib._lib.cfa_plan_status(None) == lib.CFA_ERR_INVALID_ARG
     buf = ctypes.create_string_buffer(8)

@@ -215,3 +215,33 @@ def test_bounded_wait_times_out_cleanly(cfa):
     assert cfa.cfa_selftest_wait_timeout(2000) == cfa.CFA_ERR_TIMEOUT
     x = torch.ones(4, device="cuda")
     assert float(x.sum().item()) == 4.0
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_chained_steps_respect_dependencies(cfa, oracle, overlap):
+    """Decode chain on one stream: step t+1 takes step t's `out` as its x and
+    reads the cache row step t appended. With launch overlap on, each step may
+    start before the previous one ends, so this checks that nothing dependent
+    is read or written early. Every step is compared with the oracle on the
+    exact inputs it saw (x and the cache as left by the earlier steps)."""
+    wl = workloads.custom(2, 1024, 8, 128, 40, max_ctx=64)
+    t = workloads.make_inputs(wl, seed=60, device="cuda", poison_tail=True)
+    n_steps = 6
+    xs = [t["x"]]
+    outs = []
+    with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx, overlap=overlap) as plan:
+        for k in range(n_steps):
+            out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+            plan.decode_step(xs[-1], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"],
+                             wl.ctx_len + k, out)
+            outs.append(out)
+            xs.append(out)
+        torch.cuda.synchronize()
+        assert plan.status() == cfa.CFA_OK
+    W_qkv, W_o = t["W_qkv"].cpu(), t["W_o"].cpu()
+    kc, vc = t["k_cache"].cpu(), t["v_cache"].cpu()
+    for k in range(n_steps):
+        ref = oracle.decode_step(xs[k].cpu(), W_qkv, W_o, kc, vc, wl.ctx_len + k,
+                                 nthreads=NTHREADS)
+        check_close(f"out[{k}]", outs[k].float().cpu().numpy(), ref["out"])
+        check_close(f"k_new[{k}]", kc[:, :, wl.ctx_len + k].float().numpy(), ref["k_new"])
