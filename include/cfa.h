@@ -119,6 +119,38 @@ cfa_status cfa_decode_step_host(cfa_plan *plan, const void *x_host, const void *
                                 int ctx_len, void *out_host, void *stream);
 
 /*
+ * The same decode step for callers that cannot allocate device memory while
+ * they run: engines whose device memory is owned and budgeted by a host
+ * framework (plugins that receive only their input and output buffers), and
+ * serving loops that forbid cudaMalloc after start-up because it may
+ * synchronize the device and may fail under memory pressure. The paper has no
+ * counterpart to this entry point; it exists only for such callers.
+ *
+ * No plan is involved: the shape is passed directly, with the same meaning,
+ * limits and cluster-size choice as cfa_plan_create, and the arguments after
+ * it mean what they mean for cfa_decode_step. Nothing is allocated: the
+ * kernel's scratch (arrival counters, status word and the fp32 per-head
+ * output-projection partials) lives in one fixed array inside the library,
+ * 8 MiB + 256 bytes, which every GPU that loads the library keeps until the
+ * process exits. Shapes with n_heads * B * hidden > 2^21 do not fit and
+ * return CFA_ERR_UNSUPPORTED before anything is launched.
+ *
+ * The first call on a device sets the array up (looks up its device address
+ * and zeroes its counters, synchronizing that device once); make that first
+ * call before any stream capture. Every call then clears the counters with an
+ * asynchronous memset on `stream` and launches the kernel there, without
+ * launch overlap. All calls on a device share the one array, so calls whose
+ * kernels may run at the same time on that device (other streams, other host
+ * threads) race and must be serialized by the caller. Device-side wait
+ * timeouts are not reported by this entry point.
+ * Errors: as cfa_plan_create and cfa_decode_step.
+ */
+cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, int head_dim, int max_ctx,
+                                   const void *x, const void *W_qkv, const void *W_o,
+                                   void *k_cache, void *v_cache, int ctx_len, void *out,
+                                   void *stream);
+
+/*
  * Override the cluster size (thread blocks per head): 1, 2, 4, 8 or 16.
  * CFA_ERR_UNSUPPORTED if the shape does not split evenly at that size, the
  * device cannot co-schedule such a cluster, or its shared memory does not fit.

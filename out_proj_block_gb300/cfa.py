@@ -36,6 +36,8 @@ _lib.cfa_decode_step.restype = _i
 _lib.cfa_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp]
 _lib.cfa_decode_step_host.restype = _i
 _lib.cfa_decode_step_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp]
+_lib.cfa_decode_step_noalloc.restype = _i
+_lib.cfa_decode_step_noalloc.argtypes = [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp]
 _lib.cfa_plan_set_cluster_size.restype = _i
 _lib.cfa_plan_set_cluster_size.argtypes = [_vp, _i]
 _lib.cfa_plan_set_stages.restype = _i
@@ -64,6 +66,7 @@ CFA_ERR_ALIGNMENT = 5
 
 EXPORTED_SYMBOLS = (
     "cfa_plan_create", "cfa_plan_destroy", "cfa_decode_step", "cfa_decode_step_host",
+    "cfa_decode_step_noalloc",
     "cfa_plan_set_cluster_size", "cfa_plan_set_stages", "cfa_plan_set_overlap",
     "cfa_plan_cluster_size",
     "cfa_plan_describe", "cfa_plan_status", "cfa_last_error", "cfa_status_string",
@@ -125,6 +128,17 @@ def cfa_decode_step_host(plan, x_host, W_qkv, W_o, k_cache, v_cache, ctx_len: in
     return int(_lib.cfa_decode_step_host(plan, _ptr(x_host), _ptr(W_qkv), _ptr(W_o),
                                          _ptr(k_cache), _ptr(v_cache), int(ctx_len),
                                          _ptr(out_host), _stream(stream)))
+
+
+def cfa_decode_step_noalloc(B: int, hidden: int, n_heads: int, head_dim: int, max_ctx: int,
+                            x, W_qkv, W_o, k_cache, v_cache, ctx_len: int, out,
+                            stream=None) -> int:
+    """The decode step for callers that cannot allocate device memory (see
+    include/cfa.h); its scratch is a fixed array inside the library."""
+    return int(_lib.cfa_decode_step_noalloc(B, hidden, n_heads, head_dim, max_ctx, _ptr(x),
+                                            _ptr(W_qkv), _ptr(W_o), _ptr(k_cache),
+                                            _ptr(v_cache), int(ctx_len), _ptr(out),
+                                            _stream(stream)))
 
 
 def cfa_plan_set_cluster_size(plan, C: int) -> int:

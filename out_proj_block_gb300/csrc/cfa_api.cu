@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "cfa.h"
@@ -522,3 +523,145 @@ cfa_status cfa_selftest_wait_timeout(int limit_us, void *stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode step without any device allocation.
+//
+// Some callers cannot allocate device memory once they are running: engines
+// whose device memory is owned and budgeted by a host framework (plugins that
+// are handed only their input and output buffers), and serving loops that
+// forbid cudaMalloc after start-up because it can synchronize the device and
+// can fail under memory pressure. For them, cfa_decode_step_noalloc runs the
+// same fused kernel as cfa_decode_step but keeps its scratch (the per-column
+// arrival counters, the status word and the fp32 per-head output-projection
+// partials) in the file-scope array below, which every GPU that loads this
+// library holds until the process exits.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr size_t kNoallocWordsBytes = 256;                  // counters + status word
+constexpr size_t kNoallocPartialFloats = size_t(1) << 21;   // n_heads * B * hidden limit
+constexpr size_t kNoallocBytes = kNoallocWordsBytes + kNoallocPartialFloats * sizeof(float);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+constexpr int kNoallocMaxDevices = 64;
+std::once_flag g_noalloc_once[kNoallocMaxDevices];
+unsigned char *g_noalloc_ptr[kNoallocMaxDevices] = {};
+cudaError_t g_noalloc_setup_err[kNoallocMaxDevices] = {};
+
+// Once per device, with that device current: the array's device address (the
+// host-side name is only a stand-in) and a zeroed counter/status region.
+void noalloc_setup(int dev) {
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e == cudaSuccess) e = cudaMemset(ptr, 0, kNoallocWordsBytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        ptr = nullptr;
+    }
+    g_noalloc_ptr[dev] = static_cast<unsigned char *>(ptr);
+    g_noalloc_setup_err[dev] = e;
+}
+
+}  // namespace
+
+extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, int head_dim,
+                                              int max_ctx, const void *x, const void *W_qkv,
+                                              const void *W_o, void *k_cache, void *v_cache,
+                                              int ctx_len, void *out, void *stream) {
+    if (B < 1 || hidden < 1 || n_heads < 1 || head_dim < 1 || max_ctx < 1 ||
+        static_cast<long long>(n_heads) * head_dim != hidden)
+        return fail(CFA_ERR_INVALID_ARG);
+    if ((head_dim != 64 && head_dim != 128) || B > 16 || hidden % 64 != 0 ||
+        max_ctx > (1 << 22) || hidden > (1 << 16))
+        return fail(CFA_ERR_UNSUPPORTED);
+    if (static_cast<size_t>(n_heads) * B * hidden > kNoallocPartialFloats)
+        return fail(CFA_ERR_UNSUPPORTED);  // scratch array too small for this shape
+    if (!x || !W_qkv || !W_o || !k_cache || !v_cache || !out) return fail(CFA_ERR_INVALID_ARG);
+    if (ctx_len < 0 || ctx_len >= max_ctx) return fail(CFA_ERR_INVALID_ARG);
+    if (!aligned16(x) || !aligned16(W_qkv) || !aligned16(W_o) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || !aligned16(out))
+        return fail(CFA_ERR_ALIGNMENT);
+    const size_t H = static_cast<size_t>(hidden);
+    const size_t act = 2 * H * B;
+    const size_t cache = 2 * static_cast<size_t>(B) * n_heads * max_ctx * head_dim;
+    if (overlaps(out, act, x, act) || overlaps(out, act, W_qkv, 2 * H * 3 * H) ||
+        overlaps(out, act, W_o, 2 * H * H) || overlaps(out, act, k_cache, cache) ||
+        overlaps(out, act, v_cache, cache))
+        return fail(CFA_ERR_INVALID_ARG);
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoallocMaxDevices) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    std::call_once(g_noalloc_once[dev], noalloc_setup, dev);
+    if (g_noalloc_setup_err[dev] != cudaSuccess || !g_noalloc_ptr[dev]) return fail(CFA_ERR_CUDA);
+
+    // A plan object on the stack: same device queries, cluster-size choice and
+    // shared-memory layout as cfa_plan_create, with no workspace behind it.
+    cfa_plan pl;
+    pl.B = B;
+    pl.H = hidden;
+    pl.nh = n_heads;
+    pl.D = head_dim;
+    pl.max_ctx = max_ctx;
+    pl.device = dev;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pl.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                               dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&pl.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&pl.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    if (major != 10 || minor != 3) return fail(CFA_ERR_UNSUPPORTED);
+    const int candidates[5] = {1, 2, 4, 8, 16};
+    bool ok = false;
+    for (int C : candidates)
+        if (n_heads * C >= pl.num_sms && configure(&pl, C, 0) == CFA_OK) {
+            ok = true;
+            break;
+        }
+    for (int i = 4; i >= 0 && !ok; --i) ok = configure(&pl, candidates[i], 0) == CFA_OK;
+    if (!ok) return fail(CFA_ERR_UNSUPPORTED);
+
+    CUtensorMap tm_wqkv, tm_wo;
+    if (encode_2d(&tm_wqkv, W_qkv, 3 * H, H, cfa::kTileCols, static_cast<uint32_t>(pl.kp.TRA)) !=
+            CFA_OK ||
+        encode_2d(&tm_wo, W_o, H, H, cfa::kTileCols, static_cast<uint32_t>(head_dim)) != CFA_OK)
+        return fail(CFA_ERR_CUDA);
+
+    unsigned char *scratch = g_noalloc_ptr[dev];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Counters must start at zero; the previous call may have been cut short.
+    if (cudaMemsetAsync(scratch, 0, kNoallocWordsBytes, s) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    KernelParams kp = pl.kp;
+    kp.x = static_cast<const uint16_t *>(x);
+    kp.k_cache = static_cast<uint16_t *>(k_cache);
+    kp.v_cache = static_cast<uint16_t *>(v_cache);
+    kp.out = static_cast<uint16_t *>(out);
+    kp.counters = reinterpret_cast<unsigned *>(scratch);
+    kp.status = reinterpret_cast<unsigned *>(scratch) + cfa::kMaxCluster;
+    kp.partials = reinterpret_cast<float *>(scratch + kNoallocWordsBytes);
+    kp.ctx_len = ctx_len;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config(&pl, kp, pl.smem_bytes, s, attr);
+    void *args[3] = {&tm_wqkv, &tm_wo, &kp};
+    if (cudaLaunchKernelExC(&cfg, pl.kernel, args) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    return CFA_OK;
+}
