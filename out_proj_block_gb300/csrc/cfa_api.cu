@@ -59,9 +59,12 @@ struct cfa_plan {
     // cached tensor maps
     CUtensorMap tm_wqkv;  // 64-byte aligned by its own declaration
     CUtensorMap tm_wo;
+    CUtensorMap tm_x;
     const void *tm_wqkv_src = nullptr;
+    const void *tm_x_src = nullptr;
     const void *tm_wo_src = nullptr;
     int tm_wqkv_rows = 0;
+    bool tm_mma = false;
 };
 
 namespace {
@@ -83,7 +86,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Row-major bf16 matrix [rows][cols]; boxes of box_rows x box_cols elements.
 cfa_status encode_2d(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t rows,
-                     uint32_t box_cols, uint32_t box_rows) {
+                     uint32_t box_cols, uint32_t box_rows, bool swizzle128 = false) {
     auto fn = tensor_map_encoder();
     if (!fn) return CFA_ERR_CUDA;
     cuuint64_t gdim[2] = {cols, rows};
@@ -92,9 +95,24 @@ cfa_status encode_2d(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t 
     cuuint32_t estride[2] = {1, 1};
     CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), gdim,
                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? CFA_OK : CFA_ERR_CUDA;
+}
+
+// Tensor maps of one launch. The tensor-core path (kp.n_qk > 0) reads
+// 128-byte-swizzled [64-row x 64-col] weight boxes and [16 x 64] x boxes;
+// the CUDA-core path reads plain [TRA x 64] boxes and needs no x map.
+cfa_status encode_w_qkv(CUtensorMap *tm, const void *W_qkv, int H, const KernelParams &kp) {
+    const bool mma = kp.n_qk > 0;
+    return encode_2d(tm, W_qkv, 3ull * H, H, cfa::kTileCols, static_cast<uint32_t>(kp.TRA), mma);
+}
+cfa_status encode_w_o(CUtensorMap *tm, const void *W_o, int H, int D, const KernelParams &kp) {
+    return encode_2d(tm, W_o, H, H, cfa::kTileCols, static_cast<uint32_t>(D), kp.n_qk > 0);
+}
+cfa_status encode_x(CUtensorMap *tm, const void *x, int B, int H) {
+    return encode_2d(tm, x, H, B, cfa::kTileCols, cfa::kMmaN, true);
 }
 
 const void *kernel_for(int D, int maxb) {
@@ -120,17 +138,25 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     if (ncols % cfa::kTileCols) return CFA_ERR_UNSUPPORTED;
     int maxb = 1;
     while (maxb < B) maxb <<= 1;
+    // B >= 3 runs the projections on the tensor cores: 64-row [Q|K] stages and
+    // 128-row V stages, x staged by TMA as [16 x 64] swizzled boxes.
+    const bool mma = maxb >= 4;
+    if (mma) {
+        if (R % 128) return CFA_ERR_UNSUPPORTED;
+        TRA = 64;
+    }
 
-    const int xstage = B * TRA * 2;
+    const int xstage = mma ? cfa::kXStageMmaBytes : B * TRA * 2;
+    const int attn_t = mma ? 2 * (D / 64) * cfa::kMmaN * 128 : 0;
     const int qkv_recv = C * B * 3 * cfa::kTileCols * 4;
     const int sm_recv = C * B * (D + 4) * 4;
     const int qkv_full = B * (3 * D + 1) * 4;
     const int attn = B * D * 4;
-    const int scratch = std::max(cfa::kComputeWarps * B * cfa::kTileCols * 4,
+    const int scratch = std::max(mma ? 0 : cfa::kComputeWarps * B * cfa::kTileCols * 4,
                                  (cfa::kComputeWarps * D + 2 * cfa::kComputeWarps) * 4);
     const int fixed = align_up(qkv_recv, 128) + align_up(sm_recv, 128) +
-                      align_up(qkv_full, 128) + align_up(attn, 128) + align_up(scratch, 128) +
-                      128 /* barriers and flags, per stage added below */;
+                      align_up(qkv_full, 128) + align_up(attn, 128) + align_up(attn_t, 1024) +
+                      align_up(scratch, 128) + 1024 /* alignment slack, barriers, flags */;
     const int per_stage = cfa::kStageBytes + xstage + 16;
 
     const int grid = pl->nh * C;
@@ -148,7 +174,9 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     int off = NS * cfa::kStageBytes;
     KernelParams k{};
     k.off_xring = off;
-    off = align_up(off + NS * xstage, 128);
+    off = align_up(off + NS * xstage, 1024);
+    k.off_attn_t = off;
+    off = align_up(off + attn_t, 128);
     k.off_qkv_recv = off;
     off = align_up(off + qkv_recv, 128);
     k.off_sm_recv = off;
@@ -160,7 +188,7 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.off_scratch = off;
     off = align_up(off + scratch, 128);
     k.off_bars = off;
-    off += (2 * NS + 4) * 8 + 16;
+    off += (2 * NS + 6) * 8 + 48;
     if (off > pl->smem_optin) return CFA_ERR_UNSUPPORTED;
 
     k.B = B;
@@ -173,6 +201,8 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.R = R;
     k.TRA = TRA;
     k.nA = R / TRA;
+    k.n_qk = mma ? R / 64 : 0;
+    k.n_v = mma ? R / 128 : 0;
     k.ncols = ncols;
     k.nstages = NS;
     k.timeout_ns = kDefaultTimeoutNs;
@@ -227,7 +257,9 @@ cfa_status configure(cfa_plan *pl, int C, int stages_override) {
     pl->smem_bytes = smem;
     pl->kernel = kernel;
     pl->coresident_clusters = clusters;
-    pl->tm_wqkv_src = nullptr;  // the projection box height may have changed
+    pl->tm_wqkv_src = nullptr;  // box shapes may have changed
+    pl->tm_wo_src = nullptr;
+    pl->tm_x_src = nullptr;
     return CFA_OK;
 }
 
@@ -418,23 +450,32 @@ cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const
         overlaps(out, act, v_cache, cache))
         return fail(CFA_ERR_INVALID_ARG);
 
-    if (pl->tm_wqkv_src != W_qkv || pl->tm_wqkv_rows != pl->kp.TRA) {
-        if (encode_2d(&pl->tm_wqkv, W_qkv, 3 * H, H, cfa::kTileCols,
-                      static_cast<uint32_t>(pl->kp.TRA)) != CFA_OK) {
+    const bool mma = pl->kp.n_qk > 0;
+    if (pl->tm_wqkv_src != W_qkv || pl->tm_wqkv_rows != pl->kp.TRA || pl->tm_mma != mma) {
+        if (encode_w_qkv(&pl->tm_wqkv, W_qkv, pl->H, pl->kp) != CFA_OK) {
             pl->tm_wqkv_src = nullptr;
             return fail(CFA_ERR_CUDA);
         }
         pl->tm_wqkv_src = W_qkv;
         pl->tm_wqkv_rows = pl->kp.TRA;
+        pl->tm_wo_src = nullptr;
+        pl->tm_mma = mma;
     }
     if (pl->tm_wo_src != W_o) {
-        if (encode_2d(&pl->tm_wo, W_o, H, H, cfa::kTileCols, static_cast<uint32_t>(pl->D)) !=
-            CFA_OK) {
+        if (encode_w_o(&pl->tm_wo, W_o, pl->H, pl->D, pl->kp) != CFA_OK) {
             pl->tm_wo_src = nullptr;
             return fail(CFA_ERR_CUDA);
         }
         pl->tm_wo_src = W_o;
     }
+    if (mma && pl->tm_x_src != x) {
+        if (encode_x(&pl->tm_x, x, pl->B, pl->H) != CFA_OK) {
+            pl->tm_x_src = nullptr;
+            return fail(CFA_ERR_CUDA);
+        }
+        pl->tm_x_src = x;
+    }
+    if (!mma) pl->tm_x = pl->tm_wqkv;  // unused by the CUDA-core path
 
     KernelParams kp = pl->kp;
     kp.x = static_cast<const uint16_t *>(x);
@@ -454,7 +495,7 @@ cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 2;
     }
-    void *args[3] = {&pl->tm_wqkv, &pl->tm_wo, &kp};
+    void *args[4] = {&pl->tm_wqkv, &pl->tm_wo, &pl->tm_x, &kp};
     if (cudaLaunchKernelExC(&cfg, pl->kernel, args) != cudaSuccess) {
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);
@@ -634,11 +675,15 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     for (int i = 4; i >= 0 && !ok; --i) ok = configure(&pl, candidates[i], 0) == CFA_OK;
     if (!ok) return fail(CFA_ERR_UNSUPPORTED);
 
-    CUtensorMap tm_wqkv, tm_wo;
-    if (encode_2d(&tm_wqkv, W_qkv, 3 * H, H, cfa::kTileCols, static_cast<uint32_t>(pl.kp.TRA)) !=
-            CFA_OK ||
-        encode_2d(&tm_wo, W_o, H, H, cfa::kTileCols, static_cast<uint32_t>(head_dim)) != CFA_OK)
+    CUtensorMap tm_wqkv, tm_wo, tm_x;
+    if (encode_w_qkv(&tm_wqkv, W_qkv, hidden, pl.kp) != CFA_OK ||
+        encode_w_o(&tm_wo, W_o, hidden, head_dim, pl.kp) != CFA_OK)
         return fail(CFA_ERR_CUDA);
+    if (pl.kp.n_qk > 0) {
+        if (encode_x(&tm_x, x, B, hidden) != CFA_OK) return fail(CFA_ERR_CUDA);
+    } else {
+        tm_x = tm_wqkv;  // unused by the CUDA-core path
+    }
 
     unsigned char *scratch = g_noalloc_ptr[dev];
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -658,7 +703,7 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     kp.ctx_len = ctx_len;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config(&pl, kp, pl.smem_bytes, s, attr);
-    void *args[3] = {&tm_wqkv, &tm_wo, &kp};
+    void *args[4] = {&tm_wqkv, &tm_wo, &tm_x, &kp};
     if (cudaLaunchKernelExC(&cfg, pl.kernel, args) != cudaSuccess) {
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);

@@ -12,6 +12,8 @@ constexpr int kThreads = kComputeThreads + 32;     // + one load-issuing warp
 constexpr int kStageBytes = 16384;                 // one pipeline stage
 constexpr int kTileCols = 64;                      // weight tile width (128 bytes of bf16)
 constexpr int kMaxCluster = 16;
+constexpr int kMmaN = 16;                          // batch rows per tensor-core MMA (zero-padded)
+constexpr int kXStageMmaBytes = 2 * kMmaN * 128;   // x per stage on the tensor-core path
 
 // Status word bits, written by kernels and read by cfa_plan_status.
 constexpr unsigned kStatusTimeoutBit = 1u;
@@ -41,10 +43,12 @@ struct KernelParams {
     int RG;                // row groups of the hidden dimension: C / G
     int R;                 // hidden rows per block in the projection: H / RG
     int TRA;               // rows per projection tile
-    int nA;                // projection tiles per Q/K/V block: R / TRA
+    int nA;                // projection tiles per Q/K/V block: R / TRA (CUDA-core path)
+    int n_qk, n_v;         // tensor-core path: 64-row [Q|K] stages and 128-row V stages
     int ncols;             // output columns per block in the out-projection: H / C
     int nstages;           // pipeline depth
-    int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_scratch, off_bars;
+    int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_attn_t, off_scratch,
+        off_bars;
     unsigned long long timeout_ns;
     float qscale;          // log2(e) / sqrt(D)
 };

@@ -171,12 +171,23 @@ __device__ __forceinline__ void gemv_reduce(float (&acc)[MAXB][GemvShape<MAXB>::
     compute_bar<kComputeThreads>();
 }
 
+
+// Geometry of the tensor-core projection path (batches of 3..16 rows).
+constexpr int kXStageMma = kXStageMmaBytes;      // x bytes per stage: two [16 x 64] swizzled boxes
+constexpr uint32_t kAccQK = 0;                   // TMEM columns of the [Q|K] accumulator
+constexpr uint32_t kAccV = kMmaN;                // TMEM columns of the V accumulator
+constexpr uint32_t kTmemCols = 32;
+
 template <int D, int MAXB>
 __global__ void __launch_bounds__(kThreads, 2)
 fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     const __grid_constant__ CUtensorMap tm_wo,
+                    const __grid_constant__ CUtensorMap tm_x,
                     const KernelParams p) {
     static_assert(D == 64 || D == 128, "head_dim must be 64 or 128");
+    // B >= 3: the projections are dense [64 x K] . [K x B] contractions and run
+    // on the tensor cores (tcgen05, accumulators in TMEM); B <= 2: CUDA cores.
+    constexpr bool MMA = MAXB >= 4;
     using GS = GemvShape<MAXB>;
     constexpr int TK = kStageBytes / (4 * D);     // cache rows per K (or V) tile
     constexpr int NV = D / 64;                    // 16-byte vectors per lane per cache row
@@ -201,12 +212,15 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
 
     const uint32_t bar_full0 = smem_addr(smem + p.off_bars);
     const uint32_t bar_empty0 = bar_full0 + 8u * NS;
-    const uint32_t bar_q = bar_full0 + 16u * NS;   // q partials from every peer
-    const uint32_t bar_kv = bar_q + 8u;             // k/v partials from every peer
-    const uint32_t bar_sm = bar_q + 16u;            // softmax statistics from every peer
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 32);
+    const uint32_t bar_qk = bar_full0 + 16u * NS;   // q and k partials from every peer
+    const uint32_t bar_v = bar_qk + 8u;             // v partials from every peer
+    const uint32_t bar_sm = bar_qk + 16u;           // softmax statistics from every peer
+    const uint32_t bar_acc_a = bar_qk + 24u;        // projection accumulators ready (MMA path)
+    const uint32_t bar_acc_c = bar_qk + 32u;        // two out-projection accumulators (MMA path)
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 48);
     volatile int *timed_out = flags;      // set by the first wait that gives up
     volatile int *is_last = flags + 1;    // this block merges its column chunk
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 16 * NS + 56);
 
     const int g = r % p.G;                // column group in the projection
     const int rg = r / p.G;               // row group in the projection
@@ -223,16 +237,23 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             mbar_init(bar_full0 + 8u * s, 1);
             mbar_init(bar_empty0 + 8u * s, kComputeWarps);
         }
-        mbar_init(bar_q, 1);
-        mbar_init(bar_kv, 1);
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_v, 1);
         mbar_init(bar_sm, 1);
+        mbar_init(bar_acc_a, 1);
+        mbar_init(bar_acc_c, 1);
+        mbar_init(bar_acc_c + 8u, 1);
         *timed_out = 0;
         *is_last = 0;
         fence_mbar_init();
         // Each exchange barrier completes once every peer's bytes have landed.
-        mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>((C - 1) * B * kTileCols * 4));
-        mbar_arrive_expect_tx(bar_kv, static_cast<uint32_t>((C - 1) * B * 2 * kTileCols * 4));
+        mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>((C - 1) * B * 2 * kTileCols * 4));
+        mbar_arrive_expect_tx(bar_v, static_cast<uint32_t>((C - 1) * B * kTileCols * 4));
         mbar_arrive_expect_tx(bar_sm, static_cast<uint32_t>((C - 1) * sm_payload * 4));
+    }
+    if constexpr (MMA) {
+        if (warp == 0) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tcgen05_fence_before();
     }
     __syncthreads();
     // The next kernel in the stream may be scheduled now; it waits for this
@@ -242,12 +263,16 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     // right before the first push, so loading starts without a cluster round trip.
     cluster_arrive();
 
+    // Projection work items: CUDA-core path, 3 sections x nA tiles of [TRA x 64];
+    // MMA path, n_qk stages of 64 rows of [Q | K] then n_v stages of 128 rows of V.
+    const int n_a = MMA ? p.n_qk + p.n_v : 3 * p.nA;
+
     if (warp == kComputeWarps) {
         // ------------------------------------------------------------ load warp
         if (lane == 0) {
             const uint32_t ring = smem_addr(smem);
             const uint32_t xring = smem_addr(smem + p.off_xring);
-            const int xstage = B * p.TRA * 2;
+            const int xstage = MMA ? kXStageMma : B * p.TRA * 2;
             RingCursor cur;
             auto acquire = [&]() -> int {
                 if (cur.wrapped)
@@ -255,26 +280,53 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                              p.timeout_ns, timed_out, p.status, kSiteStageEmpty);
                 return cur.stage;
             };
-            // A: weight tiles [TRA rows x 64 cols] of Q, K, V plus the matching x
+            // A: weight tiles of this block's Q, K, V columns plus the matching x
             // rows. Weights do not depend on earlier kernels in the stream, so
             // the first ring of weight tiles is requested before waiting for
             // them; x (an earlier kernel's output) only after.
-            const int n_a = 3 * p.nA;
             const int n_pre = min(NS, n_a);
+            auto a_bytes = [&](int i) -> uint32_t {
+                if constexpr (MMA) return kStageBytes + (i < p.n_qk ? kXStageMma / 2 : kXStageMma);
+                else return p.TRA * kTileCols * 2 + xstage;
+            };
             auto issue_w = [&](int i, int s) {
-                const int sec = i / p.nA, t = i % p.nA;
-                tma_load_2d(ring + s * kStageBytes, &tm_wqkv, sec * H + h * D + g * kTileCols,
-                            rg * p.R + t * p.TRA, bar_full0 + 8u * s);
+                const uint32_t dst = ring + s * kStageBytes, bar = bar_full0 + 8u * s;
+                const int col = h * D + g * kTileCols;
+                if constexpr (MMA) {
+                    if (i < p.n_qk) {  // rows of Q and K side by side: one M=128 operand
+                        const int row = rg * p.R + 64 * i;
+                        tma_load_2d(dst, &tm_wqkv, col, row, bar);
+                        tma_load_2d(dst + kStageBytes / 2, &tm_wqkv, H + col, row, bar);
+                    } else {           // 128 rows of V as two 64-row halves
+                        const int row = rg * p.R + 128 * (i - p.n_qk);
+                        tma_load_2d(dst, &tm_wqkv, 2 * H + col, row, bar);
+                        tma_load_2d(dst + kStageBytes / 2, &tm_wqkv, 2 * H + col, row + 64, bar);
+                    }
+                } else {
+                    const int sec = i / p.nA, t = i % p.nA;
+                    tma_load_2d(dst, &tm_wqkv, sec * H + col, rg * p.R + t * p.TRA, bar);
+                }
             };
             auto issue_x = [&](int i, int s) {
-                const int row = rg * p.R + (i % p.nA) * p.TRA;
-                for (int b = 0; b < B; ++b)
-                    bulk_load_1d(xring + s * xstage + b * p.TRA * 2,
-                                 p.x + static_cast<size_t>(b) * H + row, p.TRA * 2,
-                                 bar_full0 + 8u * s);
+                const uint32_t bar = bar_full0 + 8u * s;
+                if constexpr (MMA) {
+                    const uint32_t dst = xring + s * kXStageMma;
+                    if (i < p.n_qk) {
+                        tma_load_2d(dst, &tm_x, rg * p.R + 64 * i, 0, bar);
+                    } else {
+                        const int row = rg * p.R + 128 * (i - p.n_qk);
+                        tma_load_2d(dst, &tm_x, row, 0, bar);
+                        tma_load_2d(dst + kXStageMma / 2, &tm_x, row + 64, 0, bar);
+                    }
+                } else {
+                    const int row = rg * p.R + (i % p.nA) * p.TRA;
+                    for (int b = 0; b < B; ++b)
+                        bulk_load_1d(xring + s * xstage + b * p.TRA * 2,
+                                     p.x + static_cast<size_t>(b) * H + row, p.TRA * 2, bar);
+                }
             };
             for (int i = 0; i < n_pre; ++i) {
-                mbar_arrive_expect_tx(bar_full0 + 8u * i, p.TRA * kTileCols * 2 + xstage);
+                mbar_arrive_expect_tx(bar_full0 + 8u * i, a_bytes(i));
                 issue_w(i, i);
             }
             grid_dependency_wait();
@@ -282,7 +334,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             for (int i = 0; i < n_pre; ++i) cur.advance(NS);
             for (int i = n_pre; i < n_a; ++i) {
                 const int s = acquire();
-                mbar_arrive_expect_tx(bar_full0 + 8u * s, p.TRA * kTileCols * 2 + xstage);
+                mbar_arrive_expect_tx(bar_full0 + 8u * s, a_bytes(i));
                 issue_w(i, s);
                 issue_x(i, s);
                 cur.advance(NS);
@@ -329,12 +381,16 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     } else {
         // --------------------------------------------------------- compute warps
         const uint8_t *ring = smem;
-        const uint16_t *xring = reinterpret_cast<const uint16_t *>(smem + p.off_xring);
         float *qkv_recv = reinterpret_cast<float *>(smem + p.off_qkv_recv);  // [C][B][3][64]
         float *sm_recv = reinterpret_cast<float *>(smem + p.off_sm_recv);    // [C][B][SMW]
         float *qkv_full = reinterpret_cast<float *>(smem + p.off_qkv_full);  // [B][3][D], then s_new [B]
         float *attn = reinterpret_cast<float *>(smem + p.off_attn);          // [B][D]
         float *scratch = reinterpret_cast<float *>(smem + p.off_scratch);
+        uint32_t tmem = 0;
+        if constexpr (MMA) {
+            tcgen05_fence_after();
+            tmem = *tmem_slot;
+        }
         grid_dependency_wait();  // no dependent read or global write before this
         RingCursor cur;
         auto wait_full = [&]() -> int {
@@ -345,6 +401,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         auto release = [&](int s) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty0 + 8u * s);
+            cur.advance(NS);
+        };
+        // MMA path: warp 0's elected lane issues the MMAs of a stage and hands the
+        // stage back with a commit (which counts as warp 0's arrival).
+        auto release_after_mma = [&](int s) {
+            if (lane == 0) umma_commit(bar_empty0 + 8u * s);
+            __syncwarp();
             cur.advance(NS);
         };
 
@@ -363,7 +426,67 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 push_16B(map_to_rank(my_qkv_addr + 4u * off, peer), v, map_to_rank(bar, peer));
             }
         };
-        {
+        if constexpr (MMA) {
+            const uint32_t idesc = umma_idesc_bf16(128, kMmaN, true, false);
+            const uint32_t ring_a = smem_addr(smem);
+            const uint32_t xring_a = smem_addr(smem + p.off_xring);
+            // Accumulator rows m (TMEM lanes) are weight columns: [Q | K] rows
+            // 0..63 / 64..127, V rows 0..63 (64..127 repeat them); columns are
+            // batch rows. Read back by the warps that own those lanes.
+            auto read_acc = [&](uint32_t col, int nwarps, int sec_of_row64) {
+                mbar_wait_bounded<false>(bar_acc_a, col == kAccQK ? 0u : 1u, p.timeout_ns, timed_out,
+                                         p.status, kSiteStageFull);
+                tcgen05_fence_after();
+                if (warp < nwarps) {
+                    float v[16];
+                    tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + col, v);
+                    const int m = 32 * warp + lane;
+                    const int sec = sec_of_row64 + (m >> 6), c = m & 63;
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b)
+                        if (b < B) my_qkv[(b * 3 + sec) * kTileCols + c] = v[b];
+                }
+                tcgen05_fence_before();
+                compute_bar<kComputeThreads>();
+            };
+            for (int i = 0; i < n_a; ++i) {
+                const int s = wait_full();
+                if (warp == 0) {
+                    if (lane == 0) {
+                        tcgen05_fence_after();
+                        const uint32_t a0 = ring_a + s * kStageBytes;
+                        const uint32_t b0 = xring_a + s * kXStageMma;
+                        if (i < p.n_qk) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                umma_bf16(tmem + kAccQK, umma_smem_desc(a0 + j * 2048, kStageBytes / 2, 1024),
+                                          umma_smem_desc(b0 + j * 32, 16, 1024), idesc, i > 0 || j > 0);
+                        } else {
+#pragma unroll
+                            for (int half = 0; half < 2; ++half)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    umma_bf16(tmem + kAccV,
+                                              umma_smem_desc(a0 + half * (kStageBytes / 2) + j * 2048, 0, 1024),
+                                              umma_smem_desc(b0 + half * (kXStageMma / 2) + j * 32, 16, 1024),
+                                              idesc, i > p.n_qk || half > 0 || j > 0);
+                        }
+                        if (i == p.n_qk - 1 || i == n_a - 1) umma_commit(bar_acc_a);
+                    }
+                    release_after_mma(s);
+                } else {
+                    release(s);
+                }
+                if (i == p.n_qk - 1) {
+                    read_acc(kAccQK, 4, 0);
+                    cluster_wait();  // every peer's barriers are initialised
+                    push_sections(0, 2, bar_qk);  // the q/k exchange overlaps the V stages
+                }
+            }
+            read_acc(kAccV, 2, 2);
+            push_sections(2, 1, bar_v);  // the v exchange overlaps attention
+        } else {
+            const uint16_t *xring = reinterpret_cast<const uint16_t *>(smem + p.off_xring);
             const int xstage = B * p.TRA;
             const int rpw = p.TRA / kComputeWarps;
             for (int sec = 0; sec < 3; ++sec) {
@@ -380,23 +503,43 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 }
                 gemv_reduce<MAXB>(acc, B, warp, lane, tid, scratch, my_qkv + sec * kTileCols,
                                   3 * kTileCols);
-                if (sec == 0) {
+                if (sec == 1) {
                     cluster_wait();  // every peer's barriers are initialised
-                    push_sections(0, 1, bar_q);  // the q exchange overlaps the K and V sections
+                    push_sections(0, 2, bar_qk);  // the q/k exchange overlaps the V section
                 }
             }
-            push_sections(1, 2, bar_kv);  // the k/v exchange overlaps attention
+            push_sections(2, 1, bar_v);  // the v exchange overlaps attention
         }
 
-        // ---- X1 (q): sum the row-group partials, concatenate column groups --
-        mbar_wait_bounded<true>(bar_q, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
-        for (int idx = tid; idx < B * D; idx += kComputeThreads) {
-            const int b = idx / D, j = idx % D;
+        // Sum the row-group partials of section sec in rank order (column groups
+        // concatenated) for batch row b and head dim j.
+        auto gathered = [&](int b, int sec, int j) {
             const int gg = j / kTileCols, c = j % kTileCols;
             float sum = 0.f;
             for (int q = 0; q < p.RG; ++q)
-                sum += qkv_recv[static_cast<size_t>(q * p.G + gg) * qkv_payload + (b * 3) * kTileCols + c];
-            qkv_full[b * 3 * D + j] = sum * p.qscale;
+                sum += qkv_recv[static_cast<size_t>(q * p.G + gg) * qkv_payload +
+                                (b * 3 + sec) * kTileCols + c];
+            return sum;
+        };
+        // bf16 k_new / v_new, kept on chip and appended to the cache by rank 0.
+        auto append = [&](int b, int sec, int j, float val) {
+            const __nv_bfloat16 hb = __float2bfloat16_rn(val);
+            qkv_full[(b * 3 + sec) * D + j] = __bfloat162float(hb);
+            if (r == 0) {
+                uint16_t *cache = sec == 1 ? p.k_cache : p.v_cache;
+                cache[((static_cast<size_t>(b) * p.nh + h) * p.max_ctx + L) * D + j] =
+                    __bfloat16_as_ushort(hb);
+            }
+        };
+
+        // ---- X1 (q, k): the query for attention and the new key -------------
+        mbar_wait_bounded<true>(bar_qk, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
+        for (int idx = tid; idx < B * 2 * D; idx += kComputeThreads) {
+            const int b = idx / (2 * D), rem = idx % (2 * D);
+            const int sec = rem / D, j = rem % D;
+            const float sum = gathered(b, sec, j);
+            if (sec == 0) qkv_full[b * 3 * D + j] = sum * p.qscale;
+            else append(b, 1, j, sum);
         }
         compute_bar<kComputeThreads>();
 
@@ -527,27 +670,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             }
         }
 
-        // ---- X1 (k, v) while X2 is in flight: k_new, v_new, cache append and
-        //      the new token's score; the new token is one more split of the
-        //      softmax, attended from its on-chip bf16-rounded copy.
-        mbar_wait_bounded<true>(bar_kv, 0, p.timeout_ns, timed_out, p.status, kSiteKvExchange);
-        for (int idx = tid; idx < B * 2 * D; idx += kComputeThreads) {
-            const int b = idx / (2 * D), rem = idx % (2 * D);
-            const int sec = 1 + rem / D, j = rem % D;
-            const int gg = j / kTileCols, c = j % kTileCols;
-            float sum = 0.f;
-            for (int q = 0; q < p.RG; ++q)
-                sum += qkv_recv[static_cast<size_t>(q * p.G + gg) * qkv_payload +
-                                (b * 3 + sec) * kTileCols + c];
-            const __nv_bfloat16 hb = __float2bfloat16_rn(sum);
-            qkv_full[(b * 3 + sec) * D + j] = __bfloat162float(hb);
-            if (r == 0) {
-                uint16_t *cache = sec == 1 ? p.k_cache : p.v_cache;
-                cache[((static_cast<size_t>(b) * p.nh + h) * p.max_ctx + L) * D + j] =
-                    __bfloat16_as_ushort(hb);
-            }
-        }
-        compute_bar<kComputeThreads>();
+        // ---- X1 (v) while X2 is in flight: v_new, its cache append and the new
+        //      token's score; the new token is one more split of the softmax,
+        //      attended from its on-chip bf16-rounded copy.
+        mbar_wait_bounded<true>(bar_v, 0, p.timeout_ns, timed_out, p.status, kSiteKvExchange);
+        for (int idx = tid; idx < B * D; idx += kComputeThreads)
+            append(idx / D, 2, idx % D, gathered(idx / D, 2, idx % D));
         float *s_new = qkv_full + static_cast<size_t>(B) * 3 * D;  // [B]
         for (int b = warp; b < B; b += kComputeWarps) {
             const float *qb = qkv_full + static_cast<size_t>(b) * 3 * D;
@@ -579,9 +707,72 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         compute_bar<kComputeThreads>();
 
         // ---- C: output projection of this block's column chunk --------------
-        {
+        const size_t head_stride = static_cast<size_t>(B) * H;
+        if constexpr (MMA) {
+            // attn^T as a K-major, 128-byte-swizzled [16 x D] bf16 operand, split
+            // into hi + lo halves so the product keeps ~16 mantissa bits of attn.
+            uint8_t *at_hi = smem + p.off_attn_t;
+            uint8_t *at_lo = at_hi + (D / 64) * kMmaN * 128;
+            for (int idx = tid; idx < kMmaN * D; idx += kComputeThreads) {
+                const int n = idx / D, k = idx % D;
+                const float a = n < B ? attn[n * D + k] : 0.f;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
+                const int kk = k & 63;
+                const int off = (k >> 6) * (kMmaN * 128) + n * 128 + (((kk >> 3) ^ (n & 7)) << 4) +
+                                (kk & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(at_hi + off) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(at_lo + off) = lo;
+            }
+            fence_proxy_async_smem();
+            compute_bar<kComputeThreads>();
+            const uint32_t idesc = umma_idesc_bf16(128, kMmaN, true, false);
+            const uint32_t ring_a = smem_addr(smem);
+            const uint32_t hi_a = smem_addr(at_hi), lo_a = smem_addr(at_lo);
+            // Rows 0..63 of accumulator t & 1 (warps 0 and 1) -> partials of tile t.
+            auto read_tile = [&](int t) {
+                mbar_wait_bounded<false>(bar_acc_c + 8u * (t & 1), (t >> 1) & 1, p.timeout_ns,
+                                         timed_out, p.status, kSiteStageFull);
+                tcgen05_fence_after();
+                if (warp < 2) {
+                    float v[16];
+                    tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kMmaN * (t & 1), v);
+                    float *dst = p.partials + static_cast<size_t>(h) * head_stride + col0 +
+                                 t * kTileCols + 32 * warp + lane;
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b)
+                        if (b < B) dst[static_cast<size_t>(b) * H] = v[b];
+                }
+            };
+            for (int ct = 0; ct < n_out_tiles; ++ct) {
+                const int s = wait_full();
+                if (warp == 0) {
+                    if (lane == 0) {
+                        tcgen05_fence_after();
+                        const uint32_t a0 = ring_a + s * kStageBytes;
+                        const uint32_t d = tmem + kMmaN * (ct & 1);
+#pragma unroll
+                        for (int j = 0; j < D / 16; ++j) {
+                            const uint64_t da = umma_smem_desc(a0 + j * 2048, 0, 1024);
+                            const uint32_t boff = (j >> 2) * (kMmaN * 128) + (j & 3) * 32;
+                            umma_bf16(d, da, umma_smem_desc(hi_a + boff, 16, 1024), idesc, j > 0);
+                            umma_bf16(d, da, umma_smem_desc(lo_a + boff, 16, 1024), idesc, true);
+                        }
+                        umma_commit(bar_acc_c + 8u * (ct & 1));
+                    }
+                    release_after_mma(s);
+                } else {
+                    release(s);
+                }
+                if (ct > 0) read_tile(ct - 1);
+                tcgen05_fence_before();
+                compute_bar<kComputeThreads>();  // accumulator (ct-1)&1 is free again
+            }
+            read_tile(n_out_tiles - 1);
+            tcgen05_fence_before();
+            compute_bar<kComputeThreads>();
+        } else {
             const int rpw = D / kComputeWarps;
-            const size_t head_stride = static_cast<size_t>(B) * H;
             for (int ct = 0; ct < n_out_tiles; ++ct) {
                 const int s = wait_full();
                 float acc[MAXB][GS::CPL];
@@ -596,37 +787,43 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                       ct * kTileCols,
                                   H);
             }
+        }
 
-            // ---- D: the last head to finish this chunk merges it ------------
-            // gemv_reduce ended with a barrier after this block's last partial
-            // store, so one thread's release covers the whole block's stores.
-            if (tid == 0) {
-                const unsigned prev = atomic_add_acq_rel_gpu(p.counters + r, 1u);
-                const bool last = prev == static_cast<unsigned>(p.nh - 1);
-                if (last) p.counters[r] = 0u;  // ready for the next launch
-                *is_last = last ? 1 : 0;
-            }
-            compute_bar<kComputeThreads>();
-            if (*is_last) {
-                const int n4 = p.ncols / 4;
-                for (int idx = tid; idx < B * n4; idx += kComputeThreads) {
-                    const int b = idx / n4;
-                    const int c = col0 + 4 * (idx % n4);
-                    const float *src = p.partials + static_cast<size_t>(b) * H + c;
-                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        // ---- D: the last head to finish this chunk merges it ----------------
+        // A barrier follows this block's last partial store, so one thread's
+        // release covers the whole block's stores.
+        if (tid == 0) {
+            const unsigned prev = atomic_add_acq_rel_gpu(p.counters + r, 1u);
+            const bool last = prev == static_cast<unsigned>(p.nh - 1);
+            if (last) p.counters[r] = 0u;  // ready for the next launch
+            *is_last = last ? 1 : 0;
+        }
+        compute_bar<kComputeThreads>();
+        if (*is_last) {
+            const int n4 = p.ncols / 4;
+            for (int idx = tid; idx < B * n4; idx += kComputeThreads) {
+                const int b = idx / n4;
+                const int c = col0 + 4 * (idx % n4);
+                const float *src = p.partials + static_cast<size_t>(b) * H + c;
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 16
-                    for (int hh = 0; hh < p.nh; ++hh) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + hh * head_stride));
-                        sum.x += v.x;
-                        sum.y += v.y;
-                        sum.z += v.z;
-                        sum.w += v.w;
-                    }
-                    uint2 packed;
-                    packed.x = pack2_bf16(sum.x, sum.y);
-                    packed.y = pack2_bf16(sum.z, sum.w);
-                    *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+                for (int hh = 0; hh < p.nh; ++hh) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + hh * head_stride));
+                    sum.x += v.x;
+                    sum.y += v.y;
+                    sum.z += v.z;
+                    sum.w += v.w;
                 }
+                uint2 packed;
+                packed.x = pack2_bf16(sum.x, sum.y);
+                packed.y = pack2_bf16(sum.z, sum.w);
+                *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+            }
+        }
+        if constexpr (MMA) {
+            if (warp == 0) {
+                tcgen05_fence_after();
+                tmem_dealloc(tmem, kTmemCols);
             }
         }
     }
