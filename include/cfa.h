@@ -70,8 +70,9 @@ typedef enum cfa_status {
  * cache capacity of max_ctx positions, on the current CUDA device.
  * Chooses the cluster size (blocks per head) and the pipeline depth, sets the
  * kernel attributes, and allocates the plan's workspace (fp32 per-head
- * output-projection partials [n_heads, B, hidden], per-column-chunk arrival
- * counters, a status word, and device staging for cfa_decode_step_host).
+ * output-projection partials [n_heads, B, hidden] and per-head-group sums,
+ * arrival counters of the cross-head merge, a status word, and device staging
+ * for cfa_decode_step_host).
  * Returns NULL on failure; cfa_last_error() then says why.
  */
 cfa_plan *cfa_plan_create(int B, int hidden, int n_heads, int head_dim, int max_ctx);
@@ -129,11 +130,12 @@ cfa_status cfa_decode_step_host(cfa_plan *plan, const void *x_host, const void *
  * No plan is involved: the shape is passed directly, with the same meaning,
  * limits and cluster-size choice as cfa_plan_create, and the arguments after
  * it mean what they mean for cfa_decode_step. Nothing is allocated: the
- * kernel's scratch (arrival counters, status word and the fp32 per-head
- * output-projection partials) lives in one fixed array inside the library,
- * 8 MiB + 256 bytes, which every GPU that loads the library keeps until the
- * process exits. Shapes with n_heads * B * hidden > 2^21 do not fit and
- * return CFA_ERR_UNSUPPORTED before anything is launched.
+ * kernel's scratch (arrival counters, status word and the fp32 per-head and
+ * per-head-group output-projection partials) lives in one fixed array inside
+ * the library, 8 MiB + 16.25 KiB, which every GPU that loads the library
+ * keeps until the process exits. Shapes with (n_heads + G) * B * hidden > 2^21,
+ * where G = ceil(n_heads / 8) for n_heads >= 16 and 1 otherwise, do not fit
+ * and return CFA_ERR_UNSUPPORTED before anything is launched.
  *
  * The first call on a device sets the array up (looks up its device address
  * and zeroes its counters, synchronizing that device once); make that first

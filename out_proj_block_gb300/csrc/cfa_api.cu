@@ -39,6 +39,21 @@ constexpr int kMinStages = 2;
 
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
+// Heads per first-level group of the cross-head merge, and the group count.
+// One level (a flat sum by the last head) while the data the last block reads
+// is small; two levels (groups of 8 heads) once a flat merge would read more
+// than 256 KB through one SM.
+int merge_group_size(int nh, int B, int ncols) {
+    const long long flat_bytes = 4ll * nh * B * ncols;
+    return (nh >= 16 && flat_bytes > (256 << 10)) ? 8 : nh;
+}
+int merge_groups(int nh, int B, int ncols) {
+    const int gs = merge_group_size(nh, B, ncols);
+    return (nh + gs - 1) / gs;
+}
+// Upper bound over every cluster size (smaller chunks never need more groups).
+int merge_groups_max(int nh) { return nh >= 16 ? (nh + 7) / 8 : 1; }
+
 }  // namespace
 
 struct cfa_plan {
@@ -53,7 +68,8 @@ struct cfa_plan {
     const void *kernel = nullptr;
     // workspace
     float *partials = nullptr;    // [nh][B][H]
-    unsigned *words = nullptr;    // [0, kMaxCluster) chunk counters, [kMaxCluster] status
+    unsigned *words = nullptr;    // [0, kMaxCounters) merge counters, [kMaxCounters] status
+    float *group_sums = nullptr;  // [ceil(nh / merge_group)][B][H]
     uint16_t *x_stage = nullptr;  // [B][H] for cfa_decode_step_host
     uint16_t *out_stage = nullptr;
     // cached tensor maps
@@ -146,7 +162,9 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
         TRA = 64;
     }
 
-    const int xstage = mma ? cfa::kXStageMmaBytes : B * TRA * 2;
+    // x: per stage on the tensor-core path; the block's whole x slice once otherwise.
+    const int xstage = mma ? cfa::kXStageMmaBytes : 0;
+    const int xrows = mma ? 0 : align_up(B * R * 2, 128);
     const int attn_t = mma ? 2 * (D / 64) * cfa::kMmaN * 128 : 0;
     const int qkv_recv = C * B * 3 * cfa::kTileCols * 4;
     const int sm_recv = C * B * (D + 4) * 4;
@@ -154,19 +172,27 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     const int attn = B * D * 4;
     const int scratch = std::max(mma ? 0 : cfa::kComputeWarps * B * cfa::kTileCols * 4,
                                  (cfa::kComputeWarps * D + 2 * cfa::kComputeWarps) * 4);
-    const int fixed = align_up(qkv_recv, 128) + align_up(sm_recv, 128) +
-                      align_up(qkv_full, 128) + align_up(attn, 128) + align_up(attn_t, 1024) +
-                      align_up(scratch, 128) + 1024 /* alignment slack, barriers, flags */;
+    // Stages of x ring needed to hold attn and its hi/lo operand (tensor-core
+    // path; 0 = never alias).
+    const int alias_stages = mma ? (align_up(attn, 1024) + attn_t + xstage - 1) / xstage : 0;
+    const int fixed_common = align_up(qkv_recv, 128) + align_up(sm_recv, 128) +
+                             align_up(qkv_full, 128) + align_up(scratch, 128) + xrows +
+                             1024 /* alignment slack, barriers, flags */;
+    const int attn_bytes = align_up(attn, 128) + align_up(attn_t, 1024);
     const int per_stage = cfa::kStageBytes + xstage + 16;
 
     const int grid = pl->nh * C;
     int per_sm = (grid + pl->num_sms - 1) / std::max(pl->num_sms, 1);
     per_sm = std::min(std::max(per_sm, 1), 4);
     int NS = 0;
+    int blocks_per_sm = 1;
     for (; per_sm >= 1 && NS < kMinStages; --per_sm) {
         const int budget =
             std::min(pl->smem_optin, pl->smem_per_sm / per_sm - pl->smem_reserved);
-        NS = std::min(kMaxStages, (budget - fixed) / per_stage);
+        NS = std::min(kMaxStages, (budget - fixed_common) / per_stage);
+        if (!mma || NS < alias_stages)  // attn needs its own space
+            NS = std::min(kMaxStages, (budget - fixed_common - attn_bytes) / per_stage);
+        blocks_per_sm = per_sm;
     }
     if (stages_override > 0) NS = stages_override;
     if (NS < kMinStages || NS > 64) return CFA_ERR_UNSUPPORTED;
@@ -174,21 +200,32 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     int off = NS * cfa::kStageBytes;
     KernelParams k{};
     k.off_xring = off;
-    off = align_up(off + NS * xstage, 1024);
-    k.off_attn_t = off;
-    off = align_up(off + attn_t, 128);
+    off = align_up(off + NS * xstage + xrows, 1024);
+    // The tensor-core path reads x only in the projection phase, so attn and
+    // its hi/lo operand (written after attention) reuse the x ring when it is
+    // large enough.
+    const bool alias_attn = mma && NS >= alias_stages;
+    if (alias_attn) {
+        k.off_attn = k.off_xring;
+        k.off_attn_t = k.off_xring + align_up(attn, 1024);
+    } else {
+        k.off_attn_t = off;
+        off = align_up(off + attn_t, 128);
+    }
     k.off_qkv_recv = off;
     off = align_up(off + qkv_recv, 128);
     k.off_sm_recv = off;
     off = align_up(off + sm_recv, 128);
     k.off_qkv_full = off;
     off = align_up(off + qkv_full, 128);
-    k.off_attn = off;
-    off = align_up(off + attn, 128);
+    if (!alias_attn) {
+        k.off_attn = off;
+        off = align_up(off + attn, 128);
+    }
     k.off_scratch = off;
     off = align_up(off + scratch, 128);
     k.off_bars = off;
-    off += (2 * NS + 6) * 8 + 48;
+    off += (2 * NS + 10) * 8;
     if (off > pl->smem_optin) return CFA_ERR_UNSUPPORTED;
 
     k.B = B;
@@ -203,7 +240,20 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.nA = R / TRA;
     k.n_qk = mma ? R / 64 : 0;
     k.n_v = mma ? R / 128 : 0;
+    // TMEM: 32 columns for the projection accumulators; the out-projection
+    // keeps up to 16 tile accumulators of 16 columns. Blocks that share an SM
+    // must fit its 512 columns together.
+    unsigned cols = 32;
+    if (mma) {
+        const int want = std::min(ncols / cfa::kTileCols, 16) * cfa::kMmaN;
+        while (static_cast<int>(cols) < want) cols <<= 1;
+        const int resident = std::max(blocks_per_sm, (pl->smem_per_sm) / (off + pl->smem_reserved));
+        while (cols > 32 && static_cast<int>(cols) * resident > 512) cols >>= 1;
+    }
+    k.tmem_cols = cols;
     k.ncols = ncols;
+    k.merge_group = merge_group_size(pl->nh, B, ncols);
+    if ((merge_groups(pl->nh, B, ncols) + 1) * C > cfa::kMaxCounters) return CFA_ERR_UNSUPPORTED;
     k.nstages = NS;
     k.timeout_ns = kDefaultTimeoutNs;
     k.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
@@ -273,10 +323,12 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 void free_workspace(cfa_plan *pl) {
     if (pl->partials) cudaFree(pl->partials);
     if (pl->words) cudaFree(pl->words);
+    if (pl->group_sums) cudaFree(pl->group_sums);
     if (pl->x_stage) cudaFree(pl->x_stage);
     if (pl->out_stage) cudaFree(pl->out_stage);
     pl->partials = nullptr;
     pl->words = nullptr;
+    pl->group_sums = nullptr;
     pl->x_stage = pl->out_stage = nullptr;
 }
 
@@ -353,10 +405,12 @@ cfa_plan *cfa_plan_create(int B, int hidden, int n_heads, int head_dim, int max_
     const size_t part_bytes = sizeof(float) * static_cast<size_t>(n_heads) * B * hidden;
     const size_t act_bytes = 2u * static_cast<size_t>(B) * hidden;
     if (cudaMalloc(&pl->partials, part_bytes) != cudaSuccess ||
-        cudaMalloc(&pl->words, sizeof(unsigned) * (cfa::kMaxCluster + 16)) != cudaSuccess ||
+        cudaMalloc(&pl->words, sizeof(unsigned) * (cfa::kMaxCounters + 16)) != cudaSuccess ||
+        cudaMalloc(&pl->group_sums, sizeof(float) * static_cast<size_t>(merge_groups_max(n_heads)) *
+                                        B * hidden) != cudaSuccess ||
         cudaMalloc(&pl->x_stage, act_bytes) != cudaSuccess ||
         cudaMalloc(&pl->out_stage, act_bytes) != cudaSuccess ||
-        cudaMemset(pl->words, 0, sizeof(unsigned) * (cfa::kMaxCluster + 16)) != cudaSuccess) {
+        cudaMemset(pl->words, 0, sizeof(unsigned) * (cfa::kMaxCounters + 16)) != cudaSuccess) {
         cudaGetLastError();
         free_workspace(pl);
         delete pl;
@@ -484,7 +538,8 @@ cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const
     kp.out = static_cast<uint16_t *>(out);
     kp.partials = pl->partials;
     kp.counters = pl->words;
-    kp.status = pl->words + cfa::kMaxCluster;
+    kp.status = pl->words + cfa::kMaxCounters;
+    kp.group_sums = pl->group_sums;
     kp.ctx_len = ctx_len;
 
     cudaLaunchAttribute attr[2];
@@ -529,9 +584,9 @@ cfa_status cfa_plan_status(cfa_plan *pl) {
     if (!pl) return fail(CFA_ERR_INVALID_ARG);
     unsigned word = 0;
     if (cudaDeviceSynchronize() != cudaSuccess ||
-        cudaMemcpy(&word, pl->words + cfa::kMaxCluster, sizeof word, cudaMemcpyDeviceToHost) !=
+        cudaMemcpy(&word, pl->words + cfa::kMaxCounters, sizeof word, cudaMemcpyDeviceToHost) !=
             cudaSuccess ||
-        cudaMemset(pl->words + cfa::kMaxCluster, 0, sizeof word) != cudaSuccess) {
+        cudaMemset(pl->words + cfa::kMaxCounters, 0, sizeof word) != cudaSuccess) {
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);
     }
@@ -581,8 +636,8 @@ cfa_status cfa_selftest_wait_timeout(int limit_us, void *stream) {
 
 namespace {
 
-constexpr size_t kNoallocWordsBytes = 256;                  // counters + status word
-constexpr size_t kNoallocPartialFloats = size_t(1) << 21;   // n_heads * B * hidden limit
+constexpr size_t kNoallocWordsBytes = (cfa::kMaxCounters + 64) * 4;  // counters + status word
+constexpr size_t kNoallocPartialFloats = size_t(1) << 21;   // (n_heads + groups) * B * hidden
 constexpr size_t kNoallocBytes = kNoallocWordsBytes + kNoallocPartialFloats * sizeof(float);
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
@@ -619,7 +674,9 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     if ((head_dim != 64 && head_dim != 128) || B > 16 || hidden % 64 != 0 ||
         max_ctx > (1 << 22) || hidden > (1 << 16))
         return fail(CFA_ERR_UNSUPPORTED);
-    if (static_cast<size_t>(n_heads) * B * hidden > kNoallocPartialFloats)
+    const size_t noalloc_floats =
+        static_cast<size_t>(n_heads + merge_groups_max(n_heads)) * B * hidden;
+    if (noalloc_floats > kNoallocPartialFloats)
         return fail(CFA_ERR_UNSUPPORTED);  // scratch array too small for this shape
     if (!x || !W_qkv || !W_o || !k_cache || !v_cache || !out) return fail(CFA_ERR_INVALID_ARG);
     if (ctx_len < 0 || ctx_len >= max_ctx) return fail(CFA_ERR_INVALID_ARG);
@@ -698,8 +755,9 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     kp.v_cache = static_cast<uint16_t *>(v_cache);
     kp.out = static_cast<uint16_t *>(out);
     kp.counters = reinterpret_cast<unsigned *>(scratch);
-    kp.status = reinterpret_cast<unsigned *>(scratch) + cfa::kMaxCluster;
+    kp.status = reinterpret_cast<unsigned *>(scratch) + cfa::kMaxCounters;
     kp.partials = reinterpret_cast<float *>(scratch + kNoallocWordsBytes);
+    kp.group_sums = kp.partials + static_cast<size_t>(n_heads) * B * hidden;
     kp.ctx_len = ctx_len;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config(&pl, kp, pl.smem_bytes, s, attr);

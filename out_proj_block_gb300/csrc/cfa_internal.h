@@ -12,6 +12,7 @@ constexpr int kThreads = kComputeThreads + 32;     // + one load-issuing warp
 constexpr int kStageBytes = 16384;                 // one pipeline stage
 constexpr int kTileCols = 64;                      // weight tile width (128 bytes of bf16)
 constexpr int kMaxCluster = 16;
+constexpr int kMaxCounters = 4096;                 // merge counters; the status word follows
 constexpr int kMmaN = 16;                          // batch rows per tensor-core MMA (zero-padded)
 constexpr int kXStageMmaBytes = 2 * kMmaN * 128;   // x per stage on the tensor-core path
 
@@ -35,7 +36,8 @@ struct KernelParams {
     uint16_t *v_cache;
     uint16_t *out;         // [B][H] bf16
     float *partials;       // [nh][B][H] fp32 per-head output-projection partials
-    unsigned *counters;    // [C] arrivals per output-column chunk
+    float *group_sums;     // [ceil(nh / merge_group)][B][H] fp32 per-group sums
+    unsigned *counters;    // [groups][C] then [C]: arrivals per column chunk, two levels
     unsigned *status;      // device status word
     int B, H, nh, max_ctx, ctx_len;
     int C;                 // blocks per cluster (= per head)
@@ -45,7 +47,9 @@ struct KernelParams {
     int TRA;               // rows per projection tile
     int nA;                // projection tiles per Q/K/V block: R / TRA (CUDA-core path)
     int n_qk, n_v;         // tensor-core path: 64-row [Q|K] stages and 128-row V stages
+    unsigned tmem_cols;    // tensor-core path: TMEM columns per block (power of two >= 32)
     int ncols;             // output columns per block in the out-projection: H / C
+    int merge_group;       // heads per first-level merge group
     int nstages;           // pipeline depth
     int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_attn_t, off_scratch,
         off_bars;

@@ -40,10 +40,10 @@
 //  C  Output projection [CF §3.2]: the block owns H/C output columns and
 //     multiplies attn (head h's d rows of W_o) into fp32 partials, written to
 //     a per-head workspace row.
-//  D  Cross-head merge: instead of the page's atomicAdd merge [CF §3.2], the
-//     last of the n_heads blocks to finish a column chunk (a release/acquire
-//     counter) sums the n_heads partials in head order and writes bf16 out.
-//     Deterministic.
+//  D  Cross-head merge: instead of the page's atomicAdd merge [CF §3.2], a
+//     two-level tree of release/acquire counters: the last head of each group
+//     of heads to finish a column chunk sums that group's partials, the last
+//     group sums the group totals into bf16 out. Fixed order, deterministic.
 #pragma once
 
 #include <cuda.h>
@@ -176,7 +176,6 @@ __device__ __forceinline__ void gemv_reduce(float (&acc)[MAXB][GemvShape<MAXB>::
 constexpr int kXStageMma = kXStageMmaBytes;      // x bytes per stage: two [16 x 64] swizzled boxes
 constexpr uint32_t kAccQK = 0;                   // TMEM columns of the [Q|K] accumulator
 constexpr uint32_t kAccV = kMmaN;                // TMEM columns of the V accumulator
-constexpr uint32_t kTmemCols = 32;
 
 template <int D, int MAXB>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -216,11 +215,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     const uint32_t bar_v = bar_qk + 8u;             // v partials from every peer
     const uint32_t bar_sm = bar_qk + 16u;           // softmax statistics from every peer
     const uint32_t bar_acc_a = bar_qk + 24u;        // projection accumulators ready (MMA path)
-    const uint32_t bar_acc_c = bar_qk + 32u;        // two out-projection accumulators (MMA path)
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 48);
+    const uint32_t bar_acc_c = bar_qk + 32u;        // out-projection accumulator groups (MMA path)
+    const uint32_t bar_x = bar_qk + 40u;            // the block's x rows (CUDA-core path)
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 56);
     volatile int *timed_out = flags;      // set by the first wait that gives up
     volatile int *is_last = flags + 1;    // this block merges its column chunk
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 16 * NS + 56);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 16 * NS + 64);
 
     const int g = r % p.G;                // column group in the projection
     const int rg = r / p.G;               // row group in the projection
@@ -242,7 +242,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         mbar_init(bar_sm, 1);
         mbar_init(bar_acc_a, 1);
         mbar_init(bar_acc_c, 1);
-        mbar_init(bar_acc_c + 8u, 1);
+        mbar_init(bar_x, 1);
         *timed_out = 0;
         *is_last = 0;
         fence_mbar_init();
@@ -252,7 +252,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         mbar_arrive_expect_tx(bar_sm, static_cast<uint32_t>((C - 1) * sm_payload * 4));
     }
     if constexpr (MMA) {
-        if (warp == 0) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        if (warp == 0) tmem_alloc(smem_addr(tmem_slot), p.tmem_cols);
         tcgen05_fence_before();
     }
     __syncthreads();
@@ -272,7 +272,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         if (lane == 0) {
             const uint32_t ring = smem_addr(smem);
             const uint32_t xring = smem_addr(smem + p.off_xring);
-            const int xstage = MMA ? kXStageMma : B * p.TRA * 2;
             RingCursor cur;
             auto acquire = [&]() -> int {
                 if (cur.wrapped)
@@ -287,7 +286,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             const int n_pre = min(NS, n_a);
             auto a_bytes = [&](int i) -> uint32_t {
                 if constexpr (MMA) return kStageBytes + (i < p.n_qk ? kXStageMma / 2 : kXStageMma);
-                else return p.TRA * kTileCols * 2 + xstage;
+                else return p.TRA * kTileCols * 2;
             };
             auto issue_w = [&](int i, int s) {
                 const uint32_t dst = ring + s * kStageBytes, bar = bar_full0 + 8u * s;
@@ -318,11 +317,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                         tma_load_2d(dst, &tm_x, row, 0, bar);
                         tma_load_2d(dst + kXStageMma / 2, &tm_x, row + 64, 0, bar);
                     }
-                } else {
-                    const int row = rg * p.R + (i % p.nA) * p.TRA;
-                    for (int b = 0; b < B; ++b)
-                        bulk_load_1d(xring + s * xstage + b * p.TRA * 2,
-                                     p.x + static_cast<size_t>(b) * H + row, p.TRA * 2, bar);
                 }
             };
             for (int i = 0; i < n_pre; ++i) {
@@ -330,6 +324,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 issue_w(i, i);
             }
             grid_dependency_wait();
+            if constexpr (!MMA) {
+                // CUDA-core path: the block's x rows [rg*R, rg*R + R) once, for all stages
+                mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(B * p.R * 2));
+                for (int b = 0; b < B; ++b)
+                    bulk_load_1d(xring + b * p.R * 2, p.x + static_cast<size_t>(b) * H + rg * p.R,
+                                 p.R * 2, bar_x);
+            }
             for (int i = 0; i < n_pre; ++i) issue_x(i, i);
             for (int i = 0; i < n_pre; ++i) cur.advance(NS);
             for (int i = n_pre; i < n_a; ++i) {
@@ -486,9 +487,9 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             read_acc(kAccV, 2, 2);
             push_sections(2, 1, bar_v);  // the v exchange overlaps attention
         } else {
-            const uint16_t *xring = reinterpret_cast<const uint16_t *>(smem + p.off_xring);
-            const int xstage = B * p.TRA;
+            const uint16_t *xrows = reinterpret_cast<const uint16_t *>(smem + p.off_xring);  // [B][R]
             const int rpw = p.TRA / kComputeWarps;
+            mbar_wait_bounded<false>(bar_x, 0, p.timeout_ns, timed_out, p.status, kSiteStageFull);
             for (int sec = 0; sec < 3; ++sec) {
                 float acc[MAXB][GS::CPL];
 #pragma unroll
@@ -497,7 +498,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     for (int c = 0; c < GS::CPL; ++c) acc[b][c] = 0.f;
                 for (int t = 0; t < p.nA; ++t) {
                     const int s = wait_full();
-                    gemv_tile<MAXB>(ring + s * kStageBytes, rpw, xring + s * xstage, p.TRA, B,
+                    gemv_tile<MAXB>(ring + s * kStageBytes, rpw, xrows + t * p.TRA, p.R, B,
                                     warp, lane, acc);
                     release(s);
                 }
@@ -729,20 +730,34 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             const uint32_t idesc = umma_idesc_bf16(128, kMmaN, true, false);
             const uint32_t ring_a = smem_addr(smem);
             const uint32_t hi_a = smem_addr(at_hi), lo_a = smem_addr(at_lo);
-            // Rows 0..63 of accumulator t & 1 (warps 0 and 1) -> partials of tile t.
-            auto read_tile = [&](int t) {
-                mbar_wait_bounded<false>(bar_acc_c + 8u * (t & 1), (t >> 1) & 1, p.timeout_ns,
-                                         timed_out, p.status, kSiteStageFull);
+            // One TMEM accumulator per output tile (up to kbuf of them): the MMAs
+            // of consecutive tiles are issued back to back and read out in groups.
+            const int kbuf = static_cast<int>(p.tmem_cols) / kMmaN;
+            int group0 = 0, group_n = 0;
+            uint32_t acc_phase = 0;
+            auto flush = [&]() {
+                if (warp == 0 && lane == 0) umma_commit(bar_acc_c);
+                mbar_wait_bounded<false>(bar_acc_c, acc_phase, p.timeout_ns, timed_out, p.status,
+                                         kSiteStageFull);
+                acc_phase ^= 1u;
                 tcgen05_fence_after();
                 if (warp < 2) {
-                    float v[16];
-                    tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kMmaN * (t & 1), v);
-                    float *dst = p.partials + static_cast<size_t>(h) * head_stride + col0 +
-                                 t * kTileCols + 32 * warp + lane;
+                    for (int t = group0; t < group0 + group_n; ++t) {
+                        float v[16];
+                        tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) +
+                                        static_cast<uint32_t>(kMmaN * (t % kbuf)),
+                                    v);
+                        float *dst = p.partials + static_cast<size_t>(h) * head_stride + col0 +
+                                     t * kTileCols + 32 * warp + lane;
 #pragma unroll
-                    for (int b = 0; b < MAXB; ++b)
-                        if (b < B) dst[static_cast<size_t>(b) * H] = v[b];
+                        for (int b = 0; b < MAXB; ++b)
+                            if (b < B) dst[static_cast<size_t>(b) * H] = v[b];
+                    }
                 }
+                tcgen05_fence_before();
+                compute_bar<kComputeThreads>();  // the group's accumulators are free again
+                group0 += group_n;
+                group_n = 0;
             };
             for (int ct = 0; ct < n_out_tiles; ++ct) {
                 const int s = wait_full();
@@ -750,7 +765,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     if (lane == 0) {
                         tcgen05_fence_after();
                         const uint32_t a0 = ring_a + s * kStageBytes;
-                        const uint32_t d = tmem + kMmaN * (ct & 1);
+                        const uint32_t d = tmem + static_cast<uint32_t>(kMmaN * (ct % kbuf));
 #pragma unroll
                         for (int j = 0; j < D / 16; ++j) {
                             const uint64_t da = umma_smem_desc(a0 + j * 2048, 0, 1024);
@@ -758,19 +773,14 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                             umma_bf16(d, da, umma_smem_desc(hi_a + boff, 16, 1024), idesc, j > 0);
                             umma_bf16(d, da, umma_smem_desc(lo_a + boff, 16, 1024), idesc, true);
                         }
-                        umma_commit(bar_acc_c + 8u * (ct & 1));
                     }
                     release_after_mma(s);
                 } else {
                     release(s);
                 }
-                if (ct > 0) read_tile(ct - 1);
-                tcgen05_fence_before();
-                compute_bar<kComputeThreads>();  // accumulator (ct-1)&1 is free again
+                if (++group_n == kbuf) flush();
             }
-            read_tile(n_out_tiles - 1);
-            tcgen05_fence_before();
-            compute_bar<kComputeThreads>();
+            if (group_n > 0) flush();
         } else {
             const int rpw = D / kComputeWarps;
             for (int ct = 0; ct < n_out_tiles; ++ct) {
@@ -789,41 +799,75 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             }
         }
 
-        // ---- D: the last head to finish this chunk merges it ----------------
-        // A barrier follows this block's last partial store, so one thread's
-        // release covers the whole block's stores.
-        if (tid == 0) {
-            const unsigned prev = atomic_add_acq_rel_gpu(p.counters + r, 1u);
-            const bool last = prev == static_cast<unsigned>(p.nh - 1);
-            if (last) p.counters[r] = 0u;  // ready for the next launch
-            *is_last = last ? 1 : 0;
-        }
-        compute_bar<kComputeThreads>();
-        if (*is_last) {
+        // ---- D: two-level deterministic cross-head merge -----------------------
+        // Heads form groups of p.merge_group. The last head of a group to finish
+        // this chunk sums the group's partials (in head order); the last group
+        // to finish sums the group totals (in group order) into bf16 out. A
+        // barrier follows each block's last store, so one thread's release
+        // covers the whole block's stores.
+        {
+            const int GS = p.merge_group;
+            const int ng = (p.nh + GS - 1) / GS;
+            const int grp = h / GS;
+            const int gsz = min(GS, p.nh - grp * GS);
             const int n4 = p.ncols / 4;
-            for (int idx = tid; idx < B * n4; idx += kComputeThreads) {
-                const int b = idx / n4;
-                const int c = col0 + 4 * (idx % n4);
-                const float *src = p.partials + static_cast<size_t>(b) * H + c;
-                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 16
-                for (int hh = 0; hh < p.nh; ++hh) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + hh * head_stride));
-                    sum.x += v.x;
-                    sum.y += v.y;
-                    sum.z += v.z;
-                    sum.w += v.w;
+            // Sum n blocks of partials src[i * stride] for this chunk; fp32 to dst_f
+            // (row stride H) or, when dst_f is null, bf16 to out.
+            auto merge = [&](const float *src0, size_t stride, int n, float *dst_f) {
+                for (int idx = tid; idx < B * n4; idx += kComputeThreads) {
+                    const int b = idx / n4;
+                    const int c = col0 + 4 * (idx % n4);
+                    const float *src = src0 + static_cast<size_t>(b) * H + c;
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                    for (int i = 0; i < n; ++i) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i * stride));
+                        sum.x += v.x;
+                        sum.y += v.y;
+                        sum.z += v.z;
+                        sum.w += v.w;
+                    }
+                    if (dst_f) {
+                        *reinterpret_cast<float4 *>(dst_f + static_cast<size_t>(b) * H + c) = sum;
+                    } else {
+                        uint2 packed;
+                        packed.x = pack2_bf16(sum.x, sum.y);
+                        packed.y = pack2_bf16(sum.z, sum.w);
+                        *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+                    }
                 }
-                uint2 packed;
-                packed.x = pack2_bf16(sum.x, sum.y);
-                packed.y = pack2_bf16(sum.z, sum.w);
-                *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+            };
+            unsigned *ctr1 = p.counters + grp * C + r;
+            unsigned *ctr2 = p.counters + ng * C + r;
+            if (tid == 0) {
+                const unsigned prev = atomic_add_acq_rel_gpu(ctr1, 1u);
+                const bool last = prev == static_cast<unsigned>(gsz - 1);
+                if (last) *ctr1 = 0u;  // ready for the next launch
+                *is_last = last ? 1 : 0;
+            }
+            compute_bar<kComputeThreads>();
+            if (*is_last) {
+                const float *grp_src = p.partials + static_cast<size_t>(grp * GS) * head_stride;
+                if (ng == 1) {
+                    merge(grp_src, head_stride, gsz, nullptr);
+                } else {
+                    merge(grp_src, head_stride, gsz, p.group_sums + static_cast<size_t>(grp) * head_stride);
+                    compute_bar<kComputeThreads>();
+                    if (tid == 0) {
+                        const unsigned prev = atomic_add_acq_rel_gpu(ctr2, 1u);
+                        const bool last = prev == static_cast<unsigned>(ng - 1);
+                        if (last) *ctr2 = 0u;
+                        *is_last = last ? 2 : 0;
+                    }
+                    compute_bar<kComputeThreads>();
+                    if (*is_last == 2) merge(p.group_sums, head_stride, ng, nullptr);
+                }
             }
         }
         if constexpr (MMA) {
             if (warp == 0) {
                 tcgen05_fence_after();
-                tmem_dealloc(tmem, kTmemCols);
+                tmem_dealloc(tmem, p.tmem_cols);
             }
         }
     }
