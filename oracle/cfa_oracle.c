@@ -28,6 +28,9 @@
  *   - the new token is attended: T = ctx_len + 1 keys, the new k/v at
  *     position ctx_len;
  *   - one ctx_len shared by every batch row.
+ * cfa_oracle_decode_step_ex widens the last two: one context length per batch
+ * row, and an optional rotary embedding of the new q and k (rotate-half form
+ * as in Llama2-style models).
  *
  * All inputs arrive as bf16 bit patterns (uint16) and are widened exactly to
  * double; every sum, product, exp and division is fp64.
@@ -269,4 +272,126 @@ int cfa_oracle_threads(int n)
     (void)n;
     return 1;
 #endif
+}
+
+/*
+ * Rotary position embedding, in the rotate-half form of Llama2-style models
+ * (a reading: the ClusterFusion page names no positional encoding for its
+ * block, [CF §1.1]). For i < d/2, with w_i = theta^(-2i/d) and angle a = pos w_i:
+ *   y_i       = x_i cos a - x_{i+d/2} sin a
+ *   y_{i+d/2} = x_{i+d/2} cos a + x_i sin a.
+ * d must be even; y may not alias x.
+ */
+void cfa_oracle_rope(int d, const double *x, int pos, double theta, double *y)
+{
+    const int half = d / 2;
+    for (int i = 0; i < half; ++i) {
+        const double w = pow(theta, -2.0 * i / d);
+        const double a = (double)pos * w;
+        const double c = cos(a), s = sin(a);
+        y[i] = x[i] * c - x[i + half] * s;
+        y[i + half] = x[i + half] * c + x[i] * s;
+    }
+}
+
+/*
+ * The decode step with one context length per sequence and optional rotary
+ * embedding of the new token's q and k at its own position ctx_lens[b]
+ * (cached keys are taken as already rotated when they were appended).
+ * rope_theta <= 0 disables the rotation. Everything else as
+ * cfa_oracle_decode_step [CF §1.1, §3.2, §5.1]; k_new is reported after
+ * rotation (the row that is appended).
+ */
+int cfa_oracle_decode_step_ex(int B, int H, int nh, int d, int max_ctx, const int *ctx_lens,
+                              double rope_theta, const uint16_t *x, const uint16_t *W_qkv,
+                              const uint16_t *W_o, const uint16_t *k_cache,
+                              const uint16_t *v_cache, double *out, double *k_new,
+                              double *v_new, double *attn, int nthreads)
+{
+    if (B < 1 || nh < 1 || d < 2 || (d & 1) || H != nh * d)
+        return -1;
+    for (int b = 0; b < B; ++b)
+        if (ctx_lens[b] < 0 || ctx_lens[b] >= max_ctx)
+            return -1;
+    const double scale = 1.0 / sqrt((double)d);
+    double *a_all = (double *)malloc(sizeof(double) * (size_t)B * nh * d);
+    if (!a_all)
+        return -1;
+#ifdef _OPENMP
+    if (nthreads < 1)
+        nthreads = 1;
+#else
+    (void)nthreads;
+#endif
+
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int bh = 0; bh < B * nh; ++bh) {
+        const int b = bh / nh, h = bh % nh;
+        const int L = ctx_lens[b], T = L + 1;
+        double *q0 = (double *)malloc(sizeof(double) * (size_t)d);
+        double *k0 = (double *)malloc(sizeof(double) * (size_t)d);
+        double *q = (double *)malloc(sizeof(double) * (size_t)d);
+        double *K = (double *)malloc(sizeof(double) * (size_t)T * d);
+        double *V = (double *)malloc(sizeof(double) * (size_t)T * d);
+        double *kk = K + (size_t)L * d;
+        double *vv = V + (size_t)L * d;
+        for (int j = 0; j < d; ++j) {
+            q0[j] = 0.0;
+            k0[j] = 0.0;
+            vv[j] = 0.0;
+        }
+        for (int i = 0; i < H; ++i) {
+            const double xi = widen_bf16(x[(size_t)b * H + i]);
+            const uint16_t *row = W_qkv + (size_t)i * 3 * H;
+            for (int j = 0; j < d; ++j) {
+                q0[j] += xi * widen_bf16(row[0 * H + h * d + j]);
+                k0[j] += xi * widen_bf16(row[1 * H + h * d + j]);
+                vv[j] += xi * widen_bf16(row[2 * H + h * d + j]);
+            }
+        }
+        if (rope_theta > 0.0) {
+            cfa_oracle_rope(d, q0, L, rope_theta, q);
+            cfa_oracle_rope(d, k0, L, rope_theta, kk);
+        } else {
+            memcpy(q, q0, sizeof(double) * (size_t)d);
+            memcpy(kk, k0, sizeof(double) * (size_t)d);
+        }
+        const size_t base = ((size_t)b * nh + h) * (size_t)max_ctx * d;
+        for (int t = 0; t < L; ++t)
+            for (int j = 0; j < d; ++j) {
+                K[(size_t)t * d + j] = widen_bf16(k_cache[base + (size_t)t * d + j]);
+                V[(size_t)t * d + j] = widen_bf16(v_cache[base + (size_t)t * d + j]);
+            }
+        for (int j = 0; j < d; ++j) {
+            k_new[(size_t)bh * d + j] = kk[j];
+            v_new[(size_t)bh * d + j] = vv[j];
+        }
+        cfa_oracle_attention(T, d, q, K, V, scale, a_all + (size_t)bh * d);
+        free(q0);
+        free(k0);
+        free(q);
+        free(K);
+        free(V);
+    }
+
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int b = 0; b < B; ++b) {
+        double *acc = out + (size_t)b * H;
+        for (int j = 0; j < H; ++j)
+            acc[j] = 0.0;
+        for (int r = 0; r < H; ++r) {
+            const double ar = a_all[(size_t)b * H + r];
+            const uint16_t *row = W_o + (size_t)r * H;
+            for (int j = 0; j < H; ++j)
+                acc[j] += ar * widen_bf16(row[j]);
+        }
+    }
+    if (attn)
+        memcpy(attn, a_all, sizeof(double) * (size_t)B * nh * d);
+    free(a_all);
+    return 0;
 }

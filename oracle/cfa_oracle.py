@@ -66,6 +66,12 @@ def _load():
                 ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp]
             lib.cfa_oracle_widen_bf16.restype = None
             lib.cfa_oracle_widen_bf16.argtypes = [_u16p, _dp, ctypes.c_long]
+            lib.cfa_oracle_decode_step_ex.restype = ctypes.c_int
+            lib.cfa_oracle_decode_step_ex.argtypes = (
+                [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int), ctypes.c_double]
+                + [_u16p] * 5 + [_dp] * 4 + [ctypes.c_int])
+            lib.cfa_oracle_rope.restype = None
+            lib.cfa_oracle_rope.argtypes = [ctypes.c_int, _dp, ctypes.c_int, ctypes.c_double, _dp]
             lib.cfa_oracle_threads.restype = ctypes.c_int
             lib.cfa_oracle_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -165,3 +171,38 @@ def split_combine(m, l, o) -> np.ndarray:
     _load().cfa_oracle_split_combine(n, d, m.ctypes.data_as(_dp), l.ctypes.data_as(_dp),
                                      o.ctypes.data_as(_dp), a.ctypes.data_as(_dp))
     return a
+
+
+def rope(x, pos: int, theta: float) -> np.ndarray:
+    """Rotate-half rotary embedding of x [d] at position pos (fp64)."""
+    x = _f64(x)
+    y = np.empty_like(x)
+    _load().cfa_oracle_rope(x.shape[0], x.ctypes.data_as(_dp), int(pos), float(theta),
+                            y.ctypes.data_as(_dp))
+    return y
+
+
+def decode_step_ex(x, W_qkv, W_o, k_cache, v_cache, ctx_lens, rope_theta: float = 0.0,
+                   nthreads: int = 1):
+    """fp64 decode step with per-sequence context lengths and optional RoPE of
+    the new q/k at position ctx_lens[b]. Same outputs as decode_step."""
+    xb, wq, wo, kc, vc = (_bits(t) for t in (x, W_qkv, W_o, k_cache, v_cache))
+    B, H = xb.shape
+    _, nh, max_ctx, d = kc.shape
+    lens = np.ascontiguousarray(np.asarray(ctx_lens, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("ctx_lens must have one entry per batch row")
+    out = np.empty((B, H), np.float64)
+    k_new = np.empty((B, nh, d), np.float64)
+    v_new = np.empty((B, nh, d), np.float64)
+    attn = np.empty((B, nh, d), np.float64)
+    rc = _load().cfa_oracle_decode_step_ex(
+        B, H, nh, d, max_ctx, lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+        float(rope_theta),
+        xb.ctypes.data_as(_u16p), wq.ctypes.data_as(_u16p), wo.ctypes.data_as(_u16p),
+        kc.ctypes.data_as(_u16p), vc.ctypes.data_as(_u16p),
+        out.ctypes.data_as(_dp), k_new.ctypes.data_as(_dp),
+        v_new.ctypes.data_as(_dp), attn.ctypes.data_as(_dp), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return {"out": out, "k_new": k_new, "v_new": v_new, "attn": attn}

@@ -354,3 +354,87 @@ def test_rejects_bad_arguments(oracle):
     t = rand_inputs(1, 64, 2, 32, 3, 4, seed=31)
     with pytest.raises(ValueError):
         oracle.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], 4)
+
+
+# ------------------------------------- rotary embedding and ragged lengths
+
+
+def test_rope_position_zero_is_identity(oracle):
+    x = np.random.default_rng(40).standard_normal(128)
+    np.testing.assert_array_equal(oracle.rope(x, 0, 10000.0), x)
+
+
+@pytest.mark.parametrize("pos", [1, 7, 1000, 16383])
+def test_rope_d2_is_a_plain_rotation(oracle, pos):
+    """d = 2: one pair, frequency theta^0 = 1, so the angle is pos radians."""
+    x = np.array([0.6, -1.3])
+    c, s = math.cos(pos), math.sin(pos)
+    np.testing.assert_allclose(oracle.rope(x, pos, 10000.0),
+                               [x[0] * c - x[1] * s, x[1] * c + x[0] * s], rtol=0, atol=1e-15)
+
+
+def test_rope_pairs_dimension_i_with_i_plus_half(oracle):
+    """Rotate-half convention: basis vector e_i only mixes with e_{i+d/2}."""
+    d = 16
+    for i in range(d // 2):
+        e = np.zeros(d)
+        e[i] = 1.0
+        y = oracle.rope(e, 5, 10000.0)
+        nz = set(np.nonzero(np.abs(y) > 1e-15)[0].tolist())
+        assert nz <= {i, i + d // 2}
+
+
+def test_rope_preserves_norm_and_relative_position(oracle):
+    rng = np.random.default_rng(41)
+    d = 128
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    for pos in (3, 333, 4096):
+        assert np.linalg.norm(oracle.rope(q, pos, 10000.0)) == pytest.approx(np.linalg.norm(q), rel=1e-13)
+    base = np.dot(oracle.rope(q, 100, 10000.0), oracle.rope(k, 40, 10000.0))
+    for shift in (1, 17, 2000):
+        shifted = np.dot(oracle.rope(q, 100 + shift, 10000.0), oracle.rope(k, 40 + shift, 10000.0))
+        assert shifted == pytest.approx(base, rel=1e-10, abs=1e-10)
+
+
+def test_ex_without_rope_equals_uniform_step(oracle):
+    B, H, nh, d, L = 3, 128, 2, 64, 20
+    t = rand_inputs(B, H, nh, d, L, 32, seed=42)
+    a = oracle.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], L)
+    b = oracle.decode_step_ex(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], [L] * B)
+    for key in ("out", "k_new", "v_new", "attn"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_ragged_rows_are_independent_sequences(oracle):
+    """Each batch row with its own ctx_len equals a one-row step at that length."""
+    B, H, nh, d = 3, 128, 2, 64
+    lens = [0, 13, 31]
+    t = rand_inputs(B, H, nh, d, 31, 32, seed=43)
+    r = oracle.decode_step_ex(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], lens,
+                              rope_theta=10000.0)
+    for b, L in enumerate(lens):
+        one = oracle.decode_step_ex(t["x"][b:b + 1], t["W_qkv"], t["W_o"], t["k_cache"][b:b + 1],
+                                    t["v_cache"][b:b + 1], [L], rope_theta=10000.0)
+        np.testing.assert_array_equal(r["out"][b], one["out"][0])
+
+
+def test_rope_step_is_attention_over_rotated_q_and_new_key(oracle):
+    """Assembled by hand: q and k_new projected with numpy, rotated at their
+    position, attended against the cached (already rotated) keys."""
+    B, H, nh, d = 2, 128, 2, 64
+    lens = [9, 30]
+    t = rand_inputs(B, H, nh, d, 30, 32, seed=44)
+    r = oracle.decode_step_ex(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], lens,
+                              rope_theta=500.0)
+    x, Wqkv = f64(t["x"]), f64(t["W_qkv"])
+    for b, L in enumerate(lens):
+        for h in range(nh):
+            cols = slice(h * d, (h + 1) * d)
+            q = oracle.rope(x[b] @ Wqkv[:, cols], L, 500.0)
+            k = oracle.rope(x[b] @ Wqkv[:, H:][:, cols], L, 500.0)
+            v = x[b] @ Wqkv[:, 2 * H:][:, cols]
+            K = np.concatenate([f64(t["k_cache"][b, h, :L]), k[None]])
+            V = np.concatenate([f64(t["v_cache"][b, h, :L]), v[None]])
+            np.testing.assert_allclose(r["k_new"][b, h], k, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(r["attn"][b, h], oracle.attention(q, K, V, 1 / math.sqrt(d)),
+                                       rtol=1e-12, atol=1e-14)
