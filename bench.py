@@ -213,9 +213,9 @@ def oracle_baseline(wl, cpu_inputs, budget_s: float, max_reps: int = 50):
     t_start = time.perf_counter()
     while len(times) < max_reps:
         t0 = time.perf_counter()
-        ref = cfa_oracle.decode_step(cpu_inputs["x"], cpu_inputs["W_qkv"], cpu_inputs["W_o"],
-                                     cpu_inputs["k_cache"], cpu_inputs["v_cache"],
-                                     wl.ctx_len, nthreads=used)
+        ref = cfa_oracle.decode_step_ex(cpu_inputs["x"], cpu_inputs["W_qkv"], cpu_inputs["W_o"],
+                                        cpu_inputs["k_cache"], cpu_inputs["v_cache"],
+                                        list(wl.lens), rope_theta=wl.rope_theta, nthreads=used)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_start >= budget_s:
             break
@@ -242,8 +242,9 @@ def run_reference(args):
     t = workloads.make_inputs(wl, seed=0, device="cpu")
     cores = os.cpu_count() or 1
     used = cfa_oracle.threads_used(cores)
-    run = lambda: cfa_oracle.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"],
-                                         t["v_cache"], wl.ctx_len, nthreads=used)
+    run = lambda: cfa_oracle.decode_step_ex(t["x"], t["W_qkv"], t["W_o"], t["k_cache"],
+                                            t["v_cache"], list(wl.lens), rope_theta=wl.rope_theta,
+                                            nthreads=used)
     for _ in range(max(args.warmup, 0)):
         run()
     times = []
@@ -302,10 +303,16 @@ def run_ours(args):
     desc = plan.describe()
     stream = torch.cuda.current_stream(dev)
 
+    uniform = wl.ctx_lens is None and wl.rope_theta == 0.0
+
     def step(i):
         c = copies[i % len(copies)]
-        plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
-                         wl.ctx_len, outs[i % len(copies)], stream)
+        if uniform:
+            plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
+                             wl.ctx_len, outs[i % len(copies)], stream)
+        else:
+            plan.decode_step_ex(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
+                                list(wl.lens), outs[i % len(copies)], wl.rope_theta, stream)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -366,8 +373,12 @@ def run_ours(args):
             with torch.cuda.graph(g, stream=s2):
                 for k in range(len(copies)):
                     c = copies[k]
-                    plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
-                                     wl.ctx_len, outs[k], s2)
+                    if uniform:
+                        plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"],
+                                         c["v_cache"], wl.ctx_len, outs[k], s2)
+                    else:
+                        plan.decode_step_ex(c["x"], c["W_qkv"], c["W_o"], c["k_cache"],
+                                            c["v_cache"], list(wl.lens), outs[k], wl.rope_theta, s2)
         stream.wait_stream(s2)
         reps = max(1, K // len(copies))
         for _ in range(3):
@@ -385,7 +396,7 @@ def run_ours(args):
 
     # end-to-end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and uniform:
         x_host = [c["x"].cpu().pin_memory() for c in copies]
         out_host = [torch.empty(B, H, dtype=torch.bfloat16).pin_memory() for _ in copies]
 

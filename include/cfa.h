@@ -107,6 +107,27 @@ cfa_status cfa_decode_step(cfa_plan *plan, const void *x, const void *W_qkv,
                            int ctx_len, void *out, void *stream);
 
 /*
+ * The decode step with one context length per sequence and, optionally, a
+ * rotary position embedding of the new token's q and k. This widens the
+ * page's block (which names no positional encoding, §1.1) toward a
+ * Llama2-style layer:
+ *   ctx_lens   host array [B]: cached positions of sequence b before this
+ *              token, each in [0, max_ctx); row ctx_lens[b] of sequence b is
+ *              written, rows [0, ctx_lens[b]) are read.
+ *   rope_theta 0 disables the rotation; > 0 rotates dims i and i + d/2 of
+ *              q and k_new by ctx_lens[b] * rope_theta^(-2i/d) (rotate-half
+ *              form; e.g. 10000 for Llama2). Cached keys are taken as
+ *              already rotated, and the appended k row is the rotated one.
+ * Other arguments as cfa_decode_step, which equals this call with every
+ * ctx_lens[b] = ctx_len and rope_theta = 0. Errors: CFA_ERR_INVALID_ARG
+ * also for a NULL ctx_lens, a length out of range or a negative theta.
+ */
+cfa_status cfa_decode_step_ex(cfa_plan *plan, const void *x, const void *W_qkv,
+                              const void *W_o, void *k_cache, void *v_cache,
+                              const int *ctx_lens, double rope_theta, void *out,
+                              void *stream);
+
+/*
  * The same step for a caller whose token activations live in host memory:
  * copies x_host (bf16 [B, hidden]) to the plan's device staging buffer,
  * runs cfa_decode_step on `stream`, copies the result back to out_host

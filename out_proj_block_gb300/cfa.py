@@ -34,6 +34,9 @@ _lib.cfa_plan_destroy.restype = None
 _lib.cfa_plan_destroy.argtypes = [_vp]
 _lib.cfa_decode_step.restype = _i
 _lib.cfa_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp]
+_lib.cfa_decode_step_ex.restype = _i
+_lib.cfa_decode_step_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(ctypes.c_int),
+                                    ctypes.c_double, _vp, _vp]
 _lib.cfa_decode_step_host.restype = _i
 _lib.cfa_decode_step_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp]
 _lib.cfa_decode_step_noalloc.restype = _i
@@ -65,7 +68,8 @@ CFA_ERR_TIMEOUT = 4
 CFA_ERR_ALIGNMENT = 5
 
 EXPORTED_SYMBOLS = (
-    "cfa_plan_create", "cfa_plan_destroy", "cfa_decode_step", "cfa_decode_step_host",
+    "cfa_plan_create", "cfa_plan_destroy", "cfa_decode_step", "cfa_decode_step_ex",
+    "cfa_decode_step_host",
     "cfa_decode_step_noalloc",
     "cfa_plan_set_cluster_size", "cfa_plan_set_stages", "cfa_plan_set_overlap",
     "cfa_plan_cluster_size",
@@ -121,6 +125,14 @@ def cfa_plan_destroy(plan: int) -> None:
 def cfa_decode_step(plan, x, W_qkv, W_o, k_cache, v_cache, ctx_len: int, out, stream=None) -> int:
     return int(_lib.cfa_decode_step(plan, _ptr(x), _ptr(W_qkv), _ptr(W_o), _ptr(k_cache),
                                     _ptr(v_cache), int(ctx_len), _ptr(out), _stream(stream)))
+
+
+def cfa_decode_step_ex(plan, x, W_qkv, W_o, k_cache, v_cache, ctx_lens, rope_theta: float,
+                       out, stream=None) -> int:
+    lens = (ctypes.c_int * len(ctx_lens))(*[int(v) for v in ctx_lens])
+    return int(_lib.cfa_decode_step_ex(plan, _ptr(x), _ptr(W_qkv), _ptr(W_o), _ptr(k_cache),
+                                       _ptr(v_cache), lens, float(rope_theta), _ptr(out),
+                                       _stream(stream)))
 
 
 def cfa_decode_step_host(plan, x_host, W_qkv, W_o, k_cache, v_cache, ctx_len: int, out_host,
@@ -260,6 +272,18 @@ class Plan:
         st = cfa_decode_step(self.handle, x, W_qkv, W_o, k_cache, v_cache, ctx_len, out, stream)
         if st != CFA_OK:
             raise CfaError(st, "cfa_decode_step")
+        return out
+
+    def decode_step_ex(self, x, W_qkv, W_o, k_cache, v_cache, ctx_lens, out,
+                       rope_theta: float = 0.0, stream=None):
+        """Decode step with per-sequence lengths and optional rotary embedding."""
+        self._check(x, W_qkv, W_o, k_cache, v_cache, out, host_io=False)
+        if len(ctx_lens) != self.B:
+            raise ValueError("ctx_lens needs one entry per batch row")
+        st = cfa_decode_step_ex(self.handle, x, W_qkv, W_o, k_cache, v_cache, ctx_lens,
+                                rope_theta, out, stream)
+        if st != CFA_OK:
+            raise CfaError(st, "cfa_decode_step_ex")
         return out
 
     def decode_step_host(self, x_host, W_qkv, W_o, k_cache, v_cache, ctx_len: int, out_host,

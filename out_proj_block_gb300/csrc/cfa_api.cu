@@ -487,12 +487,20 @@ cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
     return CFA_OK;
 }
 
-cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const void *W_o,
-                           void *k_cache, void *v_cache, int ctx_len, void *out,
-                           void *stream) {
-    if (!pl || !x || !W_qkv || !W_o || !k_cache || !v_cache || !out)
+}  // extern "C"
+
+namespace {
+
+// The launch behind cfa_decode_step and cfa_decode_step_ex: lens[b] cached
+// positions per sequence, rope_theta > 0 enables the rotary embedding.
+cfa_status launch_step(cfa_plan *pl, const void *x, const void *W_qkv, const void *W_o,
+                       void *k_cache, void *v_cache, const int *lens, double rope_theta,
+                       void *out, void *stream) {
+    if (!pl || !x || !W_qkv || !W_o || !k_cache || !v_cache || !out || !lens)
         return fail(CFA_ERR_INVALID_ARG);
-    if (ctx_len < 0 || ctx_len >= pl->max_ctx) return fail(CFA_ERR_INVALID_ARG);
+    for (int b = 0; b < pl->B; ++b)
+        if (lens[b] < 0 || lens[b] >= pl->max_ctx) return fail(CFA_ERR_INVALID_ARG);
+    if (!(rope_theta >= 0.0) || rope_theta > 1e30) return fail(CFA_ERR_INVALID_ARG);
     if (!aligned16(x) || !aligned16(W_qkv) || !aligned16(W_o) || !aligned16(k_cache) ||
         !aligned16(v_cache) || !aligned16(out))
         return fail(CFA_ERR_ALIGNMENT);
@@ -540,7 +548,11 @@ cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const
     kp.counters = pl->words;
     kp.status = pl->words + cfa::kMaxCounters;
     kp.group_sums = pl->group_sums;
-    kp.ctx_len = ctx_len;
+    for (int b = 0; b < pl->B; ++b) kp.ctx_lens[b] = lens[b];
+    kp.rope = rope_theta > 0.0 ? 1 : 0;
+    if (kp.rope)
+        for (int i = 0; i < pl->D / 2; ++i)
+            kp.rope_inv_freq[i] = std::pow(rope_theta, -2.0 * i / pl->D);
 
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
@@ -556,6 +568,25 @@ cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const
         return fail(CFA_ERR_CUDA);
     }
     return CFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cfa_status cfa_decode_step(cfa_plan *pl, const void *x, const void *W_qkv, const void *W_o,
+                           void *k_cache, void *v_cache, int ctx_len, void *out,
+                           void *stream) {
+    if (!pl) return fail(CFA_ERR_INVALID_ARG);
+    int lens[cfa::kMaxBatch];
+    for (int b = 0; b < pl->B; ++b) lens[b] = ctx_len;
+    return launch_step(pl, x, W_qkv, W_o, k_cache, v_cache, lens, 0.0, out, stream);
+}
+
+cfa_status cfa_decode_step_ex(cfa_plan *pl, const void *x, const void *W_qkv, const void *W_o,
+                              void *k_cache, void *v_cache, const int *ctx_lens,
+                              double rope_theta, void *out, void *stream) {
+    return launch_step(pl, x, W_qkv, W_o, k_cache, v_cache, ctx_lens, rope_theta, out, stream);
 }
 
 cfa_status cfa_decode_step_host(cfa_plan *pl, const void *x_host, const void *W_qkv,
@@ -758,7 +789,8 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     kp.status = reinterpret_cast<unsigned *>(scratch) + cfa::kMaxCounters;
     kp.partials = reinterpret_cast<float *>(scratch + kNoallocWordsBytes);
     kp.group_sums = kp.partials + static_cast<size_t>(n_heads) * B * hidden;
-    kp.ctx_len = ctx_len;
+    for (int b = 0; b < B; ++b) kp.ctx_lens[b] = ctx_len;
+    kp.rope = 0;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config(&pl, kp, pl.smem_bytes, s, attr);
     void *args[4] = {&tm_wqkv, &tm_wo, &tm_x, &kp};

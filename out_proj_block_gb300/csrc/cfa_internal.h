@@ -12,6 +12,8 @@ constexpr int kThreads = kComputeThreads + 32;     // + one load-issuing warp
 constexpr int kStageBytes = 16384;                 // one pipeline stage
 constexpr int kTileCols = 64;                      // weight tile width (128 bytes of bf16)
 constexpr int kMaxCluster = 16;
+constexpr int kMaxBatch = 16;
+constexpr int kMaxRopePairs = 64;                  // head_dim / 2
 constexpr int kMaxCounters = 4096;                 // merge counters; the status word follows
 constexpr int kMmaN = 16;                          // batch rows per tensor-core MMA (zero-padded)
 constexpr int kXStageMmaBytes = 2 * kMmaN * 128;   // x per stage on the tensor-core path
@@ -39,7 +41,10 @@ struct KernelParams {
     float *group_sums;     // [ceil(nh / merge_group)][B][H] fp32 per-group sums
     unsigned *counters;    // [groups][C] then [C]: arrivals per column chunk, two levels
     unsigned *status;      // device status word
-    int B, H, nh, max_ctx, ctx_len;
+    int B, H, nh, max_ctx;
+    int ctx_lens[kMaxBatch];   // cached positions of each sequence before this token
+    int rope;                  // 1: rotate the new q and k (rotate-half form)
+    double rope_inv_freq[kMaxRopePairs];  // theta^(-2i/D), i < D/2
     int C;                 // blocks per cluster (= per head)
     int G;                 // column groups of 64 inside one head's Q/K/V block: D/64 or fewer
     int RG;                // row groups of the hidden dimension: C / G

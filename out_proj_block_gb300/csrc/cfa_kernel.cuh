@@ -206,7 +206,6 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     const int h = blockIdx.x / C;
     const int B = p.B;
     const int H = p.H;
-    const int L = p.ctx_len;
     const int NS = p.nstages;
 
     const uint32_t bar_full0 = smem_addr(smem + p.off_bars);
@@ -224,9 +223,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
 
     const int g = r % p.G;                // column group in the projection
     const int rg = r / p.G;               // row group in the projection
-    const int kv_s = static_cast<int>((static_cast<long long>(L) * r) / C);
-    const int kv_e = static_cast<int>((static_cast<long long>(L) * (r + 1)) / C);
-    const int n_kv_tiles = (kv_e - kv_s + TK - 1) / TK;
+    // Cached positions [kv_s, kv_e) of sequence b owned by this block.
+    auto kv_range = [&](int b, int &s0, int &e0) {
+        const long long Lb = p.ctx_lens[b];
+        s0 = static_cast<int>((Lb * r) / C);
+        e0 = static_cast<int>((Lb * (r + 1)) / C);
+    };
     const int col0 = r * p.ncols;
     const int n_out_tiles = p.ncols / kTileCols;
     const int qkv_payload = B * 3 * kTileCols;   // floats one block contributes
@@ -343,6 +345,9 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             // B: contiguous runs of cached K and V rows
             for (int b = 0; b < B; ++b) {
                 const size_t base = (static_cast<size_t>(b) * p.nh + h) * p.max_ctx * D;
+                int kv_s, kv_e;
+                kv_range(b, kv_s, kv_e);
+                const int n_kv_tiles = (kv_e - kv_s + TK - 1) / TK;
                 for (int t = 0; t < n_kv_tiles; ++t) {
                     const int s = acquire();
                     const uint32_t full = bar_full0 + 8u * s;
@@ -528,19 +533,36 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             qkv_full[(b * 3 + sec) * D + j] = __bfloat162float(hb);
             if (r == 0) {
                 uint16_t *cache = sec == 1 ? p.k_cache : p.v_cache;
-                cache[((static_cast<size_t>(b) * p.nh + h) * p.max_ctx + L) * D + j] =
+                cache[((static_cast<size_t>(b) * p.nh + h) * p.max_ctx + p.ctx_lens[b]) * D + j] =
                     __bfloat16_as_ushort(hb);
             }
         };
 
         // ---- X1 (q, k): the query for attention and the new key -------------
+        // With rotary embedding, dims i and i + D/2 of q and k_new are rotated
+        // by ctx_lens[b] * theta^(-2i/D) (rotate-half form); the angle is taken
+        // in fp64 and reduced to (-pi, pi] before the fp32 sine and cosine.
         mbar_wait_bounded<true>(bar_qk, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
-        for (int idx = tid; idx < B * 2 * D; idx += kComputeThreads) {
-            const int b = idx / (2 * D), rem = idx % (2 * D);
-            const int sec = rem / D, j = rem % D;
-            const float sum = gathered(b, sec, j);
-            if (sec == 0) qkv_full[b * 3 * D + j] = sum * p.qscale;
-            else append(b, 1, j, sum);
+        for (int idx = tid; idx < B * D; idx += kComputeThreads) {
+            const int b = idx / D, rem = idx % D;
+            const int sec = rem / (D / 2), i = rem % (D / 2);
+            float y0 = gathered(b, sec, i), y1 = gathered(b, sec, i + D / 2);
+            if (p.rope) {
+                const double ang = static_cast<double>(p.ctx_lens[b]) * p.rope_inv_freq[i];
+                const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+                float sn, cs;
+                sincosf(static_cast<float>(red), &sn, &cs);
+                const float x0 = y0, x1 = y1;
+                y0 = x0 * cs - x1 * sn;
+                y1 = x1 * cs + x0 * sn;
+            }
+            if (sec == 0) {
+                qkv_full[b * 3 * D + i] = y0 * p.qscale;
+                qkv_full[b * 3 * D + i + D / 2] = y1 * p.qscale;
+            } else {
+                append(b, 1, i, y0);
+                append(b, 1, i + D / 2, y1);
+            }
         }
         compute_bar<kComputeThreads>();
 
@@ -556,6 +578,9 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             float *st_l = st_m + kComputeWarps;             // [8]
             for (int b = 0; b < B; ++b) {
                 const float *qb = qkv_full + static_cast<size_t>(b) * 3 * D;
+                int kv_s, kv_e;
+                kv_range(b, kv_s, kv_e);
+                const int n_kv_tiles = (kv_e - kv_s + TK - 1) / TK;
                 float q[DPL], o[DPL];
 #pragma unroll
                 for (int v = 0; v < NV; ++v)

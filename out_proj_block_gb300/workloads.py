@@ -14,7 +14,7 @@ be filled with NaN so that a stray read shows up in the result.
 from __future__ import annotations
 
 import dataclasses
-from typing import Dict, Optional
+from typing import Dict, Optional, Tuple
 
 import torch
 
@@ -35,6 +35,12 @@ class Workload:
     spiky_frac: float = 0.0
     spiky_scale: float = 1.0
     description: str = ""
+    ctx_lens: Optional[Tuple[int, ...]] = None  # per-sequence lengths; None = ctx_len for all
+    rope_theta: float = 0.0                     # > 0: rotary embedding of the new q, k
+
+    @property
+    def lens(self) -> Tuple[int, ...]:
+        return self.ctx_lens if self.ctx_lens is not None else (self.ctx_len,) * self.B
 
     @property
     def algorithmic_bytes(self) -> int:
@@ -42,25 +48,32 @@ class Workload:
         rows that are read (the appended row, x and out are not counted)."""
         H = self.hidden
         return (2 * H * 3 * H + 2 * H * H
-                + self.B * 2 * self.n_heads * self.ctx_len * self.head_dim * 2)
+                + sum(self.lens) * 2 * self.n_heads * self.head_dim * 2)
 
     @property
     def flops(self) -> int:
         H, B = self.hidden, self.B
-        T = self.ctx_len + 1
         return (2 * B * H * 3 * H + 2 * B * H * H
-                + B * self.n_heads * T * self.head_dim * 4)
+                + sum(L + 1 for L in self.lens) * self.n_heads * self.head_dim * 4)
 
     def as_config(self) -> Dict[str, object]:
-        return {"workload": self.name, "B": self.B, "hidden": self.hidden,
-                "n_heads": self.n_heads, "head_dim": self.head_dim,
-                "ctx_len": self.ctx_len, "max_ctx": self.max_ctx}
+        cfg = {"workload": self.name, "B": self.B, "hidden": self.hidden,
+               "n_heads": self.n_heads, "head_dim": self.head_dim,
+               "ctx_len": self.ctx_len, "max_ctx": self.max_ctx}
+        if self.ctx_lens is not None:
+            cfg["ctx_lens"] = list(self.ctx_lens)
+        if self.rope_theta > 0:
+            cfg["rope_theta"] = self.rope_theta
+        return cfg
 
 
-def _wl(name, B, H, nh, d, L, desc, spiky_frac=0.0, spiky_scale=1.0, max_ctx=None):
+def _wl(name, B, H, nh, d, L, desc, spiky_frac=0.0, spiky_scale=1.0, max_ctx=None,
+        ctx_lens=None, rope_theta=0.0):
+    top = max(ctx_lens) if ctx_lens else L
     return Workload(name, B, H, nh, d, L,
-                    max_ctx if max_ctx is not None else _round_up(L + 1, 64),
-                    spiky_frac, spiky_scale, desc)
+                    max_ctx if max_ctx is not None else _round_up(top + 1, 64),
+                    spiky_frac, spiky_scale, desc,
+                    tuple(ctx_lens) if ctx_lens else None, rope_theta)
 
 
 WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
@@ -77,6 +90,12 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
         spiky_frac=0.05, spiky_scale=4.0),
     _wl("hd64_b8_ctx2k", 8, 4096, 64, 64, 2048,
         "hidden 4096, 64 heads x 64, B=8, ctx_len 2048"),
+    # Widened steps: per-sequence lengths and rotary embedding (base 10000).
+    _wl("llama7b_b1_ctx4k_rope", 1, 4096, 32, 128, 4096,
+        "Llama2-7B-shaped block, B=1, ctx_len 4096, RoPE", rope_theta=10000.0),
+    _wl("llama7b_b16_ragged_rope", 16, 4096, 32, 128, 4096,
+        "Llama2-7B-shaped block, B=16, ctx_lens 1024..6784 (step 384), RoPE",
+        ctx_lens=[1024 + 384 * i for i in range(16)], rope_theta=10000.0),
 ]}
 
 
@@ -125,7 +144,9 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu",
             for h in range(nh):
                 pos = torch.randperm(L, generator=g)[:n_spiky].to(device)
                 k_cache[b, h, pos] = k_cache[b, h, pos] * wl.spiky_scale
-    if poison_tail and L < mc:
-        k_cache[:, :, L:, :] = float("nan")
-        v_cache[:, :, L:, :] = float("nan")
+    if poison_tail:
+        for b, Lb in enumerate(wl.lens):
+            if Lb < mc:
+                k_cache[b, :, Lb:, :] = float("nan")
+                v_cache[b, :, Lb:, :] = float("nan")
     return {"x": x, "W_qkv": W_qkv, "W_o": W_o, "k_cache": k_cache, "v_cache": v_cache}

@@ -66,6 +66,7 @@ def test_plan_create_rejects_bad_shapes_on_host(lib, args, code):
 def test_null_plan_is_rejected(lib):
     assert lib._lib.cfa_decode_step(None, 16, 16, 16, 16, 16, 0, 16, None) == lib.CFA_ERR_INVALID_ARG
     assert lib._lib.cfa_decode_step_host(None, 16, 16, 16, 16, 16, 0, 16, None) == lib.CFA_ERR_INVALID_ARG
+    assert lib._lib.cfa_decode_step_ex(None, 16, 16, 16, 16, 16, None, 0.0, 16, None) == lib.CFA_ERR_INVALID_ARG
     assert lib._lib.cfa_plan_set_cluster_size(None, 2) == lib.CFA_ERR_INVALID_ARG
     assert lib._lib.cfa_plan_set_stages(None, 2) == lib.CFA_ERR_INVALID_ARG
     assert lib._lib.cfa_plan_set_overlap(None, 1) == lib.CFA_ERR_INVALID_ARG

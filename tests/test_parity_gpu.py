@@ -81,7 +81,11 @@ def run_and_check(cfa, oracle, wl, seed=1, C=None, stages=None, check_untouched=
 
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
 def test_workload_default_plan(cfa, oracle, name):
-    errs, C, _ = run_and_check(cfa, oracle, workloads.WORKLOADS[name], seed=1)
+    wl = workloads.WORKLOADS[name]
+    if wl.ctx_lens is not None or wl.rope_theta > 0:
+        run_ex_and_check(cfa, oracle, wl, list(wl.lens), wl.rope_theta, seed=1)
+        return
+    errs, C, _ = run_and_check(cfa, oracle, wl, seed=1)
     print(f"{name}: C={C} out rel {errs['out'][0]:.2e} abs {errs['out'][1]:.2e}")
 
 
@@ -245,3 +249,69 @@ def test_chained_steps_respect_dependencies(cfa, oracle, overlap):
                                  nthreads=NTHREADS)
         check_close(f"out[{k}]", outs[k].float().cpu().numpy(), ref["out"])
         check_close(f"k_new[{k}]", kc[:, :, wl.ctx_len + k].float().numpy(), ref["k_new"])
+
+
+# ------------------------------------ per-sequence lengths and rotary embedding
+
+
+def run_ex_and_check(cfa, oracle, wl, lens, theta, seed, C=None):
+    t = workloads.make_inputs(wl, seed=seed, device="cuda", poison_tail=False)
+    # rows past each sequence's own length are never read: poison them
+    for b, L in enumerate(lens):
+        t["k_cache"][b, :, L:] = float("nan")
+        t["v_cache"][b, :, L:] = float("nan")
+    k_before, v_before = t["k_cache"].clone(), t["v_cache"].clone()
+    cpu = {k: v.cpu() for k, v in t.items()}
+    out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx, cluster_size=C) as plan:
+        plan.decode_step_ex(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], lens, out,
+                            rope_theta=theta)
+        torch.cuda.synchronize()
+        assert plan.status() == cfa.CFA_OK
+    ref = oracle.decode_step_ex(cpu["x"], cpu["W_qkv"], cpu["W_o"], cpu["k_cache"],
+                                cpu["v_cache"], lens, rope_theta=theta, nthreads=NTHREADS)
+    check_close("out", out.float().cpu().numpy(), ref["out"])
+    rows_k = np.stack([t["k_cache"][b, :, L].float().cpu().numpy() for b, L in enumerate(lens)])
+    rows_v = np.stack([t["v_cache"][b, :, L].float().cpu().numpy() for b, L in enumerate(lens)])
+    check_close("k_new", rows_k, ref["k_new"])
+    check_close("v_new", rows_v, ref["v_new"])
+    for name, before, after in (("k", k_before, t["k_cache"]), ("v", v_before, t["v_cache"])):
+        b_ = before.view(torch.int16).clone()
+        a_ = after.view(torch.int16).clone()
+        for b, L in enumerate(lens):
+            b_[b, :, L] = 0
+            a_[b, :, L] = 0
+        assert torch.equal(a_, b_), f"{name}_cache changed outside the appended rows"
+
+
+@pytest.mark.parametrize("theta", [0.0, 10000.0])
+@pytest.mark.parametrize("B,lens", [(1, [300]), (3, [0, 77, 301]), (5, [5, 64, 1, 200, 63])])
+def test_ragged_lengths_and_rope(cfa, oracle, theta, B, lens):
+    wl = workloads.custom(B, 1024, 8, 128, max(lens), max_ctx=320)
+    run_ex_and_check(cfa, oracle, wl, lens, theta, seed=80 + B, C=4)
+
+
+@pytest.mark.parametrize("C", [2, 8])
+def test_rope_head_dim_64_and_long_positions(cfa, oracle, C):
+    wl = workloads.custom(4, 1024, 16, 64, 4000, max_ctx=4096)
+    run_ex_and_check(cfa, oracle, wl, [4000, 17, 2500, 4095], 10000.0, seed=90, C=C)
+
+
+def test_ex_with_equal_lengths_matches_decode_step(cfa):
+    wl = workloads.custom(2, 1024, 8, 128, 100, max_ctx=128)
+    t = workloads.make_inputs(wl, seed=91, device="cuda")
+    a = torch.empty(2, 1024, dtype=torch.bfloat16, device="cuda")
+    b = torch.empty_like(a)
+    with cfa.Plan(2, 1024, 8, 128, 128) as plan:
+        plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], 100, a)
+        plan.decode_step_ex(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], [100, 100], b)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_ex_rejects_bad_lengths(cfa):
+    with cfa.Plan(2, 512, 4, 128, 64) as plan:
+        h = plan.handle
+        assert cfa.cfa_decode_step_ex(h, 16, 16, 16, 16, 16, [3, 64], 0.0, 16) == cfa.CFA_ERR_INVALID_ARG
+        assert cfa.cfa_decode_step_ex(h, 16, 16, 16, 16, 16, [3, -1], 0.0, 16) == cfa.CFA_ERR_INVALID_ARG
+        assert cfa.cfa_decode_step_ex(h, 16, 16, 16, 16, 16, [3, 4], -1.0, 16) == cfa.CFA_ERR_INVALID_ARG
