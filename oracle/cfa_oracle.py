@@ -19,7 +19,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "cfa_oracle.c")
+_SRCS = [os.path.join(_HERE, "cfa_oracle.c"), os.path.join(_HERE, "cfa_oracle_layer.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libcfa_oracle.so")
 _lock = threading.Lock()
@@ -33,10 +33,10 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (OpenMP when the compiler has it)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(s) for s in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", *_SRCS, "-o", tmp, "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
                        capture_output=True)
@@ -72,6 +72,24 @@ def _load():
                 + [_u16p] * 5 + [_dp] * 4 + [ctypes.c_int])
             lib.cfa_oracle_rope.restype = None
             lib.cfa_oracle_rope.argtypes = [ctypes.c_int, _dp, ctypes.c_int, ctypes.c_double, _dp]
+            lib.cfa_oracle_round_bf16.restype = ctypes.c_uint16
+            lib.cfa_oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.cfa_oracle_round_bf16_array.restype = None
+            lib.cfa_oracle_round_bf16_array.argtypes = [_dp, _u16p, ctypes.c_long]
+            lib.cfa_oracle_rmsnorm.restype = None
+            lib.cfa_oracle_rmsnorm.argtypes = [ctypes.c_int, _dp, _dp, ctypes.c_double, _dp]
+            lib.cfa_oracle_silu.restype = ctypes.c_double
+            lib.cfa_oracle_silu.argtypes = [ctypes.c_double]
+            lib.cfa_oracle_rmsnorm_bf16.restype = ctypes.c_int
+            lib.cfa_oracle_rmsnorm_bf16.argtypes = [ctypes.c_int, ctypes.c_int, _u16p, _u16p,
+                                                    ctypes.c_double, _u16p]
+            lib.cfa_oracle_mlp.restype = ctypes.c_int
+            lib.cfa_oracle_mlp.argtypes = (
+                [ctypes.c_int] * 3 + [ctypes.c_double] + [_u16p] * 6 + [_dp, _u16p, ctypes.c_int])
+            lib.cfa_oracle_layer_step.restype = ctypes.c_int
+            lib.cfa_oracle_layer_step.argtypes = (
+                [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int), ctypes.c_double, ctypes.c_double]
+                + [_u16p] * 10 + [_u16p] * 4 + [_dp, _dp, ctypes.c_int])
             lib.cfa_oracle_threads.restype = ctypes.c_int
             lib.cfa_oracle_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -206,3 +224,123 @@ def decode_step_ex(x, W_qkv, W_o, k_cache, v_cache, ctx_lens, rope_theta: float 
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return {"out": out, "k_new": k_new, "v_new": v_new, "attn": attn}
+
+
+# --------------------------------------------------------------------------
+# Decoder layer stack (cfa_oracle_layer.c): RMSNorm, SwiGLU MLP, residuals.
+
+
+def _u16(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint16)
+
+
+def round_bf16(v) -> np.ndarray:
+    """Round float64 values to bf16 bit patterns, nearest-even, in one step."""
+    v = _f64(v)
+    out = np.empty(v.shape, np.uint16)
+    _load().cfa_oracle_round_bf16_array(v.ctypes.data_as(_dp), out.ctypes.data_as(_u16p), v.size)
+    return out
+
+
+def rmsnorm(x, g, eps: float) -> np.ndarray:
+    """fp64 g * x / sqrt(mean(x^2) + eps) of one vector."""
+    x, g = _f64(x), _f64(g)
+    y = np.empty_like(x)
+    _load().cfa_oracle_rmsnorm(x.shape[0], x.ctypes.data_as(_dp), g.ctypes.data_as(_dp),
+                               float(eps), y.ctypes.data_as(_dp))
+    return y
+
+
+def silu(z: float) -> float:
+    return float(_load().cfa_oracle_silu(float(z)))
+
+
+def rmsnorm_bf16(x, g, eps: float) -> np.ndarray:
+    """Row-wise bf16(rmsnorm(x[b]; g)) of bf16 inputs x [B, n], g [n]; bits out."""
+    xb, gb = _bits(x), _bits(g)
+    B, n = xb.shape
+    if gb.shape != (n,):
+        raise ValueError("norm weight must have one entry per column")
+    y = np.empty((B, n), np.uint16)
+    if _load().cfa_oracle_rmsnorm_bf16(B, n, xb.ctypes.data_as(_u16p), gb.ctypes.data_as(_u16p),
+                                       float(eps), y.ctypes.data_as(_u16p)) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return y
+
+
+def mlp(h, g, W_gate, W_up, W_down, eps: float, nthreads: int = 1):
+    """SwiGLU MLP with pre-norm and residual (see cfa_oracle_layer.c).
+
+    Returns dict(u [B, F] bits, delta [B, H] fp64, y [B, H] bits)."""
+    hb, gb, wg, wu, wd = (_bits(t) for t in (h, g, W_gate, W_up, W_down))
+    B, H = hb.shape
+    F = wg.shape[1]
+    if gb.shape != (H,) or wg.shape != (H, F) or wu.shape != (H, F) or wd.shape != (F, H):
+        raise ValueError("inconsistent shapes")
+    u = np.empty((B, F), np.uint16)
+    delta = np.empty((B, H), np.float64)
+    y = np.empty((B, H), np.uint16)
+    rc = _load().cfa_oracle_mlp(B, H, F, float(eps), hb.ctypes.data_as(_u16p),
+                                gb.ctypes.data_as(_u16p), wg.ctypes.data_as(_u16p),
+                                wu.ctypes.data_as(_u16p), wd.ctypes.data_as(_u16p),
+                                u.ctypes.data_as(_u16p), delta.ctypes.data_as(_dp),
+                                y.ctypes.data_as(_u16p), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return {"u": u, "delta": delta, "y": y}
+
+
+def layer_step(x, layer, k_cache, v_cache, ctx_lens, rope_theta: float, eps: float,
+               nthreads: int = 1):
+    """One decoder layer for one token (see cfa_oracle_layer.c).
+
+    layer: mapping with attn_norm [H], W_qkv, W_o, mlp_norm [H], W_gate, W_up,
+    W_down (bf16). Returns dict(xn, h, u, y as bits; k_new, v_new fp64)."""
+    xb = _bits(x)
+    kc, vc = _bits(k_cache), _bits(v_cache)
+    g1, wq, wo, g2, wg, wu, wd = (_bits(layer[k]) for k in (
+        "attn_norm", "W_qkv", "W_o", "mlp_norm", "W_gate", "W_up", "W_down"))
+    B, H = xb.shape
+    _, nh, max_ctx, d = kc.shape
+    F = wg.shape[1]
+    if (g1.shape != (H,) or g2.shape != (H,) or wq.shape != (H, 3 * H) or wo.shape != (H, H)
+            or wg.shape != (H, F) or wu.shape != (H, F) or wd.shape != (F, H)
+            or vc.shape != kc.shape or kc.shape[0] != B or nh * d != H):
+        raise ValueError("inconsistent shapes")
+    lens = np.ascontiguousarray(np.asarray(ctx_lens, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("ctx_lens must have one entry per batch row")
+    xn = np.empty((B, H), np.uint16)
+    hb = np.empty((B, H), np.uint16)
+    u = np.empty((B, F), np.uint16)
+    y = np.empty((B, H), np.uint16)
+    k_new = np.empty((B, nh, d), np.float64)
+    v_new = np.empty((B, nh, d), np.float64)
+    ptrs = [a.ctypes.data_as(_u16p) for a in (xb, g1, wq, wo, kc, vc, g2, wg, wu, wd)]
+    rc = _load().cfa_oracle_layer_step(
+        B, H, nh, d, F, max_ctx, lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+        float(rope_theta), float(eps), *ptrs,
+        xn.ctypes.data_as(_u16p), hb.ctypes.data_as(_u16p), u.ctypes.data_as(_u16p),
+        y.ctypes.data_as(_u16p), k_new.ctypes.data_as(_dp), v_new.ctypes.data_as(_dp),
+        int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return {"xn": xn, "h": hb, "u": u, "y": y, "k_new": k_new, "v_new": v_new}
+
+
+def stack_step(x, layers, caches, ctx_lens, rope_theta: float, eps: float, nthreads: int = 1):
+    """One token through every layer of a stack [CF §3.3, §5.1].
+
+    caches: one (k_cache, v_cache) pair of uint16 bit arrays per layer; the
+    bf16-rounded new rows are written into them at ctx_lens[b] (in place), as
+    the decode loop appends them. Returns (y bits [B, H], per-layer results)."""
+    cur = _bits(x)
+    per_layer = []
+    for layer, (kc, vc) in zip(layers, caches):
+        r = layer_step(cur, layer, kc, vc, ctx_lens, rope_theta, eps, nthreads)
+        for b, L in enumerate(ctx_lens):
+            kc[b, :, L, :] = round_bf16(r["k_new"][b])
+            vc[b, :, L, :] = round_bf16(r["v_new"][b])
+        per_layer.append(r)
+        cur = r["y"]
+    return cur, per_layer

@@ -10,6 +10,10 @@ to bf16. The long-context workload additionally multiplies 5% of the cached
 key rows of every (batch, head) by 4, at positions drawn without replacement.
 Cache rows at positions >= ctx_len are never part of the computation; they can
 be filled with NaN so that a stray read shows up in the result.
+
+Layer stacks (a decode loop over several decoder layers) add, per layer,
+RMSNorm weights 1 + N(0, 0.1) and MLP weights W_gate, W_up, W_down
+~ N(0, 0.02), all bf16, each layer with its own K/V cache.
 """
 from __future__ import annotations
 
@@ -150,3 +154,101 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu",
                 k_cache[b, :, Lb:, :] = float("nan")
                 v_cache[b, :, Lb:, :] = float("nan")
     return {"x": x, "W_qkv": W_qkv, "W_o": W_o, "k_cache": k_cache, "v_cache": v_cache}
+
+
+# --------------------------------------------------------------------------
+# Layer stacks: the decode loop over n_layers decoder layers.
+
+
+@dataclasses.dataclass(frozen=True)
+class StackWorkload:
+    name: str
+    n_layers: int
+    B: int
+    hidden: int
+    n_heads: int
+    head_dim: int
+    ffn: int
+    ctx_len: int
+    max_ctx: int
+    rope_theta: float = 10000.0
+    eps: float = 1e-5
+    description: str = ""
+
+    @property
+    def lens(self) -> Tuple[int, ...]:
+        return (self.ctx_len,) * self.B
+
+    @property
+    def layer_weight_bytes(self) -> int:
+        H, F = self.hidden, self.ffn
+        return 2 * (3 * H * H + H * H + 3 * H * F)
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Bytes one token must move from HBM: every layer's weight matrices plus
+        the cached K/V rows it reads (norm weights, activations and the appended
+        rows are not counted)."""
+        kv = sum(self.lens) * 2 * self.n_heads * self.head_dim * 2
+        return self.n_layers * (self.layer_weight_bytes + kv)
+
+    def as_config(self) -> Dict[str, object]:
+        return {"workload": self.name, "n_layers": self.n_layers, "B": self.B,
+                "hidden": self.hidden, "n_heads": self.n_heads, "head_dim": self.head_dim,
+                "ffn": self.ffn, "ctx_len": self.ctx_len, "max_ctx": self.max_ctx,
+                "rope_theta": self.rope_theta, "eps": self.eps}
+
+
+def _sw(name, n_layers, B, H, nh, d, F, L, desc, max_ctx=None, rope_theta=10000.0, eps=1e-5):
+    return StackWorkload(name, n_layers, B, H, nh, d, F, L,
+                         max_ctx if max_ctx is not None else _round_up(L + 1, 64),
+                         rope_theta, eps, desc)
+
+
+STACKS: Dict[str, StackWorkload] = {w.name: w for w in [
+    _sw("stack_tiny", 2, 1, 256, 2, 128, 512, 64,
+        "2 tiny layers: hidden 256, 2 heads x 128, ffn 512, ctx_len 64", max_ctx=128),
+    _sw("llama7b_32l_b1_ctx1k", 32, 1, 4096, 32, 128, 11008, 1024,
+        "32 Llama2-7B-shaped layers (SwiGLU MLP, ffn 11008), B=1, ctx_len 1024"),
+    _sw("llama7b_32l_b16_ctx1k", 32, 16, 4096, 32, 128, 11008, 1024,
+        "32 Llama2-7B-shaped layers (SwiGLU MLP, ffn 11008), B=16, ctx_len 1024"),
+]}
+
+
+def custom_stack(n_layers: int, B: int, hidden: int, n_heads: int, head_dim: int, ffn: int,
+                 ctx_len: int, max_ctx: Optional[int] = None, rope_theta: float = 10000.0,
+                 eps: float = 1e-5, name: str = "custom_stack") -> StackWorkload:
+    return _sw(name, n_layers, B, hidden, n_heads, head_dim, ffn, ctx_len,
+               f"{name}: {n_layers} layers, B={B}, hidden {hidden}, {n_heads}x{head_dim}, "
+               f"ffn {ffn}, ctx_len {ctx_len}", max_ctx, rope_theta, eps)
+
+
+def make_stack_inputs(wl: StackWorkload, seed: int = 0, device="cpu",
+                      poison_tail: bool = False) -> Dict[str, object]:
+    """Seeded bf16 inputs of a layer stack: x [B, H] and one dict per layer
+    (attn_norm, W_qkv, W_o, mlp_norm, W_gate, W_up, W_down, k_cache, v_cache).
+    ``poison_tail`` fills cache rows at positions >= ctx_len with NaN."""
+    device = torch.device(device)
+    B, H, nh, d, F, L, mc = (wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.ffn, wl.ctx_len,
+                             wl.max_ctx)
+    s = 7000003 * (seed + 1)
+    x = _normal((B, H), 1.0, device, s + 1)
+    layers = []
+    for l in range(wl.n_layers):
+        t = s + 100 * (l + 1)
+        layer = {
+            "attn_norm": (_normal((H,), 0.1, device, t + 1).float() + 1.0).to(torch.bfloat16),
+            "W_qkv": _normal((H, 3 * H), 0.02, device, t + 2),
+            "W_o": _normal((H, H), 0.02, device, t + 3),
+            "mlp_norm": (_normal((H,), 0.1, device, t + 4).float() + 1.0).to(torch.bfloat16),
+            "W_gate": _normal((H, F), 0.02, device, t + 5),
+            "W_up": _normal((H, F), 0.02, device, t + 6),
+            "W_down": _normal((F, H), 0.02, device, t + 7),
+            "k_cache": _normal((B, nh, mc, d), 1.0, device, t + 8),
+            "v_cache": _normal((B, nh, mc, d), 1.0, device, t + 9),
+        }
+        if poison_tail and L < mc:
+            layer["k_cache"][:, :, L:, :] = float("nan")
+            layer["v_cache"][:, :, L:, :] = float("nan")
+        layers.append(layer)
+    return {"x": x, "layers": layers}
