@@ -21,6 +21,12 @@ cpu_baseline / --impl reference = the fp64 CPU oracle on the host cores.
 Inputs live in three rotating copies (each larger than the 129 MB L2), so no
 step reads what the previous step left in L2. Multi-GPU runs are independent
 replicas (the step has no exchange between GPUs).
+
+--workload llama7b_32l_b1_ctx1k (or another layer stack) measures the decode
+loop instead: a step is one token through every layer (RMSNorm, the fused
+attention block, residual, RMSNorm + SwiGLU MLP, residual), replayed from one
+CUDA graph; its bytes are all layers' weight matrices plus the cache rows
+read (13.5 GB per token for 32 Llama2-7B layers, far above L2).
 """
 from __future__ import annotations
 
@@ -469,8 +475,239 @@ def run_ours(args):
     return 0
 
 
+# ------------------------------------------------- the decode loop (stack)
+
+
+def stack_oracle_tokens(wl, t_cpu, budget_s: float, max_tokens: int = 20):
+    """The fp64 oracle stack on all host cores, one token (every layer) at a
+    time until the budget is spent (at least one)."""
+    import numpy as np
+    import torch
+    from oracle import cfa_oracle
+    cfa_oracle.build()
+    cores = os.cpu_count() or 1
+    used = cfa_oracle.threads_used(cores)
+    caches = [(l["k_cache"].view(torch.int16).numpy().view(np.uint16).copy(),
+               l["v_cache"].view(torch.int16).numpy().view(np.uint16).copy())
+              for l in t_cpu["layers"]]
+    times, y = [], None
+    t_start = time.perf_counter()
+    while len(times) < max_tokens:
+        t0 = time.perf_counter()
+        y, _ = cfa_oracle.stack_step(t_cpu["x"], t_cpu["layers"], caches, list(wl.lens),
+                                     wl.rope_theta, wl.eps, used)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    return times, used, y
+
+
+def run_stack_reference(args, wl):
+    import torch
+    from out_proj_block_gb300 import workloads
+    t = workloads.make_stack_inputs(wl, seed=0, device="cpu")
+    budget = 1e9  # the reference arm runs exactly warmup + steps tokens
+    for _ in range(max(args.warmup, 0)):
+        stack_oracle_tokens(wl, t, 0.0, max_tokens=1)
+    t0 = time.perf_counter()
+    times, used, _ = stack_oracle_tokens(wl, t, budget, max_tokens=args.steps)
+    total = time.perf_counter() - t0
+    value = wl.algorithmic_bytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wl.as_config(), l2="host run; no GPU L2 involved"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": f"{args.steps} tokens through all {wl.n_layers} layers"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    del torch
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_stack(args, wl):
+    """The decode loop: one token through every layer per step, from a graph."""
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from out_proj_block_gb300 import build as cuda_build
+    if rank == 0 or world == 1:
+        cuda_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from out_proj_block_gb300 import cfa, workloads
+
+    t = workloads.make_stack_inputs(wl, seed=0, device=dev)
+    stack = cfa.Stack(wl.n_layers, wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.ffn, wl.max_ctx,
+                      layers=t["layers"])
+    desc = stack.describe()
+    pos = torch.tensor(list(wl.lens), dtype=torch.int32, device=dev)
+    x = t["x"]
+    out = torch.empty_like(x)
+    stream = torch.cuda.Stream(dev)
+    launches_per_token = desc["launches_per_token"]
+
+    def token(graph=True):
+        (stack.step_graph if graph else stack.step)(x, pos, out, wl.rope_theta, wl.eps,
+                                                    advance=False, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            token()
+    torch.cuda.synchronize(dev)
+    st = stack.status()
+    if st != cfa.CFA_OK:
+        raise RuntimeError(f"device status after warm-up: {cfa.cfa_status_string(st)}")
+
+    sampler = ClockSampler(local).start()
+    t_end = time.perf_counter() + args.preload_seconds
+    with torch.cuda.stream(stream):
+        while time.perf_counter() < t_end:
+            for _ in range(8):
+                token()
+            torch.cuda.synchronize(dev)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            token()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_s = e0.elapsed_time(e1) / 1e3
+    st = stack.status()
+    if st != cfa.CFA_OK:
+        raise RuntimeError(f"device status after timing: {cfa.cfa_status_string(st)}")
+    max_total_s = aggregate_max(total_s, world, dev)
+    value = whole_job_gbs(wl.algorithmic_bytes, K, world, max_total_s)
+    mean_s = total_s / K
+
+    # per-token latency with an event after every token, and eager launches
+    n_iso = min(K, 100)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for k in range(n_iso):
+            token()
+            ev[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    tok_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(n_iso)]
+    n_eager = min(K, 100)
+    with torch.cuda.stream(stream):
+        token(graph=False)
+        e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(n_eager):
+            token(graph=False)
+        e3.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_ms = e2.elapsed_time(e3) / n_eager
+
+    # end to end: pinned host x in, pinned host out back, every token
+    e2e = None
+    if not args.no_e2e:
+        x_host = x.cpu().pin_memory()
+        out_host = torch.empty(x.shape, dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(x)
+
+        def host_token():
+            with torch.cuda.stream(stream):
+                x_dev.copy_(x_host, non_blocking=True)
+                stack.step_graph(x_dev, pos, out, wl.rope_theta, wl.eps, advance=False,
+                                 stream=stream)
+                out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            host_token()
+        n_e2e = min(K, 200)
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_token()
+        e2e_s = aggregate_max(time.perf_counter() - t0, world, dev)
+        e2e = {"value": whole_job_gbs(wl.algorithmic_bytes, n_e2e, world, e2e_s), "unit": "GB/s",
+               "h2d_bytes_per_step": int(x_host.numel() * 2),
+               "d2h_bytes_per_step": int(out_host.numel() * 2),
+               "ms_per_step": e2e_s / n_e2e * 1e3, "steps": n_e2e}
+
+    peak, peak_kind = measured_peaks()
+    achieved = wl.algorithmic_bytes / mean_s / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+            "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+            "kernel": f"whole token ({launches_per_token} kernels from one graph launch)"}
+
+    cpu_base, parity = None, None
+    if rank == 0 and not args.no_cpu_baseline:
+        t_cpu = {"x": x.cpu(), "layers": [{k: v.cpu() for k, v in l.items()} for l in t["layers"]]}
+        times, used, y_ref = stack_oracle_tokens(wl, t_cpu, args.cpu_seconds)
+        tok_s = statistics.median(times)
+        cpu_base = {"value": wl.algorithmic_bytes / tok_s / 1e9, "unit": "GB/s", "cores": used,
+                    "kind": "oracle",
+                    "sample": f"{len(times)} fp64 tokens through all {wl.n_layers} layers "
+                              f"(median {tok_s * 1e3:.0f} ms per token)",
+                    "step_ms": tok_s * 1e3}
+        got = out.double().cpu().numpy()
+        ref = (np.ascontiguousarray(y_ref).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        parity = {"out_rel_l2": float(np.linalg.norm(got - ref) / np.linalg.norm(ref)),
+                  "out_max_abs": float(np.abs(got - ref).max())}
+
+    stack.close()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": max_total_s / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(wl.as_config(),
+                       l2=f"one token reads {wl.algorithmic_bytes / 1e9:.1f} GB (> 129 MB L2)",
+                       parallelism=f"replicas x{world}"),
+        "latency_us": {"graph_back_to_back_mean": mean_s * 1e6,
+                       "graph_isolated_p10": percentile(tok_ms, 0.1) * 1e3,
+                       "graph_isolated_p50": percentile(tok_ms, 0.5) * 1e3,
+                       "graph_isolated_p90": percentile(tok_ms, 0.9) * 1e3,
+                       "eager_mean": eager_ms * 1e3},
+        "roofline": roof,
+        "cpu_baseline": cpu_base,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": K * launches_per_token,
+        "parity": parity,
+        "plan": desc,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    from out_proj_block_gb300 import workloads
+    if args.workload in workloads.STACKS:
+        wl = workloads.STACKS[args.workload]
+        if args.impl == "reference":
+            world, rank, _ = dist_env()
+            return run_stack_reference(args, wl) if rank == 0 else 0
+        return run_stack(args, wl)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -211,8 +211,9 @@ cfa_status cfa_plan_describe(const cfa_plan *plan, char *buf, int len);
 /*
  * Device-side status of the plan: synchronizes the device, reads and clears
  * the status word the kernels set when a bounded wait gives up. CFA_OK when
- * nothing happened, CFA_ERR_TIMEOUT after a timed-out wait, CFA_ERR_CUDA if
- * the read itself fails.
+ * nothing happened, CFA_ERR_TIMEOUT after a timed-out wait,
+ * CFA_ERR_INVALID_ARG after a device-resident position out of range (layer
+ * stack), CFA_ERR_CUDA if the read itself fails.
  */
 cfa_status cfa_plan_status(cfa_plan *plan);
 
@@ -231,6 +232,131 @@ const char *cfa_status_string(cfa_status status);
  * limit_us must be in [1, 1<<20]. No GPU fault or hang is involved.
  */
 cfa_status cfa_selftest_wait_timeout(int limit_us, void *stream);
+
+/* ==========================================================================
+ * Decoder layers around the attention block, and the multi-layer decode loop.
+ *
+ * The page reports time per output token of a whole Llama2-7B decoder
+ * [§3.3, §5.1] but describes only the attention block of a layer (§1.1). The
+ * rest of a layer follows the Llama2 arrangement (a reading, not the page):
+ *
+ *   xn = bf16( rmsnorm(x; attn_norm) )
+ *   h  = bf16( x + attention_block(xn) )          (the fused step above)
+ *   hn = bf16( rmsnorm(h; mlp_norm) )
+ *   y  = bf16( h + (bf16(silu(hn . W_gate) * (hn . W_up))) . W_down )
+ *
+ * rmsnorm(v; g)_i = g_i v_i / sqrt(mean_j v_j^2 + eps), silu(z) = z/(1+e^-z).
+ * Same conventions as above: bf16 row-major tensors in caller-owned device
+ * memory, weights [in, out] applied as v . W, fp32 accumulation, 16-byte
+ * aligned pointers, asynchronous on `stream`, fixed-order (bitwise
+ * reproducible) reductions.
+ * ========================================================================== */
+
+typedef struct cfa_mlp cfa_mlp;     /* opaque */
+typedef struct cfa_stack cfa_stack; /* opaque */
+
+/*
+ * y[b] = bf16(g * x[b] / sqrt(mean(x[b]^2) + eps)) for b < B; x, y [B, n],
+ * g [n]. n a multiple of 8 in [8, 1<<20], B in [1, 65535], eps >= 0 finite;
+ * y must not overlap x or g. CFA_ERR_INVALID_ARG / CFA_ERR_ALIGNMENT before
+ * any launch, CFA_ERR_CUDA if the launch fails.
+ */
+cfa_status cfa_rmsnorm(int B, int n, const void *x, const void *g, float eps, void *y,
+                       void *stream);
+
+/*
+ * Plan for the MLP half of a layer at batch B: hidden a multiple of 64
+ * (<= 65536), ffn a multiple of 128 (<= 1<<18), 1 <= B <= 16
+ * (CFA_ERR_UNSUPPORTED otherwise). Allocates the [B, ffn] SwiGLU buffer, the
+ * fp32 split partials and arrival counters of its two GEMVs, and a status
+ * word. NULL on failure; cfa_last_error() says why.
+ */
+cfa_mlp *cfa_mlp_create(int B, int hidden, int ffn);
+
+/* Release the plan (synchronizes the device first). NULL is a no-op. */
+void cfa_mlp_destroy(cfa_mlp *mlp);
+
+/*
+ * y = h + down(silu(gate(hn)) * up(hn)) with hn = bf16(rmsnorm(h; norm_w)):
+ *   h, y [B, hidden]; norm_w [hidden]; W_gate, W_up [hidden, ffn];
+ *   W_down [ffn, hidden].
+ * Two kernel launches (RMSNorm + gate/up + SwiGLU; down + residual). y must
+ * not overlap h, norm_w or a weight. One plan must not run on two streams at
+ * once. Errors as cfa_rmsnorm.
+ */
+cfa_status cfa_mlp_step(cfa_mlp *mlp, const void *h, const void *norm_w, float eps,
+                        const void *W_gate, const void *W_up, const void *W_down, void *y,
+                        void *stream);
+
+/*
+ * Override the MLP kernels' occupancy (blocks per SM, 1..4) and pipeline depth
+ * (16 KB stages per block, 2..12); 0 keeps the automatic choice. For sweeps.
+ * CFA_ERR_UNSUPPORTED if it does not fit (the plan is then unchanged).
+ */
+cfa_status cfa_mlp_set_pipeline(cfa_mlp *mlp, int blocks_per_sm, int stages);
+
+/* Synchronizes, reads and clears the plan's device status word (as cfa_plan_status). */
+cfa_status cfa_mlp_status(cfa_mlp *mlp);
+
+/* One-line JSON description of the plan's two GEMVs (grid, units, stages, shared memory). */
+cfa_status cfa_mlp_describe(const cfa_mlp *mlp, char *buf, int len);
+
+/*
+ * A stack of n_layers decoder layers (shapes as cfa_plan_create and
+ * cfa_mlp_create) for the decode loop. Owns one attention plan, one MLP plan
+ * and three [B, hidden] activation buffers; the layers' weights and caches
+ * stay the caller's. NULL on failure; cfa_last_error() says why.
+ */
+cfa_stack *cfa_stack_create(int n_layers, int B, int hidden, int n_heads, int head_dim, int ffn,
+                            int max_ctx);
+
+/* Release the stack (synchronizes the device first). NULL is a no-op. */
+void cfa_stack_destroy(cfa_stack *stack);
+
+/*
+ * Bind layer `layer` (0-based) to its weights and caches: attn_norm,
+ * mlp_norm [hidden]; W_qkv [hidden, 3*hidden]; W_o [hidden, hidden]; caches
+ * [B, n_heads, max_ctx, head_dim]; W_gate, W_up [hidden, ffn]; W_down
+ * [ffn, hidden]. The pointers must stay valid while the stack is used.
+ * Rebinding a layer invalidates a recorded graph (it is recorded again on
+ * the next cfa_stack_step_graph).
+ */
+cfa_status cfa_stack_set_layer(cfa_stack *stack, int layer, const void *attn_norm,
+                               const void *W_qkv, const void *W_o, void *k_cache, void *v_cache,
+                               const void *mlp_norm, const void *W_gate, const void *W_up,
+                               const void *W_down);
+
+/*
+ * One token through every layer: x [B, hidden] in, out [B, hidden] out (x and
+ * out may be the same buffer). positions: device int [B], the cached length
+ * of every sequence, read by each layer's attention kernel on the device
+ * (so a recorded graph serves every position); each must lie in
+ * [0, max_ctx - 1]. A value outside that range is not caught on the host: the
+ * kernels flag it in the status word (cfa_stack_status then returns
+ * CFA_ERR_INVALID_ARG), read no cache rows and append nothing for that
+ * sequence. advance != 0 adds 1 to every position after the last layer (the
+ * decode loop's next token). rope_theta > 0 rotates q and the new k as in
+ * cfa_decode_step_ex; eps is the RMSNorm epsilon. All layers must be bound.
+ * 4 kernels per layer (+1 with advance).
+ */
+cfa_status cfa_stack_step(cfa_stack *stack, const void *x, int *positions, double rope_theta,
+                          float eps, int advance, void *out, void *stream);
+
+/*
+ * The same token step, recorded into a CUDA graph on the first call (and
+ * again whenever x, out, positions, rope_theta, eps, advance, the stream or a
+ * layer binding changes) and replayed with one graph launch afterwards.
+ * `stream` must not be the legacy default stream (CFA_ERR_INVALID_ARG).
+ */
+cfa_status cfa_stack_step_graph(cfa_stack *stack, const void *x, int *positions,
+                                double rope_theta, float eps, int advance, void *out,
+                                void *stream);
+
+/* Synchronizes and reads (and clears) the status of both plans of the stack. */
+cfa_status cfa_stack_status(cfa_stack *stack);
+
+/* One-line JSON description (layers, launches per token, both plans). */
+cfa_status cfa_stack_describe(const cfa_stack *stack, char *buf, int len);
 
 #ifdef __cplusplus
 }

@@ -59,6 +59,35 @@ _lib.cfa_status_string.restype = ctypes.c_char_p
 _lib.cfa_status_string.argtypes = [_i]
 _lib.cfa_selftest_wait_timeout.restype = _i
 _lib.cfa_selftest_wait_timeout.argtypes = [_i, _vp]
+_lib.cfa_rmsnorm.restype = _i
+_lib.cfa_rmsnorm.argtypes = [_i, _i, _vp, _vp, ctypes.c_float, _vp, _vp]
+_lib.cfa_mlp_create.restype = _vp
+_lib.cfa_mlp_create.argtypes = [_i, _i, _i]
+_lib.cfa_mlp_destroy.restype = None
+_lib.cfa_mlp_destroy.argtypes = [_vp]
+_lib.cfa_mlp_step.restype = _i
+_lib.cfa_mlp_step.argtypes = [_vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
+_lib.cfa_mlp_set_pipeline.restype = _i
+_lib.cfa_mlp_set_pipeline.argtypes = [_vp, _i, _i]
+_lib.cfa_mlp_status.restype = _i
+_lib.cfa_mlp_status.argtypes = [_vp]
+_lib.cfa_mlp_describe.restype = _i
+_lib.cfa_mlp_describe.argtypes = [_vp, ctypes.c_char_p, _i]
+_lib.cfa_stack_create.restype = _vp
+_lib.cfa_stack_create.argtypes = [_i] * 7
+_lib.cfa_stack_destroy.restype = None
+_lib.cfa_stack_destroy.argtypes = [_vp]
+_lib.cfa_stack_set_layer.restype = _i
+_lib.cfa_stack_set_layer.argtypes = [_vp, _i] + [_vp] * 9
+_lib.cfa_stack_step.restype = _i
+_lib.cfa_stack_step.argtypes = [_vp, _vp, _vp, ctypes.c_double, ctypes.c_float, _i, _vp, _vp]
+_lib.cfa_stack_step_graph.restype = _i
+_lib.cfa_stack_step_graph.argtypes = [_vp, _vp, _vp, ctypes.c_double, ctypes.c_float, _i, _vp,
+                                      _vp]
+_lib.cfa_stack_status.restype = _i
+_lib.cfa_stack_status.argtypes = [_vp]
+_lib.cfa_stack_describe.restype = _i
+_lib.cfa_stack_describe.argtypes = [_vp, ctypes.c_char_p, _i]
 
 CFA_OK = 0
 CFA_ERR_INVALID_ARG = 1
@@ -75,6 +104,10 @@ EXPORTED_SYMBOLS = (
     "cfa_plan_cluster_size",
     "cfa_plan_describe", "cfa_plan_status", "cfa_last_error", "cfa_status_string",
     "cfa_selftest_wait_timeout",
+    "cfa_rmsnorm", "cfa_mlp_create", "cfa_mlp_destroy", "cfa_mlp_step", "cfa_mlp_status",
+    "cfa_mlp_set_pipeline",
+    "cfa_mlp_describe", "cfa_stack_create", "cfa_stack_destroy", "cfa_stack_set_layer",
+    "cfa_stack_step", "cfa_stack_step_graph", "cfa_stack_status", "cfa_stack_describe",
 )
 
 
@@ -295,3 +328,228 @@ class Plan:
         if st != CFA_OK:
             raise CfaError(st, "cfa_decode_step_host")
         return out_host
+
+
+# ----------------------------------------------- decoder layers and the loop
+
+
+def cfa_rmsnorm(B: int, n: int, x, g, eps: float, y, stream=None) -> int:
+    return int(_lib.cfa_rmsnorm(int(B), int(n), _ptr(x), _ptr(g), float(eps), _ptr(y),
+                                _stream(stream)))
+
+
+def cfa_mlp_create(B: int, hidden: int, ffn: int) -> int:
+    h = _lib.cfa_mlp_create(B, hidden, ffn)
+    if not h:
+        raise CfaError(cfa_last_error(), "cfa_mlp_create")
+    return h
+
+
+def cfa_mlp_destroy(mlp: int) -> None:
+    _lib.cfa_mlp_destroy(mlp)
+
+
+def cfa_mlp_step(mlp, h, norm_w, eps: float, W_gate, W_up, W_down, y, stream=None) -> int:
+    return int(_lib.cfa_mlp_step(mlp, _ptr(h), _ptr(norm_w), float(eps), _ptr(W_gate),
+                                 _ptr(W_up), _ptr(W_down), _ptr(y), _stream(stream)))
+
+
+def cfa_mlp_set_pipeline(mlp, blocks_per_sm: int, stages: int) -> int:
+    return int(_lib.cfa_mlp_set_pipeline(mlp, int(blocks_per_sm), int(stages)))
+
+
+def cfa_mlp_status(mlp) -> int:
+    return int(_lib.cfa_mlp_status(mlp))
+
+
+def cfa_mlp_describe(mlp) -> dict:
+    buf = ctypes.create_string_buffer(1024)
+    st = _lib.cfa_mlp_describe(mlp, buf, len(buf))
+    if st != CFA_OK:
+        raise CfaError(st, "cfa_mlp_describe")
+    return json.loads(buf.value.decode())
+
+
+def cfa_stack_create(n_layers: int, B: int, hidden: int, n_heads: int, head_dim: int, ffn: int,
+                     max_ctx: int) -> int:
+    h = _lib.cfa_stack_create(n_layers, B, hidden, n_heads, head_dim, ffn, max_ctx)
+    if not h:
+        raise CfaError(cfa_last_error(), "cfa_stack_create")
+    return h
+
+
+def cfa_stack_destroy(stack: int) -> None:
+    _lib.cfa_stack_destroy(stack)
+
+
+def cfa_stack_set_layer(stack, layer: int, attn_norm, W_qkv, W_o, k_cache, v_cache, mlp_norm,
+                        W_gate, W_up, W_down) -> int:
+    return int(_lib.cfa_stack_set_layer(stack, int(layer), _ptr(attn_norm), _ptr(W_qkv),
+                                        _ptr(W_o), _ptr(k_cache), _ptr(v_cache), _ptr(mlp_norm),
+                                        _ptr(W_gate), _ptr(W_up), _ptr(W_down)))
+
+
+def cfa_stack_step(stack, x, positions, rope_theta: float, eps: float, advance: bool, out,
+                   stream=None) -> int:
+    return int(_lib.cfa_stack_step(stack, _ptr(x), _ptr(positions), float(rope_theta),
+                                   float(eps), 1 if advance else 0, _ptr(out), _stream(stream)))
+
+
+def cfa_stack_step_graph(stack, x, positions, rope_theta: float, eps: float, advance: bool, out,
+                         stream=None) -> int:
+    return int(_lib.cfa_stack_step_graph(stack, _ptr(x), _ptr(positions), float(rope_theta),
+                                         float(eps), 1 if advance else 0, _ptr(out),
+                                         _stream(stream)))
+
+
+def cfa_stack_status(stack) -> int:
+    return int(_lib.cfa_stack_status(stack))
+
+
+def cfa_stack_describe(stack) -> dict:
+    buf = ctypes.create_string_buffer(2048)
+    st = _lib.cfa_stack_describe(stack, buf, len(buf))
+    if st != CFA_OK:
+        raise CfaError(st, "cfa_stack_describe")
+    return json.loads(buf.value.decode())
+
+
+def _check_tensor(name, t, shape, dtype=torch.bfloat16):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on the GPU")
+
+
+def rmsnorm(x, g, eps: float, y, stream=None):
+    """y = bf16(g * x / sqrt(mean(x^2) + eps)) row by row, on the GPU."""
+    B, n = x.shape
+    _check_tensor("x", x, (B, n))
+    _check_tensor("g", g, (n,))
+    _check_tensor("y", y, (B, n))
+    st = cfa_rmsnorm(B, n, x, g, eps, y, stream)
+    if st != CFA_OK:
+        raise CfaError(st, "cfa_rmsnorm")
+    return y
+
+
+class Mlp:
+    """Owns a cfa_mlp: y = h + down(silu(gate(hn)) * up(hn)), hn = rmsnorm(h)."""
+
+    def __init__(self, B: int, hidden: int, ffn: int):
+        self.B, self.hidden, self.ffn = B, hidden, ffn
+        self.handle = cfa_mlp_create(B, hidden, ffn)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            cfa_mlp_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def describe(self) -> dict:
+        return cfa_mlp_describe(self.handle)
+
+    def set_pipeline(self, blocks_per_sm: int = 0, stages: int = 0) -> None:
+        st = cfa_mlp_set_pipeline(self.handle, blocks_per_sm, stages)
+        if st != CFA_OK:
+            raise CfaError(st, f"pipeline {blocks_per_sm} x {stages}")
+
+    def status(self) -> int:
+        return cfa_mlp_status(self.handle)
+
+    def step(self, h, norm_w, W_gate, W_up, W_down, y, eps: float = 1e-5, stream=None):
+        B, H, F = self.B, self.hidden, self.ffn
+        for name, t, shape in (("h", h, (B, H)), ("norm_w", norm_w, (H,)),
+                               ("W_gate", W_gate, (H, F)), ("W_up", W_up, (H, F)),
+                               ("W_down", W_down, (F, H)), ("y", y, (B, H))):
+            _check_tensor(name, t, shape)
+        st = cfa_mlp_step(self.handle, h, norm_w, eps, W_gate, W_up, W_down, y, stream)
+        if st != CFA_OK:
+            raise CfaError(st, "cfa_mlp_step")
+        return y
+
+
+class Stack:
+    """Owns a cfa_stack: n_layers decoder layers run token by token.
+
+    layers: sequence of mappings with attn_norm, W_qkv, W_o, k_cache, v_cache,
+    mlp_norm, W_gate, W_up, W_down (device bf16 tensors, kept referenced here
+    so they outlive the stack's use of them)."""
+
+    _KEYS = ("attn_norm", "W_qkv", "W_o", "k_cache", "v_cache", "mlp_norm", "W_gate", "W_up",
+             "W_down")
+
+    def __init__(self, n_layers: int, B: int, hidden: int, n_heads: int, head_dim: int,
+                 ffn: int, max_ctx: int, layers=None):
+        self.n_layers, self.B, self.hidden, self.n_heads, self.head_dim = (
+            n_layers, B, hidden, n_heads, head_dim)
+        self.ffn, self.max_ctx = ffn, max_ctx
+        self.handle = cfa_stack_create(n_layers, B, hidden, n_heads, head_dim, ffn, max_ctx)
+        self._layers = [None] * n_layers
+        if layers is not None:
+            for i, layer in enumerate(layers):
+                self.set_layer(i, layer)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            cfa_stack_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def describe(self) -> dict:
+        return cfa_stack_describe(self.handle)
+
+    def status(self) -> int:
+        return cfa_stack_status(self.handle)
+
+    def set_layer(self, i: int, layer) -> None:
+        B, H, nh, d, F, mc = (self.B, self.hidden, self.n_heads, self.head_dim, self.ffn,
+                              self.max_ctx)
+        shapes = {"attn_norm": (H,), "W_qkv": (H, 3 * H), "W_o": (H, H),
+                  "k_cache": (B, nh, mc, d), "v_cache": (B, nh, mc, d), "mlp_norm": (H,),
+                  "W_gate": (H, F), "W_up": (H, F), "W_down": (F, H)}
+        for k in self._KEYS:
+            _check_tensor(k, layer[k], shapes[k])
+        st = cfa_stack_set_layer(self.handle, i, *[layer[k] for k in self._KEYS])
+        if st != CFA_OK:
+            raise CfaError(st, f"cfa_stack_set_layer({i})")
+        self._layers[i] = {k: layer[k] for k in self._KEYS}
+
+    def _check_io(self, x, positions, out):
+        _check_tensor("x", x, (self.B, self.hidden))
+        _check_tensor("out", out, (self.B, self.hidden))
+        _check_tensor("positions", positions, (self.B,), torch.int32)
+
+    def step(self, x, positions, out, rope_theta: float = 10000.0, eps: float = 1e-5,
+             advance: bool = False, stream=None):
+        """One token through every layer (eager launches)."""
+        self._check_io(x, positions, out)
+        st = cfa_stack_step(self.handle, x, positions, rope_theta, eps, advance, out, stream)
+        if st != CFA_OK:
+            raise CfaError(st, "cfa_stack_step")
+        return out
+
+    def step_graph(self, x, positions, out, rope_theta: float = 10000.0, eps: float = 1e-5,
+                   advance: bool = False, stream=None):
+        """One token through every layer, recorded once into a CUDA graph and
+        replayed; `stream` must not be the legacy default stream."""
+        self._check_io(x, positions, out)
+        st = cfa_stack_step_graph(self.handle, x, positions, rope_theta, eps, advance, out,
+                                  stream)
+        if st != CFA_OK:
+            raise CfaError(st, "cfa_stack_step_graph")
+        return out

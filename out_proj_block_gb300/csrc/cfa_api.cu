@@ -491,6 +491,46 @@ cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
 
 namespace {
 
+// One launch of the fused kernel with the given tensor maps. lens (host,
+// one per sequence) or lens_dev (device-resident, read by the kernel) gives
+// the cached positions; resid (or null) is added to out.
+cfa_status launch_fused(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensorMap *tm_wo,
+                        const CUtensorMap *tm_x, const void *x, void *k_cache, void *v_cache,
+                        const int *lens, const int *lens_dev, double rope_theta,
+                        const void *resid, void *out, cudaStream_t stream) {
+    KernelParams kp = pl->kp;
+    kp.x = static_cast<const uint16_t *>(x);
+    kp.k_cache = static_cast<uint16_t *>(k_cache);
+    kp.v_cache = static_cast<uint16_t *>(v_cache);
+    kp.out = static_cast<uint16_t *>(out);
+    kp.resid = static_cast<const uint16_t *>(resid);
+    kp.lens_dev = lens_dev;
+    kp.partials = pl->partials;
+    kp.counters = pl->words;
+    kp.status = pl->words + cfa::kMaxCounters;
+    kp.group_sums = pl->group_sums;
+    for (int b = 0; b < pl->B; ++b) kp.ctx_lens[b] = lens ? lens[b] : 0;
+    kp.rope = rope_theta > 0.0 ? 1 : 0;
+    if (kp.rope)
+        for (int i = 0; i < pl->D / 2; ++i)
+            kp.rope_inv_freq[i] = std::pow(rope_theta, -2.0 * i / pl->D);
+
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config(pl, kp, pl->smem_bytes, stream, attr);
+    if (pl->overlap) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    CUtensorMap m_wqkv = *tm_wqkv, m_wo = *tm_wo, m_x = *tm_x;
+    void *args[4] = {&m_wqkv, &m_wo, &m_x, &kp};
+    if (cudaLaunchKernelExC(&cfg, pl->kernel, args) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    return CFA_OK;
+}
+
 // The launch behind cfa_decode_step and cfa_decode_step_ex: lens[b] cached
 // positions per sequence, rope_theta > 0 enables the rotary embedding.
 cfa_status launch_step(cfa_plan *pl, const void *x, const void *W_qkv, const void *W_o,
@@ -539,35 +579,8 @@ cfa_status launch_step(cfa_plan *pl, const void *x, const void *W_qkv, const voi
     }
     if (!mma) pl->tm_x = pl->tm_wqkv;  // unused by the CUDA-core path
 
-    KernelParams kp = pl->kp;
-    kp.x = static_cast<const uint16_t *>(x);
-    kp.k_cache = static_cast<uint16_t *>(k_cache);
-    kp.v_cache = static_cast<uint16_t *>(v_cache);
-    kp.out = static_cast<uint16_t *>(out);
-    kp.partials = pl->partials;
-    kp.counters = pl->words;
-    kp.status = pl->words + cfa::kMaxCounters;
-    kp.group_sums = pl->group_sums;
-    for (int b = 0; b < pl->B; ++b) kp.ctx_lens[b] = lens[b];
-    kp.rope = rope_theta > 0.0 ? 1 : 0;
-    if (kp.rope)
-        for (int i = 0; i < pl->D / 2; ++i)
-            kp.rope_inv_freq[i] = std::pow(rope_theta, -2.0 * i / pl->D);
-
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg =
-        launch_config(pl, kp, pl->smem_bytes, static_cast<cudaStream_t>(stream), attr);
-    if (pl->overlap) {
-        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[1].val.programmaticStreamSerializationAllowed = 1;
-        cfg.numAttrs = 2;
-    }
-    void *args[4] = {&pl->tm_wqkv, &pl->tm_wo, &pl->tm_x, &kp};
-    if (cudaLaunchKernelExC(&cfg, pl->kernel, args) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(CFA_ERR_CUDA);
-    }
-    return CFA_OK;
+    return launch_fused(pl, &pl->tm_wqkv, &pl->tm_wo, &pl->tm_x, x, k_cache, v_cache, lens,
+                        nullptr, rope_theta, nullptr, out, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -622,6 +635,7 @@ cfa_status cfa_plan_status(cfa_plan *pl) {
         return fail(CFA_ERR_CUDA);
     }
     if (word & cfa::kStatusTimeoutBit) return fail(CFA_ERR_TIMEOUT);
+    if (word & cfa::kStatusBadLengthBit) return fail(CFA_ERR_INVALID_ARG);
     return CFA_OK;
 }
 
@@ -800,3 +814,41 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     }
     return CFA_OK;
 }
+
+// ------------------------------------------------------------------------
+// Internal entry points for the decoder-layer stack (cfa_stack.cu).
+
+namespace cfa {
+
+cfa_status plan_encode_layer(const cfa_plan *pl, const void *W_qkv, const void *W_o,
+                             CUtensorMap *tm_wqkv, CUtensorMap *tm_wo) {
+    if (encode_w_qkv(tm_wqkv, W_qkv, pl->H, pl->kp) != CFA_OK ||
+        encode_w_o(tm_wo, W_o, pl->H, pl->D, pl->kp) != CFA_OK)
+        return CFA_ERR_CUDA;
+    return CFA_OK;
+}
+
+cfa_status plan_encode_input(const cfa_plan *pl, const void *x, CUtensorMap *tm_x) {
+    std::memset(tm_x, 0, sizeof *tm_x);  // unused by the CUDA-core path
+    if (pl->kp.n_qk > 0 && encode_x(tm_x, x, pl->B, pl->H) != CFA_OK) return CFA_ERR_CUDA;
+    return CFA_OK;
+}
+
+cfa_status plan_launch_layer(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensorMap *tm_wo,
+                             const CUtensorMap *tm_x, const void *x, void *k_cache,
+                             void *v_cache, const int *lens_dev, double rope_theta,
+                             const void *resid, void *out, cudaStream_t stream) {
+    return launch_fused(pl, tm_wqkv, tm_wo, tm_x, x, k_cache, v_cache, nullptr, lens_dev,
+                        rope_theta, resid, out, stream);
+}
+
+unsigned *plan_status_word(cfa_plan *pl) { return pl->words + kMaxCounters; }
+
+cfa_status encode_bf16_2d(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t rows,
+                          uint32_t box_cols, uint32_t box_rows) {
+    return encode_2d(tm, base, cols, rows, box_cols, box_rows, false);
+}
+
+cfa_status set_last_error(cfa_status s) { return fail(s); }
+
+}  // namespace cfa

@@ -1,0 +1,25 @@
+// Instantiations of the decoder-layer kernels around the attention block.
+#include "cfa_gemv.cuh"
+
+namespace cfa {
+
+const void *gemv_kernel(int mode, int maxb) {
+#define CFA_GEMV_CASES(M)                                                                   \
+    switch (maxb) {                                                                         \
+        case 1: return reinterpret_cast<const void *>(&gemv_streamk_kernel<1, M>);          \
+        case 2: return reinterpret_cast<const void *>(&gemv_streamk_kernel<2, M>);          \
+        case 4: return reinterpret_cast<const void *>(&gemv_streamk_kernel<4, M>);          \
+        case 8: return reinterpret_cast<const void *>(&gemv_streamk_kernel<8, M>);          \
+        case 16: return reinterpret_cast<const void *>(&gemv_streamk_kernel<16, M>);        \
+        default: return nullptr;                                                            \
+    }
+    if (mode == kGemvSwiGLU) { CFA_GEMV_CASES(kGemvSwiGLU) }
+    if (mode == kGemvResidual) { CFA_GEMV_CASES(kGemvResidual) }
+#undef CFA_GEMV_CASES
+    return nullptr;
+}
+
+const void *rmsnorm_kernel_ptr() { return reinterpret_cast<const void *>(&rmsnorm_kernel); }
+const void *advance_kernel_ptr() { return reinterpret_cast<const void *>(&advance_positions_kernel); }
+
+}  // namespace cfa

@@ -1,0 +1,35 @@
+// cfa_host.h -- host-side declarations shared between the translation units of
+// the library (not part of the public ABI, which is include/cfa.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "cfa.h"
+
+namespace cfa {
+
+// Kernel entry points (cfa_gemv.cu).
+const void *gemv_kernel(int mode, int maxb);
+const void *rmsnorm_kernel_ptr();
+const void *advance_kernel_ptr();
+
+// The attention plan, seen from the layer stack (cfa_api.cu).
+cfa_status plan_encode_layer(const cfa_plan *pl, const void *W_qkv, const void *W_o,
+                             CUtensorMap *tm_wqkv, CUtensorMap *tm_wo);
+cfa_status plan_encode_input(const cfa_plan *pl, const void *x, CUtensorMap *tm_x);
+cfa_status plan_launch_layer(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensorMap *tm_wo,
+                             const CUtensorMap *tm_x, const void *x, void *k_cache,
+                             void *v_cache, const int *lens_dev, double rope_theta,
+                             const void *resid, void *out, cudaStream_t stream);
+unsigned *plan_status_word(cfa_plan *pl);
+
+// Tensor map of a row-major bf16 matrix [rows][cols] with [box_rows x
+// box_cols] boxes, no swizzle (cfa_api.cu).
+cfa_status encode_bf16_2d(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t rows,
+                          uint32_t box_cols, uint32_t box_rows);
+
+// Records s as the calling thread's last error and returns it.
+cfa_status set_last_error(cfa_status s);
+
+}  // namespace cfa

@@ -11,6 +11,8 @@ constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kThreads = kComputeThreads + 32;     // + one load-issuing warp
 constexpr int kStageBytes = 16384;                 // one pipeline stage
 constexpr int kTileCols = 64;                      // weight tile width (128 bytes of bf16)
+constexpr int kGemvTileCols = 128;                 // stream-K GEMV tile width (256 bytes)
+constexpr int kGemvThreads = kComputeThreads + 64; // GEMV block: + load warp + epilogue warp
 constexpr int kMaxCluster = 16;
 constexpr int kMaxBatch = 16;
 constexpr int kMaxRopePairs = 64;                  // head_dim / 2
@@ -20,6 +22,7 @@ constexpr int kXStageMmaBytes = 2 * kMmaN * 128;   // x per stage on the tensor-
 
 // Status word bits, written by kernels and read by cfa_plan_status.
 constexpr unsigned kStatusTimeoutBit = 1u;
+constexpr unsigned kStatusBadLengthBit = 2u;  // a device-resident length was out of range
 constexpr unsigned kStatusSiteShift = 8;  // site code of the first timeout
 
 // Site codes recorded with a timeout in the status word.
@@ -37,6 +40,9 @@ struct KernelParams {
     uint16_t *k_cache;     // [B][nh][max_ctx][D] bf16
     uint16_t *v_cache;
     uint16_t *out;         // [B][H] bf16
+    const uint16_t *resid; // [B][H] bf16 added to out before rounding, or null
+    const int *lens_dev;   // [B] device-resident ctx_lens (read after the grid dependency
+                           // wait), or null to use ctx_lens below
     float *partials;       // [nh][B][H] fp32 per-head output-projection partials
     float *group_sums;     // [ceil(nh / merge_group)][B][H] fp32 per-group sums
     unsigned *counters;    // [groups][C] then [C]: arrivals per column chunk, two levels
@@ -60,6 +66,37 @@ struct KernelParams {
         off_bars;
     unsigned long long timeout_ns;
     float qscale;          // log2(e) / sqrt(D)
+};
+
+// ------------------------------------------------------------ stream-K GEMV
+// y[b, n] = epilogue( sum_k in[b, k] W[k, n] ) over 128-column tiles, with the
+// (tile, row-chunk) units of work split evenly over a persistent grid.
+
+enum GemvMode : int {
+    kGemvSwiGLU = 0,    // two matrices (gate, up), RMSNorm of the input, silu(gate) * up
+    kGemvResidual = 1,  // one matrix, residual added
+};
+
+struct GemvParams {
+    const uint16_t *x;       // [B][K] bf16 input rows
+    const uint16_t *norm_w;  // [K] bf16 RMSNorm weight (SwiGLU mode)
+    const uint16_t *resid;   // [B][N] bf16 residual (residual mode)
+    uint16_t *y;             // [B][N] bf16 output
+    float *partials;         // [nblocks][max_tiles][B][nmat * 128] fp32 tile partials
+    unsigned *counters;      // [n_tiles] arrivals per tile
+    unsigned *status;        // device status word
+    int B, K, N;
+    int rows;                // weight rows per unit (and per stage): 32 (two matrices) or 64
+    int chunks;              // units per tile: K / rows
+    int n_tiles;             // N / 128
+    int units;               // n_tiles * chunks
+    int nblocks;             // grid size
+    int max_tiles;           // tiles one block can touch
+    int nstages;
+    int xstage_bytes;        // bytes of one x (+ norm weight) stage
+    int off_xring, off_xn, off_scratch, off_tile, off_misc, off_bars;
+    float eps;
+    unsigned long long timeout_ns;
 };
 
 }  // namespace cfa

@@ -1,0 +1,714 @@
+// cfa_stack.cu -- host side of the decoder layer around the fused attention
+// block: RMSNorm, the SwiGLU MLP (two stream-K GEMV launches), and the
+// multi-layer decode loop, launched eagerly or recorded once into a CUDA graph
+// and replayed token after token.
+//
+// Cited page: "ClusterFusion框架解析：LLM推理优化的集群通信革命" (ClusterFusion
+// framework analysis), written [CF §n]: the page reports time per output
+// token of a whole Llama2-7B decoder [CF §3.3, §5.1]; a layer here is its
+// fused attention block plus the Llama2-arrangement norms, residuals and MLP.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "cfa.h"
+#include "cfa_host.h"
+#include "cfa_internal.h"
+
+using cfa::GemvParams;
+
+namespace {
+
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per device-side wait
+constexpr int kMaxGemvStages = 12;
+
+cfa_status fail(cfa_status s) { return cfa::set_last_error(s); }
+
+int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+struct Device {
+    int id = -1, sms = 0, smem_per_sm = 0, smem_optin = 0, smem_reserved = 0;
+};
+
+cfa_status query_device(Device *d) {
+    int major = 0, minor = 0;
+    if (cudaGetDevice(&d->id) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d->id) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d->id) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, d->id) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                               d->id) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d->id) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d->smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock,
+                               d->id) != cudaSuccess) {
+        cudaGetLastError();
+        return CFA_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return CFA_ERR_UNSUPPORTED;  // built for sm_103a only
+    return CFA_OK;
+}
+
+// Launch with programmatic dependent launch allowed (the kernels wait for
+// their predecessor before reading its output).
+cfa_status launch_pdl(const void *kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      void **args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
+        cudaGetLastError();
+        return CFA_ERR_CUDA;
+    }
+    return CFA_OK;
+}
+
+cfa_status launch_rmsnorm(int B, int n, const void *x, const void *g, float eps, void *y,
+                          cudaStream_t stream) {
+    const uint16_t *xp = static_cast<const uint16_t *>(x);
+    const uint16_t *gp = static_cast<const uint16_t *>(g);
+    uint16_t *yp = static_cast<uint16_t *>(y);
+    void *args[5] = {&xp, &gp, &yp, &n, &eps};
+    return launch_pdl(cfa::rmsnorm_kernel_ptr(), dim3(B), dim3(256), 0, stream, args);
+}
+
+// ------------------------------------------------------------ stream-K GEMV plan
+
+struct GemvPlan {
+    GemvParams gp{};
+    const void *kernel = nullptr;
+    int smem = 0;
+    size_t partial_floats = 0;
+};
+
+// Shared-memory layout, pipeline depth and grid of one stream-K GEMV.
+// bps_req / ns_req > 0 ask for that many blocks per SM / stages.
+cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan *out,
+                     int bps_req = 0, int ns_req = 0) {
+    const bool dual = mode == cfa::kGemvSwiGLU;
+    const int TW = cfa::kGemvTileCols;
+    const int R = dual ? 32 : 64;  // 16 KB of weights per unit either way
+    if (K < R || K % R || N < TW || N % TW) return CFA_ERR_UNSUPPORTED;
+    int maxb = 1;
+    while (maxb < B) maxb <<= 1;
+    const void *kernel = cfa::gemv_kernel(mode, maxb);
+    if (!kernel) return CFA_ERR_UNSUPPORTED;
+    const int NW = (dual ? 2 : 1) * TW;
+
+    GemvParams p{};
+    p.B = B;
+    p.K = K;
+    p.N = N;
+    p.rows = R;
+    p.chunks = K / R;
+    p.n_tiles = N / TW;
+    p.units = p.n_tiles * p.chunks;
+    p.xstage_bytes = align_up(B * R * 2 + (dual ? R * 2 : 0), 128);
+    // per-warp normalized input rows: 8 warps x [B][R/4] floats
+    const int xn = dual ? align_up(cfa::kComputeWarps * B * (R / 4) * 4, 128) : 0;
+    const int scratch = align_up(cfa::kComputeWarps * B * cfa::kTileCols * 4, 128);
+    const int tile = align_up(2 * B * NW * 4, 128);  // two tile buffers
+    const int misc = 128;
+    const int fixed = xn + scratch + tile + misc + 1024;  // + barriers, flags, slack
+    const int per_stage = cfa::kStageBytes + p.xstage_bytes + 16;
+    // Two blocks per SM with at least 4 stages each, else one deeper block.
+    int bps = 2, NS = 0;
+    for (; bps >= 1; --bps) {
+        const int budget = std::min(dev.smem_optin, dev.smem_per_sm / bps - dev.smem_reserved);
+        NS = std::min(kMaxGemvStages, (budget - fixed) / per_stage);
+        if (NS >= (bps == 2 ? 4 : 2)) break;
+    }
+    if (bps_req > 0) {
+        bps = bps_req;
+        const int budget = std::min(dev.smem_optin, dev.smem_per_sm / bps - dev.smem_reserved);
+        NS = std::min(kMaxGemvStages, (budget - fixed) / per_stage);
+    }
+    if (ns_req > 0) {
+        if (ns_req > NS) return CFA_ERR_UNSUPPORTED;  // does not fit at this occupancy
+        NS = ns_req;
+    }
+    if (bps < 1 || NS < 2) return CFA_ERR_UNSUPPORTED;
+    int off = NS * cfa::kStageBytes;
+    p.off_xring = off;
+    off += NS * p.xstage_bytes;
+    p.off_xn = off;
+    off += xn;
+    p.off_scratch = off;
+    off += scratch;
+    p.off_tile = off;
+    off += tile;
+    p.off_misc = off;
+    off += misc;
+    p.off_bars = off;
+    off += 16 * NS + 32 + 16;  // stage barriers, tile barriers, flags
+    if (off > dev.smem_optin) return CFA_ERR_UNSUPPORTED;
+    p.nstages = NS;
+    p.timeout_ns = kTimeoutNs;
+
+    // The attribute is per kernel and shared by every plan: set the device limit.
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dev.smem_optin) != cudaSuccess) {
+        cudaGetLastError();
+        return CFA_ERR_CUDA;
+    }
+    int resident = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, cfa::kGemvThreads, off) !=
+            cudaSuccess ||
+        resident < 1) {
+        cudaGetLastError();
+        return CFA_ERR_UNSUPPORTED;
+    }
+    // One persistent wave; every block owns an equal share of the units.
+    p.nblocks = std::min(p.units, dev.sms * std::min(resident, bps));
+    const int per_block = (p.units + p.nblocks - 1) / p.nblocks;
+    p.max_tiles = (per_block + p.chunks - 1) / p.chunks + 1;
+    out->gp = p;
+    out->kernel = kernel;
+    out->smem = off;
+    out->partial_floats = static_cast<size_t>(p.nblocks) * p.max_tiles * B * NW;
+    return CFA_OK;
+}
+
+cfa_status launch_gemv(const GemvPlan &g, const GemvParams &p, const CUtensorMap *w0,
+                       const CUtensorMap *w1, const CUtensorMap *x, cudaStream_t stream) {
+    CUtensorMap m0 = *w0, m1 = *w1, mx = *x;
+    GemvParams pp = p;
+    void *args[4] = {&m0, &m1, &mx, &pp};
+    return launch_pdl(g.kernel, dim3(p.nblocks), dim3(cfa::kGemvThreads), static_cast<size_t>(g.smem),
+                      stream, args);
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------- MLP
+
+struct cfa_mlp {
+    int B = 0, H = 0, F = 0;
+    Device dev;
+    GemvPlan gu, dn;              // gate/up (+ norm, SwiGLU) and down (+ residual)
+    uint16_t *u = nullptr;        // [B][F] SwiGLU output
+    float *partials = nullptr;    // gate/up partials, then down partials
+    size_t partial_cap = 0;       // floats allocated
+    unsigned *words = nullptr;    // gate/up counters, down counters, status word
+    CUtensorMap tm_u;             // down projection's input rows
+    // tensor maps cached by source pointer for cfa_mlp_step
+    CUtensorMap tm_wg, tm_wu, tm_wd, tm_h;
+    const void *src_wg = nullptr, *src_wu = nullptr, *src_wd = nullptr, *src_h = nullptr;
+};
+
+namespace {
+
+unsigned *mlp_status_word(cfa_mlp *m) {
+    return m->words + m->gu.gp.n_tiles + m->dn.gp.n_tiles;
+}
+
+cfa_status mlp_encode_weights(const cfa_mlp *m, const void *W_gate, const void *W_up,
+                              const void *W_down, CUtensorMap *wg, CUtensorMap *wu,
+                              CUtensorMap *wd) {
+    const uint32_t tw = cfa::kGemvTileCols;
+    if (cfa::encode_bf16_2d(wg, W_gate, m->F, m->H, tw, m->gu.gp.rows) != CFA_OK ||
+        cfa::encode_bf16_2d(wu, W_up, m->F, m->H, tw, m->gu.gp.rows) != CFA_OK ||
+        cfa::encode_bf16_2d(wd, W_down, m->H, m->F, tw, m->dn.gp.rows) != CFA_OK)
+        return CFA_ERR_CUDA;
+    return CFA_OK;
+}
+
+cfa_status mlp_encode_input(const cfa_mlp *m, const void *h, CUtensorMap *tm) {
+    return cfa::encode_bf16_2d(tm, h, m->H, m->B, m->gu.gp.rows, m->B);
+}
+
+// y = h + down(silu(gate(hn)) * up(hn)), hn = bf16(rmsnorm(h; norm_w)).
+cfa_status mlp_launch(cfa_mlp *m, const CUtensorMap *wg, const CUtensorMap *wu,
+                      const CUtensorMap *wd, const CUtensorMap *th, const void *h,
+                      const void *norm_w, float eps, void *y, cudaStream_t stream) {
+    unsigned *status = mlp_status_word(m);
+    GemvParams a = m->gu.gp;
+    a.x = static_cast<const uint16_t *>(h);
+    a.norm_w = static_cast<const uint16_t *>(norm_w);
+    a.y = m->u;
+    a.partials = m->partials;
+    a.counters = m->words;
+    a.status = status;
+    a.eps = eps;
+    cfa_status st = launch_gemv(m->gu, a, wg, wu, th, stream);
+    if (st != CFA_OK) return st;
+    GemvParams d = m->dn.gp;
+    d.x = m->u;
+    d.resid = static_cast<const uint16_t *>(h);
+    d.y = static_cast<uint16_t *>(y);
+    d.partials = m->partials + m->gu.partial_floats;
+    d.counters = m->words + m->gu.gp.n_tiles;
+    d.status = status;
+    return launch_gemv(m->dn, d, wd, wd, &m->tm_u, stream);
+}
+
+void mlp_free(cfa_mlp *m) {
+    if (m->u) cudaFree(m->u);
+    if (m->partials) cudaFree(m->partials);
+    if (m->words) cudaFree(m->words);
+    m->u = nullptr;
+    m->partials = nullptr;
+    m->words = nullptr;
+}
+
+// Reads and clears a device status word (synchronizes the device).
+cfa_status read_status(unsigned *word) {
+    unsigned v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(word, 0, sizeof v) != cudaSuccess) {
+        cudaGetLastError();
+        return CFA_ERR_CUDA;
+    }
+    if (v & cfa::kStatusTimeoutBit) return CFA_ERR_TIMEOUT;
+    if (v & cfa::kStatusBadLengthBit) return CFA_ERR_INVALID_ARG;
+    return CFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cfa_status cfa_rmsnorm(int B, int n, const void *x, const void *g, float eps, void *y,
+                       void *stream) {
+    if (B < 1 || B > 65535 || n < 8 || n % 8 || n > (1 << 20) || !x || !g || !y ||
+        !(eps >= 0.0f) || !std::isfinite(eps))
+        return fail(CFA_ERR_INVALID_ARG);
+    if (!aligned16(x) || !aligned16(g) || !aligned16(y)) return fail(CFA_ERR_ALIGNMENT);
+    const size_t rows = 2u * static_cast<size_t>(B) * n;
+    if (overlaps(y, rows, x, rows) || overlaps(y, rows, g, 2u * n)) return fail(CFA_ERR_INVALID_ARG);
+    const cfa_status st = launch_rmsnorm(B, n, x, g, eps, y, static_cast<cudaStream_t>(stream));
+    return st == CFA_OK ? CFA_OK : fail(st);
+}
+
+cfa_mlp *cfa_mlp_create(int B, int hidden, int ffn) {
+    if (B < 1 || hidden < 1 || ffn < 1) {
+        fail(CFA_ERR_INVALID_ARG);
+        return nullptr;
+    }
+    if (B > cfa::kMaxBatch || hidden % 128 || hidden > (1 << 16) || ffn % 128 || ffn > (1 << 18)) {
+        fail(CFA_ERR_UNSUPPORTED);
+        return nullptr;
+    }
+    Device dev;
+    cfa_status st = query_device(&dev);
+    if (st != CFA_OK) {
+        fail(st);
+        return nullptr;
+    }
+    cfa_mlp *m = new (std::nothrow) cfa_mlp();
+    if (!m) {
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    m->B = B;
+    m->H = hidden;
+    m->F = ffn;
+    m->dev = dev;
+    if ((st = make_gemv(dev, cfa::kGemvSwiGLU, B, hidden, ffn, &m->gu)) != CFA_OK ||
+        (st = make_gemv(dev, cfa::kGemvResidual, B, ffn, hidden, &m->dn)) != CFA_OK) {
+        delete m;
+        fail(st);
+        return nullptr;
+    }
+    const size_t nwords = static_cast<size_t>(m->gu.gp.n_tiles + m->dn.gp.n_tiles + 1);
+    m->partial_cap = m->gu.partial_floats + m->dn.partial_floats;
+    if (cudaMalloc(&m->u, 2u * static_cast<size_t>(B) * ffn) != cudaSuccess ||
+        cudaMalloc(&m->partials, sizeof(float) * m->partial_cap) != cudaSuccess ||
+        cudaMalloc(&m->words, sizeof(unsigned) * nwords) != cudaSuccess ||
+        cudaMemset(m->words, 0, sizeof(unsigned) * nwords) != cudaSuccess) {
+        cudaGetLastError();
+        mlp_free(m);
+        delete m;
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    if (cfa::encode_bf16_2d(&m->tm_u, m->u, ffn, B, m->dn.gp.rows, B) != CFA_OK) {
+        mlp_free(m);
+        delete m;
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    return m;
+}
+
+void cfa_mlp_destroy(cfa_mlp *m) {
+    if (!m) return;
+    cudaDeviceSynchronize();
+    mlp_free(m);
+    delete m;
+}
+
+cfa_status cfa_mlp_step(cfa_mlp *m, const void *h, const void *norm_w, float eps,
+                        const void *W_gate, const void *W_up, const void *W_down, void *y,
+                        void *stream) {
+    if (!m || !h || !norm_w || !W_gate || !W_up || !W_down || !y || !(eps >= 0.0f) ||
+        !std::isfinite(eps))
+        return fail(CFA_ERR_INVALID_ARG);
+    if (!aligned16(h) || !aligned16(norm_w) || !aligned16(W_gate) || !aligned16(W_up) ||
+        !aligned16(W_down) || !aligned16(y))
+        return fail(CFA_ERR_ALIGNMENT);
+    const size_t act = 2u * static_cast<size_t>(m->B) * m->H;
+    const size_t w = 2u * static_cast<size_t>(m->H) * m->F;
+    if (overlaps(y, act, h, act) || overlaps(y, act, norm_w, 2u * m->H) ||
+        overlaps(y, act, W_gate, w) || overlaps(y, act, W_up, w) || overlaps(y, act, W_down, w))
+        return fail(CFA_ERR_INVALID_ARG);
+    if (m->src_wg != W_gate || m->src_wu != W_up || m->src_wd != W_down) {
+        m->src_wg = m->src_wu = m->src_wd = nullptr;
+        if (mlp_encode_weights(m, W_gate, W_up, W_down, &m->tm_wg, &m->tm_wu, &m->tm_wd) != CFA_OK)
+            return fail(CFA_ERR_CUDA);
+        m->src_wg = W_gate;
+        m->src_wu = W_up;
+        m->src_wd = W_down;
+    }
+    if (m->src_h != h) {
+        m->src_h = nullptr;
+        if (mlp_encode_input(m, h, &m->tm_h) != CFA_OK) return fail(CFA_ERR_CUDA);
+        m->src_h = h;
+    }
+    const cfa_status st = mlp_launch(m, &m->tm_wg, &m->tm_wu, &m->tm_wd, &m->tm_h, h, norm_w, eps,
+                                     y, static_cast<cudaStream_t>(stream));
+    return st == CFA_OK ? CFA_OK : fail(st);
+}
+
+cfa_status cfa_mlp_set_pipeline(cfa_mlp *m, int blocks_per_sm, int stages) {
+    if (!m || blocks_per_sm < 0 || blocks_per_sm > 4 || stages < 0 || stages > kMaxGemvStages)
+        return fail(CFA_ERR_INVALID_ARG);
+    GemvPlan gu, dn;
+    cfa_status st = make_gemv(m->dev, cfa::kGemvSwiGLU, m->B, m->H, m->F, &gu, blocks_per_sm, stages);
+    if (st == CFA_OK)
+        st = make_gemv(m->dev, cfa::kGemvResidual, m->B, m->F, m->H, &dn, blocks_per_sm, stages);
+    if (st != CFA_OK) return fail(st);  // the plan is unchanged
+    const size_t need = gu.partial_floats + dn.partial_floats;
+    if (need > m->partial_cap) {
+        float *p = nullptr;
+        if (cudaDeviceSynchronize() != cudaSuccess || cudaMalloc(&p, sizeof(float) * need) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(CFA_ERR_CUDA);
+        }
+        cudaFree(m->partials);
+        m->partials = p;
+        m->partial_cap = need;
+    }
+    // the counters keep their size: the tile counts do not depend on the pipeline
+    m->gu = gu;
+    m->dn = dn;
+    return CFA_OK;
+}
+
+cfa_status cfa_mlp_status(cfa_mlp *m) {
+    if (!m) return fail(CFA_ERR_INVALID_ARG);
+    const cfa_status st = read_status(mlp_status_word(m));
+    return st == CFA_OK ? CFA_OK : fail(st);
+}
+
+cfa_status cfa_mlp_describe(const cfa_mlp *m, char *buf, int len) {
+    if (!m || !buf || len < 1) return fail(CFA_ERR_INVALID_ARG);
+    const GemvParams &a = m->gu.gp, &d = m->dn.gp;
+    std::snprintf(buf, static_cast<size_t>(len),
+                  "{\"B\": %d, \"hidden\": %d, \"ffn\": %d, "
+                  "\"gate_up\": {\"grid\": %d, \"units\": %d, \"rows_per_unit\": %d, "
+                  "\"stages\": %d, \"smem_bytes\": %d}, "
+                  "\"down\": {\"grid\": %d, \"units\": %d, \"rows_per_unit\": %d, "
+                  "\"stages\": %d, \"smem_bytes\": %d}}",
+                  m->B, m->H, m->F, a.nblocks, a.units, a.rows, a.nstages, m->gu.smem, d.nblocks,
+                  d.units, d.rows, d.nstages, m->dn.smem);
+    return CFA_OK;
+}
+
+}  // extern "C"
+
+// --------------------------------------------------------------------- stack
+
+namespace {
+
+struct StackLayer {
+    const void *attn_norm = nullptr, *W_qkv = nullptr, *W_o = nullptr;
+    const void *mlp_norm = nullptr, *W_gate = nullptr, *W_up = nullptr, *W_down = nullptr;
+    void *k_cache = nullptr, *v_cache = nullptr;
+    CUtensorMap tm_wqkv, tm_wo, tm_wg, tm_wu, tm_wd;
+    bool set = false;
+};
+
+struct GraphKey {
+    const void *x = nullptr;
+    void *out = nullptr;
+    int *pos = nullptr;
+    double theta = 0.0;
+    float eps = 0.0f;
+    int advance = 0;
+    cudaStream_t stream = nullptr;
+    unsigned version = 0;
+    bool operator==(const GraphKey &o) const {
+        return x == o.x && out == o.out && pos == o.pos && theta == o.theta && eps == o.eps &&
+               advance == o.advance && stream == o.stream && version == o.version;
+    }
+};
+
+}  // namespace
+
+struct cfa_stack {
+    int L = 0, B = 0, H = 0, nh = 0, D = 0, F = 0, max_ctx = 0;
+    cfa_plan *attn = nullptr;
+    cfa_mlp *mlp = nullptr;
+    std::vector<StackLayer> layers;
+    uint16_t *xn = nullptr;   // [B][H] normalized attention input
+    uint16_t *h = nullptr;    // [B][H] residual stream after attention
+    uint16_t *xr = nullptr;   // [B][H] residual stream between layers
+    CUtensorMap tm_xn, tm_h;
+    unsigned version = 1;     // bumped whenever a layer changes
+    cudaGraphExec_t exec = nullptr;
+    GraphKey key;
+};
+
+namespace {
+
+void stack_free(cfa_stack *s) {
+    if (s->exec) cudaGraphExecDestroy(s->exec);
+    s->exec = nullptr;
+    if (s->attn) cfa_plan_destroy(s->attn);
+    if (s->mlp) cfa_mlp_destroy(s->mlp);
+    s->attn = nullptr;
+    s->mlp = nullptr;
+    if (s->xn) cudaFree(s->xn);
+    if (s->h) cudaFree(s->h);
+    if (s->xr) cudaFree(s->xr);
+    s->xn = s->h = s->xr = nullptr;
+}
+
+cfa_status stack_check(const cfa_stack *s, const void *x, int *positions, double rope_theta,
+                       float eps, void *out) {
+    if (!s || !x || !positions || !out || !(eps >= 0.0f) || !std::isfinite(eps) ||
+        !(rope_theta >= 0.0) || rope_theta > 1e30)
+        return CFA_ERR_INVALID_ARG;
+    for (const StackLayer &l : s->layers)
+        if (!l.set) return CFA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(positions) & 3u))
+        return CFA_ERR_ALIGNMENT;
+    const size_t act = 2u * static_cast<size_t>(s->B) * s->H;
+    if (overlaps(positions, sizeof(int) * s->B, out, act) ||
+        overlaps(positions, sizeof(int) * s->B, x, act))
+        return CFA_ERR_INVALID_ARG;
+    return CFA_OK;
+}
+
+// Every kernel of one token, in stream order. x and out may be the same
+// buffer: x is consumed by the first layer before the last layer writes out.
+cfa_status stack_enqueue(cfa_stack *s, const void *x, int *positions, double rope_theta, float eps,
+                         int advance, void *out, cudaStream_t stream) {
+    const void *cur = x;
+    for (int l = 0; l < s->L; ++l) {
+        const StackLayer &ly = s->layers[l];
+        cfa_status st = launch_rmsnorm(s->B, s->H, cur, ly.attn_norm, eps, s->xn, stream);
+        if (st != CFA_OK) return st;
+        st = cfa::plan_launch_layer(s->attn, &ly.tm_wqkv, &ly.tm_wo, &s->tm_xn, s->xn, ly.k_cache,
+                                    ly.v_cache, positions, rope_theta, cur, s->h, stream);
+        if (st != CFA_OK) return st;
+        void *next = l == s->L - 1 ? out : s->xr;
+        st = mlp_launch(s->mlp, &ly.tm_wg, &ly.tm_wu, &ly.tm_wd, &s->tm_h, s->h, ly.mlp_norm, eps,
+                        next, stream);
+        if (st != CFA_OK) return st;
+        cur = next;
+    }
+    if (advance) {
+        int B = s->B;
+        void *args[2] = {&positions, &B};
+        return launch_pdl(cfa::advance_kernel_ptr(), dim3(1), dim3(32), 0, stream, args);
+    }
+    return CFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cfa_stack *cfa_stack_create(int n_layers, int B, int hidden, int n_heads, int head_dim, int ffn,
+                            int max_ctx) {
+    if (n_layers < 1 || n_layers > 4096 || B < 1 || hidden < 1 || n_heads < 1 ||
+        head_dim < 1 || ffn < 1 || max_ctx < 1 ||
+        static_cast<long long>(n_heads) * head_dim != hidden) {
+        fail(CFA_ERR_INVALID_ARG);
+        return nullptr;
+    }
+    cfa_stack *s = new (std::nothrow) cfa_stack();
+    if (!s) {
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    s->L = n_layers;
+    s->B = B;
+    s->H = hidden;
+    s->nh = n_heads;
+    s->D = head_dim;
+    s->F = ffn;
+    s->max_ctx = max_ctx;
+    s->attn = cfa_plan_create(B, hidden, n_heads, head_dim, max_ctx);
+    if (!s->attn) {
+        const cfa_status st = cfa_last_error();
+        delete s;
+        fail(st);
+        return nullptr;
+    }
+    s->mlp = cfa_mlp_create(B, hidden, ffn);
+    if (!s->mlp) {
+        const cfa_status st = cfa_last_error();
+        stack_free(s);
+        delete s;
+        fail(st);
+        return nullptr;
+    }
+    const size_t act = 2u * static_cast<size_t>(B) * hidden;
+    if (cudaMalloc(&s->xn, act) != cudaSuccess || cudaMalloc(&s->h, act) != cudaSuccess ||
+        cudaMalloc(&s->xr, act) != cudaSuccess) {
+        cudaGetLastError();
+        stack_free(s);
+        delete s;
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    if (cfa::plan_encode_input(s->attn, s->xn, &s->tm_xn) != CFA_OK ||
+        mlp_encode_input(s->mlp, s->h, &s->tm_h) != CFA_OK) {
+        stack_free(s);
+        delete s;
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    s->layers.resize(static_cast<size_t>(n_layers));
+    return s;
+}
+
+void cfa_stack_destroy(cfa_stack *s) {
+    if (!s) return;
+    cudaDeviceSynchronize();
+    stack_free(s);
+    delete s;
+}
+
+cfa_status cfa_stack_set_layer(cfa_stack *s, int layer, const void *attn_norm, const void *W_qkv,
+                               const void *W_o, void *k_cache, void *v_cache,
+                               const void *mlp_norm, const void *W_gate, const void *W_up,
+                               const void *W_down) {
+    if (!s || layer < 0 || layer >= s->L || !attn_norm || !W_qkv || !W_o || !k_cache ||
+        !v_cache || !mlp_norm || !W_gate || !W_up || !W_down)
+        return fail(CFA_ERR_INVALID_ARG);
+    const void *ptrs[9] = {attn_norm, W_qkv, W_o, k_cache, v_cache, mlp_norm, W_gate, W_up, W_down};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return fail(CFA_ERR_ALIGNMENT);
+    StackLayer ly;
+    if (cfa::plan_encode_layer(s->attn, W_qkv, W_o, &ly.tm_wqkv, &ly.tm_wo) != CFA_OK ||
+        mlp_encode_weights(s->mlp, W_gate, W_up, W_down, &ly.tm_wg, &ly.tm_wu, &ly.tm_wd) != CFA_OK)
+        return fail(CFA_ERR_CUDA);
+    ly.attn_norm = attn_norm;
+    ly.W_qkv = W_qkv;
+    ly.W_o = W_o;
+    ly.k_cache = k_cache;
+    ly.v_cache = v_cache;
+    ly.mlp_norm = mlp_norm;
+    ly.W_gate = W_gate;
+    ly.W_up = W_up;
+    ly.W_down = W_down;
+    ly.set = true;
+    s->layers[static_cast<size_t>(layer)] = ly;
+    ++s->version;
+    return CFA_OK;
+}
+
+cfa_status cfa_stack_step(cfa_stack *s, const void *x, int *positions, double rope_theta,
+                          float eps, int advance, void *out, void *stream) {
+    cfa_status st = stack_check(s, x, positions, rope_theta, eps, out);
+    if (st != CFA_OK) return fail(st);
+    st = stack_enqueue(s, x, positions, rope_theta, eps, advance, out,
+                       static_cast<cudaStream_t>(stream));
+    return st == CFA_OK ? CFA_OK : fail(st);
+}
+
+cfa_status cfa_stack_step_graph(cfa_stack *s, const void *x, int *positions, double rope_theta,
+                                float eps, int advance, void *out, void *stream) {
+    cfa_status st = stack_check(s, x, positions, rope_theta, eps, out);
+    if (st != CFA_OK) return fail(st);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (!cs) return fail(CFA_ERR_INVALID_ARG);  // the legacy default stream cannot be captured
+    GraphKey k;
+    k.x = x;
+    k.out = out;
+    k.pos = positions;
+    k.theta = rope_theta;
+    k.eps = eps;
+    k.advance = advance ? 1 : 0;
+    k.stream = cs;
+    k.version = s->version;
+    if (!s->exec || !(s->key == k)) {
+        if (s->exec) {
+            cudaGraphExecDestroy(s->exec);
+            s->exec = nullptr;
+        }
+        if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(CFA_ERR_CUDA);
+        }
+        st = stack_enqueue(s, x, positions, rope_theta, eps, k.advance, out, cs);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t end = cudaStreamEndCapture(cs, &graph);
+        if (st != CFA_OK || end != cudaSuccess || !graph) {
+            cudaGetLastError();
+            if (graph) cudaGraphDestroy(graph);
+            return fail(st != CFA_OK ? st : CFA_ERR_CUDA);
+        }
+        const cudaError_t inst = cudaGraphInstantiate(&s->exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (inst != cudaSuccess) {
+            cudaGetLastError();
+            s->exec = nullptr;
+            return fail(CFA_ERR_CUDA);
+        }
+        s->key = k;
+    }
+    if (cudaGraphLaunch(s->exec, cs) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CFA_ERR_CUDA);
+    }
+    return CFA_OK;
+}
+
+cfa_status cfa_stack_status(cfa_stack *s) {
+    if (!s) return fail(CFA_ERR_INVALID_ARG);
+    const cfa_status a = cfa_plan_status(s->attn);
+    const cfa_status m = cfa_mlp_status(s->mlp);
+    if (a != CFA_OK) return fail(a);
+    return m == CFA_OK ? CFA_OK : fail(m);
+}
+
+cfa_status cfa_stack_describe(const cfa_stack *s, char *buf, int len) {
+    if (!s || !buf || len < 64) return fail(CFA_ERR_INVALID_ARG);
+    char a[512], m[512];
+    if (cfa_plan_describe(s->attn, a, sizeof a) != CFA_OK ||
+        cfa_mlp_describe(s->mlp, m, sizeof m) != CFA_OK)
+        return fail(CFA_ERR_INVALID_ARG);
+    std::snprintf(buf, static_cast<size_t>(len),
+                  "{\"n_layers\": %d, \"launches_per_token\": %d, \"attention\": %s, \"mlp\": %s}",
+                  s->L, 4 * s->L, a, m);
+    return CFA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,317 @@
+"""GPU parity of the decoder-layer kernels (RMSNorm, stream-K SwiGLU MLP) and
+the multi-layer decode loop (eager and CUDA-graph) against the fp64 oracle,
+through the C ABI.
+
+Tolerance as for the attention block: relative L2 <= 5e-3 and max abs <= 3e-2
+against the oracle on the same bf16 inputs. The oracle keeps the bf16 storage
+points of the layer (xn, h, hn, u, y), so both sides round at the same
+places. Where a residual would dominate the compared tensor, the residual
+stream is scaled down (RMSNorm makes every stage after it blind to that
+scale), so the compared values are carried by the layer's own arithmetic.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from out_proj_block_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 5e-3
+MAX_ABS = 3e-2
+NTHREADS = os.cpu_count() or 1
+THETA = 10000.0
+EPS = 1e-5
+
+
+@pytest.fixture(scope="module")
+def cfa():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from out_proj_block_gb300 import build
+    build.build()
+    from out_proj_block_gb300 import cfa as mod
+    return mod
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64_bits(b) -> np.ndarray:
+    u = np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def check_close(name, got, ref, rel=REL_L2, max_abs=MAX_ABS):
+    """rel L2 <= rel and max abs <= max_abs, the latter for unit-scale values:
+    it is applied to got/s, ref/s with s = max(1, rms(ref))."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    scale = max(1.0, float(np.sqrt(np.mean(ref * ref))))
+    e_rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    e_abs = float(np.abs(got - ref).max()) / scale
+    print(f"{name}: rel L2 {e_rel:.3e}, max abs/scale {e_abs:.3e} (scale {scale:.3g})")
+    assert e_rel <= rel and e_abs <= max_abs, (
+        f"{name}: rel L2 {e_rel:.3e} (<= {rel}), max abs {e_abs:.3e} (<= {max_abs})")
+    return e_rel, e_abs
+
+
+def scaled(t: torch.Tensor, s: float) -> torch.Tensor:
+    return (t.float() * s).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+
+@pytest.mark.parametrize("B,n", [(1, 256), (3, 4096), (16, 1024), (2, 11008)])
+def test_rmsnorm_matches_oracle(cfa, oracle, B, n):
+    g = torch.Generator().manual_seed(B * 7 + n)
+    x = (3.0 * torch.randn(B, n, generator=g)).to(torch.bfloat16)
+    w = (1.0 + 0.1 * torch.randn(n, generator=g)).to(torch.bfloat16)
+    y = torch.empty(B, n, dtype=torch.bfloat16, device="cuda")
+    cfa.rmsnorm(x.cuda(), w.cuda(), EPS, y)
+    torch.cuda.synchronize()
+    ref = f64_bits(oracle.rmsnorm_bf16(x, w, EPS))
+    got = y.double().cpu().numpy()
+    check_close("rmsnorm", got, ref)
+    # both sides round one fp32/fp64 value to bf16: at most one unit apart
+    ulp = np.abs(ref) * 2.0 ** -7
+    assert (np.abs(got - ref) <= ulp + 1e-30).all()
+
+
+def test_rmsnorm_rejects_bad_arguments(cfa):
+    x = torch.zeros(2, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    assert cfa.cfa_rmsnorm(2, 60, x, w, EPS, x.clone(), None) == cfa.CFA_ERR_INVALID_ARG
+    assert cfa.cfa_rmsnorm(2, 64, x, w, -1.0, x.clone(), None) == cfa.CFA_ERR_INVALID_ARG
+    assert cfa.cfa_rmsnorm(2, 64, x, w, EPS, x, None) == cfa.CFA_ERR_INVALID_ARG  # y aliases x
+    y = torch.empty(2 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    assert cfa.cfa_rmsnorm(2, 64, x, w, EPS, y.data_ptr() + 2, None) == cfa.CFA_ERR_ALIGNMENT
+
+
+# -------------------------------------------------------------------- MLP
+
+
+def mlp_inputs(B, H, F, seed, h_scale=2.0 ** -6):
+    wl = workloads.custom_stack(1, B, H, max(1, H // 128), min(128, H), F, 1, max_ctx=64)
+    t = workloads.make_stack_inputs(wl, seed=seed)
+    layer = t["layers"][0]
+    h = scaled(t["x"], h_scale)  # small residual: y is carried by the MLP term
+    return h, layer["mlp_norm"], layer["W_gate"], layer["W_up"], layer["W_down"]
+
+
+def run_mlp(cfa, oracle, B, H, F, seed):
+    h, nw, Wg, Wu, Wd = mlp_inputs(B, H, F, seed)
+    dev = [t.cuda() for t in (h, nw, Wg, Wu, Wd)]
+    y = torch.empty(B, H, dtype=torch.bfloat16, device="cuda")
+    mlp = cfa.Mlp(B, H, F)
+    mlp.step(*dev, y, eps=EPS)
+    torch.cuda.synchronize()
+    assert mlp.status() == cfa.CFA_OK
+    ref = oracle.mlp(h, nw, Wg, Wu, Wd, EPS, nthreads=NTHREADS)
+    got = y.double().cpu().numpy()
+    check_close("mlp y", got, f64_bits(ref["y"]))
+    # the MLP term alone, against the oracle's unrounded delta
+    check_close("mlp delta", got - h.double().numpy(), ref["delta"], rel=1e-2)
+    return mlp, dev, y
+
+
+@pytest.mark.parametrize("B,H,F", [(1, 256, 512), (2, 512, 1024), (3, 256, 384),
+                                   (8, 1024, 768), (16, 256, 512), (5, 4096, 1024)])
+def test_mlp_matches_oracle(cfa, oracle, B, H, F):
+    run_mlp(cfa, oracle, B, H, F, seed=B + H + F)
+
+
+def test_mlp_full_llama_shape_b1(cfa, oracle):
+    """Hidden 4096, ffn 11008: hundreds of blocks, tiles shared by 2-3 blocks."""
+    mlp, _, _ = run_mlp(cfa, oracle, 1, 4096, 11008, seed=3)
+    d = mlp.describe()
+    assert d["gate_up"]["units"] > d["gate_up"]["grid"] > 1
+    assert d["down"]["units"] > d["down"]["grid"] > 1
+
+
+def test_mlp_is_deterministic(cfa, oracle):
+    mlp, dev, y = run_mlp(cfa, oracle, 2, 4096, 2048, seed=4)
+    first = y.clone()
+    for _ in range(3):
+        mlp.step(*dev, y, eps=EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), y.view(torch.int16))
+
+
+def test_mlp_rejects_bad_shapes(cfa):
+    with pytest.raises(cfa.CfaError):
+        cfa.Mlp(1, 256, 500)      # ffn not a multiple of 128
+    with pytest.raises(cfa.CfaError):
+        cfa.Mlp(17, 256, 512)     # batch above 16
+
+
+# -------------------------------------------------- the decode loop (stack)
+
+
+def stack_setup(wl, seed, x_scale=2.0 ** -6):
+    t = workloads.make_stack_inputs(wl, seed=seed, poison_tail=True)
+    x = scaled(t["x"], x_scale)
+    dev_layers = [{k: v.cuda() for k, v in layer.items()} for layer in t["layers"]]
+    ora_caches = [(bits(l["k_cache"]).copy(), bits(l["v_cache"]).copy()) for l in t["layers"]]
+    return x, t["layers"], dev_layers, ora_caches
+
+
+def compare_token(name, cfa_out, y_ref, dev_layers, per_layer, lens):
+    check_close(f"{name} out", cfa_out.double().cpu().numpy(), f64_bits(y_ref))
+    for l, (dl, r) in enumerate(zip(dev_layers, per_layer)):
+        k_rows = np.stack([dl["k_cache"][b, :, L].double().cpu().numpy() for b, L in enumerate(lens)])
+        v_rows = np.stack([dl["v_cache"][b, :, L].double().cpu().numpy() for b, L in enumerate(lens)])
+        check_close(f"{name} layer {l} k_new", k_rows, r["k_new"])
+        check_close(f"{name} layer {l} v_new", v_rows, r["v_new"])
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_stack_decode_loop_matches_oracle(cfa, oracle, graph):
+    """Three tokens through 2 tiny layers with positions advanced on the device:
+    each token reads the rows the previous one appended (rows past the
+    position are NaN, so a missing or misplaced append shows)."""
+    wl = workloads.STACKS["stack_tiny"]
+    x, layers, dev_layers, caches = stack_setup(wl, seed=1)
+    stack = cfa.Stack(wl.n_layers, wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.ffn, wl.max_ctx,
+                      layers=dev_layers)
+    pos = torch.full((wl.B,), wl.ctx_len, dtype=torch.int32, device="cuda")
+    out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    cur = x
+    for tok in range(3):
+        lens = [wl.ctx_len + tok] * wl.B
+        with torch.cuda.stream(stream):
+            xin = cur.cuda()
+            if graph:
+                stack.step_graph(xin, pos, out, THETA, EPS, advance=True, stream=stream)
+            else:
+                stack.step(xin, pos, out, THETA, EPS, advance=True, stream=stream)
+        stream.synchronize()
+        assert stack.status() == cfa.CFA_OK
+        y_ref, per = oracle.stack_step(cur, layers, caches, lens, THETA, EPS, NTHREADS)
+        compare_token(f"token {tok}", out, y_ref, dev_layers, per, lens)
+        cur = scaled(out.cpu(), 2.0 ** -4)  # next token's input, kept small as above
+    assert pos.cpu().tolist() == [wl.ctx_len + 3] * wl.B
+
+
+def test_stack_graph_equals_eager_bitwise(cfa, oracle):
+    wl = workloads.custom_stack(3, 2, 512, 4, 128, 1024, 40, max_ctx=64)
+    outs = []
+    for graph in (False, True):
+        x, layers, dev_layers, _ = stack_setup(wl, seed=2)
+        stack = cfa.Stack(wl.n_layers, wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.ffn,
+                          wl.max_ctx, layers=dev_layers)
+        pos = torch.tensor([40, 17], dtype=torch.int32, device="cuda")
+        out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            xin = x.cuda()
+            for _ in range(2):  # second replay reuses the recorded graph
+                (stack.step_graph if graph else stack.step)(xin, pos, out, THETA, EPS,
+                                                            advance=False, stream=stream)
+        stream.synchronize()
+        assert stack.status() == cfa.CFA_OK
+        outs.append((out.clone(), [l["k_cache"].clone() for l in dev_layers]))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    for a, b in zip(outs[0][1], outs[1][1]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("B", [1, 16])
+def test_stack_ragged_positions_and_batch(cfa, oracle, B):
+    """Per-sequence positions from device memory; B=16 runs the tensor-core
+    attention projections and the 16-row GEMV."""
+    wl = workloads.custom_stack(2, B, 256, 2, 128, 512, 48, max_ctx=64)
+    x, layers, dev_layers, caches = stack_setup(wl, seed=5)
+    lens = [(7 * b + 3) % 48 for b in range(B)]
+    stack = cfa.Stack(wl.n_layers, B, wl.hidden, wl.n_heads, wl.head_dim, wl.ffn, wl.max_ctx,
+                      layers=dev_layers)
+    pos = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    stack.step(x.cuda(), pos, out, THETA, EPS)
+    torch.cuda.synchronize()
+    assert stack.status() == cfa.CFA_OK
+    y_ref, per = oracle.stack_step(x, layers, caches, lens, THETA, EPS, NTHREADS)
+    compare_token("ragged", out, y_ref, dev_layers, per, lens)
+
+
+def test_stack_full_llama_layers(cfa, oracle):
+    """Two Llama2-7B-shaped layers (hidden 4096, 32 x 128, ffn 11008) at ctx 1024,
+    in the launch configuration of the decode-loop benchmark (graph replay).
+
+    Layer by layer, each GPU layer is fed the oracle's output of the layer
+    before (so its error is its own) and held to the block tolerance. The
+    two-layer run end to end is held to twice that: the first layer's
+    one-ulp rounding differences pass through the second layer's residual and
+    its MLP, whose output is quadratic in its normalised input (gain about 2
+    in this synthetic model)."""
+    wl = workloads.custom_stack(2, 1, 4096, 32, 128, 11008, 1024)
+    x, layers, dev_layers, caches = stack_setup(wl, seed=6)
+    pristine = [(l["k_cache"].clone(), l["v_cache"].clone()) for l in dev_layers]
+    y_ref, per = oracle.stack_step(x, layers, caches, [1024], THETA, EPS, NTHREADS)
+    pos = torch.tensor([1024], dtype=torch.int32, device="cuda")
+    out = torch.empty(1, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    # each layer alone, on the oracle's input to that layer
+    inp = x
+    for l in range(2):
+        one = cfa.Stack(1, 1, wl.hidden, wl.n_heads, wl.head_dim, wl.ffn, wl.max_ctx,
+                        layers=[dev_layers[l]])
+        with torch.cuda.stream(stream):
+            one.step_graph(inp.cuda(), pos, out, THETA, EPS, advance=False, stream=stream)
+        stream.synchronize()
+        assert one.status() == cfa.CFA_OK
+        compare_token(f"llama layer {l} alone", out, per[l]["y"], [dev_layers[l]], [per[l]],
+                      [1024])
+        inp = torch.from_numpy(per[l]["y"].view(np.int16).copy()).view(torch.bfloat16)
+        one.close()
+    # both layers in one graph
+    for l, (k, v) in zip(dev_layers, pristine):
+        l["k_cache"].copy_(k)
+        l["v_cache"].copy_(v)
+    stack = cfa.Stack(wl.n_layers, 1, wl.hidden, wl.n_heads, wl.head_dim, wl.ffn, wl.max_ctx,
+                      layers=dev_layers)
+    with torch.cuda.stream(stream):
+        stack.step_graph(x.cuda(), pos, out, THETA, EPS, advance=False, stream=stream)
+    stream.synchronize()
+    assert stack.status() == cfa.CFA_OK
+    check_close("llama 2 layers out", out.double().cpu().numpy(), f64_bits(y_ref),
+                rel=2 * REL_L2, max_abs=2 * MAX_ABS)
+
+
+def test_stack_flags_a_device_position_out_of_range(cfa):
+    """A position the host cannot see is checked on the device: the step reads
+    no cache row and appends nothing for it, and the status reports it."""
+    wl = workloads.custom_stack(1, 2, 256, 2, 128, 512, 8, max_ctx=64)
+    _, _, dev_layers, _ = stack_setup(wl, seed=7)
+    k_before = dev_layers[0]["k_cache"].clone()
+    stack = cfa.Stack(1, 2, 256, 2, 128, 512, 64, layers=dev_layers)
+    pos = torch.tensor([8, 64], dtype=torch.int32, device="cuda")  # 64 == max_ctx: invalid
+    out = torch.empty(2, 256, dtype=torch.bfloat16, device="cuda")
+    x = torch.randn(2, 256, device="cuda").to(torch.bfloat16)
+    stack.step(x, pos, out, THETA, EPS)
+    assert stack.status() == cfa.CFA_ERR_INVALID_ARG
+    after = dev_layers[0]["k_cache"]
+    assert torch.equal(after[1].view(torch.int16), k_before[1].view(torch.int16))
+    assert not torch.equal(after[0, :, 8].view(torch.int16), k_before[0, :, 8].view(torch.int16))
+    assert stack.status() == cfa.CFA_OK  # the status word was cleared
+
+
+def test_stack_requires_every_layer_and_a_stream_for_graphs(cfa):
+    wl = workloads.custom_stack(2, 1, 256, 2, 128, 512, 8, max_ctx=64)
+    _, _, dev_layers, _ = stack_setup(wl, seed=8)
+    stack = cfa.Stack(2, 1, 256, 2, 128, 512, 64)
+    stack.set_layer(0, dev_layers[0])
+    pos = torch.tensor([8], dtype=torch.int32, device="cuda")
+    x = torch.zeros(1, 256, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    with pytest.raises(cfa.CfaError):
+        stack.step(x, pos, out)
+    stack.set_layer(1, dev_layers[1])
+    with pytest.raises(cfa.CfaError):
+        stack.step_graph(x, pos, out, stream=0)  # the legacy default stream
