@@ -19,7 +19,8 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "cfa_oracle.c"), os.path.join(_HERE, "cfa_oracle_layer.c")]
+_SRCS = [os.path.join(_HERE, "cfa_oracle.c"), os.path.join(_HERE, "cfa_oracle_layer.c"),
+         os.path.join(_HERE, "cfa_oracle_mla.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libcfa_oracle.so")
 _lock = threading.Lock()
@@ -90,6 +91,12 @@ def _load():
             lib.cfa_oracle_layer_step.argtypes = (
                 [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int), ctypes.c_double, ctypes.c_double]
                 + [_u16p] * 10 + [_u16p] * 4 + [_dp, _dp, ctypes.c_int])
+            lib.cfa_oracle_attention_kv.restype = None
+            lib.cfa_oracle_attention_kv.argtypes = [ctypes.c_int] * 3 + [_dp] * 3 + [ctypes.c_double, _dp]
+            lib.cfa_oracle_mla_step.restype = ctypes.c_int
+            lib.cfa_oracle_mla_step.argtypes = (
+                [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int), ctypes.c_double, ctypes.c_double]
+                + [_u16p] * 8 + [_dp] * 4 + [ctypes.c_int])
             lib.cfa_oracle_threads.restype = ctypes.c_int
             lib.cfa_oracle_threads.argtypes = [ctypes.c_int]
             _lib = lib
@@ -344,3 +351,58 @@ def stack_step(x, layers, caches, ctx_lens, rope_theta: float, eps: float, nthre
         per_layer.append(r)
         cur = r["y"]
     return cur, per_layer
+
+
+# --------------------------------------------------------------------------
+# Multi-head latent attention (cfa_oracle_mla.c)
+
+MLA_KV, MLA_NOPE, MLA_ROPE, MLA_V = 512, 128, 64, 128
+MLA_QK = MLA_NOPE + MLA_ROPE
+MLA_ROW = MLA_KV + MLA_ROPE
+
+
+def attention_kv(q, K, V, scale: float) -> np.ndarray:
+    """Single-query softmax attention with keys [T, dk] and values [T, dv]."""
+    q, K, V = _f64(q), _f64(K), _f64(V)
+    T, dk = K.shape
+    dv = V.shape[1]
+    a = np.empty(dv, np.float64)
+    _load().cfa_oracle_attention_kv(T, dk, dv, q.ctypes.data_as(_dp), K.ctypes.data_as(_dp),
+                                    V.ctypes.data_as(_dp), float(scale), a.ctypes.data_as(_dp))
+    return a
+
+
+def mla_step(x, W_a, g_q, g_kv, W_uq, W_kvb, W_o, cache, ctx_lens, rope_theta: float,
+             eps: float, nthreads: int = 1):
+    """fp64 MLA decode step (see cfa_oracle_mla.c).
+
+    x [B, H]; W_a [H, q_lora + 576]; g_q [q_lora]; g_kv [512];
+    W_uq [q_lora, nh*192]; W_kvb [512, nh*256]; W_o [nh*128, H];
+    cache [B, max_ctx, 576]. Returns dict(out [B, H], new_row [B, 576],
+    v [B, nh*128], attn [B, nh*128]) as float64 arrays."""
+    xb, wa, gq, gkv, wuq, wkvb, wo, cb = (_bits(t) for t in (
+        x, W_a, g_q, g_kv, W_uq, W_kvb, W_o, cache))
+    B, H = xb.shape
+    q_lora = gq.shape[0]
+    nh = wuq.shape[1] // MLA_QK
+    max_ctx = cb.shape[1]
+    if (wa.shape != (H, q_lora + MLA_ROW) or gkv.shape != (MLA_KV,)
+            or wuq.shape != (q_lora, nh * MLA_QK) or wkvb.shape != (MLA_KV, nh * (MLA_NOPE + MLA_V))
+            or wo.shape != (nh * MLA_V, H) or cb.shape != (B, max_ctx, MLA_ROW)):
+        raise ValueError("inconsistent shapes")
+    lens = np.ascontiguousarray(np.asarray(ctx_lens, dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("ctx_lens must have one entry per batch row")
+    out = np.empty((B, H), np.float64)
+    new_row = np.empty((B, MLA_ROW), np.float64)
+    v = np.empty((B, nh * MLA_V), np.float64)
+    attn = np.empty((B, nh * MLA_V), np.float64)
+    ptrs = [t.ctypes.data_as(_u16p) for t in (xb, wa, gq, gkv, wuq, wkvb, wo, cb)]
+    rc = _load().cfa_oracle_mla_step(
+        B, H, nh, q_lora, max_ctx, lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+        float(rope_theta), float(eps), *ptrs, out.ctypes.data_as(_dp),
+        new_row.ctypes.data_as(_dp), v.ctypes.data_as(_dp), attn.ctypes.data_as(_dp),
+        int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return {"out": out, "new_row": new_row, "v": v, "attn": attn}

@@ -252,3 +252,105 @@ def make_stack_inputs(wl: StackWorkload, seed: int = 0, device="cpu",
             layer["v_cache"][:, :, L:, :] = float("nan")
         layers.append(layer)
     return {"x": x, "layers": layers}
+
+
+# --------------------------------------------------------------------------
+# Multi-head latent attention (DeepSeek-V2/V3 dimensions: latent 512, per-head
+# nope / rope / value widths 128 / 64 / 128). Inputs: x ~ N(0, 1); W_a, W_uq,
+# W_kvb, W_o ~ N(0, 0.02); norm weights 1 + N(0, 0.1); latent cache rows
+# ~ N(0, 1); all bf16.
+
+MLA_KV, MLA_NOPE, MLA_ROPE, MLA_V = 512, 128, 64, 128
+MLA_ROW = MLA_KV + MLA_ROPE
+
+
+@dataclasses.dataclass(frozen=True)
+class MlaWorkload:
+    name: str
+    B: int
+    hidden: int
+    n_heads: int
+    q_lora: int
+    ctx_len: int
+    max_ctx: int
+    rope_theta: float = 10000.0
+    eps: float = 1e-6
+    description: str = ""
+
+    @property
+    def lens(self) -> Tuple[int, ...]:
+        return (self.ctx_len,) * self.B
+
+    @property
+    def weight_bytes(self) -> int:
+        H, nh, ql = self.hidden, self.n_heads, self.q_lora
+        return 2 * (H * (ql + MLA_ROW) + ql * nh * (MLA_NOPE + MLA_ROPE)
+                    + MLA_KV * nh * (MLA_NOPE + MLA_V) + nh * MLA_V * H)
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Every weight once plus the latent cache rows read."""
+        return self.weight_bytes + sum(self.lens) * MLA_ROW * 2
+
+    @property
+    def attention_flops(self) -> int:
+        """Multiply-adds x 2 of the latent attention in absorbed form:
+        q absorption, scores over 576 dims, latent output, value projection."""
+        nh = self.n_heads
+        per_b = [nh * (2 * MLA_KV * MLA_NOPE + (L + 1) * (MLA_ROW + MLA_KV) + MLA_KV * MLA_V)
+                 for L in self.lens]
+        return 2 * sum(per_b)
+
+    def as_config(self) -> Dict[str, object]:
+        return {"workload": self.name, "B": self.B, "hidden": self.hidden,
+                "n_heads": self.n_heads, "q_lora": self.q_lora, "kv_lora": MLA_KV,
+                "qk_nope": MLA_NOPE, "qk_rope": MLA_ROPE, "v_head": MLA_V,
+                "ctx_len": self.ctx_len, "max_ctx": self.max_ctx,
+                "rope_theta": self.rope_theta, "eps": self.eps}
+
+
+def _mw(name, B, H, nh, ql, L, desc, max_ctx=None, rope_theta=10000.0, eps=1e-6):
+    return MlaWorkload(name, B, H, nh, ql, L,
+                       max_ctx if max_ctx is not None else _round_up(L + 1, 64),
+                       rope_theta, eps, desc)
+
+
+MLAS: Dict[str, MlaWorkload] = {w.name: w for w in [
+    _mw("mla_tiny", 1, 256, 2, 128, 64, "MLA, hidden 256, 2 heads, q_lora 128, ctx_len 64",
+        max_ctx=128),
+    _mw("mla_v3_b1_ctx4k", 1, 7168, 128, 1536, 4096,
+        "DeepSeek-V3-shaped MLA (hidden 7168, 128 heads, q_lora 1536), B=1, ctx_len 4096"),
+    _mw("mla_v3_b1_ctx16k", 1, 7168, 128, 1536, 16384,
+        "DeepSeek-V3-shaped MLA (hidden 7168, 128 heads, q_lora 1536), B=1, ctx_len 16384"),
+]}
+
+
+def custom_mla(B: int, hidden: int, n_heads: int, q_lora: int, ctx_len: int,
+               max_ctx: Optional[int] = None, name: str = "custom_mla") -> MlaWorkload:
+    return _mw(name, B, hidden, n_heads, q_lora, ctx_len,
+               f"{name}: B={B}, hidden {hidden}, {n_heads} heads, q_lora {q_lora}, "
+               f"ctx_len {ctx_len}", max_ctx)
+
+
+def make_mla_inputs(wl: MlaWorkload, seed: int = 0, device="cpu",
+                    poison_tail: bool = False) -> Dict[str, torch.Tensor]:
+    """Seeded bf16 inputs of an MLA step: x [B, H], W_a [H, q_lora + 576],
+    g_q [q_lora], g_kv [512], W_uq [q_lora, nh*192], W_kvb [512, nh*256],
+    W_o [nh*128, H], cache [B, max_ctx, 576]. ``poison_tail`` fills cache rows
+    at positions >= ctx_len with NaN."""
+    device = torch.device(device)
+    B, H, nh, ql, L, mc = wl.B, wl.hidden, wl.n_heads, wl.q_lora, wl.ctx_len, wl.max_ctx
+    s = 3000017 * (seed + 1)
+    t = {
+        "x": _normal((B, H), 1.0, device, s + 1),
+        "W_a": _normal((H, ql + MLA_ROW), 0.02, device, s + 2),
+        "g_q": (_normal((ql,), 0.1, device, s + 3).float() + 1.0).to(torch.bfloat16),
+        "g_kv": (_normal((MLA_KV,), 0.1, device, s + 4).float() + 1.0).to(torch.bfloat16),
+        "W_uq": _normal((ql, nh * (MLA_NOPE + MLA_ROPE)), 0.02, device, s + 5),
+        "W_kvb": _normal((MLA_KV, nh * (MLA_NOPE + MLA_V)), 0.02, device, s + 6),
+        "W_o": _normal((nh * MLA_V, H), 0.02, device, s + 7),
+        "cache": _normal((B, mc, MLA_ROW), 1.0, device, s + 8),
+    }
+    if poison_tail and L < mc:
+        t["cache"][:, L:, :] = float("nan")
+    return t
