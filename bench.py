@@ -22,6 +22,10 @@ Inputs live in three rotating copies (each larger than the 129 MB L2), so no
 step reads what the previous step left in L2. Multi-GPU runs are independent
 replicas (the step has no exchange between GPUs).
 
+--workload mla_v3_b1_ctx4k (or another MLA workload) measures a
+DeepSeek-style latent-attention step (4 launches); its bytes are every weight
+of the block plus the latent cache rows read.
+
 --workload llama7b_32l_b1_ctx1k (or another layer stack) measures the decode
 loop instead: a step is one token through every layer (RMSNorm, the fused
 attention block, residual, RMSNorm + SwiGLU MLP, residual), replayed from one
@@ -699,9 +703,193 @@ def run_stack(args, wl):
     return 0
 
 
+# ------------------------------------------- multi-head latent attention
+
+
+def mla_oracle_steps(wl, t_cpu, budget_s: float, max_steps: int = 20):
+    """The fp64 MLA oracle on all host cores, whole steps until the budget is spent."""
+    from oracle import cfa_oracle
+    cfa_oracle.build()
+    used = cfa_oracle.threads_used(os.cpu_count() or 1)
+    times, ref = [], None
+    t_start = time.perf_counter()
+    while len(times) < max_steps:
+        t0 = time.perf_counter()
+        ref = cfa_oracle.mla_step(t_cpu["x"], t_cpu["W_a"], t_cpu["g_q"], t_cpu["g_kv"],
+                                  t_cpu["W_uq"], t_cpu["W_kvb"], t_cpu["W_o"], t_cpu["cache"],
+                                  list(wl.lens), wl.rope_theta, wl.eps, used)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    return times, used, ref
+
+
+def run_mla_reference(args, wl):
+    from out_proj_block_gb300 import workloads
+    t = workloads.make_mla_inputs(wl, seed=0, device="cpu")
+    for _ in range(max(args.warmup, 0)):
+        mla_oracle_steps(wl, t, 0.0, max_steps=1)
+    t0 = time.perf_counter()
+    times, used, _ = mla_oracle_steps(wl, t, 1e9, max_steps=args.steps)
+    total = time.perf_counter() - t0
+    value = wl.algorithmic_bytes * args.steps / total / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wl.as_config(), l2="host run; no GPU L2 involved"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": f"{args.steps} full fp64 MLA steps of {wl.name}"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0}), flush=True)
+    return 0
+
+
+def run_mla(args, wl):
+    """MLA decode steps (4 launches each) back to back."""
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from out_proj_block_gb300 import build as cuda_build
+    if rank == 0 or world == 1:
+        cuda_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from out_proj_block_gb300 import cfa, workloads
+
+    t = workloads.make_mla_inputs(wl, seed=0, device=dev)
+    mla = cfa.Mla(wl.B, wl.hidden, wl.n_heads, wl.q_lora, wl.max_ctx)
+    desc = mla.describe()
+    out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    lens = list(wl.lens)
+
+    def step():
+        mla.step(t["x"], t, t["cache"], lens, out, wl.rope_theta, wl.eps, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if mla.status() != cfa.CFA_OK:
+        raise RuntimeError("device status after warm-up")
+    sampler = ClockSampler(local).start()
+    t_end = time.perf_counter() + args.preload_seconds
+    while time.perf_counter() < t_end:
+        for _ in range(32):
+            step()
+        torch.cuda.synchronize(dev)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_s = e0.elapsed_time(e1) / 1e3
+    if mla.status() != cfa.CFA_OK:
+        raise RuntimeError("device status after timing")
+    max_total_s = aggregate_max(total_s, world, dev)
+    value = whole_job_gbs(wl.algorithmic_bytes, K, world, max_total_s)
+    mean_s = total_s / K
+    n_iso = min(K, 200)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso + 1)]
+    ev[0].record(stream)
+    for k in range(n_iso):
+        step()
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(n_iso)]
+
+    e2e = None
+    if not args.no_e2e:
+        x_host = t["x"].cpu().pin_memory()
+        out_host = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        x_dev = torch.empty_like(t["x"])
+
+        def host_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            mla.step(x_dev, t, t["cache"], lens, out, wl.rope_theta, wl.eps, stream)
+            out_host.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            host_step()
+        n_e2e = min(K, 500)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            host_step()
+        e2e_s = aggregate_max(time.perf_counter() - t0, world, dev)
+        e2e = {"value": whole_job_gbs(wl.algorithmic_bytes, n_e2e, world, e2e_s), "unit": "GB/s",
+               "h2d_bytes_per_step": int(x_host.numel() * 2),
+               "d2h_bytes_per_step": int(out_host.numel() * 2),
+               "ms_per_step": e2e_s / n_e2e * 1e3, "steps": n_e2e}
+
+    peak, peak_kind = measured_peaks()
+    achieved = wl.algorithmic_bytes / mean_s / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+            "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+            "kernel": "whole MLA step (4 kernels)",
+            "attention_flops_per_step": wl.attention_flops}
+    cpu_base, parity = None, None
+    if rank == 0 and not args.no_cpu_baseline:
+        t_cpu = {k: v.cpu() for k, v in t.items()}
+        times, used, ref = mla_oracle_steps(wl, t_cpu, args.cpu_seconds)
+        st_s = statistics.median(times)
+        cpu_base = {"value": wl.algorithmic_bytes / st_s / 1e9, "unit": "GB/s", "cores": used,
+                    "kind": "oracle",
+                    "sample": f"{len(times)} full fp64 MLA steps of {wl.name} "
+                              f"(median {st_s * 1e3:.0f} ms per step)", "step_ms": st_s * 1e3}
+        step()
+        torch.cuda.synchronize(dev)
+        got = out.double().cpu().numpy()
+        parity = {"out_rel_l2": float(np.linalg.norm(got - ref["out"]) / np.linalg.norm(ref["out"])),
+                  "out_max_abs": float(np.abs(got - ref["out"]).max())}
+    mla.close()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": max_total_s / K * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(wl.as_config(),
+                       l2=f"one step reads {wl.algorithmic_bytes / 1e6:.0f} MB (> 129 MB L2)",
+                       parallelism=f"replicas x{world}"),
+        "latency_us": {"back_to_back_mean": mean_s * 1e6,
+                       "isolated_p10": percentile(step_ms, 0.1) * 1e3,
+                       "isolated_p50": percentile(step_ms, 0.5) * 1e3,
+                       "isolated_p90": percentile(step_ms, 0.9) * 1e3},
+        "roofline": roof, "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": 4 * K, "parity": parity, "plan": desc,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from out_proj_block_gb300 import workloads
+    if args.workload in workloads.MLAS:
+        wl = workloads.MLAS[args.workload]
+        if args.impl == "reference":
+            world, rank, _ = dist_env()
+            return run_mla_reference(args, wl) if rank == 0 else 0
+        return run_mla(args, wl)
     if args.workload in workloads.STACKS:
         wl = workloads.STACKS[args.workload]
         if args.impl == "reference":

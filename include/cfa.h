@@ -358,6 +358,59 @@ cfa_status cfa_stack_status(cfa_stack *stack);
 /* One-line JSON description (layers, launches per token, both plans). */
 cfa_status cfa_stack_describe(const cfa_stack *stack, char *buf, int len);
 
+/* ==========================================================================
+ * Multi-head latent attention (MLA), the DeepSeek variant the page adapts
+ * ClusterFusion to: the latent key/value cache partitioned across clusters,
+ * combined by a sparse cluster reduction (§5.2). The page gives no formula or
+ * dimension; the block is DeepSeek-V2/V3's attention with their widths:
+ * latent 512, per-head nope / rope / value 128 / 64 / 128 (fixed here).
+ *
+ * One step for B sequences at positions ctx_lens[b] (weights [in, out]):
+ *   a   = bf16(x . W_a)                    W_a  [hidden, q_lora + 576]
+ *   q   = bf16(bf16(rmsnorm(a[:q_lora]; g_q)) . W_uq)     W_uq [q_lora, n_heads*192]
+ *         per head: [q_nope (128) | q_rope (64)]
+ *   row = [bf16(rmsnorm(a[q_lora:q_lora+512]; g_kv)) | bf16(rope(a[q_lora+512:], L))]
+ *         appended to the latent cache at L    cache [B, max_ctx, 576]
+ *   per head h, with W_kvb [512, n_heads*256] holding per head [W_k (128) | W_v (128)]:
+ *     keys    k_t = [c_t . W_k,h | k_rope_t], values v_t = c_t . W_v,h  (c_t = latent of row t)
+ *     o_h     = softmax_t((q_nope . k_nope_t + rope(q_rope) . k_rope_t) / sqrt(192)) . v
+ *   out = bf16(bf16(concat_h o_h) . W_o)   W_o  [n_heads*128, hidden]
+ * rope is the rotate-half form of cfa_decode_step_ex over the 64 rope dims
+ * (rope_theta 0 disables it); rmsnorm as cfa_rmsnorm. The attention runs in
+ * absorbed form (q_nope folded into W_k, values projected after the sum), one
+ * thread-block cluster per (sequence, group of 16 heads).
+ * ========================================================================== */
+
+typedef struct cfa_mla cfa_mla; /* opaque */
+
+/*
+ * Plan for batch B (1..16), hidden a multiple of 64, n_heads even (the
+ * cluster holds the largest power-of-two group of heads up to 16 that divides
+ * n_heads), q_lora a multiple of 64, max_ctx latent rows per sequence.
+ * Allocates the intermediate a, q, v buffers, GEMV workspace and status words.
+ * NULL on failure; cfa_last_error() says why.
+ */
+cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx);
+
+/* Release the plan (synchronizes the device first). NULL is a no-op. */
+void cfa_mla_destroy(cfa_mla *mla);
+
+/*
+ * One MLA decode step (4 kernel launches). ctx_lens: host array [B], each in
+ * [0, max_ctx - 1]; row ctx_lens[b] of the cache is written, rows below it are
+ * read. out must not overlap x, the cache or W_o. Errors as cfa_decode_step.
+ */
+cfa_status cfa_mla_step(cfa_mla *mla, const void *x, const void *W_a, const void *g_q,
+                        const void *g_kv, const void *W_uq, const void *W_kvb, const void *W_o,
+                        void *cache, const int *ctx_lens, double rope_theta, float eps,
+                        void *out, void *stream);
+
+/* Synchronizes, reads and clears the plan's device status words. */
+cfa_status cfa_mla_status(cfa_mla *mla);
+
+/* One-line JSON description (cluster shape, grid, shared memory, GEMV grids). */
+cfa_status cfa_mla_describe(const cfa_mla *mla, char *buf, int len);
+
 #ifdef __cplusplus
 }
 #endif

@@ -86,6 +86,17 @@ _lib.cfa_stack_step_graph.argtypes = [_vp, _vp, _vp, ctypes.c_double, ctypes.c_f
                                       _vp]
 _lib.cfa_stack_status.restype = _i
 _lib.cfa_stack_status.argtypes = [_vp]
+_lib.cfa_mla_create.restype = _vp
+_lib.cfa_mla_create.argtypes = [_i] * 5
+_lib.cfa_mla_destroy.restype = None
+_lib.cfa_mla_destroy.argtypes = [_vp]
+_lib.cfa_mla_step.restype = _i
+_lib.cfa_mla_step.argtypes = ([_vp] * 9 + [ctypes.POINTER(ctypes.c_int), ctypes.c_double,
+                                           ctypes.c_float, _vp, _vp])
+_lib.cfa_mla_status.restype = _i
+_lib.cfa_mla_status.argtypes = [_vp]
+_lib.cfa_mla_describe.restype = _i
+_lib.cfa_mla_describe.argtypes = [_vp, ctypes.c_char_p, _i]
 _lib.cfa_stack_describe.restype = _i
 _lib.cfa_stack_describe.argtypes = [_vp, ctypes.c_char_p, _i]
 
@@ -108,6 +119,7 @@ EXPORTED_SYMBOLS = (
     "cfa_mlp_set_pipeline",
     "cfa_mlp_describe", "cfa_stack_create", "cfa_stack_destroy", "cfa_stack_set_layer",
     "cfa_stack_step", "cfa_stack_step_graph", "cfa_stack_status", "cfa_stack_describe",
+    "cfa_mla_create", "cfa_mla_destroy", "cfa_mla_step", "cfa_mla_status", "cfa_mla_describe",
 )
 
 
@@ -552,4 +564,88 @@ class Stack:
                                   stream)
         if st != CFA_OK:
             raise CfaError(st, "cfa_stack_step_graph")
+        return out
+
+
+# ------------------------------------------------ multi-head latent attention
+
+MLA_KV, MLA_NOPE, MLA_ROPE, MLA_V = 512, 128, 64, 128
+MLA_ROW = MLA_KV + MLA_ROPE
+
+
+def cfa_mla_create(B: int, hidden: int, n_heads: int, q_lora: int, max_ctx: int) -> int:
+    h = _lib.cfa_mla_create(B, hidden, n_heads, q_lora, max_ctx)
+    if not h:
+        raise CfaError(cfa_last_error(), "cfa_mla_create")
+    return h
+
+
+def cfa_mla_destroy(mla: int) -> None:
+    _lib.cfa_mla_destroy(mla)
+
+
+def cfa_mla_step(mla, x, W_a, g_q, g_kv, W_uq, W_kvb, W_o, cache, ctx_lens, rope_theta: float,
+                 eps: float, out, stream=None) -> int:
+    lens = (ctypes.c_int * len(ctx_lens))(*[int(v) for v in ctx_lens])
+    return int(_lib.cfa_mla_step(mla, _ptr(x), _ptr(W_a), _ptr(g_q), _ptr(g_kv), _ptr(W_uq),
+                                 _ptr(W_kvb), _ptr(W_o), _ptr(cache), lens, float(rope_theta),
+                                 float(eps), _ptr(out), _stream(stream)))
+
+
+def cfa_mla_status(mla) -> int:
+    return int(_lib.cfa_mla_status(mla))
+
+
+def cfa_mla_describe(mla) -> dict:
+    buf = ctypes.create_string_buffer(1024)
+    st = _lib.cfa_mla_describe(mla, buf, len(buf))
+    if st != CFA_OK:
+        raise CfaError(st, "cfa_mla_describe")
+    return json.loads(buf.value.decode())
+
+
+class Mla:
+    """Owns a cfa_mla: DeepSeek-style latent-attention decode steps."""
+
+    _KEYS = ("W_a", "g_q", "g_kv", "W_uq", "W_kvb", "W_o")
+
+    def __init__(self, B: int, hidden: int, n_heads: int, q_lora: int, max_ctx: int):
+        self.B, self.hidden, self.n_heads, self.q_lora, self.max_ctx = (
+            B, hidden, n_heads, q_lora, max_ctx)
+        self.handle = cfa_mla_create(B, hidden, n_heads, q_lora, max_ctx)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            cfa_mla_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def describe(self) -> dict:
+        return cfa_mla_describe(self.handle)
+
+    def status(self) -> int:
+        return cfa_mla_status(self.handle)
+
+    def step(self, x, weights, cache, ctx_lens, out, rope_theta: float = 10000.0,
+             eps: float = 1e-6, stream=None):
+        B, H, nh, ql, mc = self.B, self.hidden, self.n_heads, self.q_lora, self.max_ctx
+        shapes = {"W_a": (H, ql + MLA_ROW), "g_q": (ql,), "g_kv": (MLA_KV,),
+                  "W_uq": (ql, nh * (MLA_NOPE + MLA_ROPE)), "W_kvb": (MLA_KV, nh * (MLA_NOPE + MLA_V)),
+                  "W_o": (nh * MLA_V, H)}
+        for k in self._KEYS:
+            _check_tensor(k, weights[k], shapes[k])
+        _check_tensor("x", x, (B, H))
+        _check_tensor("out", out, (B, H))
+        _check_tensor("cache", cache, (B, mc, MLA_ROW))
+        if len(ctx_lens) != B:
+            raise ValueError("ctx_lens needs one entry per batch row")
+        st = cfa_mla_step(self.handle, x, *[weights[k] for k in self._KEYS], cache, ctx_lens,
+                          rope_theta, eps, out, stream)
+        if st != CFA_OK:
+            raise CfaError(st, "cfa_mla_step")
         return out

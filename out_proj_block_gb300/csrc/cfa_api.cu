@@ -849,6 +849,22 @@ cfa_status encode_bf16_2d(CUtensorMap *tm, const void *base, uint64_t cols, uint
     return encode_2d(tm, base, cols, rows, box_cols, box_rows, false);
 }
 
+cfa_status encode_bf16_2d_ex(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t rows,
+                             uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
+                             bool swizzle128) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return CFA_ERR_CUDA;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {row_stride * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), gdim,
+                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? CFA_OK : CFA_ERR_CUDA;
+}
+
 cfa_status set_last_error(cfa_status s) { return fail(s); }
 
 }  // namespace cfa

@@ -15,6 +15,8 @@ const void *gemv_kernel(int mode, int maxb) {
     }
     if (mode == kGemvSwiGLU) { CFA_GEMV_CASES(kGemvSwiGLU) }
     if (mode == kGemvResidual) { CFA_GEMV_CASES(kGemvResidual) }
+    if (mode == kGemvPlain) { CFA_GEMV_CASES(kGemvPlain) }
+    if (mode == kGemvNormPlain) { CFA_GEMV_CASES(kGemvNormPlain) }
 #undef CFA_GEMV_CASES
     return nullptr;
 }

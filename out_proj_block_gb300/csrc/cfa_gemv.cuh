@@ -115,6 +115,7 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
                     const __grid_constant__ CUtensorMap tm_x,
                     const GemvParams p) {
     constexpr bool DUAL = MODE == kGemvSwiGLU;          // gate and up side by side
+    constexpr bool NORM = DUAL || MODE == kGemvNormPlain;  // RMSNorm of the input rows
     constexpr int NW = (DUAL ? 2 : 1) * kGemvTileCols;  // partial floats per batch row
     constexpr int BOX_BYTES = DUAL ? kStageBytes / 2 : kStageBytes;
     using GS = GemvShape<MAXB>;
@@ -156,7 +157,7 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
     __syncthreads();
     grid_dependents_launch();
 
-    const uint32_t stage_tx = kStageBytes + static_cast<uint32_t>(B * R * 2 + (DUAL ? R * 2 : 0));
+    const uint32_t stage_tx = kStageBytes + static_cast<uint32_t>(B * R * 2 + (NORM ? R * 2 : 0));
 
     if (warp == kComputeWarps) {
         // ---------------------------------------------------------------- load warp
@@ -177,7 +178,7 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
                 const int k0 = (u % p.chunks) * R;
                 const uint32_t dst = xring + s * p.xstage_bytes, bar = bar_full0 + 8u * s;
                 tma_load_2d(dst, &tm_x, k0, 0, bar);
-                if constexpr (DUAL) bulk_load_1d(dst + B * R * 2, p.norm_w + k0, R * 2, bar);
+                if constexpr (NORM) bulk_load_1d(dst + B * R * 2, p.norm_w + k0, R * 2, bar);
             };
             const int n = u1 - u0;
             const int n_pre = min(NS, n);
@@ -258,14 +259,14 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
                     a1.w += __shfl_xor_sync(0xffffffffu, a1.w, off);
                 }
             }
-            if (sub != 0) continue;
+            if (sub != 0 || t * kGemvTileCols + c >= p.N) continue;  // masked columns of a last half tile
             float v[V] = {a0.x, a0.y, a0.z, a0.w};
             const size_t o2 = static_cast<size_t>(b) * p.N + static_cast<size_t>(t) * kGemvTileCols + c;
             if constexpr (DUAL) {
                 const float up[V] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                 for (int e = 0; e < V; ++e) v[e] = v[e] / (1.0f + expf(-v[e])) * up[e];  // silu(gate) * up
-            } else {
+            } else if constexpr (MODE == kGemvResidual) {
                 const uint2 rv = __ldcg(reinterpret_cast<const uint2 *>(p.resid + o2));
                 v[0] += bf16_lo(rv.x);
                 v[1] += bf16_hi(rv.x);
@@ -335,11 +336,11 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
     float *xn = reinterpret_cast<float *>(smem + p.off_xn) + warp * B * RPW;  // [B][RPW]
     grid_dependency_wait();  // no dependent read or global write before this
 
-    if constexpr (DUAL) {
+    if constexpr (NORM) {
         // RMSNorm statistics: 1 / sqrt(mean_k x[b, k]^2 + eps) for every row,
         // in a fixed order (lane tree, then warps in order).
         for (int b = 0; b < B; ++b) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(b) * p.K);
+            const uint4 *row = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(b) * p.x_stride);
             float ss = 0.f;
 #pragma unroll 4
             for (int i = tid; i < p.K / 8; i += kComputeThreads) {
@@ -416,9 +417,9 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
                                  kSiteStageFull);
         const uint16_t *xs = reinterpret_cast<const uint16_t *>(xring + s * p.xstage_bytes);
         const uint8_t *ws = ring + s * kStageBytes + half * (kTileCols * 2);
-        if constexpr (DUAL) {
-            // This warp's rows of bf16(g * x * inv_rms): the operand of both
-            // projections, rounded as a stored bf16 tensor would be.
+        if constexpr (NORM) {
+            // This warp's rows of bf16(g * x * inv_rms): the operand of the
+            // projection(s), rounded as a stored bf16 tensor would be.
             const uint16_t *gw = xs + B * R;
             for (int idx = lane; idx < B * RPW; idx += 32) {
                 const int b = idx / RPW, j = idx % RPW;
@@ -427,7 +428,8 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
             }
             __syncwarp();
             gemv_rows<MAXB, RPW>(ws, kGemvTileCols * 2, r0, xn, RPW, B, lane, acc0);
-            gemv_rows<MAXB, RPW>(ws + BOX_BYTES, kGemvTileCols * 2, r0, xn, RPW, B, lane, acc1);
+            if constexpr (DUAL)
+                gemv_rows<MAXB, RPW>(ws + BOX_BYTES, kGemvTileCols * 2, r0, xn, RPW, B, lane, acc1);
         } else {
             gemv_rows<MAXB, RPW>(ws, kGemvTileCols * 2, r0, xs + r0, R, B, lane, acc0);
         }

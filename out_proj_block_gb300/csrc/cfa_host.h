@@ -13,6 +13,7 @@ namespace cfa {
 const void *gemv_kernel(int mode, int maxb);
 const void *rmsnorm_kernel_ptr();
 const void *advance_kernel_ptr();
+const void *mla_kernel_ptr(int heads_per_cluster);  // cfa_mla.cu
 
 // The attention plan, seen from the layer stack (cfa_api.cu).
 cfa_status plan_encode_layer(const cfa_plan *pl, const void *W_qkv, const void *W_o,
@@ -28,6 +29,10 @@ unsigned *plan_status_word(cfa_plan *pl);
 // box_cols] boxes, no swizzle (cfa_api.cu).
 cfa_status encode_bf16_2d(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t rows,
                           uint32_t box_cols, uint32_t box_rows);
+// Same with an explicit row stride (elements) and optional 128-byte swizzle.
+cfa_status encode_bf16_2d_ex(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t rows,
+                             uint64_t row_stride, uint32_t box_cols, uint32_t box_rows,
+                             bool swizzle128);
 
 // Records s as the calling thread's last error and returns it.
 cfa_status set_last_error(cfa_status s);

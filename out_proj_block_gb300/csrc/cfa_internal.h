@@ -75,10 +75,12 @@ struct KernelParams {
 enum GemvMode : int {
     kGemvSwiGLU = 0,    // two matrices (gate, up), RMSNorm of the input, silu(gate) * up
     kGemvResidual = 1,  // one matrix, residual added
+    kGemvPlain = 2,     // one matrix, result stored as is
+    kGemvNormPlain = 3, // one matrix, RMSNorm of the input, result stored as is
 };
 
 struct GemvParams {
-    const uint16_t *x;       // [B][K] bf16 input rows
+    const uint16_t *x;       // [B][x_stride] bf16 input rows (the first K of each are used)
     const uint16_t *norm_w;  // [K] bf16 RMSNorm weight (SwiGLU mode)
     const uint16_t *resid;   // [B][N] bf16 residual (residual mode)
     uint16_t *y;             // [B][N] bf16 output
@@ -86,9 +88,10 @@ struct GemvParams {
     unsigned *counters;      // [n_tiles] arrivals per tile
     unsigned *status;        // device status word
     int B, K, N;
+    int x_stride;            // elements between input rows (>= K)
     int rows;                // weight rows per unit (and per stage): 32 (two matrices) or 64
     int chunks;              // units per tile: K / rows
-    int n_tiles;             // N / 128
+    int n_tiles;             // ceil(N / 128); a last tile of 64 columns is masked
     int units;               // n_tiles * chunks
     int nblocks;             // grid size
     int max_tiles;           // tiles one block can touch
@@ -96,6 +99,36 @@ struct GemvParams {
     int xstage_bytes;        // bytes of one x (+ norm weight) stage
     int off_xring, off_xn, off_scratch, off_tile, off_misc, off_bars;
     float eps;
+    unsigned long long timeout_ns;
+};
+
+// ---------------------------------------------------- multi-head latent attention
+
+constexpr int kMlaKv = 512, kMlaNope = 128, kMlaRope = 64, kMlaV = 128;
+constexpr int kMlaRow = kMlaKv + kMlaRope;          // 576 latent-row elements
+constexpr int kMlaQk = kMlaNope + kMlaRope;         // 192 query / key width
+constexpr int kMlaTileRows = 32;                    // latent rows per tile (one per lane)
+constexpr int kMlaBoxes = kMlaRow / 64;             // 9 swizzled [32 x 64] boxes per tile
+constexpr int kMlaTileBytes = kMlaBoxes * kMlaTileRows * 128;
+constexpr int kMlaMaxHG = 16;
+
+struct MlaParams {
+    const uint16_t *q;       // [B][nh*192] bf16: per head [q_nope | q_rope]
+    const uint16_t *a;       // [B][a_stride] bf16: latent at a_off, rope key at a_off + 512
+    const uint16_t *g_kv;    // [512] bf16 RMSNorm weight of the latent
+    const uint16_t *W_kvb;   // [512][nh*256] bf16
+    uint16_t *cache;         // [B][max_ctx][576] bf16
+    uint16_t *v;             // [B][nh*128] bf16 output
+    unsigned *status;
+    int B, nh, max_ctx, a_stride, a_off;
+    int ctx_lens[kMaxBatch];
+    int rope;
+    double rope_inv_freq[kMlaRope / 2];
+    float eps;
+    float qscale;            // log2(e) / sqrt(192): scores in base-2 units
+    int HG, C, HPB;          // heads per cluster, blocks per cluster, heads per block
+    int nstages;
+    int off_ring, off_newrow, off_qt, off_p, off_alpha, off_recv, off_ofin, off_scr, off_bars;
     unsigned long long timeout_ns;
 };
 

@@ -107,9 +107,12 @@ struct GemvPlan {
 cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan *out,
                      int bps_req = 0, int ns_req = 0) {
     const bool dual = mode == cfa::kGemvSwiGLU;
+    const bool norm = dual || mode == cfa::kGemvNormPlain;
     const int TW = cfa::kGemvTileCols;
     const int R = dual ? 32 : 64;  // 16 KB of weights per unit either way
-    if (K < R || K % R || N < TW || N % TW) return CFA_ERR_UNSUPPORTED;
+    // N a multiple of 64: a last tile of 64 columns reads zeros past N and
+    // stores nothing there.
+    if (K < R || K % R || N < 64 || N % 64) return CFA_ERR_UNSUPPORTED;
     int maxb = 1;
     while (maxb < B) maxb <<= 1;
     const void *kernel = cfa::gemv_kernel(mode, maxb);
@@ -122,11 +125,12 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     p.N = N;
     p.rows = R;
     p.chunks = K / R;
-    p.n_tiles = N / TW;
+    p.n_tiles = (N + TW - 1) / TW;
+    p.x_stride = K;
     p.units = p.n_tiles * p.chunks;
-    p.xstage_bytes = align_up(B * R * 2 + (dual ? R * 2 : 0), 128);
+    p.xstage_bytes = align_up(B * R * 2 + (norm ? R * 2 : 0), 128);
     // per-warp normalized input rows: 8 warps x [B][R/4] floats
-    const int xn = dual ? align_up(cfa::kComputeWarps * B * (R / 4) * 4, 128) : 0;
+    const int xn = norm ? align_up(cfa::kComputeWarps * B * (R / 4) * 4, 128) : 0;
     const int scratch = align_up(cfa::kComputeWarps * B * cfa::kTileCols * 4, 128);
     const int tile = align_up(2 * B * NW * 4, 128);  // two tile buffers
     const int misc = 128;
@@ -708,6 +712,306 @@ cfa_status cfa_stack_describe(const cfa_stack *s, char *buf, int len) {
     std::snprintf(buf, static_cast<size_t>(len),
                   "{\"n_layers\": %d, \"launches_per_token\": %d, \"attention\": %s, \"mlp\": %s}",
                   s->L, 4 * s->L, a, m);
+    return CFA_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------- MLA
+
+struct cfa_mla {
+    int B = 0, H = 0, nh = 0, q_lora = 0, max_ctx = 0;
+    Device dev;
+    GemvPlan ga, gq, go;          // x.W_a, norm(cq).W_uq, v.W_o
+    uint16_t *a = nullptr;        // [B][q_lora + 576]
+    uint16_t *q = nullptr;        // [B][nh*192]
+    uint16_t *v = nullptr;        // [B][nh*128]
+    float *partials = nullptr;
+    unsigned *words = nullptr;    // counters of the three GEMVs, GEMV status, kernel status
+    CUtensorMap tm_aq, tm_v;      // inputs of the q and output GEMVs (fixed buffers)
+    cfa::MlaParams mp{};
+    int smem = 0;
+    int coresident_clusters = 0;
+};
+
+namespace {
+
+constexpr int kMlaStages = 3;
+
+void mla_free(cfa_mla *m) {
+    if (m->a) cudaFree(m->a);
+    if (m->q) cudaFree(m->q);
+    if (m->v) cudaFree(m->v);
+    if (m->partials) cudaFree(m->partials);
+    if (m->words) cudaFree(m->words);
+    m->a = m->q = m->v = nullptr;
+    m->partials = nullptr;
+    m->words = nullptr;
+}
+
+unsigned *mla_gemv_status(cfa_mla *m) {
+    return m->words + m->ga.gp.n_tiles + m->gq.gp.n_tiles + m->go.gp.n_tiles;
+}
+
+GemvParams gemv_params(const GemvPlan &g, const void *x, const void *norm_w, const void *resid,
+                       void *y, float *partials, unsigned *counters, unsigned *status, float eps) {
+    GemvParams p = g.gp;
+    p.x = static_cast<const uint16_t *>(x);
+    p.norm_w = static_cast<const uint16_t *>(norm_w);
+    p.resid = static_cast<const uint16_t *>(resid);
+    p.y = static_cast<uint16_t *>(y);
+    p.partials = partials;
+    p.counters = counters;
+    p.status = status;
+    p.eps = eps;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx) {
+    if (B < 1 || hidden < 1 || n_heads < 1 || q_lora < 1 || max_ctx < 1) {
+        fail(CFA_ERR_INVALID_ARG);
+        return nullptr;
+    }
+    int HG = 1;
+    while (HG < cfa::kMlaMaxHG && n_heads % (2 * HG) == 0) HG *= 2;
+    if (B > cfa::kMaxBatch || hidden % 64 || hidden > (1 << 16) || q_lora % 64 ||
+        q_lora > (1 << 14) || HG < 2 || max_ctx > (1 << 22) || n_heads > 4096) {
+        fail(CFA_ERR_UNSUPPORTED);
+        return nullptr;
+    }
+    Device dev;
+    cfa_status st = query_device(&dev);
+    if (st != CFA_OK) {
+        fail(st);
+        return nullptr;
+    }
+    cfa_mla *m = new (std::nothrow) cfa_mla();
+    if (!m) {
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    m->B = B;
+    m->H = hidden;
+    m->nh = n_heads;
+    m->q_lora = q_lora;
+    m->max_ctx = max_ctx;
+    m->dev = dev;
+    const int NA = q_lora + cfa::kMlaRow, NQ = n_heads * cfa::kMlaQk, NV = n_heads * cfa::kMlaV;
+    if ((st = make_gemv(dev, cfa::kGemvPlain, B, hidden, NA, &m->ga)) != CFA_OK ||
+        (st = make_gemv(dev, cfa::kGemvNormPlain, B, q_lora, NQ, &m->gq)) != CFA_OK ||
+        (st = make_gemv(dev, cfa::kGemvPlain, B, NV, hidden, &m->go)) != CFA_OK) {
+        delete m;
+        fail(st);
+        return nullptr;
+    }
+    m->gq.gp.x_stride = NA;  // the query GEMV reads the first q_lora columns of a
+
+    // The attention kernel: C = HG blocks per cluster, one head each in the
+    // gather and the reduce-scatter.
+    cfa::MlaParams &mp = m->mp;
+    mp.B = B;
+    mp.nh = n_heads;
+    mp.max_ctx = max_ctx;
+    mp.a_stride = NA;
+    mp.a_off = q_lora;
+    mp.HG = HG;
+    mp.C = HG;
+    mp.HPB = 1;
+    mp.nstages = kMlaStages;
+    mp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(cfa::kMlaQk)));
+    mp.timeout_ns = kTimeoutNs;
+    int off = 0;
+    mp.off_ring = off;
+    off += kMlaStages * cfa::kMlaTileBytes;
+    mp.off_newrow = off;
+    off += align_up(cfa::kMlaRow * 2, 128);
+    mp.off_qt = off;
+    off += align_up(HG * cfa::kMlaRow * 4, 128);
+    mp.off_p = off;
+    off += align_up(cfa::kMlaTileRows * HG * 4, 128);
+    mp.off_alpha = off;
+    off += 128;
+    mp.off_recv = off;
+    off += align_up(mp.HPB * mp.C * (cfa::kMlaKv + 4) * 4, 128);
+    mp.off_ofin = off;
+    off += align_up(mp.HPB * cfa::kMlaKv * 4, 128);
+    mp.off_scr = off;
+    off += align_up((cfa::kComputeWarps * cfa::kMlaV + 64) * 4, 128);
+    mp.off_bars = off;
+    off += 16 * kMlaStages + 32;
+    m->smem = off;
+    const void *kernel = cfa::mla_kernel_ptr(HG);
+    if (!kernel || off > dev.smem_optin ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        delete m;
+        fail(CFA_ERR_UNSUPPORTED);
+        return nullptr;
+    }
+    {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = mp.C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(B * (n_heads / HG) * mp.C);
+        cfg.blockDim = dim3(cfa::kThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(m->smem);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            delete m;
+            fail(CFA_ERR_UNSUPPORTED);
+            return nullptr;
+        }
+        m->coresident_clusters = clusters;
+    }
+
+    const size_t nwords = static_cast<size_t>(m->ga.gp.n_tiles + m->gq.gp.n_tiles +
+                                              m->go.gp.n_tiles + 2);
+    const size_t pf = std::max(m->ga.partial_floats, std::max(m->gq.partial_floats, m->go.partial_floats));
+    if (cudaMalloc(&m->a, 2u * static_cast<size_t>(B) * NA) != cudaSuccess ||
+        cudaMalloc(&m->q, 2u * static_cast<size_t>(B) * NQ) != cudaSuccess ||
+        cudaMalloc(&m->v, 2u * static_cast<size_t>(B) * NV) != cudaSuccess ||
+        cudaMalloc(&m->partials, sizeof(float) * pf) != cudaSuccess ||
+        cudaMalloc(&m->words, sizeof(unsigned) * nwords) != cudaSuccess ||
+        cudaMemset(m->words, 0, sizeof(unsigned) * nwords) != cudaSuccess) {
+        cudaGetLastError();
+        mla_free(m);
+        delete m;
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    if (cfa::encode_bf16_2d_ex(&m->tm_aq, m->a, q_lora, B, NA, 64, B, false) != CFA_OK ||
+        cfa::encode_bf16_2d(&m->tm_v, m->v, NV, B, 64, B) != CFA_OK) {
+        mla_free(m);
+        delete m;
+        fail(CFA_ERR_CUDA);
+        return nullptr;
+    }
+    return m;
+}
+
+void cfa_mla_destroy(cfa_mla *m) {
+    if (!m) return;
+    cudaDeviceSynchronize();
+    mla_free(m);
+    delete m;
+}
+
+cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *g_q,
+                        const void *g_kv, const void *W_uq, const void *W_kvb, const void *W_o,
+                        void *cache, const int *ctx_lens, double rope_theta, float eps, void *out,
+                        void *stream) {
+    if (!m || !x || !W_a || !g_q || !g_kv || !W_uq || !W_kvb || !W_o || !cache || !ctx_lens ||
+        !out || !(eps >= 0.0f) || !std::isfinite(eps) || !(rope_theta >= 0.0) || rope_theta > 1e30)
+        return fail(CFA_ERR_INVALID_ARG);
+    for (int b = 0; b < m->B; ++b)
+        if (ctx_lens[b] < 0 || ctx_lens[b] >= m->max_ctx) return fail(CFA_ERR_INVALID_ARG);
+    const void *ptrs[9] = {x, W_a, g_q, g_kv, W_uq, W_kvb, W_o, cache, out};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr)) return fail(CFA_ERR_ALIGNMENT);
+    const size_t act = 2u * static_cast<size_t>(m->B) * m->H;
+    const size_t cache_bytes = 2u * static_cast<size_t>(m->B) * m->max_ctx * cfa::kMlaRow;
+    if (overlaps(out, act, x, act) || overlaps(out, act, cache, cache_bytes) ||
+        overlaps(out, act, W_o, 2u * static_cast<size_t>(m->nh) * cfa::kMlaV * m->H))
+        return fail(CFA_ERR_INVALID_ARG);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int NA = m->q_lora + cfa::kMlaRow, NQ = m->nh * cfa::kMlaQk, NV = m->nh * cfa::kMlaV;
+
+    // tensor maps of this call's operands (host work only)
+    CUtensorMap tm_x, tm_wa, tm_wuq, tm_wo, tm_cache, tm_wkvb;
+    if (cfa::encode_bf16_2d(&tm_x, x, m->H, m->B, 64, m->B) != CFA_OK ||
+        cfa::encode_bf16_2d(&tm_wa, W_a, NA, m->H, cfa::kGemvTileCols, 64) != CFA_OK ||
+        cfa::encode_bf16_2d(&tm_wuq, W_uq, NQ, m->q_lora, cfa::kGemvTileCols, 64) != CFA_OK ||
+        cfa::encode_bf16_2d(&tm_wo, W_o, m->H, NV, cfa::kGemvTileCols, 64) != CFA_OK ||
+        cfa::encode_bf16_2d_ex(&tm_cache, cache, cfa::kMlaRow,
+                               static_cast<uint64_t>(m->B) * m->max_ctx, cfa::kMlaRow, 64,
+                               cfa::kMlaTileRows, true) != CFA_OK ||
+        cfa::encode_bf16_2d_ex(&tm_wkvb, W_kvb, static_cast<uint64_t>(m->nh) * 256, cfa::kMlaKv,
+                               static_cast<uint64_t>(m->nh) * 256, 128, 256, false) != CFA_OK)
+        return fail(CFA_ERR_CUDA);
+
+    unsigned *gst = mla_gemv_status(m);
+    unsigned *ctr = m->words;
+    // a = bf16(x . W_a)
+    GemvParams pa = gemv_params(m->ga, x, nullptr, nullptr, m->a, m->partials, ctr, gst, eps);
+    cfa_status st = launch_gemv(m->ga, pa, &tm_wa, &tm_wa, &tm_x, cs);
+    if (st != CFA_OK) return fail(st);
+    ctr += m->ga.gp.n_tiles;
+    // q = bf16(bf16(rmsnorm(a[:, :q_lora]; g_q)) . W_uq)
+    GemvParams pq = gemv_params(m->gq, m->a, g_q, nullptr, m->q, m->partials, ctr, gst, eps);
+    if ((st = launch_gemv(m->gq, pq, &tm_wuq, &tm_wuq, &m->tm_aq, cs)) != CFA_OK) return fail(st);
+    ctr += m->gq.gp.n_tiles;
+    // v: the latent attention core
+    cfa::MlaParams mp = m->mp;
+    mp.q = m->q;
+    mp.a = m->a;
+    mp.g_kv = static_cast<const uint16_t *>(g_kv);
+    mp.W_kvb = static_cast<const uint16_t *>(W_kvb);
+    mp.cache = static_cast<uint16_t *>(cache);
+    mp.v = m->v;
+    mp.status = gst + 1;
+    mp.eps = eps;
+    for (int b = 0; b < m->B; ++b) mp.ctx_lens[b] = ctx_lens[b];
+    mp.rope = rope_theta > 0.0 ? 1 : 0;
+    for (int i = 0; i < cfa::kMlaRope / 2; ++i)
+        mp.rope_inv_freq[i] = mp.rope ? std::pow(rope_theta, -2.0 * i / cfa::kMlaRope) : 0.0;
+    {
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = mp.C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(m->B * (m->nh / mp.HG) * mp.C);
+        cfg.blockDim = dim3(cfa::kThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(m->smem);
+        cfg.stream = cs;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        void *args[3] = {&tm_cache, &tm_wkvb, &mp};
+        if (cudaLaunchKernelExC(&cfg, cfa::mla_kernel_ptr(mp.HG), args) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(CFA_ERR_CUDA);
+        }
+    }
+    // out = bf16(v . W_o)
+    GemvParams po = gemv_params(m->go, m->v, nullptr, nullptr, out, m->partials, ctr, gst, eps);
+    if ((st = launch_gemv(m->go, po, &tm_wo, &tm_wo, &m->tm_v, cs)) != CFA_OK) return fail(st);
+    return CFA_OK;
+}
+
+cfa_status cfa_mla_status(cfa_mla *m) {
+    if (!m) return fail(CFA_ERR_INVALID_ARG);
+    cfa_status a = read_status(mla_gemv_status(m));
+    cfa_status b = read_status(mla_gemv_status(m) + 1);
+    if (a != CFA_OK) return fail(a);
+    return b == CFA_OK ? CFA_OK : fail(b);
+}
+
+cfa_status cfa_mla_describe(const cfa_mla *m, char *buf, int len) {
+    if (!m || !buf || len < 1) return fail(CFA_ERR_INVALID_ARG);
+    std::snprintf(buf, static_cast<size_t>(len),
+                  "{\"B\": %d, \"hidden\": %d, \"n_heads\": %d, \"q_lora\": %d, \"max_ctx\": %d, "
+                  "\"heads_per_cluster\": %d, \"cluster_size\": %d, \"grid\": %d, "
+                  "\"smem_bytes\": %d, \"stages\": %d, \"coresident_clusters\": %d, "
+                  "\"gemv_grids\": [%d, %d, %d]}",
+                  m->B, m->H, m->nh, m->q_lora, m->max_ctx, m->mp.HG, m->mp.C,
+                  m->B * (m->nh / m->mp.HG) * m->mp.C, m->smem, m->mp.nstages,
+                  m->coresident_clusters, m->ga.gp.nblocks, m->gq.gp.nblocks, m->go.gp.nblocks);
     return CFA_OK;
 }
 
