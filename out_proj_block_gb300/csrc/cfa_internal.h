@@ -4,6 +4,8 @@
 
 #include <cstdint>
 
+#include <cuda.h>
+
 namespace cfa {
 
 constexpr int kComputeWarps = 8;                   // warps doing arithmetic
@@ -107,10 +109,12 @@ struct GemvParams {
 constexpr int kMlaKv = 512, kMlaNope = 128, kMlaRope = 64, kMlaV = 128;
 constexpr int kMlaRow = kMlaKv + kMlaRope;          // 576 latent-row elements
 constexpr int kMlaQk = kMlaNope + kMlaRope;         // 192 query / key width
-constexpr int kMlaTileRows = 32;                    // latent rows per tile (one per lane)
-constexpr int kMlaBoxes = kMlaRow / 64;             // 9 swizzled [32 x 64] boxes per tile
-constexpr int kMlaTileBytes = kMlaBoxes * kMlaTileRows * 128;
-constexpr int kMlaMaxHG = 16;
+constexpr int kMlaTileRows = 128;                   // latent rows per tile (MMA M)
+constexpr int kMlaBoxes = kMlaRow / 64;             // 9 swizzled [128 x 64] boxes per tile
+constexpr int kMlaBoxBytes = kMlaTileRows * 128;    // 16 KB
+constexpr int kMlaStageBytes = 2 * kMlaBoxBytes;    // a stage holds two boxes
+constexpr int kMlaMaxHG = 16;                       // heads per cluster = MMA N
+constexpr int kMlaAtomBytes = kMlaMaxHG * 128;      // a [16 x 64] K-major swizzled atom
 
 struct MlaParams {
     const uint16_t *q;       // [B][nh*192] bf16: per head [q_nope | q_rope]
@@ -128,8 +132,15 @@ struct MlaParams {
     float qscale;            // log2(e) / sqrt(192): scores in base-2 units
     int HG, C, HPB;          // heads per cluster, blocks per cluster, heads per block
     int nstages;
-    int off_ring, off_newrow, off_qt, off_p, off_alpha, off_recv, off_ofin, off_scr, off_bars;
+    int off_ring, off_qhi, off_qlo, off_pb, off_qt, off_newrow, off_stat, off_recv, off_ofin,
+        off_scr, off_bars;
     unsigned long long timeout_ns;
+};
+
+// One latent-cache tensor map per sequence, limited to its cached rows, so a
+// tile running past them reads zeros.
+struct __align__(64) MlaMaps {
+    CUtensorMap cache[kMaxBatch];
 };
 
 }  // namespace cfa

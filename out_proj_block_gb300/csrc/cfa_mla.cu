@@ -1,15 +1,12 @@
-// Instantiations of the multi-head latent attention core kernel (see cfa_mla.cuh).
+// The multi-head latent attention core kernel (see cfa_mla.cuh).
 #include "cfa_mla.cuh"
 
 namespace cfa {
 
-// heads_per_cluster <= 8: one head scored per warp; 16: two.
+// Any head-group size up to 16 runs the same kernel (the MMA's N is 16).
 const void *mla_kernel_ptr(int heads_per_cluster) {
-    if (heads_per_cluster <= kComputeWarps)
-        return reinterpret_cast<const void *>(&mla_attention_kernel<1>);
-    if (heads_per_cluster == 2 * kComputeWarps)
-        return reinterpret_cast<const void *>(&mla_attention_kernel<2>);
-    return nullptr;
+    if (heads_per_cluster < 2 || heads_per_cluster > kMlaMaxHG) return nullptr;
+    return reinterpret_cast<const void *>(&mla_attention_kernel);
 }
 
 }  // namespace cfa

@@ -13,7 +13,9 @@
 // value blocks of W_kvb [512, nh*256],
 //   q~_h  = W_k,h q_nope,h            (512)      score_t = q~_h . c_t + rope(q_rope,h) . k_rope_t
 //   o_h   = sum_t softmax_t c_t       (512)      v_h     = o_h . W_v,h   (128)
-// which equals attention over the decompressed keys and values.
+// which equals attention over the decompressed keys and values. The heads of a
+// group share every latent byte, so the latent attention is a dense
+// contraction and runs on the tensor cores.
 //
 // Grid: B x (nh / HG) clusters of C blocks; cluster (b, g) owns heads
 // [g HG, (g+1) HG) of sequence b and block r of it owns the latent rows
@@ -22,13 +24,18 @@
 //     rotated rope query of its HPB = HG / C heads (reading their W_k block
 //     once) and pushes them to every block of the cluster (ClusterGather over
 //     DSMEM, st.async + transaction counts), so every block holds all HG
-//     queries. The last block builds the new latent row (RMSNorm of the
-//     latent part, rope of the key part, bf16) on chip; one block appends it.
-//  B  Latent attention over the block's rows for all HG heads: latent rows
-//     arrive by TMA in 128-byte-swizzled [32 x 64] boxes through a stage
-//     ring; per 32-row tile, each warp scores its heads (lane = row), keeps a
-//     base-2 online softmax per head, and all warps accumulate the
-//     unnormalised latent outputs o_h (head quad x 256 latent dims each).
+//     queries; they become bf16 hi + lo operands (about 16 bits together).
+//     The last block builds the new latent row (RMSNorm of the latent part,
+//     rope of the key part, bf16) on chip; one block appends it.
+//  B  Latent attention over the block's cached rows, 128 rows per tile, with
+//     tcgen05 and TMEM accumulators: S^T = C Q^T (M = 128 rows, N = 16 heads,
+//     K = 576; the row tile is the K-major A operand, straight from its
+//     128-byte-swizzled TMA boxes), a base-2 online softmax per head across
+//     the tile (TMEM lane = row), P written as a bf16 K-major operand, then
+//     O^T = C^T P^T (M = 4 x 128 latent dims, the same boxes read MN-major,
+//     K = 128 rows), folded into fp32 registers. The latent boxes stream
+//     through a ring of two-box stages twice per tile (scores, then values;
+//     the second pass hits L2). The new row is attended on CUDA cores.
 //  C  Sparse ClusterReduce [CF §5.2]: a reduce-scatter over the cluster --
 //     block r receives, for its own HPB heads only, every block's (m, l, o)
 //     and combines them in block order (deterministic); then v_h = o_h W_v,h.
@@ -43,16 +50,38 @@
 
 namespace cfa {
 
-// Byte offset of row t, latent columns [64 kc + 8 j, +8) in a tile of
-// [rows x 64] boxes with 128-byte swizzle (box_stride bytes apart).
-__device__ __forceinline__ uint32_t mla_tile_off(int box_stride, int t, int kc, int j) {
-    return static_cast<uint32_t>(kc * box_stride + t * 128 + ((j ^ (t & 7)) << 4));
+// 8 consecutive fp32 TMEM columns of this warp's 32 lanes (one lane per thread).
+__device__ __forceinline__ void mla_tmem_ld_x8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// HPW: heads each warp scores (HG / 8, at least 1).
-template <int HPW>
+// Byte offset of element (row n, column k < 64) of a [rows x 64] K-major
+// operand atom with 128-byte swizzle (16-byte chunks permuted by n mod 8).
+__device__ __forceinline__ uint32_t mla_atom_off(int n, int k) {
+    return static_cast<uint32_t>(n * 128 + (((k >> 3) ^ (n & 7)) << 4) + (k & 7) * 2);
+}
+
+// Rotate-half rotation of (x0, x1) = dims (k, k + 32) by pos * inv_freq, the
+// angle taken in fp64 and reduced to (-pi, pi] before the fp32 sine/cosine.
+__device__ __forceinline__ void mla_rope(float &x0, float &x1, int pos, double inv_freq) {
+    const double ang = static_cast<double>(pos) * inv_freq;
+    const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+    float sn, cs;
+    sincosf(static_cast<float>(red), &sn, &cs);
+    const float y0 = x0 * cs - x1 * sn, y1 = x1 * cs + x0 * sn;
+    x0 = y0;
+    x1 = y1;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
+mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                      const __grid_constant__ CUtensorMap tm_wkvb, const MlaParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -68,32 +97,49 @@ mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
     const int cache_e = min(row_e, L);                       // rows read from the cache
     const bool has_new = row_e == T;                         // this block attends the new row
     const int n_tiles = cache_e > row_s ? (cache_e - row_s + kMlaTileRows - 1) / kMlaTileRows : 0;
+    constexpr int kSStages = (kMlaBoxes + 1) / 2;            // score pass: 5 stages (last: one box)
+    constexpr int kVStages = kMlaKv / 128;                   // value pass: 4 stages of 128 dims
 
-    float *qt = reinterpret_cast<float *>(smem + p.off_qt);        // [HG][576] scaled queries
-    float *pbuf = reinterpret_cast<float *>(smem + p.off_p);       // [32][HG] probabilities
-    float *alpha = reinterpret_cast<float *>(smem + p.off_alpha);  // [HG] rescale of o
-    float *recv = reinterpret_cast<float *>(smem + p.off_recv);    // [HPB][C][516]
-    float *ofin = reinterpret_cast<float *>(smem + p.off_ofin);    // [HPB][512]
-    float *scr = reinterpret_cast<float *>(smem + p.off_scr);      // [8][128] + 64
-    uint8_t *newrow = smem + p.off_newrow;                         // 1-row tile (1152 B)
+    float *qt = reinterpret_cast<float *>(smem + p.off_qt);      // [HG][576] scaled queries, fp32
+    float *stat = reinterpret_cast<float *>(smem + p.off_stat);
+    float *m_st = stat;               // [16] running max per head (base 2)
+    float *l_st = stat + 16;          // [16] running sum
+    float *alpha = stat + 32;         // [16] rescale of o for the current tile
+    float *red_max = stat + 48;       // [8 warps][16]
+    float *red_sum = stat + 176;      // [8 warps][16]
+    float *s_new = stat + 304;        // [16] score, then probability, of the new row
+    float *recv = reinterpret_cast<float *>(smem + p.off_recv);  // [HPB][C][516]
+    float *ofin = reinterpret_cast<float *>(smem + p.off_ofin);  // [HPB][512]
+    float *scr = reinterpret_cast<float *>(smem + p.off_scr);    // [8][128] + 64
+    uint16_t *newrow = reinterpret_cast<uint16_t *>(smem + p.off_newrow);  // [576] bf16
+    const uint32_t ring = smem_addr(smem + p.off_ring);
+    const uint32_t qhi = smem_addr(smem + p.off_qhi), qlo = smem_addr(smem + p.off_qlo);
+    const uint32_t pb = smem_addr(smem + p.off_pb);
     const uint32_t bar_full0 = smem_addr(smem + p.off_bars);
     const uint32_t bar_empty0 = bar_full0 + 8u * NS;
     const uint32_t bar_q = bar_full0 + 16u * NS;      // every peer's queries have landed
     const uint32_t bar_red = bar_q + 8u;              // every peer's partials for my heads
-    volatile int *timed_out = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 16);
+    const uint32_t bar_s = bar_q + 16u;               // a tile's scores are in TMEM
+    const uint32_t bar_o = bar_q + 24u;               // a tile's latent outputs are in TMEM
+    volatile int *timed_out = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 32);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 16 * NS + 48);
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar_full0 + 8u * s, 1);
-            mbar_init(bar_empty0 + 8u * s, kComputeWarps);
+            mbar_init(bar_empty0 + 8u * s, 1);     // released by the MMAs' commit
         }
         mbar_init(bar_q, 1);
         mbar_init(bar_red, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
         *timed_out = 0;
         fence_mbar_init();
         mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>((C - 1) * HPB * kMlaRow * 4));
         mbar_arrive_expect_tx(bar_red, static_cast<uint32_t>((C - 1) * HPB * (kMlaKv + 4) * 4));
     }
+    if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 128);  // S: cols [0,16); O: [16,80)
+    tcgen05_fence_before();
     __syncthreads();
     grid_dependents_launch();
     cluster_arrive();  // barriers announced; waited for before the first push
@@ -111,18 +157,23 @@ mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
                                  : "memory");
             }
             grid_dependency_wait();  // cache rows may come from the previous step
+            const CUtensorMap *tm = &maps.cache[b];
             RingCursor cur;
-            for (int i = 0; i < n_tiles; ++i) {
+            auto stage_in = [&](int kc0, int nbox, int row) {
                 if (cur.wrapped)
                     mbar_wait_bounded<false>(bar_empty0 + 8u * cur.stage, cur.phase ^ 1u,
                                              p.timeout_ns, timed_out, p.status, kSiteStageEmpty);
                 const uint32_t full = bar_full0 + 8u * cur.stage;
-                const uint32_t dst = smem_addr(smem + p.off_ring) + cur.stage * kMlaTileBytes;
-                mbar_arrive_expect_tx(full, kMlaTileBytes);
-                const int row = b * p.max_ctx + row_s + i * kMlaTileRows;
-                for (int kc = 0; kc < kMlaBoxes; ++kc)
-                    tma_load_2d(dst + kc * kMlaTileRows * 128, &tm_cache, kc * 64, row, full);
+                const uint32_t dst = ring + cur.stage * kMlaStageBytes;
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox * kMlaBoxBytes));
+                for (int i = 0; i < nbox; ++i)
+                    tma_load_2d(dst + i * kMlaBoxBytes, tm, (kc0 + i) * 64, row, full);
                 cur.advance(NS);
+            };
+            for (int t = 0; t < n_tiles; ++t) {
+                const int row = row_s + t * kMlaTileRows;  // rows past the map's end read as zero
+                for (int sp = 0; sp < kSStages; ++sp) stage_in(2 * sp, min(2, kMlaBoxes - 2 * sp), row);
+                for (int vp = 0; vp < kVStages; ++vp) stage_in(2 * vp, 2, row);
             }
             for (int s = 0; s < NS; ++s) {  // drain
                 if (s >= cur.stage && !cur.wrapped) break;
@@ -140,6 +191,8 @@ mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
     }
 
     // --------------------------------------------------------------- compute
+    tcgen05_fence_after();
+    const uint32_t tmem = *tmem_slot;
     grid_dependency_wait();
     // ---- A: absorbed queries of this block's heads, pushed to the cluster ----
     {
@@ -179,21 +232,11 @@ mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
                 dst[tid] = a0 * p.qscale;
                 dst[tid + kComputeThreads] = a1 * p.qscale;
             }
-            // rope of the rope query at position L (rotate-half, angle in fp64)
             if (tid < kMlaRope / 2) {
-                const int k = tid;
-                float x0 = bf16_bits(qh[kMlaNope + k]), x1 = bf16_bits(qh[kMlaNope + k + kMlaRope / 2]);
-                if (p.rope) {
-                    const double ang = static_cast<double>(L) * p.rope_inv_freq[k];
-                    const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
-                    float sn, cs;
-                    sincosf(static_cast<float>(red), &sn, &cs);
-                    const float y0 = x0 * cs - x1 * sn, y1 = x1 * cs + x0 * sn;
-                    x0 = y0;
-                    x1 = y1;
-                }
-                dst[kMlaKv + k] = x0 * p.qscale;
-                dst[kMlaKv + k + kMlaRope / 2] = x1 * p.qscale;
+                float x0 = bf16_bits(qh[kMlaNope + tid]), x1 = bf16_bits(qh[kMlaNope + tid + kMlaRope / 2]);
+                if (p.rope) mla_rope(x0, x1, L, p.rope_inv_freq[tid]);
+                dst[kMlaKv + tid] = x0 * p.qscale;
+                dst[kMlaKv + tid + kMlaRope / 2] = x1 * p.qscale;
             }
             compute_bar<kComputeThreads>();
         }
@@ -209,7 +252,7 @@ mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
         }
     }
     // The new token's latent row (last block): bf16 RMSNorm of the latent and
-    // bf16 rope of the key, in the one-row tile layout; one block appends it.
+    // bf16 rope of the key; one block appends it to the cache.
     if (has_new) {
         const uint16_t *ar = p.a + static_cast<size_t>(b) * p.a_stride + p.a_off;
         float ss = 0.f;
@@ -225,171 +268,222 @@ mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
 #pragma unroll
         for (int w = 0; w < kComputeWarps; ++w) tot += scr[kMlaNope + w];
         const float inv = 1.0f / sqrtf(tot / static_cast<float>(kMlaKv) + p.eps);
-        uint16_t *nr = reinterpret_cast<uint16_t *>(newrow);  // row 0: plain 1152-byte row
         for (int i = tid; i < kMlaKv; i += kComputeThreads)
-            nr[i] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits(p.g_kv[i]) * bf16_bits(ar[i]) * inv));
+            newrow[i] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits(p.g_kv[i]) * bf16_bits(ar[i]) * inv));
         if (tid < kMlaRope / 2) {
-            const int k = tid;
-            float x0 = bf16_bits(ar[kMlaKv + k]), x1 = bf16_bits(ar[kMlaKv + k + kMlaRope / 2]);
-            if (p.rope) {
-                const double ang = static_cast<double>(L) * p.rope_inv_freq[k];
-                const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
-                float sn, cs;
-                sincosf(static_cast<float>(red), &sn, &cs);
-                const float y0 = x0 * cs - x1 * sn, y1 = x1 * cs + x0 * sn;
-                x0 = y0;
-                x1 = y1;
-            }
-            nr[kMlaKv + k] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
-            nr[kMlaKv + k + kMlaRope / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(x1));
+            float x0 = bf16_bits(ar[kMlaKv + tid]), x1 = bf16_bits(ar[kMlaKv + tid + kMlaRope / 2]);
+            if (p.rope) mla_rope(x0, x1, L, p.rope_inv_freq[tid]);
+            newrow[kMlaKv + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
+            newrow[kMlaKv + tid + kMlaRope / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(x1));
         }
         compute_bar<kComputeThreads>();
         if (g == 0) {
             uint16_t *crow = p.cache + (static_cast<size_t>(b) * p.max_ctx + L) * kMlaRow;
             for (int i = tid; i < kMlaRow / 8; i += kComputeThreads)
-                reinterpret_cast<uint4 *>(crow)[i] = reinterpret_cast<const uint4 *>(nr)[i];
+                reinterpret_cast<uint4 *>(crow)[i] = reinterpret_cast<const uint4 *>(newrow)[i];
         }
     }
     mbar_wait_bounded<true>(bar_q, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
 
-    // ---- B: latent attention over this block's rows, all HG heads --------------
-    const int h_sc = warp * HPW;                                    // first head this warp scores
-    const bool scores_warp = h_sc < HG;
-    float m_run[HPW], l_run[HPW];
-#pragma unroll
-    for (int hh = 0; hh < HPW; ++hh) {
-        m_run[hh] = -INFINITY;
-        l_run[hh] = 0.f;
+    // Queries as the B operand of the score MMA: bf16 hi and lo parts in
+    // [16 x 64] K-major swizzled atoms (heads past HG are zero), and the
+    // running softmax state.
+    for (int i = tid; i < kMlaMaxHG * kMlaRow; i += kComputeThreads) {
+        const int n = i / kMlaRow, k = i % kMlaRow;
+        const float v = n < HG ? qt[n * kMlaRow + k] : 0.f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        const uint32_t off = (k >> 6) * kMlaAtomBytes + mla_atom_off(n, k & 63);
+        *reinterpret_cast<uint16_t *>(smem + p.off_qhi + off) = __bfloat16_as_ushort(hi);
+        *reinterpret_cast<uint16_t *>(smem + p.off_qlo + off) = __bfloat16_as_ushort(lo);
     }
-    const int hq = warp % 4;                   // output head quad
-    const int dh = warp / 4;                   // output latent half
-    float acc[4][8];
-#pragma unroll
-    for (int hh = 0; hh < 4; ++hh)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[hh][e] = 0.f;
+    if (tid < kMlaMaxHG) {
+        m_st[tid] = -INFINITY;
+        l_st[tid] = 0.f;
+    }
+    fence_proxy_async_smem();
+    compute_bar<kComputeThreads>();
 
-    auto process_tile = [&](const uint8_t *tile, int box_stride, int nvalid) {
-        // scores: lane = row, this warp's heads
-        if (scores_warp) {
-            // two partial sums per head (even / odd 8-column chunks) for ILP
-            float s[HPW][2];
+    // ---- B: latent attention on the tensor cores --------------------------------
+    // TMEM lanes 32 (warp % 4) + lane are this thread's tile row (scores) and
+    // latent dim within a 128-dim block (outputs); warps 0-3 take heads 0-7 of
+    // the scores and latent blocks 0-1, warps 4-7 heads 8-15 and blocks 2-3.
+    const int wq = warp & 3, wh = warp >> 2;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * wq) << 16);
+    float acc[2][kMlaMaxHG];  // unnormalised o^T, latent dims 128 (2 wh + i) + 32 wq + lane
 #pragma unroll
-            for (int hh = 0; hh < HPW; ++hh) s[hh][0] = s[hh][1] = 0.f;
-            if (lane < nvalid) {
-#pragma unroll 1
-                for (int kc = 0; kc < kMlaBoxes; ++kc) {
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float c8[8];
-                        unpack8_bf16(*reinterpret_cast<const uint4 *>(tile + mla_tile_off(box_stride, lane, kc, j)), c8);
+        for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = 0.f;
+    const uint32_t idesc_s = umma_idesc_bf16(128, kMlaMaxHG, false, false);  // A K-major
+    const uint32_t idesc_o = umma_idesc_bf16(128, kMlaMaxHG, true, false);   // A MN-major
+    RingCursor cur;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int nvalid = min(kMlaTileRows, cache_e - row_s - t * kMlaTileRows);
+        if (tid == 0) {
+            // S^T = C Q^T over the 9 latent boxes (hi and lo parts of Q)
+            tcgen05_fence_after();
+            for (int sp = 0; sp < kSStages; ++sp) {
+                mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out,
+                                         p.status, kSiteStageFull);
+                tcgen05_fence_after();
+                const uint32_t st = ring + cur.stage * kMlaStageBytes;
+                for (int bx = 0; bx < 2 && 2 * sp + bx < kMlaBoxes; ++bx) {
+                    const int kc = 2 * sp + bx;
 #pragma unroll
-                        for (int hh = 0; hh < HPW; ++hh) {
-                            const float4 *qv = reinterpret_cast<const float4 *>(qt + (h_sc + hh) * kMlaRow + kc * 64 + j * 8);
-                            const float4 q0 = qv[0], q1 = qv[1];
-                            float a = s[hh][j & 1];
-                            a = fmaf(c8[0], q0.x, a);
-                            a = fmaf(c8[1], q0.y, a);
-                            a = fmaf(c8[2], q0.z, a);
-                            a = fmaf(c8[3], q0.w, a);
-                            a = fmaf(c8[4], q1.x, a);
-                            a = fmaf(c8[5], q1.y, a);
-                            a = fmaf(c8[6], q1.z, a);
-                            a = fmaf(c8[7], q1.w, a);
-                            s[hh][j & 1] = a;
-                        }
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t da = umma_smem_desc(st + bx * kMlaBoxBytes + ks * 32, 16, 1024);
+                        umma_bf16(tmem, da, umma_smem_desc(qhi + kc * kMlaAtomBytes + ks * 32, 16, 1024),
+                                  idesc_s, kc > 0 || ks > 0);
+                        umma_bf16(tmem, da, umma_smem_desc(qlo + kc * kMlaAtomBytes + ks * 32, 16, 1024),
+                                  idesc_s, true);
                     }
                 }
+                umma_commit(bar_empty0 + 8u * cur.stage);
+                cur.advance(NS);
             }
-#pragma unroll
-            for (int hh = 0; hh < HPW; ++hh) {
-                const float sv = s[hh][0] + s[hh][1];
-                float mt = lane < nvalid ? sv : -INFINITY;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
-                const float m_new = fmaxf(m_run[hh], mt);
-                const float pr = lane < nvalid ? exp2f(sv - m_new) : 0.f;
-                float ps = pr;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-                const float al = exp2f(m_run[hh] - m_new);  // 0 while nothing was seen
-                l_run[hh] = l_run[hh] * al + ps;
-                m_run[hh] = m_new;
-                pbuf[lane * HG + h_sc + hh] = pr;
-                if (lane == 0) alpha[h_sc + hh] = al;
-            }
+            umma_commit(bar_s);
         }
-        compute_bar<kComputeThreads>();
-        // o_h += sum_t p[t][h] c_t: 4 heads x 8 latent dims per thread
-        if (hq * 4 < HG) {
-            const int kc = dh * 4 + lane / 8, j = lane % 8;
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                const float al = hq * 4 + hh < HG ? alpha[hq * 4 + hh] : 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[hh][e] *= al;
-            }
-            for (int t = 0; t < nvalid; ++t) {
-                float c8[8];
-                unpack8_bf16(*reinterpret_cast<const uint4 *>(tile + mla_tile_off(box_stride, t, kc, j)), c8);
-                const float *pr = pbuf + t * HG + hq * 4;
-#pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                    const float pv = hq * 4 + hh < HG ? pr[hh] : 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[hh][e] = fmaf(pv, c8[e], acc[hh][e]);
-                }
-            }
-        }
-        compute_bar<kComputeThreads>();
-    };
-
-    RingCursor cur;
-    for (int i = 0; i < n_tiles; ++i) {
-        const int s = cur.stage;
-        mbar_wait_bounded<false>(bar_full0 + 8u * s, cur.phase, p.timeout_ns, timed_out, p.status,
-                                 kSiteStageFull);
-        const int nvalid = min(kMlaTileRows, cache_e - row_s - i * kMlaTileRows);
-        process_tile(smem + p.off_ring + s * kMlaTileBytes, kMlaTileRows * 128, nvalid);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty0 + 8u * s);
-        cur.advance(NS);
+        mbar_wait_bounded<false>(bar_s, t & 1, p.timeout_ns, timed_out, p.status, kSiteStageFull);
+        tcgen05_fence_after();
+        // scores of tile row 32 wq + lane, heads 8 wh .. + 8 (base-2 units)
+        float sv[8];
+        mla_tmem_ld_x8(tl + 8 * wh, sv);
+        const int row = 32 * wq + lane;
+        const bool valid = row < nvalid;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float mx = valid ? sv[j] : -INFINITY;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane == 0) red_max[warp * 16 + j] = mx;
+        }
+        tcgen05_fence_before();
+        compute_bar<kComputeThreads>();
+        // probabilities against the new running max; P as the K-major B
+        // operand of the value MMA (element (head, row))
+        float pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int h = 8 * wh + j;
+            float tmax = red_max[(4 * wh) * 16 + j];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) tmax = fmaxf(tmax, red_max[(4 * wh + w) * 16 + j]);
+            const float m_new = fmaxf(m_st[h], tmax);
+            pv[j] = valid && h < HG ? exp2f(sv[j] - m_new) : 0.f;
+            const uint32_t off = (row >> 6) * kMlaAtomBytes + mla_atom_off(h, row & 63);
+            *reinterpret_cast<uint16_t *>(smem + p.off_pb + off) =
+                __bfloat16_as_ushort(__float2bfloat16_rn(pv[j]));
+            float sm = pv[j];
+#pragma unroll
+            for (int off2 = 16; off2 > 0; off2 >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off2);
+            if (lane == 0) red_sum[warp * 16 + j] = sm;
+        }
+        fence_proxy_async_smem();  // P is read by the tensor cores
+        compute_bar<kComputeThreads>();
+        // per-head state: new max, rescale factor, running sum (fixed warp order)
+        if (tid < kMlaMaxHG) {
+            const int h = tid, hw = h >> 3, j = h & 7;
+            float tmax = red_max[(4 * hw) * 16 + j], tsum = red_sum[(4 * hw) * 16 + j];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) {
+                tmax = fmaxf(tmax, red_max[(4 * hw + w) * 16 + j]);
+                tsum += red_sum[(4 * hw + w) * 16 + j];
+            }
+            const float m_old = m_st[h];
+            const float m_new = fmaxf(m_old, tmax);
+            const float al = exp2f(m_old - m_new);  // 0 while nothing was seen
+            alpha[h] = al;
+            l_st[h] = l_st[h] * al + tsum;
+            m_st[h] = m_new;
+        }
+        compute_bar<kComputeThreads>();
+        if (tid == 0) {
+            // O^T = C^T P^T for the 4 latent blocks of 128 dims
+            tcgen05_fence_after();
+            for (int vp = 0; vp < kVStages; ++vp) {
+                mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out,
+                                         p.status, kSiteStageFull);
+                tcgen05_fence_after();
+                const uint32_t st = ring + cur.stage * kMlaStageBytes;
+#pragma unroll
+                for (int ks = 0; ks < kMlaTileRows / 16; ++ks)
+                    umma_bf16(tmem + 16 + 16 * vp, umma_smem_desc(st + ks * 2048, kMlaBoxBytes, 1024),
+                              umma_smem_desc(pb + (ks >> 2) * kMlaAtomBytes + (ks & 3) * 32, 16, 1024),
+                              idesc_o, ks > 0);
+                umma_commit(bar_empty0 + 8u * cur.stage);
+                cur.advance(NS);
+            }
+            umma_commit(bar_o);
+        }
+        __syncwarp();
+        mbar_wait_bounded<false>(bar_o, t & 1, p.timeout_ns, timed_out, p.status, kSiteStageFull);
+        tcgen05_fence_after();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float o[16];
+            tmem_ld_x16(tl + 16 + 16 * (2 * wh + i), o);
+#pragma unroll
+            for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = acc[i][h] * alpha[h] + o[h];
+        }
+        tcgen05_fence_before();
+        compute_bar<kComputeThreads>();
     }
-    if (has_new) process_tile(newrow, 128, 1);
+    // The new row, attended on CUDA cores: its score per head, the state
+    // update, and its value folded into the partial output.
+    if (has_new) {
+        for (int h = warp; h < HG; h += kComputeWarps) {
+            float s = 0.f;
+            for (int k = lane; k < kMlaRow; k += 32) s = fmaf(qt[h * kMlaRow + k], bf16_bits(newrow[k]), s);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (lane == 0) s_new[h] = s;
+        }
+        compute_bar<kComputeThreads>();
+        if (tid < HG) {
+            const int h = tid;
+            const float m_old = m_st[h];
+            const float m_new = fmaxf(m_old, s_new[h]);
+            const float al = exp2f(m_old - m_new), pn = exp2f(s_new[h] - m_new);
+            alpha[h] = al;
+            s_new[h] = pn;
+            l_st[h] = l_st[h] * al + pn;
+            m_st[h] = m_new;
+        }
+        compute_bar<kComputeThreads>();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float c = bf16_bits(newrow[128 * (2 * wh + i) + 32 * wq + lane]);
+#pragma unroll
+            for (int h = 0; h < kMlaMaxHG; ++h)
+                if (h < HG) acc[i][h] = acc[i][h] * alpha[h] + s_new[h] * c;
+        }
+    }
 
     // ---- C: sparse ClusterReduce -- each head goes to the block that owns it --
     {
-        // (m, l) of the heads this warp scored, then o of the heads this thread holds
-        if (scores_warp && lane == 0) {
+        // stage o^T as [head][512] in the (now idle) ring, then ship each head's
+        // row and (m, l) to its owner
+        float *stage = reinterpret_cast<float *>(smem + p.off_ring);
 #pragma unroll
-            for (int hh = 0; hh < HPW; ++hh) {
-                const int h = h_sc + hh, owner = h / HPB, slot = h % HPB;
-                float *dst = recv + (slot * C + r) * (kMlaKv + 4) + kMlaKv;
-                const float4 st = make_float4(m_run[hh], l_run[hh], 0.f, 0.f);
-                if (owner == r) {
-                    *reinterpret_cast<float4 *>(dst) = st;
-                } else {
-                    push_16B(map_to_rank(smem_addr(dst), owner), st, map_to_rank(bar_red, owner));
-                }
-            }
-        }
-        if (hq * 4 < HG) {
-            const int d0 = dh * 256 + lane * 8;
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-                const int h = hq * 4 + hh;
-                if (h >= HG) continue;
-                const int owner = h / HPB, slot = h % HPB;
-                float *dst = recv + (slot * C + r) * (kMlaKv + 4) + d0;
-                const float4 v0 = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-                const float4 v1 = make_float4(acc[hh][4], acc[hh][5], acc[hh][6], acc[hh][7]);
-                if (owner == r) {
-                    reinterpret_cast<float4 *>(dst)[0] = v0;
-                    reinterpret_cast<float4 *>(dst)[1] = v1;
-                } else {
-                    push_16B(map_to_rank(smem_addr(dst), owner), v0, map_to_rank(bar_red, owner));
-                    push_16B(map_to_rank(smem_addr(dst + 4), owner), v1, map_to_rank(bar_red, owner));
-                }
+            for (int h = 0; h < kMlaMaxHG; ++h)
+                stage[h * kMlaKv + 128 * (2 * wh + i) + 32 * wq + lane] = acc[i][h];
+        compute_bar<kComputeThreads>();
+        const int per_head = kMlaKv / 4 + 1;  // 128 chunks of o, then (m, l, 0, 0)
+        for (int idx = tid; idx < HG * per_head; idx += kComputeThreads) {
+            const int h = idx / per_head, c = idx % per_head;
+            const int owner = h / HPB, slot = h % HPB;
+            float *dst = recv + (slot * C + r) * (kMlaKv + 4) + 4 * c;
+            const float4 val = c < kMlaKv / 4
+                                   ? reinterpret_cast<const float4 *>(stage + h * kMlaKv)[c]
+                                   : make_float4(m_st[h], l_st[h], 0.f, 0.f);
+            if (owner == r) {
+                *reinterpret_cast<float4 *>(dst) = val;
+            } else {
+                push_16B(map_to_rank(smem_addr(dst), owner), val, map_to_rank(bar_red, owner));
             }
         }
         compute_bar<kComputeThreads>();  // own partials written
@@ -449,6 +543,10 @@ mla_attention_kernel(const __grid_constant__ CUtensorMap tm_cache,
             }
             compute_bar<kComputeThreads>();
         }
+    }
+    if (warp == 0) {
+        tcgen05_fence_after();
+        tmem_dealloc(tmem, 128);
     }
     cluster_sync_all();  // no block leaves while a peer may still push into it
 }

@@ -736,7 +736,7 @@ struct cfa_mla {
 
 namespace {
 
-constexpr int kMlaStages = 3;
+constexpr int kMlaStages = 3;  // two-box (32 KB) stages of the latent ring
 
 void mla_free(cfa_mla *m) {
     if (m->a) cudaFree(m->a);
@@ -810,8 +810,8 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
     }
     m->gq.gp.x_stride = NA;  // the query GEMV reads the first q_lora columns of a
 
-    // The attention kernel: C = HG blocks per cluster, one head each in the
-    // gather and the reduce-scatter.
+    // The attention kernel: one cluster of C blocks per (sequence, group of HG
+    // heads); each block gathers and finishes HG / C heads.
     cfa::MlaParams &mp = m->mp;
     mp.B = B;
     mp.nh = n_heads;
@@ -819,33 +819,40 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
     mp.a_stride = NA;
     mp.a_off = q_lora;
     mp.HG = HG;
-    mp.C = HG;
-    mp.HPB = 1;
     mp.nstages = kMlaStages;
     mp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(cfa::kMlaQk)));
     mp.timeout_ns = kTimeoutNs;
-    int off = 0;
-    mp.off_ring = off;
-    off += kMlaStages * cfa::kMlaTileBytes;
-    mp.off_newrow = off;
-    off += align_up(cfa::kMlaRow * 2, 128);
-    mp.off_qt = off;
-    off += align_up(HG * cfa::kMlaRow * 4, 128);
-    mp.off_p = off;
-    off += align_up(cfa::kMlaTileRows * HG * 4, 128);
-    mp.off_alpha = off;
-    off += 128;
-    mp.off_recv = off;
-    off += align_up(mp.HPB * mp.C * (cfa::kMlaKv + 4) * 4, 128);
-    mp.off_ofin = off;
-    off += align_up(mp.HPB * cfa::kMlaKv * 4, 128);
-    mp.off_scr = off;
-    off += align_up((cfa::kComputeWarps * cfa::kMlaV + 64) * 4, 128);
-    mp.off_bars = off;
-    off += 16 * kMlaStages + 32;
-    m->smem = off;
+    // Shared memory of one block when a cluster has C blocks (HG / C heads each).
+    auto layout = [&](int C) {
+        mp.C = C;
+        mp.HPB = HG / C;
+        int off = 0;
+        mp.off_ring = off;                          // two-box stages (1024-aligned boxes)
+        off += kMlaStages * cfa::kMlaStageBytes;
+        mp.off_qhi = off;                           // 9 swizzled [16 x 64] query atoms, hi
+        off += cfa::kMlaBoxes * cfa::kMlaAtomBytes;
+        mp.off_qlo = off;                           // and lo parts
+        off += cfa::kMlaBoxes * cfa::kMlaAtomBytes;
+        mp.off_pb = off;                            // P: 2 atoms [16 heads x 64 rows]
+        off += 2 * cfa::kMlaAtomBytes;
+        mp.off_qt = off;                            // fp32 queries [HG][576]
+        off += align_up(HG * cfa::kMlaRow * 4, 128);
+        mp.off_newrow = off;
+        off += align_up(cfa::kMlaRow * 2, 128);
+        mp.off_stat = off;                          // m, l, alpha, two [8][16] reductions, new row
+        off += align_up(320 * 4, 128);
+        mp.off_recv = off;                          // partials of my heads [HPB][C][516]
+        off += align_up(mp.HPB * mp.C * (cfa::kMlaKv + 4) * 4, 128);
+        mp.off_ofin = off;                          // combined latent outputs [HPB][512]
+        off += align_up(mp.HPB * cfa::kMlaKv * 4, 128);
+        mp.off_scr = off;
+        off += align_up((cfa::kComputeWarps * cfa::kMlaV + 64) * 4, 128);
+        mp.off_bars = off;
+        off += 16 * kMlaStages + 64;
+        return off;
+    };
     const void *kernel = cfa::mla_kernel_ptr(HG);
-    if (!kernel || off > dev.smem_optin ||
+    if (!kernel ||
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
@@ -855,26 +862,48 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
         fail(CFA_ERR_UNSUPPORTED);
         return nullptr;
     }
+    // Cluster size: the largest C (blocks per head group, each finishing HG / C
+    // heads) whose clusters all fit on the GPU at once. A 16-block cluster
+    // needs 16 SMs of one GPC, and not every GPC has them.
     {
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = mp.C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(B * (n_heads / HG) * mp.C);
-        cfg.blockDim = dim3(cfa::kThreads);
-        cfg.dynamicSmemBytes = static_cast<size_t>(m->smem);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) {
-            cudaGetLastError();
+        const int n_clusters = B * (n_heads / HG);
+        int chosen = 0, chosen_fit = 0;
+        for (int C = HG; C >= 2; C /= 2) {
+            if (layout(C) > dev.smem_optin) continue;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = C;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(n_clusters * C);
+            cfg.blockDim = dim3(cfa::kThreads);
+            cfg.dynamicSmemBytes = static_cast<size_t>(layout(C));
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                continue;
+            }
+            if (clusters < 1) continue;
+            if (!chosen) {
+                chosen = C;
+                chosen_fit = clusters;
+            }
+            if (clusters >= n_clusters) {
+                chosen = C;
+                chosen_fit = clusters;
+                break;
+            }
+        }
+        if (!chosen) {
             delete m;
             fail(CFA_ERR_UNSUPPORTED);
             return nullptr;
         }
-        m->coresident_clusters = clusters;
+        m->smem = layout(chosen);
+        m->coresident_clusters = chosen_fit;
     }
 
     const size_t nwords = static_cast<size_t>(m->ga.gp.n_tiles + m->gq.gp.n_tiles +
@@ -930,16 +959,26 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
     const int NA = m->q_lora + cfa::kMlaRow, NQ = m->nh * cfa::kMlaQk, NV = m->nh * cfa::kMlaV;
 
     // tensor maps of this call's operands (host work only)
-    CUtensorMap tm_x, tm_wa, tm_wuq, tm_wo, tm_cache, tm_wkvb;
-    if (cfa::encode_bf16_2d(&tm_x, x, m->H, m->B, 64, m->B) != CFA_OK ||
-        cfa::encode_bf16_2d(&tm_wa, W_a, NA, m->H, cfa::kGemvTileCols, 64) != CFA_OK ||
-        cfa::encode_bf16_2d(&tm_wuq, W_uq, NQ, m->q_lora, cfa::kGemvTileCols, 64) != CFA_OK ||
-        cfa::encode_bf16_2d(&tm_wo, W_o, m->H, NV, cfa::kGemvTileCols, 64) != CFA_OK ||
-        cfa::encode_bf16_2d_ex(&tm_cache, cache, cfa::kMlaRow,
-                               static_cast<uint64_t>(m->B) * m->max_ctx, cfa::kMlaRow, 64,
-                               cfa::kMlaTileRows, true) != CFA_OK ||
+    CUtensorMap tm_x, tm_wa, tm_wuq, tm_wo, tm_wkvb;
+    cfa::MlaMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    bool enc_ok =
+        cfa::encode_bf16_2d(&tm_x, x, m->H, m->B, 64, m->B) == CFA_OK &&
+        cfa::encode_bf16_2d(&tm_wa, W_a, NA, m->H, cfa::kGemvTileCols, 64) == CFA_OK &&
+        cfa::encode_bf16_2d(&tm_wuq, W_uq, NQ, m->q_lora, cfa::kGemvTileCols, 64) == CFA_OK &&
+        cfa::encode_bf16_2d(&tm_wo, W_o, m->H, NV, cfa::kGemvTileCols, 64) == CFA_OK &&
         cfa::encode_bf16_2d_ex(&tm_wkvb, W_kvb, static_cast<uint64_t>(m->nh) * 256, cfa::kMlaKv,
-                               static_cast<uint64_t>(m->nh) * 256, 128, 256, false) != CFA_OK)
+                               static_cast<uint64_t>(m->nh) * 256, 128, 256, false) == CFA_OK;
+    // one map per sequence over its cached rows only: a tile running past
+    // them reads zeros (never another row or a NaN-filled tail)
+    for (int b = 0; b < m->B && enc_ok; ++b) {
+        const uint16_t *base = static_cast<const uint16_t *>(cache) +
+                               static_cast<size_t>(b) * m->max_ctx * cfa::kMlaRow;
+        enc_ok = cfa::encode_bf16_2d_ex(&maps.cache[b], base, cfa::kMlaRow,
+                                        std::max(ctx_lens[b], 1), cfa::kMlaRow, 64,
+                                        cfa::kMlaTileRows, true) == CFA_OK;
+    }
+    if (!enc_ok)
         return fail(CFA_ERR_CUDA);
 
     unsigned *gst = mla_gemv_status(m);
@@ -982,7 +1021,7 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
         cfg.stream = cs;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        void *args[3] = {&tm_cache, &tm_wkvb, &mp};
+        void *args[3] = {&maps, &tm_wkvb, &mp};
         if (cudaLaunchKernelExC(&cfg, cfa::mla_kernel_ptr(mp.HG), args) != cudaSuccess) {
             cudaGetLastError();
             return fail(CFA_ERR_CUDA);
