@@ -115,6 +115,7 @@ constexpr int kMlaBoxBytes = kMlaTileRows * 128;    // 16 KB
 constexpr int kMlaStageBytes = 2 * kMlaBoxBytes;    // a stage holds two boxes
 constexpr int kMlaMaxHG = 16;                       // heads per cluster = MMA N
 constexpr int kMlaAtomBytes = kMlaMaxHG * 128;      // a [16 x 64] K-major swizzled atom
+constexpr int kMlaWeightRows = 256;                 // a W_kvb box is [256 x 64] (one stage)
 
 struct MlaParams {
     const uint16_t *q;       // [B][nh*192] bf16: per head [q_nope | q_rope]
@@ -139,7 +140,7 @@ struct MlaParams {
 
 // One latent-cache tensor map per sequence, limited to its cached rows, so a
 // tile running past them reads zeros.
-struct __align__(64) MlaMaps {
+struct __align__(128) MlaMaps {
     CUtensorMap cache[kMaxBatch];
 };
 

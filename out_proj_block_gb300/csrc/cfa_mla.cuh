@@ -146,23 +146,42 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
 
     if (warp == kComputeWarps) {
         // ------------------------------------------------------------ load warp
+        // Ring order (the compute side consumes in the same order): the W_k
+        // blocks of this block's heads, the cache tiles (scores, then values,
+        // per tile), the W_v blocks of its heads. Weight boxes are [256 x 64].
         if (lane == 0) {
-            // W_v blocks of this block's heads, wanted at the end: warm L2 now.
-            for (int i = 0; i < HPB; ++i) {
-                const int h = g * HG + r * HPB + i;
-                for (int y = 0; y < kMlaKv; y += 256)
-                    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                                 :: "l"(reinterpret_cast<uint64_t>(&tm_wkvb)),
-                                    "r"(h * (kMlaNope + kMlaV) + kMlaNope), "r"(y)
-                                 : "memory");
-            }
-            grid_dependency_wait();  // cache rows may come from the previous step
-            const CUtensorMap *tm = &maps.cache[b];
             RingCursor cur;
-            auto stage_in = [&](int kc0, int nbox, int row) {
+            auto wait_slot = [&]() {
                 if (cur.wrapped)
                     mbar_wait_bounded<false>(bar_empty0 + 8u * cur.stage, cur.phase ^ 1u,
                                              p.timeout_ns, timed_out, p.status, kSiteStageEmpty);
+            };
+            auto weight_block = [&](int col0) {  // [512 x 128] of W_kvb in 4 stages
+                for (int rb = 0; rb < 2; ++rb)
+                    for (int cb = 0; cb < 2; ++cb) {
+                        wait_slot();
+                        const uint32_t full = bar_full0 + 8u * cur.stage;
+                        mbar_arrive_expect_tx(full, static_cast<uint32_t>(kMlaStageBytes));
+                        tma_load_2d(ring + cur.stage * kMlaStageBytes, &tm_wkvb, col0 + 64 * cb,
+                                    kMlaWeightRows * rb, full);
+                        cur.advance(NS);
+                    }
+            };
+            for (int i = 0; i < HPB; ++i) {  // W_v blocks, wanted at the end: warm L2 now
+                const int col0 = (g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope;
+                for (int rb = 0; rb < 2; ++rb)
+                    for (int cb = 0; cb < 2; ++cb)
+                        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                                     :: "l"(reinterpret_cast<uint64_t>(&tm_wkvb)), "r"(col0 + 64 * cb),
+                                        "r"(kMlaWeightRows * rb)
+                                     : "memory");
+            }
+            for (int i = 0; i < HPB; ++i)  // weights: independent of the previous kernel
+                weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV));
+            grid_dependency_wait();  // cache rows may come from the previous step
+            const CUtensorMap *tm = &maps.cache[b];
+            auto stage_in = [&](int kc0, int nbox, int row) {
+                wait_slot();
                 const uint32_t full = bar_full0 + 8u * cur.stage;
                 const uint32_t dst = ring + cur.stage * kMlaStageBytes;
                 mbar_arrive_expect_tx(full, static_cast<uint32_t>(nbox * kMlaBoxBytes));
@@ -175,6 +194,8 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 for (int sp = 0; sp < kSStages; ++sp) stage_in(2 * sp, min(2, kMlaBoxes - 2 * sp), row);
                 for (int vp = 0; vp < kVStages; ++vp) stage_in(2 * vp, 2, row);
             }
+            for (int i = 0; i < HPB; ++i)
+                weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope);
             for (int s = 0; s < NS; ++s) {  // drain
                 if (s >= cur.stage && !cur.wrapped) break;
                 volatile int ignore = 0;
@@ -195,6 +216,17 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     const uint32_t tmem = *tmem_slot;
     grid_dependency_wait();
     // ---- A: absorbed queries of this block's heads, pushed to the cluster ----
+    RingCursor cur;  // every compute thread follows the ring through phase A
+    auto stage_ready = [&]() {
+        mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out, p.status,
+                                 kSiteStageFull);
+        return smem + p.off_ring + cur.stage * kMlaStageBytes;
+    };
+    auto stage_done = [&]() {  // every compute thread has read the stage
+        compute_bar<kComputeThreads>();
+        if (tid == 0) mbar_arrive(bar_empty0 + 8u * cur.stage);
+        cur.advance(NS);
+    };
     {
         float *qn = scr;  // [128] q_nope of the head being absorbed
         for (int i = 0; i < HPB; ++i) {
@@ -204,34 +236,23 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             if (tid < kMlaNope) qn[tid] = bf16_bits(qh[tid]);
             compute_bar<kComputeThreads>();
             float *dst = qt + hl * kMlaRow;
-            // q~[j] = sum_c W_kvb[j, h*256 + c] q_nope[c]: rows tid and tid + 256,
-            // all 32 16-byte loads of both rows issued before any use
-            {
-                const size_t ld = static_cast<size_t>(p.nh) * (kMlaNope + kMlaV);
-                const uint4 *w0 = reinterpret_cast<const uint4 *>(p.W_kvb + tid * ld + h * (kMlaNope + kMlaV));
-                const uint4 *w1 = reinterpret_cast<const uint4 *>(p.W_kvb + (tid + kComputeThreads) * ld +
-                                                                  h * (kMlaNope + kMlaV));
-                uint4 r0[kMlaNope / 8], r1[kMlaNope / 8];
+            // q~[j] = sum_c W_kvb[j, h*256 + c] q_nope[c]: thread tid takes latent
+            // rows tid and tid + 256, a swizzled 128-byte box row per stage
+            float acc_q[2] = {0.f, 0.f};
+            for (int rb = 0; rb < 2; ++rb)
+                for (int cb = 0; cb < 2; ++cb) {
+                    const uint8_t *st = stage_ready();
 #pragma unroll
-                for (int c8 = 0; c8 < kMlaNope / 8; ++c8) {
-                    r0[c8] = __ldg(w0 + c8);
-                    r1[c8] = __ldg(w1 + c8);
-                }
-                float a0 = 0.f, a1 = 0.f;
+                    for (int c = 0; c < 8; ++c) {
+                        float f[8];
+                        unpack8_bf16(*reinterpret_cast<const uint4 *>(st + tid * 128 + ((c ^ (tid & 7)) << 4)), f);
 #pragma unroll
-                for (int c8 = 0; c8 < kMlaNope / 8; ++c8) {
-                    float f0[8], f1[8];
-                    unpack8_bf16(r0[c8], f0);
-                    unpack8_bf16(r1[c8], f1);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        a0 = fmaf(f0[e], qn[c8 * 8 + e], a0);
-                        a1 = fmaf(f1[e], qn[c8 * 8 + e], a1);
+                        for (int e = 0; e < 8; ++e) acc_q[rb] = fmaf(f[e], qn[64 * cb + 8 * c + e], acc_q[rb]);
                     }
+                    stage_done();
                 }
-                dst[tid] = a0 * p.qscale;
-                dst[tid + kComputeThreads] = a1 * p.qscale;
-            }
+            dst[tid] = acc_q[0] * p.qscale;
+            dst[tid + kComputeThreads] = acc_q[1] * p.qscale;
             if (tid < kMlaRope / 2) {
                 float x0 = bf16_bits(qh[kMlaNope + tid]), x1 = bf16_bits(qh[kMlaNope + tid + kMlaRope / 2]);
                 if (p.rope) mla_rope(x0, x1, L, p.rope_inv_freq[tid]);
@@ -288,14 +309,32 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     // Queries as the B operand of the score MMA: bf16 hi and lo parts in
     // [16 x 64] K-major swizzled atoms (heads past HG are zero), and the
     // running softmax state.
-    for (int i = tid; i < kMlaMaxHG * kMlaRow; i += kComputeThreads) {
-        const int n = i / kMlaRow, k = i % kMlaRow;
-        const float v = n < HG ? qt[n * kMlaRow + k] : 0.f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        const uint32_t off = (k >> 6) * kMlaAtomBytes + mla_atom_off(n, k & 63);
-        *reinterpret_cast<uint16_t *>(smem + p.off_qhi + off) = __bfloat16_as_ushort(hi);
-        *reinterpret_cast<uint16_t *>(smem + p.off_qlo + off) = __bfloat16_as_ushort(lo);
+    for (int i = tid; i < kMlaMaxHG * (kMlaRow / 8); i += kComputeThreads) {
+        const int n = i / (kMlaRow / 8), kc = i % (kMlaRow / 8);  // head, 8-element chunk
+        float v[8];
+        if (n < HG) {
+            const float4 v0 = reinterpret_cast<const float4 *>(qt + n * kMlaRow)[2 * kc];
+            const float4 v1 = reinterpret_cast<const float4 *>(qt + n * kMlaRow)[2 * kc + 1];
+            v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+            v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+            const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * e] - __bfloat162float(h0));
+            const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1));
+            hi[e] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+            lo[e] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+        }
+        const uint32_t off = (kc >> 3) * kMlaAtomBytes + mla_atom_off(n, (kc & 7) * 8);
+        *reinterpret_cast<uint4 *>(smem + p.off_qhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(smem + p.off_qlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     if (tid < kMlaMaxHG) {
         m_st[tid] = -INFINITY;
@@ -317,7 +356,6 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
         for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = 0.f;
     const uint32_t idesc_s = umma_idesc_bf16(128, kMlaMaxHG, false, false);  // A K-major
     const uint32_t idesc_o = umma_idesc_bf16(128, kMlaMaxHG, true, false);   // A MN-major
-    RingCursor cur;
     for (int t = 0; t < n_tiles; ++t) {
         const int nvalid = min(kMlaTileRows, cache_e - row_s - t * kMlaTileRows);
         if (tid == 0) {
@@ -463,9 +501,9 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
 
     // ---- C: sparse ClusterReduce -- each head goes to the block that owns it --
     {
-        // stage o^T as [head][512] in the (now idle) ring, then ship each head's
-        // row and (m, l) to its owner
-        float *stage = reinterpret_cast<float *>(smem + p.off_ring);
+        // stage o^T as [head][512] where the query operands were (every MMA
+        // has completed), then ship each head's row and (m, l) to its owner
+        float *stage = reinterpret_cast<float *>(smem + p.off_qhi);
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -509,30 +547,32 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             }
         }
         compute_bar<kComputeThreads>();
-        // v_h = o_h W_v,h: warp w sums rows j = w (mod 8), lane takes 4 columns
+        // v_h = o_h W_v,h from the ring's [256 x 64] W_v boxes: warp w takes box
+        // rows 32 w .. 32 w + 31, lane the value columns 2 lane, 2 lane + 1
+        cur = RingCursor();
+        for (int n = 0; n < 4 * HPB + (kSStages + kVStages) * n_tiles; ++n) cur.advance(NS);
         for (int ii = 0; ii < HPB; ++ii) {
             const int h = g * HG + r * HPB + ii;
-            float part[4] = {0.f, 0.f, 0.f, 0.f};
-            const size_t ld = static_cast<size_t>(p.nh) * (kMlaNope + kMlaV);
-            const uint16_t *wv0 = p.W_kvb + h * (kMlaNope + kMlaV) + kMlaNope + lane * 4;
-            // rows j = warp + 8 i, i < 64: 16 loads in flight per round
-#pragma unroll 1
-            for (int i0 = 0; i0 < kMlaKv / kComputeWarps; i0 += 16) {
-                uint2 wv[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    wv[i] = __ldg(reinterpret_cast<const uint2 *>(wv0 + (warp + (i0 + i) * kComputeWarps) * ld));
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float oj = ofin[ii * kMlaKv + warp + (i0 + i) * kComputeWarps];
-                    part[0] = fmaf(oj, bf16_lo(wv[i].x), part[0]);
-                    part[1] = fmaf(oj, bf16_hi(wv[i].x), part[1]);
-                    part[2] = fmaf(oj, bf16_lo(wv[i].y), part[2]);
-                    part[3] = fmaf(oj, bf16_hi(wv[i].y), part[3]);
+            float part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            for (int rb = 0; rb < 2; ++rb)
+                for (int cb = 0; cb < 2; ++cb) {
+                    const uint8_t *st = stage_ready();
+#pragma unroll 8
+                    for (int k = 0; k < 32; ++k) {
+                        const int row = 32 * warp + k;
+                        const float oj = ofin[ii * kMlaKv + kMlaWeightRows * rb + row];
+                        const uint32_t w = *reinterpret_cast<const uint32_t *>(
+                            st + row * 128 + (((lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4);
+                        part[cb][0] = fmaf(oj, bf16_lo(w), part[cb][0]);
+                        part[cb][1] = fmaf(oj, bf16_hi(w), part[cb][1]);
+                    }
+                    stage_done();
                 }
-            }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) scr[warp * kMlaV + lane * 4 + e] = part[e];
+            for (int cb = 0; cb < 2; ++cb) {
+                scr[warp * kMlaV + 64 * cb + 2 * lane] = part[cb][0];
+                scr[warp * kMlaV + 64 * cb + 2 * lane + 1] = part[cb][1];
+            }
             compute_bar<kComputeThreads>();
             if (tid < kMlaV) {
                 float vsum = 0.f;

@@ -968,7 +968,7 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
         cfa::encode_bf16_2d(&tm_wuq, W_uq, NQ, m->q_lora, cfa::kGemvTileCols, 64) == CFA_OK &&
         cfa::encode_bf16_2d(&tm_wo, W_o, m->H, NV, cfa::kGemvTileCols, 64) == CFA_OK &&
         cfa::encode_bf16_2d_ex(&tm_wkvb, W_kvb, static_cast<uint64_t>(m->nh) * 256, cfa::kMlaKv,
-                               static_cast<uint64_t>(m->nh) * 256, 128, 256, false) == CFA_OK;
+                               static_cast<uint64_t>(m->nh) * 256, 64, cfa::kMlaWeightRows, true) == CFA_OK;
     // one map per sequence over its cached rows only: a tile running past
     // them reads zeros (never another row or a NaN-filled tail)
     for (int b = 0; b < m->B && enc_ok; ++b) {
