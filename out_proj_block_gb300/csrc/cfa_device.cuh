@@ -161,6 +161,13 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
     return r;
 }
 
+// Arrive, with release at cluster scope, on a barrier of another block of the
+// cluster (`remote_bar` from map_to_rank).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(remote_bar)
+                 : "memory");
+}
+
 // 16-byte store into another block's shared memory that also counts 16 bytes
 // of completion on that block's barrier `remote_bar`.
 __device__ __forceinline__ void push_16B(uint32_t remote_addr, float4 v, uint32_t remote_bar) {

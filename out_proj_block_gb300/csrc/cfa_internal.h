@@ -116,6 +116,8 @@ constexpr int kMlaStageBytes = 2 * kMlaBoxBytes;    // a stage holds two boxes
 constexpr int kMlaMaxHG = 16;                       // heads per cluster = MMA N
 constexpr int kMlaAtomBytes = kMlaMaxHG * 128;      // a [16 x 64] K-major swizzled atom
 constexpr int kMlaWeightRows = 256;                 // a W_kvb box is [256 x 64] (one stage)
+constexpr int kMlaQAtomBytes = 2 * kMlaAtomBytes;   // a [32 x 64] atom: hi rows, then lo rows
+constexpr int kMlaThreads = kComputeThreads + 64;   // + load warp + MMA warp
 
 struct MlaParams {
     const uint16_t *q;       // [B][nh*192] bf16: per head [q_nope | q_rope]
@@ -133,7 +135,7 @@ struct MlaParams {
     float qscale;            // log2(e) / sqrt(192): scores in base-2 units
     int HG, C, HPB;          // heads per cluster, blocks per cluster, heads per block
     int nstages;
-    int off_ring, off_qhi, off_qlo, off_pb, off_qt, off_newrow, off_stat, off_recv, off_ofin,
+    int off_ring, off_qb, off_pb, off_qt, off_newrow, off_stat, off_recv, off_ofin,
         off_scr, off_bars;
     unsigned long long timeout_ns;
 };

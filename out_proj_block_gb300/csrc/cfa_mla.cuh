@@ -80,7 +80,7 @@ __device__ __forceinline__ void mla_rope(float &x0, float &x1, int pos, double i
     x1 = y1;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMlaThreads, 1)
 mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                      const __grid_constant__ CUtensorMap tm_wkvb, const MlaParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -104,25 +104,28 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     float *stat = reinterpret_cast<float *>(smem + p.off_stat);
     float *m_st = stat;               // [16] running max per head (base 2)
     float *l_st = stat + 16;          // [16] running sum
-    float *alpha = stat + 32;         // [16] rescale of o for the current tile
-    float *red_max = stat + 48;       // [8 warps][16]
-    float *red_sum = stat + 176;      // [8 warps][16]
-    float *s_new = stat + 304;        // [16] score, then probability, of the new row
-    float *recv = reinterpret_cast<float *>(smem + p.off_recv);  // [HPB][C][516]
+    float *alpha = stat + 32;         // [2 tiles][16] rescale of o
+    float *red_max = stat + 64;       // [2 tiles][8 warps][16]
+    float *red_sum = stat + 320;      // [2 tiles][8 warps][16]
+    float *s_new = stat + 576;        // [16] score, then probability, of the new row
+    float *recv = reinterpret_cast<float *>(smem + p.off_recv);  // [HPB][C][516], over qt
     float *ofin = reinterpret_cast<float *>(smem + p.off_ofin);  // [HPB][512]
     float *scr = reinterpret_cast<float *>(smem + p.off_scr);    // [8][128] + 64
     uint16_t *newrow = reinterpret_cast<uint16_t *>(smem + p.off_newrow);  // [576] bf16
     const uint32_t ring = smem_addr(smem + p.off_ring);
-    const uint32_t qhi = smem_addr(smem + p.off_qhi), qlo = smem_addr(smem + p.off_qlo);
+    const uint32_t qb = smem_addr(smem + p.off_qb);
     const uint32_t pb = smem_addr(smem + p.off_pb);
     const uint32_t bar_full0 = smem_addr(smem + p.off_bars);
     const uint32_t bar_empty0 = bar_full0 + 8u * NS;
     const uint32_t bar_q = bar_full0 + 16u * NS;      // every peer's queries have landed
     const uint32_t bar_red = bar_q + 8u;              // every peer's partials for my heads
-    const uint32_t bar_s = bar_q + 16u;               // a tile's scores are in TMEM
-    const uint32_t bar_o = bar_q + 24u;               // a tile's latent outputs are in TMEM
-    volatile int *timed_out = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 32);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 16 * NS + 48);
+    const uint32_t bar_qfree = bar_q + 16u;           // every peer is done with its fp32 queries
+    const uint32_t bar_qready = bar_q + 24u;          // the query operand is built
+    const uint32_t bar_s0 = bar_q + 32u;              // [2] a tile's scores are in TMEM
+    const uint32_t bar_o0 = bar_q + 48u;              // [2] a tile's latent outputs are in TMEM
+    const uint32_t bar_p0 = bar_q + 64u;              // [2] a tile's P is written, its scores read
+    volatile int *timed_out = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 80);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 16 * NS + 88);
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -131,14 +134,21 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
         }
         mbar_init(bar_q, 1);
         mbar_init(bar_red, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
+        mbar_init(bar_qfree, C - 1);
+        mbar_init(bar_qready, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_s0 + 8u * i, 1);
+            mbar_init(bar_o0 + 8u * i, 1);
+            mbar_init(bar_p0 + 8u * i, 1);
+        }
         *timed_out = 0;
         fence_mbar_init();
         mbar_arrive_expect_tx(bar_q, static_cast<uint32_t>((C - 1) * HPB * kMlaRow * 4));
         mbar_arrive_expect_tx(bar_red, static_cast<uint32_t>((C - 1) * HPB * (kMlaKv + 4) * 4));
     }
-    if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 128);  // S: cols [0,16); O: [16,80)
+    // TMEM: scores of tile t at columns 32 (t % 2) (hi part 0-15, lo part 16-31),
+    // latent outputs at 64 + 64 (t % 2) + 16 v for latent block v
+    if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 256);
     tcgen05_fence_before();
     __syncthreads();
     grid_dependents_launch();
@@ -189,10 +199,14 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                     tma_load_2d(dst + i * kMlaBoxBytes, tm, (kc0 + i) * 64, row, full);
                 cur.advance(NS);
             };
-            for (int t = 0; t < n_tiles; ++t) {
-                const int row = row_s + t * kMlaTileRows;  // rows past the map's end read as zero
-                for (int sp = 0; sp < kSStages; ++sp) stage_in(2 * sp, min(2, kMlaBoxes - 2 * sp), row);
-                for (int vp = 0; vp < kVStages; ++vp) stage_in(2 * vp, 2, row);
+            // scores of tile t are computed while the softmax of tile t - 1 runs:
+            // stages in the MMA warp's order S0, S1, V0, S2, V1, ...
+            for (int t = 0; t <= n_tiles; ++t) {
+                if (t < n_tiles)  // rows past the map's end read as zero
+                    for (int sp = 0; sp < kSStages; ++sp)
+                        stage_in(2 * sp, min(2, kMlaBoxes - 2 * sp), row_s + t * kMlaTileRows);
+                if (t >= 1)
+                    for (int vp = 0; vp < kVStages; ++vp) stage_in(2 * vp, 2, row_s + (t - 1) * kMlaTileRows);
             }
             for (int i = 0; i < HPB; ++i)
                 weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope);
@@ -204,6 +218,71 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             }
         } else {
             grid_dependency_wait();
+        }
+        __syncwarp();
+        cluster_wait();
+        cluster_sync_all();
+        return;
+    }
+
+    if (warp == kComputeWarps + 1) {
+        // ------------------------------------------------------------- MMA warp
+        if (lane == 0 && n_tiles > 0) {
+            RingCursor cur;
+            for (int n = 0; n < 4 * HPB; ++n) cur.advance(NS);  // the W_k stages go to the compute warps
+            mbar_wait_bounded<false>(bar_qready, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
+            tcgen05_fence_after();
+            const uint32_t tmem = *tmem_slot;
+            const uint32_t idesc_s = umma_idesc_bf16(128, 2 * kMlaMaxHG, false, false);  // A K-major
+            const uint32_t idesc_o = umma_idesc_bf16(128, kMlaMaxHG, true, false);       // A MN-major
+            auto stage_wait = [&]() {
+                mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out,
+                                         p.status, kSiteStageFull);
+                tcgen05_fence_after();
+                return ring + cur.stage * kMlaStageBytes;
+            };
+            auto stage_free = [&]() {  // the stage is released once these MMAs have read it
+                umma_commit(bar_empty0 + 8u * cur.stage);
+                cur.advance(NS);
+            };
+            for (int t = 0; t <= n_tiles; ++t) {
+                if (t < n_tiles) {
+                    // S^T = C [Qhi | Qlo]^T over the 9 latent boxes: N = 32
+                    const uint32_t d = tmem + 2 * kMlaMaxHG * (t & 1);
+                    for (int sp = 0; sp < kSStages; ++sp) {
+                        const uint32_t st = stage_wait();
+                        for (int bx = 0; bx < 2 && 2 * sp + bx < kMlaBoxes; ++bx) {
+                            const int kc = 2 * sp + bx;
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                umma_bf16(d, umma_smem_desc(st + bx * kMlaBoxBytes + ks * 32, 16, 1024),
+                                          umma_smem_desc(qb + kc * kMlaQAtomBytes + ks * 32, 16, 1024),
+                                          idesc_s, kc > 0 || ks > 0);
+                        }
+                        stage_free();
+                    }
+                    umma_commit(bar_s0 + 8u * (t & 1));
+                }
+                if (t >= 1) {
+                    // O^T = C^T P^T of tile u = t - 1, 4 latent blocks of 128 dims
+                    const int u = t - 1;
+                    mbar_wait_bounded<false>(bar_p0 + 8u * (u & 1), (u >> 1) & 1, p.timeout_ns, timed_out,
+                                             p.status, kSiteStageFull);
+                    tcgen05_fence_after();
+                    const uint32_t d = tmem + 64 + 64 * (u & 1);
+                    const uint32_t pt = pb + (u & 1) * 2 * kMlaAtomBytes;
+                    for (int vp = 0; vp < kVStages; ++vp) {
+                        const uint32_t st = stage_wait();
+#pragma unroll
+                        for (int ks = 0; ks < kMlaTileRows / 16; ++ks)
+                            umma_bf16(d + 16 * vp, umma_smem_desc(st + ks * 2048, kMlaBoxBytes, 1024),
+                                      umma_smem_desc(pt + (ks >> 2) * kMlaAtomBytes + (ks & 3) * 32, 16, 1024),
+                                      idesc_o, ks > 0);
+                        stage_free();
+                    }
+                    umma_commit(bar_o0 + 8u * (u & 1));
+                }
+            }
         }
         __syncwarp();
         cluster_wait();
@@ -306,9 +385,9 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     }
     mbar_wait_bounded<true>(bar_q, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
 
-    // Queries as the B operand of the score MMA: bf16 hi and lo parts in
-    // [16 x 64] K-major swizzled atoms (heads past HG are zero), and the
-    // running softmax state.
+    // Queries as the B operand of the score MMA: [32 x 64] K-major swizzled
+    // atoms, rows 0-15 the bf16 hi parts of the 16 heads, rows 16-31 the lo
+    // parts (heads past HG are zero); and the running softmax state.
     for (int i = tid; i < kMlaMaxHG * (kMlaRow / 8); i += kComputeThreads) {
         const int n = i / (kMlaRow / 8), kc = i % (kMlaRow / 8);  // head, 8-element chunk
         float v[8];
@@ -332,145 +411,16 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             lo[e] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
                     (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
         }
-        const uint32_t off = (kc >> 3) * kMlaAtomBytes + mla_atom_off(n, (kc & 7) * 8);
-        *reinterpret_cast<uint4 *>(smem + p.off_qhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(smem + p.off_qlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        uint8_t *atom = smem + p.off_qb + (kc >> 3) * kMlaQAtomBytes;
+        *reinterpret_cast<uint4 *>(atom + mla_atom_off(n, (kc & 7) * 8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(atom + mla_atom_off(kMlaMaxHG + n, (kc & 7) * 8)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     if (tid < kMlaMaxHG) {
         m_st[tid] = -INFINITY;
         l_st[tid] = 0.f;
     }
-    fence_proxy_async_smem();
-    compute_bar<kComputeThreads>();
-
-    // ---- B: latent attention on the tensor cores --------------------------------
-    // TMEM lanes 32 (warp % 4) + lane are this thread's tile row (scores) and
-    // latent dim within a 128-dim block (outputs); warps 0-3 take heads 0-7 of
-    // the scores and latent blocks 0-1, warps 4-7 heads 8-15 and blocks 2-3.
-    const int wq = warp & 3, wh = warp >> 2;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * wq) << 16);
-    float acc[2][kMlaMaxHG];  // unnormalised o^T, latent dims 128 (2 wh + i) + 32 wq + lane
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = 0.f;
-    const uint32_t idesc_s = umma_idesc_bf16(128, kMlaMaxHG, false, false);  // A K-major
-    const uint32_t idesc_o = umma_idesc_bf16(128, kMlaMaxHG, true, false);   // A MN-major
-    for (int t = 0; t < n_tiles; ++t) {
-        const int nvalid = min(kMlaTileRows, cache_e - row_s - t * kMlaTileRows);
-        if (tid == 0) {
-            // S^T = C Q^T over the 9 latent boxes (hi and lo parts of Q)
-            tcgen05_fence_after();
-            for (int sp = 0; sp < kSStages; ++sp) {
-                mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out,
-                                         p.status, kSiteStageFull);
-                tcgen05_fence_after();
-                const uint32_t st = ring + cur.stage * kMlaStageBytes;
-                for (int bx = 0; bx < 2 && 2 * sp + bx < kMlaBoxes; ++bx) {
-                    const int kc = 2 * sp + bx;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t da = umma_smem_desc(st + bx * kMlaBoxBytes + ks * 32, 16, 1024);
-                        umma_bf16(tmem, da, umma_smem_desc(qhi + kc * kMlaAtomBytes + ks * 32, 16, 1024),
-                                  idesc_s, kc > 0 || ks > 0);
-                        umma_bf16(tmem, da, umma_smem_desc(qlo + kc * kMlaAtomBytes + ks * 32, 16, 1024),
-                                  idesc_s, true);
-                    }
-                }
-                umma_commit(bar_empty0 + 8u * cur.stage);
-                cur.advance(NS);
-            }
-            umma_commit(bar_s);
-        }
-        __syncwarp();
-        mbar_wait_bounded<false>(bar_s, t & 1, p.timeout_ns, timed_out, p.status, kSiteStageFull);
-        tcgen05_fence_after();
-        // scores of tile row 32 wq + lane, heads 8 wh .. + 8 (base-2 units)
-        float sv[8];
-        mla_tmem_ld_x8(tl + 8 * wh, sv);
-        const int row = 32 * wq + lane;
-        const bool valid = row < nvalid;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float mx = valid ? sv[j] : -INFINITY;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            if (lane == 0) red_max[warp * 16 + j] = mx;
-        }
-        tcgen05_fence_before();
-        compute_bar<kComputeThreads>();
-        // probabilities against the new running max; P as the K-major B
-        // operand of the value MMA (element (head, row))
-        float pv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int h = 8 * wh + j;
-            float tmax = red_max[(4 * wh) * 16 + j];
-#pragma unroll
-            for (int w = 1; w < 4; ++w) tmax = fmaxf(tmax, red_max[(4 * wh + w) * 16 + j]);
-            const float m_new = fmaxf(m_st[h], tmax);
-            pv[j] = valid && h < HG ? exp2f(sv[j] - m_new) : 0.f;
-            const uint32_t off = (row >> 6) * kMlaAtomBytes + mla_atom_off(h, row & 63);
-            *reinterpret_cast<uint16_t *>(smem + p.off_pb + off) =
-                __bfloat16_as_ushort(__float2bfloat16_rn(pv[j]));
-            float sm = pv[j];
-#pragma unroll
-            for (int off2 = 16; off2 > 0; off2 >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off2);
-            if (lane == 0) red_sum[warp * 16 + j] = sm;
-        }
-        fence_proxy_async_smem();  // P is read by the tensor cores
-        compute_bar<kComputeThreads>();
-        // per-head state: new max, rescale factor, running sum (fixed warp order)
-        if (tid < kMlaMaxHG) {
-            const int h = tid, hw = h >> 3, j = h & 7;
-            float tmax = red_max[(4 * hw) * 16 + j], tsum = red_sum[(4 * hw) * 16 + j];
-#pragma unroll
-            for (int w = 1; w < 4; ++w) {
-                tmax = fmaxf(tmax, red_max[(4 * hw + w) * 16 + j]);
-                tsum += red_sum[(4 * hw + w) * 16 + j];
-            }
-            const float m_old = m_st[h];
-            const float m_new = fmaxf(m_old, tmax);
-            const float al = exp2f(m_old - m_new);  // 0 while nothing was seen
-            alpha[h] = al;
-            l_st[h] = l_st[h] * al + tsum;
-            m_st[h] = m_new;
-        }
-        compute_bar<kComputeThreads>();
-        if (tid == 0) {
-            // O^T = C^T P^T for the 4 latent blocks of 128 dims
-            tcgen05_fence_after();
-            for (int vp = 0; vp < kVStages; ++vp) {
-                mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out,
-                                         p.status, kSiteStageFull);
-                tcgen05_fence_after();
-                const uint32_t st = ring + cur.stage * kMlaStageBytes;
-#pragma unroll
-                for (int ks = 0; ks < kMlaTileRows / 16; ++ks)
-                    umma_bf16(tmem + 16 + 16 * vp, umma_smem_desc(st + ks * 2048, kMlaBoxBytes, 1024),
-                              umma_smem_desc(pb + (ks >> 2) * kMlaAtomBytes + (ks & 3) * 32, 16, 1024),
-                              idesc_o, ks > 0);
-                umma_commit(bar_empty0 + 8u * cur.stage);
-                cur.advance(NS);
-            }
-            umma_commit(bar_o);
-        }
-        __syncwarp();
-        mbar_wait_bounded<false>(bar_o, t & 1, p.timeout_ns, timed_out, p.status, kSiteStageFull);
-        tcgen05_fence_after();
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            float o[16];
-            tmem_ld_x16(tl + 16 + 16 * (2 * wh + i), o);
-#pragma unroll
-            for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = acc[i][h] * alpha[h] + o[h];
-        }
-        tcgen05_fence_before();
-        compute_bar<kComputeThreads>();
-    }
-    // The new row, attended on CUDA cores: its score per head, the state
-    // update, and its value folded into the partial output.
-    if (has_new) {
+    if (has_new) {  // the new row's score per head (base 2)
         for (int h = warp; h < HG; h += kComputeWarps) {
             float s = 0.f;
             for (int k = lane; k < kMlaRow; k += 32) s = fmaf(qt[h * kMlaRow + k], bf16_bits(newrow[k]), s);
@@ -478,7 +428,108 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
             if (lane == 0) s_new[h] = s;
         }
+    }
+    fence_proxy_async_smem();
+    compute_bar<kComputeThreads>();
+    if (tid == 0) mbar_arrive(bar_qready);
+    // The fp32 queries are dead here; their space receives the peers' partials.
+    if (tid == 0)
+        for (int q = 0; q < C; ++q)
+            if (q != r) mbar_arrive_remote(map_to_rank(bar_qfree, q));
+
+    // ---- B: latent attention on the tensor cores --------------------------------
+    // The MMA warp computes the scores of tile t + 1 while these warps run the
+    // softmax of tile t. TMEM lanes 32 (warp % 4) + lane are this thread's tile
+    // row (scores) and latent dim within a 128-dim block (outputs); warps 0-3
+    // take heads 0-7 of the scores and latent blocks 0-1, warps 4-7 heads 8-15
+    // and blocks 2-3.
+    const int wq = warp & 3, wh = warp >> 2;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * wq) << 16);
+    float acc[2][kMlaMaxHG];  // unnormalised o^T, latent dims 128 (2 wh + i) + 32 wq + lane
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = 0.f;
+    auto fold = [&](int u) {  // acc = acc alpha_u + O_u
+        mbar_wait_bounded<false>(bar_o0 + 8u * (u & 1), (u >> 1) & 1, p.timeout_ns, timed_out, p.status,
+                                 kSiteStageFull);
+        tcgen05_fence_after();
+        const float *al = alpha + kMlaMaxHG * (u & 1);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float o[16];
+            tmem_ld_x16(tl + 64 + 64 * (u & 1) + 16 * (2 * wh + i), o);
+#pragma unroll
+            for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = acc[i][h] * al[h] + o[h];
+        }
+        tcgen05_fence_before();
+    };
+    for (int t = 0; t < n_tiles; ++t) {
+        const int nvalid = min(kMlaTileRows, cache_e - row_s - t * kMlaTileRows);
+        float *rmax = red_max + 8 * kMlaMaxHG * (t & 1), *rsum = red_sum + 8 * kMlaMaxHG * (t & 1);
+        mbar_wait_bounded<false>(bar_s0 + 8u * (t & 1), (t >> 1) & 1, p.timeout_ns, timed_out, p.status,
+                                 kSiteStageFull);
+        tcgen05_fence_after();
+        // scores of tile row 32 wq + lane, heads 8 wh .. + 8 (base-2 units): hi + lo
+        float sv[8], sl[8];
+        mla_tmem_ld_x8(tl + 2 * kMlaMaxHG * (t & 1) + 8 * wh, sv);
+        mla_tmem_ld_x8(tl + 2 * kMlaMaxHG * (t & 1) + kMlaMaxHG + 8 * wh, sl);
+        const int row = 32 * wq + lane;
+        const bool valid = row < nvalid;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            sv[j] += sl[j];
+            float mx = valid ? sv[j] : -INFINITY;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (lane == 0) rmax[warp * 16 + j] = mx;
+        }
+        tcgen05_fence_before();
         compute_bar<kComputeThreads>();
+        // probabilities against the new running max; P as the K-major B
+        // operand of the value MMA (element (head, row))
+        uint8_t *pt = smem + p.off_pb + (t & 1) * 2 * kMlaAtomBytes;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int h = 8 * wh + j;
+            float tmax = rmax[(4 * wh) * 16 + j];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) tmax = fmaxf(tmax, rmax[(4 * wh + w) * 16 + j]);
+            const float m_new = fmaxf(m_st[h], tmax);
+            const float pv = valid && h < HG ? exp2f(sv[j] - m_new) : 0.f;
+            *reinterpret_cast<uint16_t *>(pt + (row >> 6) * kMlaAtomBytes + mla_atom_off(h, row & 63)) =
+                __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+            float sm = pv;
+#pragma unroll
+            for (int off2 = 16; off2 > 0; off2 >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off2);
+            if (lane == 0) rsum[warp * 16 + j] = sm;
+        }
+        fence_proxy_async_smem();  // P is read by the tensor cores
+        compute_bar<kComputeThreads>();
+        if (tid == 0) mbar_arrive(bar_p0 + 8u * (t & 1));
+        // per-head state: new max, rescale factor, running sum (fixed warp order)
+        if (tid < kMlaMaxHG) {
+            const int h = tid, hw = h >> 3, j = h & 7;
+            float tmax = rmax[(4 * hw) * 16 + j], tsum = rsum[(4 * hw) * 16 + j];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) {
+                tmax = fmaxf(tmax, rmax[(4 * hw + w) * 16 + j]);
+                tsum += rsum[(4 * hw + w) * 16 + j];
+            }
+            const float m_old = m_st[h];
+            const float m_new = fmaxf(m_old, tmax);
+            const float al = exp2f(m_old - m_new);  // 0 while nothing was seen
+            alpha[kMlaMaxHG * (t & 1) + h] = al;
+            l_st[h] = l_st[h] * al + tsum;
+            m_st[h] = m_new;
+        }
+        if (t >= 1) fold(t - 1);
+    }
+    if (n_tiles > 0) fold(n_tiles - 1);
+    compute_bar<kComputeThreads>();
+    // The new row, attended on CUDA cores: its score per head, the state
+    // update, and its value folded into the partial output.
+    if (has_new) {
         if (tid < HG) {
             const int h = tid;
             const float m_old = m_st[h];
@@ -501,15 +552,16 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
 
     // ---- C: sparse ClusterReduce -- each head goes to the block that owns it --
     {
-        // stage o^T as [head][512] where the query operands were (every MMA
+        // stage o^T as [head][512] where the query operand was (every MMA
         // has completed), then ship each head's row and (m, l) to its owner
-        float *stage = reinterpret_cast<float *>(smem + p.off_qhi);
+        float *stage = reinterpret_cast<float *>(smem + p.off_qb);
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int h = 0; h < kMlaMaxHG; ++h)
                 stage[h * kMlaKv + 128 * (2 * wh + i) + 32 * wq + lane] = acc[i][h];
         compute_bar<kComputeThreads>();
+        mbar_wait_bounded<true>(bar_qfree, 0, p.timeout_ns, timed_out, p.status, kSiteSoftmaxExchange);
         const int per_head = kMlaKv / 4 + 1;  // 128 chunks of o, then (m, l, 0, 0)
         for (int idx = tid; idx < HG * per_head; idx += kComputeThreads) {
             const int h = idx / per_head, c = idx % per_head;
@@ -586,7 +638,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     }
     if (warp == 0) {
         tcgen05_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 256);
     }
     cluster_sync_all();  // no block leaves while a peer may still push into it
 }

@@ -736,7 +736,7 @@ struct cfa_mla {
 
 namespace {
 
-constexpr int kMlaStages = 3;  // two-box (32 KB) stages of the latent ring
+constexpr int kMlaStages = 4;  // two-box (32 KB) stages of the latent ring
 
 void mla_free(cfa_mla *m) {
     if (m->a) cudaFree(m->a);
@@ -829,26 +829,23 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
         int off = 0;
         mp.off_ring = off;                          // two-box stages (1024-aligned boxes)
         off += kMlaStages * cfa::kMlaStageBytes;
-        mp.off_qhi = off;                           // 9 swizzled [16 x 64] query atoms, hi
-        off += cfa::kMlaBoxes * cfa::kMlaAtomBytes;
-        mp.off_qlo = off;                           // and lo parts
-        off += cfa::kMlaBoxes * cfa::kMlaAtomBytes;
-        mp.off_pb = off;                            // P: 2 atoms [16 heads x 64 rows]
-        off += 2 * cfa::kMlaAtomBytes;
-        mp.off_qt = off;                            // fp32 queries [HG][576]
-        off += align_up(HG * cfa::kMlaRow * 4, 128);
+        mp.off_qb = off;                            // 9 swizzled [32 x 64] query atoms (hi, lo)
+        off += cfa::kMlaBoxes * cfa::kMlaQAtomBytes;
+        mp.off_pb = off;                            // P of two tiles: 2 x 2 atoms [16 heads x 64 rows]
+        off += 4 * cfa::kMlaAtomBytes;
+        mp.off_qt = off;                            // fp32 queries [HG][576], then
+        mp.off_recv = off;                          // partials of my heads [HPB][C][516]
+        off += align_up(std::max(HG * cfa::kMlaRow, mp.HPB * mp.C * (cfa::kMlaKv + 4)) * 4, 128);
         mp.off_newrow = off;
         off += align_up(cfa::kMlaRow * 2, 128);
-        mp.off_stat = off;                          // m, l, alpha, two [8][16] reductions, new row
-        off += align_up(320 * 4, 128);
-        mp.off_recv = off;                          // partials of my heads [HPB][C][516]
-        off += align_up(mp.HPB * mp.C * (cfa::kMlaKv + 4) * 4, 128);
+        mp.off_stat = off;                          // m, l, 2 alpha, 2 x two [8][16] reductions, new row
+        off += align_up(592 * 4, 128);
         mp.off_ofin = off;                          // combined latent outputs [HPB][512]
         off += align_up(mp.HPB * cfa::kMlaKv * 4, 128);
         mp.off_scr = off;
         off += align_up((cfa::kComputeWarps * cfa::kMlaV + 64) * 4, 128);
         mp.off_bars = off;
-        off += 16 * kMlaStages + 64;
+        off += 16 * kMlaStages + 128;
         return off;
     };
     const void *kernel = cfa::mla_kernel_ptr(HG);
@@ -877,7 +874,7 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
             attr[0].val.clusterDim.z = 1;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(n_clusters * C);
-            cfg.blockDim = dim3(cfa::kThreads);
+            cfg.blockDim = dim3(cfa::kMlaThreads);
             cfg.dynamicSmemBytes = static_cast<size_t>(layout(C));
             cfg.attrs = attr;
             cfg.numAttrs = 1;
@@ -1016,7 +1013,7 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(m->B * (m->nh / mp.HG) * mp.C);
-        cfg.blockDim = dim3(cfa::kThreads);
+        cfg.blockDim = dim3(cfa::kMlaThreads);
         cfg.dynamicSmemBytes = static_cast<size_t>(m->smem);
         cfg.stream = cs;
         cfg.attrs = attr;
