@@ -161,6 +161,18 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
     return r;
 }
 
+// Bulk copy from this block's shared memory into another block's (`dst` and
+// `remote_bar` from map_to_rank), counting the bytes on that block's barrier.
+// Addresses 16-byte aligned, bytes a multiple of 16; the source is read
+// asynchronously (write it, then fence_proxy_async_smem, before the copy).
+__device__ __forceinline__ void bulk_copy_to_rank(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t remote_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "r"(src), "r"(bytes), "r"(remote_bar)
+        : "memory");
+}
+
 // Arrive, with release at cluster scope, on a barrier of another block of the
 // cluster (`remote_bar` from map_to_rank).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {

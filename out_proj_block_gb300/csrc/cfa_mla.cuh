@@ -177,17 +177,22 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                         cur.advance(NS);
                     }
             };
-            for (int i = 0; i < HPB; ++i) {  // W_v blocks, wanted at the end: warm L2 now
-                const int col0 = (g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope;
+            // Weight blocks into L2 ahead of the ring (more bytes in flight than
+            // it holds): W_k now, W_v once the W_k loads are out, so that it
+            // does not queue in front of them.
+            auto prefetch_block = [&](int col0) {
                 for (int rb = 0; rb < 2; ++rb)
                     for (int cb = 0; cb < 2; ++cb)
                         asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
                                      :: "l"(reinterpret_cast<uint64_t>(&tm_wkvb)), "r"(col0 + 64 * cb),
                                         "r"(kMlaWeightRows * rb)
                                      : "memory");
-            }
+            };
+            for (int i = 0; i < HPB; ++i) prefetch_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV));
             for (int i = 0; i < HPB; ++i)  // weights: independent of the previous kernel
                 weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV));
+            for (int i = 0; i < HPB; ++i)
+                prefetch_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope);
             grid_dependency_wait();  // cache rows may come from the previous step
             const CUtensorMap *tm = &maps.cache[b];
             auto stage_in = [&](int kc0, int nbox, int row) {
@@ -318,7 +323,9 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             // q~[j] = sum_c W_kvb[j, h*256 + c] q_nope[c]: thread tid takes latent
             // rows tid and tid + 256, a swizzled 128-byte box row per stage
             float acc_q[2] = {0.f, 0.f};
+#pragma unroll
             for (int rb = 0; rb < 2; ++rb)
+#pragma unroll
                 for (int cb = 0; cb < 2; ++cb) {
                     const uint8_t *st = stage_ready();
 #pragma unroll
@@ -338,17 +345,15 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 dst[kMlaKv + tid] = x0 * p.qscale;
                 dst[kMlaKv + tid + kMlaRope / 2] = x1 * p.qscale;
             }
+            fence_proxy_async_smem();  // the rows are read by the bulk copies
             compute_bar<kComputeThreads>();
         }
-        cluster_wait();  // every peer's barriers exist before the first push
-        // ClusterGather: my heads' 576 scaled query values to every peer
-        const int chunks = HPB * kMlaRow / 4;
-        const uint32_t my0 = smem_addr(qt + r * HPB * kMlaRow);
-        for (int idx = tid; idx < (C - 1) * chunks; idx += kComputeThreads) {
-            const int pi = idx / chunks, c = idx % chunks;
-            const int peer = pi < r ? pi : pi + 1;
-            const float4 val = reinterpret_cast<const float4 *>(qt + r * HPB * kMlaRow)[c];
-            push_16B(map_to_rank(my0 + 16u * c, peer), val, map_to_rank(bar_q, peer));
+        cluster_wait();  // every peer's barriers exist before the first copy
+        // ClusterGather: my heads' 576 scaled query values, one bulk copy per peer
+        if (tid < C && tid != r) {
+            const uint32_t my0 = smem_addr(qt + r * HPB * kMlaRow);
+            bulk_copy_to_rank(map_to_rank(my0, tid), my0, static_cast<uint32_t>(HPB * kMlaRow * 4),
+                              map_to_rank(bar_q, tid));
         }
     }
     // The new token's latent row (last block): bf16 RMSNorm of the latent and
@@ -552,51 +557,59 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
 
     // ---- C: sparse ClusterReduce -- each head goes to the block that owns it --
     {
-        // stage o^T as [head][512] where the query operand was (every MMA
-        // has completed), then ship each head's row and (m, l) to its owner
-        float *stage = reinterpret_cast<float *>(smem + p.off_qb);
+        // stage each head's (o^T [512], m, l, 0, 0) where the query operand was
+        // (every MMA has completed), then one bulk copy per head to its owner
+        float *stage = reinterpret_cast<float *>(smem + p.off_qb);  // [HG][516]
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
             for (int h = 0; h < kMlaMaxHG; ++h)
-                stage[h * kMlaKv + 128 * (2 * wh + i) + 32 * wq + lane] = acc[i][h];
+                if (h < HG) stage[h * (kMlaKv + 4) + 128 * (2 * wh + i) + 32 * wq + lane] = acc[i][h];
+        if (tid < HG)
+            *reinterpret_cast<float4 *>(stage + tid * (kMlaKv + 4) + kMlaKv) =
+                make_float4(m_st[tid], l_st[tid], 0.f, 0.f);
+        fence_proxy_async_smem();
         compute_bar<kComputeThreads>();
         mbar_wait_bounded<true>(bar_qfree, 0, p.timeout_ns, timed_out, p.status, kSiteSoftmaxExchange);
-        const int per_head = kMlaKv / 4 + 1;  // 128 chunks of o, then (m, l, 0, 0)
-        for (int idx = tid; idx < HG * per_head; idx += kComputeThreads) {
-            const int h = idx / per_head, c = idx % per_head;
-            const int owner = h / HPB, slot = h % HPB;
-            float *dst = recv + (slot * C + r) * (kMlaKv + 4) + 4 * c;
-            const float4 val = c < kMlaKv / 4
-                                   ? reinterpret_cast<const float4 *>(stage + h * kMlaKv)[c]
-                                   : make_float4(m_st[h], l_st[h], 0.f, 0.f);
-            if (owner == r) {
-                *reinterpret_cast<float4 *>(dst) = val;
-            } else {
-                push_16B(map_to_rank(smem_addr(dst), owner), val, map_to_rank(bar_red, owner));
-            }
+        if (tid < HG && tid / HPB != r) {
+            const int h = tid, owner = h / HPB, slot = h % HPB;
+            bulk_copy_to_rank(map_to_rank(smem_addr(recv + (slot * C + r) * (kMlaKv + 4)), owner),
+                              smem_addr(stage + h * (kMlaKv + 4)), static_cast<uint32_t>((kMlaKv + 4) * 4),
+                              map_to_rank(bar_red, owner));
+        }
+        for (int idx = tid; idx < HPB * (kMlaKv + 4) / 4; idx += kComputeThreads) {  // my own heads
+            const int slot = idx / ((kMlaKv + 4) / 4), c = idx % ((kMlaKv + 4) / 4);
+            reinterpret_cast<float4 *>(recv + (slot * C + r) * (kMlaKv + 4))[c] =
+                reinterpret_cast<const float4 *>(stage + (r * HPB + slot) * (kMlaKv + 4))[c];
         }
         compute_bar<kComputeThreads>();  // own partials written
         mbar_wait_bounded<true>(bar_red, 0, p.timeout_ns, timed_out, p.status, kSiteSoftmaxExchange);
-        // combine in block order: o = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r
-        for (int i = 0; i < HPB; ++i) {
-            const float *rv = recv + i * C * (kMlaKv + 4);
+        // combine in block order: o = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r,
+        // the weights w_r = 2^(m_r - M) / L computed once per head
+        float *wgt = scr;  // [HPB][16]
+        if (tid < HPB) {
+            const float *rv = recv + tid * C * (kMlaKv + 4);
             float M = -INFINITY;
             for (int q = 0; q < C; ++q) M = fmaxf(M, rv[q * (kMlaKv + 4) + kMlaKv]);
             float Lsum = 0.f;
             for (int q = 0; q < C; ++q) {
                 const float mq = rv[q * (kMlaKv + 4) + kMlaKv];
-                if (mq != -INFINITY) Lsum += exp2f(mq - M) * rv[q * (kMlaKv + 4) + kMlaKv + 1];
+                const float e = mq != -INFINITY ? exp2f(mq - M) : 0.f;
+                wgt[tid * kMlaMaxHG + q] = e;
+                Lsum += e * rv[q * (kMlaKv + 4) + kMlaKv + 1];
             }
             const float inv = 1.0f / Lsum;
-            for (int d = tid; d < kMlaKv; d += kComputeThreads) {
-                float o = 0.f;
-                for (int q = 0; q < C; ++q) {
-                    const float mq = rv[q * (kMlaKv + 4) + kMlaKv];
-                    if (mq != -INFINITY) o += exp2f(mq - M) * rv[q * (kMlaKv + 4) + d];
-                }
-                ofin[i * kMlaKv + d] = o * inv;
-            }
+            for (int q = 0; q < C; ++q) wgt[tid * kMlaMaxHG + q] *= inv;
+        }
+        compute_bar<kComputeThreads>();
+        for (int idx = tid; idx < HPB * kMlaKv; idx += kComputeThreads) {
+            const int i = idx / kMlaKv, d = idx % kMlaKv;
+            const float *rv = recv + i * C * (kMlaKv + 4) + d;
+            const float *w = wgt + i * kMlaMaxHG;
+            float o = 0.f;
+#pragma unroll 4
+            for (int q = 0; q < C; ++q) o = fmaf(w[q], rv[q * (kMlaKv + 4)], o);
+            ofin[idx] = o;
         }
         compute_bar<kComputeThreads>();
         // v_h = o_h W_v,h from the ring's [256 x 64] W_v boxes: warp w takes box
@@ -606,7 +619,9 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
         for (int ii = 0; ii < HPB; ++ii) {
             const int h = g * HG + r * HPB + ii;
             float part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
             for (int rb = 0; rb < 2; ++rb)
+#pragma unroll
                 for (int cb = 0; cb < 2; ++cb) {
                     const uint8_t *st = stage_ready();
 #pragma unroll 8
