@@ -272,6 +272,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ---------------------------------------------------------------- bf16 bits
 
+// 2^x by the hardware's base-2 exponential (ex2.approx.f32: relative error
+// about 2^-22; 2^-inf = +0). Softmax weights need no more, and it is a single
+// instruction where the accurate library exp2f is a long sequence.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 __device__ __forceinline__ float bf16_bits(uint16_t v) {

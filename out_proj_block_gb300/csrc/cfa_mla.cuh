@@ -68,6 +68,17 @@ __device__ __forceinline__ uint32_t mla_atom_off(int n, int k) {
     return static_cast<uint32_t>(n * 128 + (((k >> 3) ^ (n & 7)) << 4) + (k & 7) * 2);
 }
 
+// Bounded wait by a whole warp: lane 0 polls the barrier, the other lanes wait
+// at __syncwarp (which also passes lane 0's view of the guarded data on). 32x
+// fewer polls keep the shared memory free for the TMA engine, the tensor cores
+// and the threads still working.
+template <bool CLUSTER_SCOPE>
+__device__ __forceinline__ void mla_warp_wait(uint32_t bar, uint32_t parity, const MlaParams &p,
+                                              volatile int *timed_out, unsigned site) {
+    if ((threadIdx.x & 31) == 0) mbar_wait_bounded<CLUSTER_SCOPE>(bar, parity, p.timeout_ns, timed_out, p.status, site);
+    __syncwarp();
+}
+
 // Rotate-half rotation of (x0, x1) = dims (k, k + 32) by pos * inv_freq, the
 // angle taken in fp64 and reduced to (-pi, pi] before the fp32 sine/cosine.
 __device__ __forceinline__ void mla_rope(float &x0, float &x1, int pos, double inv_freq) {
@@ -151,7 +162,6 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     if (warp == 0) tmem_alloc(smem_addr(tmem_slot), 256);
     tcgen05_fence_before();
     __syncthreads();
-    grid_dependents_launch();
     cluster_arrive();  // barriers announced; waited for before the first push
 
     if (warp == kComputeWarps) {
@@ -166,9 +176,12 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                     mbar_wait_bounded<false>(bar_empty0 + 8u * cur.stage, cur.phase ^ 1u,
                                              p.timeout_ns, timed_out, p.status, kSiteStageEmpty);
             };
-            auto weight_block = [&](int col0) {  // [512 x 128] of W_kvb in 4 stages
-                for (int rb = 0; rb < 2; ++rb)
-                    for (int cb = 0; cb < 2; ++cb) {
+            // [512 x 128] of W_kvb in 4 stages: W_k column-block major (each
+            // half of q_nope is used for both row blocks), W_v row-block major
+            auto weight_block = [&](int col0, bool col_major) {
+                for (int a = 0; a < 2; ++a)
+                    for (int c = 0; c < 2; ++c) {
+                        const int rb = col_major ? c : a, cb = col_major ? a : c;
                         wait_slot();
                         const uint32_t full = bar_full0 + 8u * cur.stage;
                         mbar_arrive_expect_tx(full, static_cast<uint32_t>(kMlaStageBytes));
@@ -188,9 +201,11 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                                         "r"(kMlaWeightRows * rb)
                                      : "memory");
             };
-            for (int i = 0; i < HPB; ++i) prefetch_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV));
-            for (int i = 0; i < HPB; ++i)  // weights: independent of the previous kernel
-                weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV));
+            // weights: independent of the previous kernel. The first head's
+            // W_k goes straight into the ring; the other heads' into L2 behind it.
+            weight_block((g * HG + r * HPB) * (kMlaNope + kMlaV), true);
+            for (int i = 1; i < HPB; ++i) prefetch_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV));
+            for (int i = 1; i < HPB; ++i) weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV), true);
             for (int i = 0; i < HPB; ++i)
                 prefetch_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope);
             grid_dependency_wait();  // cache rows may come from the previous step
@@ -214,17 +229,13 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                     for (int vp = 0; vp < kVStages; ++vp) stage_in(2 * vp, 2, row_s + (t - 1) * kMlaTileRows);
             }
             for (int i = 0; i < HPB; ++i)
-                weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope);
-            for (int s = 0; s < NS; ++s) {  // drain
-                if (s >= cur.stage && !cur.wrapped) break;
-                volatile int ignore = 0;
-                mbar_wait_bounded<false>(bar_full0 + 8u * s, s < cur.stage ? cur.phase : cur.phase ^ 1u,
-                                         p.timeout_ns, &ignore, p.status, kSiteStageFull);
-            }
+                weight_block((g * HG + r * HPB + i) * (kMlaNope + kMlaV) + kMlaNope, false);
+            // no drain: the compute warps wait for every stage this warp loads
         } else {
             grid_dependency_wait();
         }
         __syncwarp();
+        grid_dependents_launch();
         cluster_wait();
         cluster_sync_all();
         return;
@@ -290,6 +301,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             }
         }
         __syncwarp();
+        grid_dependents_launch();
         cluster_wait();
         cluster_sync_all();
         return;
@@ -302,8 +314,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     // ---- A: absorbed queries of this block's heads, pushed to the cluster ----
     RingCursor cur;  // every compute thread follows the ring through phase A
     auto stage_ready = [&]() {
-        mbar_wait_bounded<false>(bar_full0 + 8u * cur.stage, cur.phase, p.timeout_ns, timed_out, p.status,
-                                 kSiteStageFull);
+        mla_warp_wait<false>(bar_full0 + 8u * cur.stage, cur.phase, p, timed_out, kSiteStageFull);
         return smem + p.off_ring + cur.stage * kMlaStageBytes;
     };
     auto stage_done = [&]() {  // every compute thread has read the stage
@@ -321,22 +332,30 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             compute_bar<kComputeThreads>();
             float *dst = qt + hl * kMlaRow;
             // q~[j] = sum_c W_kvb[j, h*256 + c] q_nope[c]: thread tid takes latent
-            // rows tid and tid + 256, a swizzled 128-byte box row per stage
+            // rows tid and tid + 256, a swizzled 128-byte box row per stage; the
+            // 64 q_nope values of a column block stay in registers
             float acc_q[2] = {0.f, 0.f};
 #pragma unroll
-            for (int rb = 0; rb < 2; ++rb)
+            for (int cb = 0; cb < 2; ++cb) {
+                float qr[64];
 #pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
+                for (int c = 0; c < 16; ++c) {
+                    const float4 v = reinterpret_cast<const float4 *>(qn + 64 * cb)[c];
+                    qr[4 * c] = v.x; qr[4 * c + 1] = v.y; qr[4 * c + 2] = v.z; qr[4 * c + 3] = v.w;
+                }
+#pragma unroll
+                for (int rb = 0; rb < 2; ++rb) {
                     const uint8_t *st = stage_ready();
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         float f[8];
                         unpack8_bf16(*reinterpret_cast<const uint4 *>(st + tid * 128 + ((c ^ (tid & 7)) << 4)), f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc_q[rb] = fmaf(f[e], qn[64 * cb + 8 * c + e], acc_q[rb]);
+                        for (int e = 0; e < 8; ++e) acc_q[rb] = fmaf(f[e], qr[8 * c + e], acc_q[rb]);
                     }
                     stage_done();
                 }
+            }
             dst[tid] = acc_q[0] * p.qscale;
             dst[tid + kComputeThreads] = acc_q[1] * p.qscale;
             if (tid < kMlaRope / 2) {
@@ -388,7 +407,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 reinterpret_cast<uint4 *>(crow)[i] = reinterpret_cast<const uint4 *>(newrow)[i];
         }
     }
-    mbar_wait_bounded<true>(bar_q, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
+    mla_warp_wait<true>(bar_q, 0, p, timed_out, kSiteQExchange);
 
     // Queries as the B operand of the score MMA: [32 x 64] K-major swizzled
     // atoms, rows 0-15 the bf16 hi parts of the 16 heads, rows 16-31 the lo
@@ -456,8 +475,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
 #pragma unroll
         for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = 0.f;
     auto fold = [&](int u) {  // acc = acc alpha_u + O_u
-        mbar_wait_bounded<false>(bar_o0 + 8u * (u & 1), (u >> 1) & 1, p.timeout_ns, timed_out, p.status,
-                                 kSiteStageFull);
+        mla_warp_wait<false>(bar_o0 + 8u * (u & 1), (u >> 1) & 1, p, timed_out, kSiteStageFull);
         tcgen05_fence_after();
         const float *al = alpha + kMlaMaxHG * (u & 1);
 #pragma unroll
@@ -472,8 +490,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     for (int t = 0; t < n_tiles; ++t) {
         const int nvalid = min(kMlaTileRows, cache_e - row_s - t * kMlaTileRows);
         float *rmax = red_max + 8 * kMlaMaxHG * (t & 1), *rsum = red_sum + 8 * kMlaMaxHG * (t & 1);
-        mbar_wait_bounded<false>(bar_s0 + 8u * (t & 1), (t >> 1) & 1, p.timeout_ns, timed_out, p.status,
-                                 kSiteStageFull);
+        mla_warp_wait<false>(bar_s0 + 8u * (t & 1), (t >> 1) & 1, p, timed_out, kSiteStageFull);
         tcgen05_fence_after();
         // scores of tile row 32 wq + lane, heads 8 wh .. + 8 (base-2 units): hi + lo
         float sv[8], sl[8];
@@ -501,7 +518,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
 #pragma unroll
             for (int w = 1; w < 4; ++w) tmax = fmaxf(tmax, rmax[(4 * wh + w) * 16 + j]);
             const float m_new = fmaxf(m_st[h], tmax);
-            const float pv = valid && h < HG ? exp2f(sv[j] - m_new) : 0.f;
+            const float pv = valid && h < HG ? fast_exp2(sv[j] - m_new) : 0.f;
             *reinterpret_cast<uint16_t *>(pt + (row >> 6) * kMlaAtomBytes + mla_atom_off(h, row & 63)) =
                 __bfloat16_as_ushort(__float2bfloat16_rn(pv));
             float sm = pv;
@@ -523,7 +540,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             }
             const float m_old = m_st[h];
             const float m_new = fmaxf(m_old, tmax);
-            const float al = exp2f(m_old - m_new);  // 0 while nothing was seen
+            const float al = fast_exp2(m_old - m_new);  // 0 while nothing was seen
             alpha[kMlaMaxHG * (t & 1) + h] = al;
             l_st[h] = l_st[h] * al + tsum;
             m_st[h] = m_new;
@@ -532,6 +549,9 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     }
     if (n_tiles > 0) fold(n_tiles - 1);
     compute_bar<kComputeThreads>();
+    // The next kernel (the output projection) may start streaming its weights
+    // now: launched earlier, it would compete for HBM with this kernel's loads.
+    grid_dependents_launch();
     // The new row, attended on CUDA cores: its score per head, the state
     // update, and its value folded into the partial output.
     if (has_new) {
@@ -539,7 +559,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             const int h = tid;
             const float m_old = m_st[h];
             const float m_new = fmaxf(m_old, s_new[h]);
-            const float al = exp2f(m_old - m_new), pn = exp2f(s_new[h] - m_new);
+            const float al = fast_exp2(m_old - m_new), pn = fast_exp2(s_new[h] - m_new);
             alpha[h] = al;
             s_new[h] = pn;
             l_st[h] = l_st[h] * al + pn;
@@ -570,7 +590,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 make_float4(m_st[tid], l_st[tid], 0.f, 0.f);
         fence_proxy_async_smem();
         compute_bar<kComputeThreads>();
-        mbar_wait_bounded<true>(bar_qfree, 0, p.timeout_ns, timed_out, p.status, kSiteSoftmaxExchange);
+        mla_warp_wait<true>(bar_qfree, 0, p, timed_out, kSiteSoftmaxExchange);
         if (tid < HG && tid / HPB != r) {
             const int h = tid, owner = h / HPB, slot = h % HPB;
             bulk_copy_to_rank(map_to_rank(smem_addr(recv + (slot * C + r) * (kMlaKv + 4)), owner),
@@ -583,23 +603,25 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 reinterpret_cast<const float4 *>(stage + (r * HPB + slot) * (kMlaKv + 4))[c];
         }
         compute_bar<kComputeThreads>();  // own partials written
-        mbar_wait_bounded<true>(bar_red, 0, p.timeout_ns, timed_out, p.status, kSiteSoftmaxExchange);
+        mla_warp_wait<true>(bar_red, 0, p, timed_out, kSiteSoftmaxExchange);
         // combine in block order: o = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r,
         // the weights w_r = 2^(m_r - M) / L computed once per head
         float *wgt = scr;  // [HPB][16]
-        if (tid < HPB) {
-            const float *rv = recv + tid * C * (kMlaKv + 4);
-            float M = -INFINITY;
-            for (int q = 0; q < C; ++q) M = fmaxf(M, rv[q * (kMlaKv + 4) + kMlaKv]);
-            float Lsum = 0.f;
-            for (int q = 0; q < C; ++q) {
-                const float mq = rv[q * (kMlaKv + 4) + kMlaKv];
-                const float e = mq != -INFINITY ? exp2f(mq - M) : 0.f;
-                wgt[tid * kMlaMaxHG + q] = e;
-                Lsum += e * rv[q * (kMlaKv + 4) + kMlaKv + 1];
-            }
-            const float inv = 1.0f / Lsum;
-            for (int q = 0; q < C; ++q) wgt[tid * kMlaMaxHG + q] *= inv;
+        if (warp < (HPB * kMlaMaxHG + 31) / 32) {  // 16 lanes per head, lane q for block q
+            const int i = tid / kMlaMaxHG, q = tid % kMlaMaxHG;
+            const bool act = i < HPB && q < C;
+            const float *rv = recv + i * C * (kMlaKv + 4);
+            const float mq = act ? rv[q * (kMlaKv + 4) + kMlaKv] : -INFINITY;
+            float M = mq;
+#pragma unroll
+            for (int off = kMlaMaxHG / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            const float e = mq != -INFINITY ? fast_exp2(mq - M) : 0.f;
+            const float lq = act ? rv[q * (kMlaKv + 4) + kMlaKv + 1] : 0.f;
+            // block-order sum of e_q l_q: a fixed shuffle tree over the 16 lanes
+            float Lsum = e * lq;
+#pragma unroll
+            for (int off = kMlaMaxHG / 2; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+            if (i < HPB) wgt[i * kMlaMaxHG + q] = e / Lsum;
         }
         compute_bar<kComputeThreads>();
         for (int idx = tid; idx < HPB * kMlaKv; idx += kComputeThreads) {
@@ -612,34 +634,44 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             ofin[idx] = o;
         }
         compute_bar<kComputeThreads>();
-        // v_h = o_h W_v,h from the ring's [256 x 64] W_v boxes: warp w takes box
-        // rows 32 w .. 32 w + 31, lane the value columns 2 lane, 2 lane + 1
+        // v_h = o_h W_v,h from the ring's [256 x 64] W_v boxes: thread tid takes
+        // the 8 value columns of 16-byte chunk tid % 8 in box rows tid / 8 + 32 k
         cur = RingCursor();
         for (int n = 0; n < 4 * HPB + (kSStages + kVStages) * n_tiles; ++n) cur.advance(NS);
+        const int cc = tid & 7, rg = tid >> 3;
         for (int ii = 0; ii < HPB; ++ii) {
             const int h = g * HG + r * HPB + ii;
-            float part[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            float part[2][8];
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part[cb][e] = 0.f;
 #pragma unroll
             for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
                 for (int cb = 0; cb < 2; ++cb) {
                     const uint8_t *st = stage_ready();
-#pragma unroll 8
-                    for (int k = 0; k < 32; ++k) {
-                        const int row = 32 * warp + k;
+#pragma unroll
+                    for (int k = 0; k < kMlaWeightRows / 32; ++k) {
+                        const int row = rg + 32 * k;
                         const float oj = ofin[ii * kMlaKv + kMlaWeightRows * rb + row];
-                        const uint32_t w = *reinterpret_cast<const uint32_t *>(
-                            st + row * 128 + (((lane >> 2) ^ (row & 7)) << 4) + (lane & 3) * 4);
-                        part[cb][0] = fmaf(oj, bf16_lo(w), part[cb][0]);
-                        part[cb][1] = fmaf(oj, bf16_hi(w), part[cb][1]);
+                        float f[8];
+                        unpack8_bf16(*reinterpret_cast<const uint4 *>(st + row * 128 + ((cc ^ (row & 7)) << 4)), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) part[cb][e] = fmaf(oj, f[e], part[cb][e]);
                     }
                     stage_done();
                 }
+            // sum over the 32 row groups: 4 in a warp by shuffles, 8 warps in smem
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                scr[warp * kMlaV + 64 * cb + 2 * lane] = part[cb][0];
-                scr[warp * kMlaV + 64 * cb + 2 * lane + 1] = part[cb][1];
-            }
+            for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float v = part[cb][e];
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    if (lane < 8) scr[warp * kMlaV + 64 * cb + 8 * cc + e] = v;
+                }
             compute_bar<kComputeThreads>();
             if (tid < kMlaV) {
                 float vsum = 0.f;
