@@ -334,8 +334,10 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             // q~[j] = sum_c W_kvb[j, h*256 + c] q_nope[c]: thread tid takes latent
             // rows tid and tid + 256, a swizzled 128-byte box row per stage; the
             // 64 q_nope values of a column block stay in registers
-            float acc_q[2] = {0.f, 0.f};
-#pragma unroll
+            // (the stage loop is not unrolled: this code runs once per block, and
+            // a smaller body costs fewer instruction fetches)
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 1
             for (int cb = 0; cb < 2; ++cb) {
                 float qr[64];
 #pragma unroll
@@ -343,21 +345,23 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                     const float4 v = reinterpret_cast<const float4 *>(qn + 64 * cb)[c];
                     qr[4 * c] = v.x; qr[4 * c + 1] = v.y; qr[4 * c + 2] = v.z; qr[4 * c + 3] = v.w;
                 }
-#pragma unroll
+#pragma unroll 1
                 for (int rb = 0; rb < 2; ++rb) {
                     const uint8_t *st = stage_ready();
+                    float sum = 0.f;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         float f[8];
                         unpack8_bf16(*reinterpret_cast<const uint4 *>(st + tid * 128 + ((c ^ (tid & 7)) << 4)), f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc_q[rb] = fmaf(f[e], qr[8 * c + e], acc_q[rb]);
+                        for (int e = 0; e < 8; ++e) sum = fmaf(f[e], qr[8 * c + e], sum);
                     }
                     stage_done();
+                    if (rb == 0) acc0 += sum; else acc1 += sum;
                 }
             }
-            dst[tid] = acc_q[0] * p.qscale;
-            dst[tid + kComputeThreads] = acc_q[1] * p.qscale;
+            dst[tid] = acc0 * p.qscale;
+            dst[tid + kComputeThreads] = acc1 * p.qscale;
             if (tid < kMlaRope / 2) {
                 float x0 = bf16_bits(qh[kMlaNope + tid]), x1 = bf16_bits(qh[kMlaNope + tid + kMlaRope / 2]);
                 if (p.rope) mla_rope(x0, x1, L, p.rope_inv_freq[tid]);
@@ -646,22 +650,27 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             for (int cb = 0; cb < 2; ++cb)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) part[cb][e] = 0.f;
+#pragma unroll 1
+            for (int sq = 0; sq < 4; ++sq) {  // stage (row block, column block) = (sq / 2, sq % 2)
+                const int rb = sq >> 1;
+                const uint8_t *st = stage_ready();
+                float pk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int rb = 0; rb < 2; ++rb)
+                for (int k = 0; k < kMlaWeightRows / 32; ++k) {
+                    const int row = rg + 32 * k;
+                    const float oj = ofin[ii * kMlaKv + kMlaWeightRows * rb + row];
+                    float f[8];
+                    unpack8_bf16(*reinterpret_cast<const uint4 *>(st + row * 128 + ((cc ^ (row & 7)) << 4)), f);
 #pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    const uint8_t *st = stage_ready();
-#pragma unroll
-                    for (int k = 0; k < kMlaWeightRows / 32; ++k) {
-                        const int row = rg + 32 * k;
-                        const float oj = ofin[ii * kMlaKv + kMlaWeightRows * rb + row];
-                        float f[8];
-                        unpack8_bf16(*reinterpret_cast<const uint4 *>(st + row * 128 + ((cc ^ (row & 7)) << 4)), f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) part[cb][e] = fmaf(oj, f[e], part[cb][e]);
-                    }
-                    stage_done();
+                    for (int e = 0; e < 8; ++e) pk[e] = fmaf(oj, f[e], pk[e]);
                 }
+                stage_done();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (sq & 1) part[1][e] += pk[e];
+                    else part[0][e] += pk[e];
+                }
+            }
             // sum over the 32 row groups: 4 in a warp by shuffles, 8 warps in smem
 #pragma unroll
             for (int cb = 0; cb < 2; ++cb)
