@@ -323,13 +323,19 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
         cur.advance(NS);
     };
     {
-        float *qn = scr;  // [128] q_nope of the head being absorbed
+        // q_nope of this block's heads, [HPB][128], where the combined outputs
+        // go in phase C
+        float *qn_all = ofin;
+        for (int k = tid; k < HPB * kMlaNope; k += kComputeThreads) {
+            const int h = g * HG + r * HPB + k / kMlaNope;
+            qn_all[k] = bf16_bits(p.q[static_cast<size_t>(b) * p.nh * kMlaQk + h * kMlaQk + k % kMlaNope]);
+        }
+        compute_bar<kComputeThreads>();
         for (int i = 0; i < HPB; ++i) {
             const int hl = r * HPB + i;             // head within the group
             const int h = g * HG + hl;
             const uint16_t *qh = p.q + static_cast<size_t>(b) * p.nh * kMlaQk + h * kMlaQk;
-            if (tid < kMlaNope) qn[tid] = bf16_bits(qh[tid]);
-            compute_bar<kComputeThreads>();
+            const float *qn = qn_all + i * kMlaNope;
             float *dst = qt + hl * kMlaRow;
             // q~[j] = sum_c W_kvb[j, h*256 + c] q_nope[c]: thread tid takes latent
             // rows tid and tid + 256, a swizzled 128-byte box row per stage; the
@@ -553,9 +559,6 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     }
     if (n_tiles > 0) fold(n_tiles - 1);
     compute_bar<kComputeThreads>();
-    // The next kernel (the output projection) may start streaming its weights
-    // now: launched earlier, it would compete for HBM with this kernel's loads.
-    grid_dependents_launch();
     // The new row, attended on CUDA cores: its score per head, the state
     // update, and its value folded into the partial output.
     if (has_new) {
@@ -625,7 +628,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             float Lsum = e * lq;
 #pragma unroll
             for (int off = kMlaMaxHG / 2; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-            if (i < HPB) wgt[i * kMlaMaxHG + q] = e / Lsum;
+            if (i < HPB) wgt[i * kMlaMaxHG + q] = e / Lsum;  // 0 for q >= C
         }
         compute_bar<kComputeThreads>();
         for (int idx = tid; idx < HPB * kMlaKv; idx += kComputeThreads) {
@@ -633,8 +636,9 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             const float *rv = recv + i * C * (kMlaKv + 4) + d;
             const float *w = wgt + i * kMlaMaxHG;
             float o = 0.f;
-#pragma unroll 4
-            for (int q = 0; q < C; ++q) o = fmaf(w[q], rv[q * (kMlaKv + 4)], o);
+#pragma unroll
+            for (int q = 0; q < kMlaMaxHG; ++q)  // blocks past C have weight 0
+                o = fmaf(w[q], rv[min(q, C - 1) * (kMlaKv + 4)], o);
             ofin[idx] = o;
         }
         compute_bar<kComputeThreads>();
@@ -696,6 +700,9 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
         tcgen05_fence_after();
         tmem_dealloc(tmem, 256);
     }
+    // The next kernel (the output projection) may start streaming its weights
+    // now: launched earlier, its loads would compete with this kernel's.
+    grid_dependents_launch();
     cluster_sync_all();  // no block leaves while a peer may still push into it
 }
 
