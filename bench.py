@@ -123,14 +123,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The sources the fused decode kernel and its host launch are built from.
+FUSED_SOURCES = ("cfa_api.cu", "cfa_device.cuh", "cfa_internal.h", "cfa_kernel.cuh",
+                 "cfa_kernels_d128.cu", "cfa_kernels_d64.cu", "cfa_tile.cuh")
+
+
 def kernel_source_digest() -> str:
-    """Digest of the CUDA sources; ncu traffic figures are tied to it."""
+    """Digest of the fused kernel's CUDA sources; ncu traffic figures are tied to it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "out_proj_block_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in FUSED_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 

@@ -46,6 +46,7 @@
 
 #include "cfa_device.cuh"
 #include "cfa_internal.h"
+#include "cfa_layer_params.h"
 #include "cfa_tile.cuh"
 
 namespace cfa {

@@ -21,6 +21,7 @@
 #include "cfa.h"
 #include "cfa_host.h"
 #include "cfa_internal.h"
+#include "cfa_layer_params.h"
 
 using cfa::GemvParams;
 
