@@ -295,6 +295,16 @@ cfa_status cfa_mlp_step(cfa_mlp *mlp, const void *h, const void *norm_w, float e
  */
 cfa_status cfa_mlp_set_pipeline(cfa_mlp *mlp, int blocks_per_sm, int stages);
 
+/*
+ * Choose the kernel of the MLP's two GEMVs: path -1 = by batch size (the
+ * tcgen05 tensor-core kernel from B = 3 on, the CUDA-core kernel below), 0 =
+ * CUDA cores, 1 = tensor cores. The result is the same to within fp32
+ * summation order. Keeps the pipeline overrides of cfa_mlp_set_pipeline.
+ * CFA_ERR_INVALID_ARG for another path; CFA_ERR_UNSUPPORTED if the shape does
+ * not fit the kernel (the plan is then unchanged).
+ */
+cfa_status cfa_mlp_set_path(cfa_mlp *mlp, int path);
+
 /* Synchronizes, reads and clears the plan's device status word (as cfa_plan_status). */
 cfa_status cfa_mlp_status(cfa_mlp *mlp);
 

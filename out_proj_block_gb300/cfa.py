@@ -69,6 +69,8 @@ _lib.cfa_mlp_step.restype = _i
 _lib.cfa_mlp_step.argtypes = [_vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
 _lib.cfa_mlp_set_pipeline.restype = _i
 _lib.cfa_mlp_set_pipeline.argtypes = [_vp, _i, _i]
+_lib.cfa_mlp_set_path.restype = _i
+_lib.cfa_mlp_set_path.argtypes = [_vp, _i]
 _lib.cfa_mlp_status.restype = _i
 _lib.cfa_mlp_status.argtypes = [_vp]
 _lib.cfa_mlp_describe.restype = _i
@@ -116,7 +118,7 @@ EXPORTED_SYMBOLS = (
     "cfa_plan_describe", "cfa_plan_status", "cfa_last_error", "cfa_status_string",
     "cfa_selftest_wait_timeout",
     "cfa_rmsnorm", "cfa_mlp_create", "cfa_mlp_destroy", "cfa_mlp_step", "cfa_mlp_status",
-    "cfa_mlp_set_pipeline",
+    "cfa_mlp_set_pipeline", "cfa_mlp_set_path",
     "cfa_mlp_describe", "cfa_stack_create", "cfa_stack_destroy", "cfa_stack_set_layer",
     "cfa_stack_step", "cfa_stack_step_graph", "cfa_stack_status", "cfa_stack_describe",
     "cfa_mla_create", "cfa_mla_destroy", "cfa_mla_step", "cfa_mla_status", "cfa_mla_describe",
@@ -370,6 +372,14 @@ def cfa_mlp_set_pipeline(mlp, blocks_per_sm: int, stages: int) -> int:
     return int(_lib.cfa_mlp_set_pipeline(mlp, int(blocks_per_sm), int(stages)))
 
 
+# cfa_mlp_set_path: the MLP GEMVs' kernel
+PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES = -1, 0, 1
+
+
+def cfa_mlp_set_path(mlp, path: int) -> int:
+    return int(_lib.cfa_mlp_set_path(mlp, int(path)))
+
+
 def cfa_mlp_status(mlp) -> int:
     return int(_lib.cfa_mlp_status(mlp))
 
@@ -474,6 +484,12 @@ class Mlp:
         st = cfa_mlp_set_pipeline(self.handle, blocks_per_sm, stages)
         if st != CFA_OK:
             raise CfaError(st, f"pipeline {blocks_per_sm} x {stages}")
+
+    def set_path(self, path: int) -> None:
+        """PATH_AUTO (tensor cores from B = 3), PATH_CUDA_CORES or PATH_TENSOR_CORES."""
+        st = cfa_mlp_set_path(self.handle, path)
+        if st != CFA_OK:
+            raise CfaError(st, f"path {path}")
 
     def status(self) -> int:
         return cfa_mlp_status(self.handle)

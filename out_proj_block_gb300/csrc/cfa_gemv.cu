@@ -1,5 +1,6 @@
 // Instantiations of the decoder-layer kernels around the attention block.
 #include "cfa_gemv.cuh"
+#include "cfa_gemv_mma.cuh"
 
 namespace cfa {
 
@@ -19,6 +20,16 @@ const void *gemv_kernel(int mode, int maxb) {
     if (mode == kGemvNormPlain) { CFA_GEMV_CASES(kGemvNormPlain) }
 #undef CFA_GEMV_CASES
     return nullptr;
+}
+
+const void *gemv_mma_kernel_ptr(int mode) {
+    switch (mode) {
+        case kGemvSwiGLU: return reinterpret_cast<const void *>(&gemv_mma_kernel<kGemvSwiGLU>);
+        case kGemvResidual: return reinterpret_cast<const void *>(&gemv_mma_kernel<kGemvResidual>);
+        case kGemvPlain: return reinterpret_cast<const void *>(&gemv_mma_kernel<kGemvPlain>);
+        case kGemvNormPlain: return reinterpret_cast<const void *>(&gemv_mma_kernel<kGemvNormPlain>);
+        default: return nullptr;
+    }
 }
 
 const void *rmsnorm_kernel_ptr() { return reinterpret_cast<const void *>(&rmsnorm_kernel); }

@@ -109,6 +109,94 @@ __device__ __forceinline__ void gemv_reduce_halves(float (&acc)[MAXB][GemvShape<
     compute_bar<kComputeThreads>();
 }
 
+// The blocks that own units of tile t: [i_first, i_first + n_t).
+__device__ __forceinline__ void gemv_tile_owners(const GemvParams &p, int t, int &i_first, int &n_t) {
+    const long long U = p.units, P = p.nblocks;
+    i_first = unit_owner(static_cast<long long>(t) * p.chunks, U, P);
+    n_t = unit_owner(static_cast<long long>(t + 1) * p.chunks - 1, U, P) - i_first + 1;
+}
+
+// Floats per batch row of a tile partial: one or two matrices of 128 columns.
+template <int MODE>
+constexpr int gemv_nw() { return (MODE == kGemvSwiGLU ? 2 : 1) * kGemvTileCols; }
+
+// This block's workspace slot for the partial of its k-th tile.
+template <int MODE>
+__device__ __forceinline__ float4 *gemv_slot(const GemvParams &p, int k) {
+    return reinterpret_cast<float4 *>(
+        p.partials + (static_cast<size_t>(blockIdx.x) * p.max_tiles + k) * p.B * gemv_nw<MODE>());
+}
+
+// Output columns [t*128, t*128 + 128) of tile t, as quads (b, c..c+3).
+// A tile shared by n_t blocks is the sum of their fp32 partials in one
+// fixed order, whichever warps compute it: sub_s = p_s + p_{s+4} + ... for
+// s < 4 (ascending), total = (sub_0 + sub_1) + (sub_2 + sub_3), the four
+// subs held by four adjacent lanes. This block's own partial is read from
+// its tile buffer `tl`; a tile owned by one block is just that buffer.
+// nthr threads (a multiple of 32) take the work items idx = (quad, s).
+template <int MODE>
+__device__ __forceinline__ void gemv_finish_quads(const GemvParams &p, int t, int i_first, int n_t,
+                                                  const float *tl, int ti, int nthr) {
+    constexpr bool DUAL = MODE == kGemvSwiGLU;
+    constexpr int NW = gemv_nw<MODE>();
+    constexpr int V = 4;
+    const int B = p.B;
+    const long long U = p.units, P = p.nblocks;
+    for (int idx = ti; idx < B * kGemvTileCols; idx += nthr) {
+        const int sub = idx & 3, o = idx >> 2;
+        const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
+        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll 2
+        for (int j = sub; j < n_t; j += 4) {
+            const int i = i_first + j;
+            float4 v0, v1;
+            if (i == static_cast<int>(blockIdx.x)) {
+                v0 = *reinterpret_cast<const float4 *>(tl + b * NW + c);
+                if constexpr (DUAL) v1 = *reinterpret_cast<const float4 *>(tl + b * NW + kGemvTileCols + c);
+            } else {
+                const int lt = t - unit_begin(i, U, P) / p.chunks;
+                const float *src =
+                    p.partials + ((static_cast<size_t>(i) * p.max_tiles + lt) * B + b) * NW + c;
+                v0 = __ldcg(reinterpret_cast<const float4 *>(src));
+                if constexpr (DUAL) v1 = __ldcg(reinterpret_cast<const float4 *>(src + kGemvTileCols));
+            }
+            a0.x += v0.x; a0.y += v0.y; a0.z += v0.z; a0.w += v0.w;
+            if constexpr (DUAL) { a1.x += v1.x; a1.y += v1.y; a1.z += v1.z; a1.w += v1.w; }
+        }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+            a0.x += __shfl_xor_sync(0xffffffffu, a0.x, off);
+            a0.y += __shfl_xor_sync(0xffffffffu, a0.y, off);
+            a0.z += __shfl_xor_sync(0xffffffffu, a0.z, off);
+            a0.w += __shfl_xor_sync(0xffffffffu, a0.w, off);
+            if constexpr (DUAL) {
+                a1.x += __shfl_xor_sync(0xffffffffu, a1.x, off);
+                a1.y += __shfl_xor_sync(0xffffffffu, a1.y, off);
+                a1.z += __shfl_xor_sync(0xffffffffu, a1.z, off);
+                a1.w += __shfl_xor_sync(0xffffffffu, a1.w, off);
+            }
+        }
+        if (sub != 0 || t * kGemvTileCols + c >= p.N) continue;  // masked columns of a last half tile
+        float v[V] = {a0.x, a0.y, a0.z, a0.w};
+        const size_t o2 = static_cast<size_t>(b) * p.N + static_cast<size_t>(t) * kGemvTileCols + c;
+        if constexpr (DUAL) {
+            const float up[V] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int e = 0; e < V; ++e) v[e] = v[e] / (1.0f + expf(-v[e])) * up[e];  // silu(gate) * up
+        } else if constexpr (MODE == kGemvResidual) {
+            const uint2 rv = __ldcg(reinterpret_cast<const uint2 *>(p.resid + o2));
+            v[0] += bf16_lo(rv.x);
+            v[1] += bf16_hi(rv.x);
+            v[2] += bf16_lo(rv.y);
+            v[3] += bf16_hi(rv.y);
+        }
+        uint2 packed;
+        packed.x = pack2_bf16(v[0], v[1]);
+        packed.y = pack2_bf16(v[2], v[3]);
+        *reinterpret_cast<uint2 *>(p.y + o2) = packed;
+    }
+}
+
 template <int MAXB, int MODE>
 __global__ void __launch_bounds__(kGemvThreads, MAXB >= 16 ? 1 : 2)
 gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
@@ -217,77 +305,11 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
         return;
     }
 
-    // Output columns [t*128, t*128 + 128) of tile t, as quads (b, c..c+3).
-    // A tile shared by n_t blocks is the sum of their fp32 partials in one
-    // fixed order, whichever warps compute it: sub_s = p_s + p_{s+4} + ... for
-    // s < 4 (ascending), total = (sub_0 + sub_1) + (sub_2 + sub_3), the four
-    // subs held by four adjacent lanes. This block's own partial is read from
-    // its tile buffer `tl`; a tile owned by one block is just that buffer.
-    // nthr threads (a multiple of 32) take the work items idx = (quad, s).
     auto finish_quads = [&](int t, int i_first, int n_t, const float *tl, int ti, int nthr) {
-        constexpr int V = 4;
-        for (int idx = ti; idx < B * kGemvTileCols; idx += nthr) {
-            const int sub = idx & 3, o = idx >> 2;
-            const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
-            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-#pragma unroll 2
-            for (int j = sub; j < n_t; j += 4) {
-                const int i = i_first + j;
-                float4 v0, v1;
-                if (i == static_cast<int>(blockIdx.x)) {
-                    v0 = *reinterpret_cast<const float4 *>(tl + b * NW + c);
-                    if constexpr (DUAL) v1 = *reinterpret_cast<const float4 *>(tl + b * NW + kGemvTileCols + c);
-                } else {
-                    const int lt = t - unit_begin(i, U, P) / p.chunks;
-                    const float *src =
-                        p.partials + ((static_cast<size_t>(i) * p.max_tiles + lt) * B + b) * NW + c;
-                    v0 = __ldcg(reinterpret_cast<const float4 *>(src));
-                    if constexpr (DUAL) v1 = __ldcg(reinterpret_cast<const float4 *>(src + kGemvTileCols));
-                }
-                a0.x += v0.x; a0.y += v0.y; a0.z += v0.z; a0.w += v0.w;
-                if constexpr (DUAL) { a1.x += v1.x; a1.y += v1.y; a1.z += v1.z; a1.w += v1.w; }
-            }
-#pragma unroll
-            for (int off = 1; off <= 2; off <<= 1) {
-                a0.x += __shfl_xor_sync(0xffffffffu, a0.x, off);
-                a0.y += __shfl_xor_sync(0xffffffffu, a0.y, off);
-                a0.z += __shfl_xor_sync(0xffffffffu, a0.z, off);
-                a0.w += __shfl_xor_sync(0xffffffffu, a0.w, off);
-                if constexpr (DUAL) {
-                    a1.x += __shfl_xor_sync(0xffffffffu, a1.x, off);
-                    a1.y += __shfl_xor_sync(0xffffffffu, a1.y, off);
-                    a1.z += __shfl_xor_sync(0xffffffffu, a1.z, off);
-                    a1.w += __shfl_xor_sync(0xffffffffu, a1.w, off);
-                }
-            }
-            if (sub != 0 || t * kGemvTileCols + c >= p.N) continue;  // masked columns of a last half tile
-            float v[V] = {a0.x, a0.y, a0.z, a0.w};
-            const size_t o2 = static_cast<size_t>(b) * p.N + static_cast<size_t>(t) * kGemvTileCols + c;
-            if constexpr (DUAL) {
-                const float up[V] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-                for (int e = 0; e < V; ++e) v[e] = v[e] / (1.0f + expf(-v[e])) * up[e];  // silu(gate) * up
-            } else if constexpr (MODE == kGemvResidual) {
-                const uint2 rv = __ldcg(reinterpret_cast<const uint2 *>(p.resid + o2));
-                v[0] += bf16_lo(rv.x);
-                v[1] += bf16_hi(rv.x);
-                v[2] += bf16_lo(rv.y);
-                v[3] += bf16_hi(rv.y);
-            }
-            uint2 packed;
-            packed.x = pack2_bf16(v[0], v[1]);
-            packed.y = pack2_bf16(v[2], v[3]);
-            *reinterpret_cast<uint2 *>(p.y + o2) = packed;
-        }
+        gemv_finish_quads<MODE>(p, t, i_first, n_t, tl, ti, nthr);
     };
-    auto tile_owners = [&](int t, int &i_first, int &n_t) {
-        i_first = unit_owner(static_cast<long long>(t) * p.chunks, U, P);
-        n_t = unit_owner(static_cast<long long>(t + 1) * p.chunks - 1, U, P) - i_first + 1;
-    };
-    auto slot_of = [&](int k) {
-        return reinterpret_cast<float4 *>(
-            p.partials + (static_cast<size_t>(blockIdx.x) * p.max_tiles + k) * B * NW);
-    };
+    auto tile_owners = [&](int t, int &i_first, int &n_t) { gemv_tile_owners(p, t, i_first, n_t); };
+    auto slot_of = [&](int k) { return gemv_slot<MODE>(p, k); };
 
     float *tiles = reinterpret_cast<float *>(smem + p.off_tile);  // [2][B][NW]
     if (warp == kComputeWarps + 1) {

@@ -11,6 +11,7 @@ namespace cfa {
 
 // Kernel entry points (cfa_gemv.cu).
 const void *gemv_kernel(int mode, int maxb);
+const void *gemv_mma_kernel_ptr(int mode);
 const void *rmsnorm_kernel_ptr();
 const void *advance_kernel_ptr();
 const void *mla_kernel_ptr(int heads_per_cluster);  // cfa_mla.cu

@@ -40,11 +40,21 @@ struct GemvParams {
     int nblocks;             // grid size
     int max_tiles;           // tiles one block can touch
     int nstages;
-    int xstage_bytes;        // bytes of one x (+ norm weight) stage
+    int xstage_bytes;        // bytes of one x (+ norm weight) stage; on the tensor-core
+                             // path, of one whole stage (weights, input box, norm weights)
     int off_xring, off_xn, off_scratch, off_tile, off_misc, off_bars;
     float eps;
     unsigned long long timeout_ns;
 };
+
+// The tensor-core GEMV: units of 64 weight rows, read as [64 x 64] swizzled
+// boxes; the batch's input rows as one [16 x 64] box; 4 warps read TMEM, then
+// one MMA warp, one TMA warp and one epilogue warp.
+constexpr int kGemvMmaRows = 64;
+constexpr int kGemvMmaBoxBytes = kGemvMmaRows * 128;
+constexpr int kGemvMmaXBytes = kMmaN * 128;
+constexpr int kGemvMmaReaders = 4;
+constexpr int kGemvMmaThreads = (kGemvMmaReaders + 3) * 32;
 
 // ---------------------------------------------------- multi-head latent attention
 

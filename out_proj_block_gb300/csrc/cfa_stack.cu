@@ -100,24 +100,40 @@ struct GemvPlan {
     GemvParams gp{};
     const void *kernel = nullptr;
     int smem = 0;
+    int threads = 0;
+    bool mma = false;             // the tensor-core kernel
     size_t partial_floats = 0;
 };
+
+// Which kernel runs a GEMV of batch B: kGemvPathAuto takes the tensor cores
+// from B = 3 on, where the CUDA cores would spend more time on the 2B flops
+// per weight byte than HBM needs to deliver the byte.
+constexpr int kGemvPathAuto = -1, kGemvPathCudaCores = 0, kGemvPathTensorCores = 1;
+
+bool gemv_uses_mma(int path, int B) {
+    if (path == kGemvPathCudaCores) return false;
+    return path == kGemvPathTensorCores || B >= 3;
+}
 
 // Shared-memory layout, pipeline depth and grid of one stream-K GEMV.
 // bps_req / ns_req > 0 ask for that many blocks per SM / stages.
 cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan *out,
-                     int bps_req = 0, int ns_req = 0) {
+                     int bps_req = 0, int ns_req = 0, int path = kGemvPathAuto) {
     const bool dual = mode == cfa::kGemvSwiGLU;
     const bool norm = dual || mode == cfa::kGemvNormPlain;
+    const bool mma = gemv_uses_mma(path, B);
     const int TW = cfa::kGemvTileCols;
-    const int R = dual ? 32 : 64;  // 16 KB of weights per unit either way
+    // 16 KB of weights per unit on the CUDA cores; 64 rows of each matrix on
+    // the tensor cores (16 or 32 KB)
+    const int R = mma ? cfa::kGemvMmaRows : (dual ? 32 : 64);
     // N a multiple of 64: a last tile of 64 columns reads zeros past N and
     // stores nothing there.
-    if (K < R || K % R || N < 64 || N % 64) return CFA_ERR_UNSUPPORTED;
+    if (K < R || K % R || N < 64 || N % 64 || B > cfa::kMaxBatch) return CFA_ERR_UNSUPPORTED;
     int maxb = 1;
     while (maxb < B) maxb <<= 1;
-    const void *kernel = cfa::gemv_kernel(mode, maxb);
+    const void *kernel = mma ? cfa::gemv_mma_kernel_ptr(mode) : cfa::gemv_kernel(mode, maxb);
     if (!kernel) return CFA_ERR_UNSUPPORTED;
+    const int threads = mma ? cfa::kGemvMmaThreads : cfa::kGemvThreads;
     const int NW = (dual ? 2 : 1) * TW;
 
     GemvParams p{};
@@ -129,20 +145,31 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     p.n_tiles = (N + TW - 1) / TW;
     p.x_stride = K;
     p.units = p.n_tiles * p.chunks;
-    p.xstage_bytes = align_up(B * R * 2 + (norm ? R * 2 : 0), 128);
-    // per-warp normalized input rows: 8 warps x [B][R/4] floats
-    const int xn = norm ? align_up(cfa::kComputeWarps * B * (R / 4) * 4, 128) : 0;
-    const int scratch = align_up(cfa::kComputeWarps * B * cfa::kTileCols * 4, 128);
+    int fixed = 0, per_stage = 0, xn = 0, scratch = 0;
     const int tile = align_up(2 * B * NW * 4, 128);  // two tile buffers
     const int misc = 128;
-    const int fixed = xn + scratch + tile + misc + 1024;  // + barriers, flags, slack
-    const int per_stage = cfa::kStageBytes + p.xstage_bytes + 16;
-    // Two blocks per SM with at least 4 stages each, else one deeper block.
+    if (mma) {
+        // stage: weight boxes, the [16 x 64] input box, the norm weights
+        p.xstage_bytes = align_up((dual ? 2 : 1) * 2 * cfa::kGemvMmaBoxBytes + cfa::kGemvMmaXBytes +
+                                      (norm ? R * 2 : 0), 1024);
+        scratch = norm ? align_up(cfa::kGemvMmaReaders * cfa::kMaxBatch * 4, 128) : 0;
+        per_stage = p.xstage_bytes + 24;
+        fixed = scratch + tile + misc + 96 + 1024;
+    } else {
+        p.xstage_bytes = align_up(B * R * 2 + (norm ? R * 2 : 0), 128);
+        // per-warp normalized input rows: 8 warps x [B][R/4] floats
+        xn = norm ? align_up(cfa::kComputeWarps * B * (R / 4) * 4, 128) : 0;
+        scratch = align_up(cfa::kComputeWarps * B * cfa::kTileCols * 4, 128);
+        per_stage = cfa::kStageBytes + p.xstage_bytes + 16;
+        fixed = xn + scratch + tile + misc + 1024;  // + barriers, flags, slack
+    }
+    // Two blocks per SM with at least 4 stages each (3 on the tensor cores),
+    // else one deeper block.
     int bps = 2, NS = 0;
     for (; bps >= 1; --bps) {
         const int budget = std::min(dev.smem_optin, dev.smem_per_sm / bps - dev.smem_reserved);
         NS = std::min(kMaxGemvStages, (budget - fixed) / per_stage);
-        if (NS >= (bps == 2 ? 4 : 2)) break;
+        if (NS >= (bps == 2 ? (mma ? 3 : 4) : 2)) break;
     }
     if (bps_req > 0) {
         bps = bps_req;
@@ -154,11 +181,18 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
         NS = ns_req;
     }
     if (bps < 1 || NS < 2) return CFA_ERR_UNSUPPORTED;
-    int off = NS * cfa::kStageBytes;
-    p.off_xring = off;
-    off += NS * p.xstage_bytes;
-    p.off_xn = off;
-    off += xn;
+    int off = 0;
+    if (mma) {
+        off = NS * p.xstage_bytes;  // the ring: whole stages
+        p.off_xring = 0;
+        p.off_xn = off;
+    } else {
+        off = NS * cfa::kStageBytes;
+        p.off_xring = off;
+        off += NS * p.xstage_bytes;
+        p.off_xn = off;
+        off += xn;
+    }
     p.off_scratch = off;
     off += scratch;
     p.off_tile = off;
@@ -166,7 +200,8 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     p.off_misc = off;
     off += misc;
     p.off_bars = off;
-    off += 16 * NS + 32 + 16;  // stage barriers, tile barriers, flags
+    // stage barriers, tile barriers, flags (+ the TMEM address)
+    off += mma ? 24 * NS + 96 : 16 * NS + 32 + 16;
     if (off > dev.smem_optin) return CFA_ERR_UNSUPPORTED;
     p.nstages = NS;
     p.timeout_ns = kTimeoutNs;
@@ -178,8 +213,7 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
         return CFA_ERR_CUDA;
     }
     int resident = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, cfa::kGemvThreads, off) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, threads, off) != cudaSuccess ||
         resident < 1) {
         cudaGetLastError();
         return CFA_ERR_UNSUPPORTED;
@@ -191,8 +225,24 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     out->gp = p;
     out->kernel = kernel;
     out->smem = off;
+    out->threads = threads;
+    out->mma = mma;
     out->partial_floats = static_cast<size_t>(p.nblocks) * p.max_tiles * B * NW;
     return CFA_OK;
+}
+
+// Tensor map of a GEMV weight W [K rows][N cols] for plan g: [rows x 128]
+// boxes on the CUDA cores, [64 x 64] 128-byte-swizzled boxes on the tensor cores.
+cfa_status gemv_map_w(const GemvPlan &g, CUtensorMap *tm, const void *W, int N, int K) {
+    return g.mma ? cfa::encode_bf16_2d_ex(tm, W, N, K, N, 64, cfa::kGemvMmaRows, true)
+                 : cfa::encode_bf16_2d(tm, W, N, K, cfa::kGemvTileCols, g.gp.rows);
+}
+
+// Tensor map of a GEMV's input rows x [B][stride] (first K of each) for plan
+// g: [B x rows] boxes, or [16 x 64] swizzled boxes (rows past B read as zero).
+cfa_status gemv_map_x(const GemvPlan &g, CUtensorMap *tm, const void *x, int K, int B, int stride) {
+    return g.mma ? cfa::encode_bf16_2d_ex(tm, x, K, B, stride, 64, cfa::kMmaN, true)
+                 : cfa::encode_bf16_2d_ex(tm, x, K, B, stride, g.gp.rows, B, false);
 }
 
 cfa_status launch_gemv(const GemvPlan &g, const GemvParams &p, const CUtensorMap *w0,
@@ -200,7 +250,7 @@ cfa_status launch_gemv(const GemvPlan &g, const GemvParams &p, const CUtensorMap
     CUtensorMap m0 = *w0, m1 = *w1, mx = *x;
     GemvParams pp = p;
     void *args[4] = {&m0, &m1, &mx, &pp};
-    return launch_pdl(g.kernel, dim3(p.nblocks), dim3(cfa::kGemvThreads), static_cast<size_t>(g.smem),
+    return launch_pdl(g.kernel, dim3(p.nblocks), dim3(g.threads), static_cast<size_t>(g.smem),
                       stream, args);
 }
 
@@ -212,6 +262,8 @@ struct cfa_mlp {
     int B = 0, H = 0, F = 0;
     Device dev;
     GemvPlan gu, dn;              // gate/up (+ norm, SwiGLU) and down (+ residual)
+    int bps_req = 0, ns_req = 0;  // pipeline overrides (0: automatic)
+    int path = -1;                // kGemvPath*: CUDA cores, tensor cores or by batch
     uint16_t *u = nullptr;        // [B][F] SwiGLU output
     float *partials = nullptr;    // gate/up partials, then down partials
     size_t partial_cap = 0;       // floats allocated
@@ -231,16 +283,15 @@ unsigned *mlp_status_word(cfa_mlp *m) {
 cfa_status mlp_encode_weights(const cfa_mlp *m, const void *W_gate, const void *W_up,
                               const void *W_down, CUtensorMap *wg, CUtensorMap *wu,
                               CUtensorMap *wd) {
-    const uint32_t tw = cfa::kGemvTileCols;
-    if (cfa::encode_bf16_2d(wg, W_gate, m->F, m->H, tw, m->gu.gp.rows) != CFA_OK ||
-        cfa::encode_bf16_2d(wu, W_up, m->F, m->H, tw, m->gu.gp.rows) != CFA_OK ||
-        cfa::encode_bf16_2d(wd, W_down, m->H, m->F, tw, m->dn.gp.rows) != CFA_OK)
+    if (gemv_map_w(m->gu, wg, W_gate, m->F, m->H) != CFA_OK ||
+        gemv_map_w(m->gu, wu, W_up, m->F, m->H) != CFA_OK ||
+        gemv_map_w(m->dn, wd, W_down, m->H, m->F) != CFA_OK)
         return CFA_ERR_CUDA;
     return CFA_OK;
 }
 
 cfa_status mlp_encode_input(const cfa_mlp *m, const void *h, CUtensorMap *tm) {
-    return cfa::encode_bf16_2d(tm, h, m->H, m->B, m->gu.gp.rows, m->B);
+    return gemv_map_x(m->gu, tm, h, m->H, m->B, m->H);
 }
 
 // y = h + down(silu(gate(hn)) * up(hn)), hn = bf16(rmsnorm(h; norm_w)).
@@ -275,6 +326,37 @@ void mlp_free(cfa_mlp *m) {
     m->u = nullptr;
     m->partials = nullptr;
     m->words = nullptr;
+}
+
+// Rebuilds the MLP's two GEMV plans (the plan is unchanged on failure); the
+// tensor maps depend on the kernel, so the cached ones are dropped.
+cfa_status mlp_replan(cfa_mlp *m, int bps, int ns, int path) {
+    GemvPlan gu, dn;
+    cfa_status st = make_gemv(m->dev, cfa::kGemvSwiGLU, m->B, m->H, m->F, &gu, bps, ns, path);
+    if (st == CFA_OK) st = make_gemv(m->dev, cfa::kGemvResidual, m->B, m->F, m->H, &dn, bps, ns, path);
+    if (st != CFA_OK) return st;
+    CUtensorMap tm_u;
+    if (gemv_map_x(dn, &tm_u, m->u, m->F, m->B, m->F) != CFA_OK) return CFA_ERR_CUDA;
+    const size_t need = gu.partial_floats + dn.partial_floats;
+    if (need > m->partial_cap) {
+        float *p = nullptr;
+        if (cudaDeviceSynchronize() != cudaSuccess || cudaMalloc(&p, sizeof(float) * need) != cudaSuccess) {
+            cudaGetLastError();
+            return CFA_ERR_CUDA;
+        }
+        cudaFree(m->partials);
+        m->partials = p;
+        m->partial_cap = need;
+    }
+    // the counters keep their size: the tile counts do not depend on the kernel
+    m->gu = gu;
+    m->dn = dn;
+    m->tm_u = tm_u;
+    m->bps_req = bps;
+    m->ns_req = ns;
+    m->path = path;
+    m->src_wg = m->src_wu = m->src_wd = m->src_h = nullptr;
+    return CFA_OK;
 }
 
 // Reads and clears a device status word (synchronizes the device).
@@ -349,7 +431,7 @@ cfa_mlp *cfa_mlp_create(int B, int hidden, int ffn) {
         fail(CFA_ERR_CUDA);
         return nullptr;
     }
-    if (cfa::encode_bf16_2d(&m->tm_u, m->u, ffn, B, m->dn.gp.rows, B) != CFA_OK) {
+    if (gemv_map_x(m->dn, &m->tm_u, m->u, ffn, B, ffn) != CFA_OK) {
         mlp_free(m);
         delete m;
         fail(CFA_ERR_CUDA);
@@ -400,26 +482,14 @@ cfa_status cfa_mlp_step(cfa_mlp *m, const void *h, const void *norm_w, float eps
 cfa_status cfa_mlp_set_pipeline(cfa_mlp *m, int blocks_per_sm, int stages) {
     if (!m || blocks_per_sm < 0 || blocks_per_sm > 4 || stages < 0 || stages > kMaxGemvStages)
         return fail(CFA_ERR_INVALID_ARG);
-    GemvPlan gu, dn;
-    cfa_status st = make_gemv(m->dev, cfa::kGemvSwiGLU, m->B, m->H, m->F, &gu, blocks_per_sm, stages);
-    if (st == CFA_OK)
-        st = make_gemv(m->dev, cfa::kGemvResidual, m->B, m->F, m->H, &dn, blocks_per_sm, stages);
-    if (st != CFA_OK) return fail(st);  // the plan is unchanged
-    const size_t need = gu.partial_floats + dn.partial_floats;
-    if (need > m->partial_cap) {
-        float *p = nullptr;
-        if (cudaDeviceSynchronize() != cudaSuccess || cudaMalloc(&p, sizeof(float) * need) != cudaSuccess) {
-            cudaGetLastError();
-            return fail(CFA_ERR_CUDA);
-        }
-        cudaFree(m->partials);
-        m->partials = p;
-        m->partial_cap = need;
-    }
-    // the counters keep their size: the tile counts do not depend on the pipeline
-    m->gu = gu;
-    m->dn = dn;
-    return CFA_OK;
+    const cfa_status st = mlp_replan(m, blocks_per_sm, stages, m->path);
+    return st == CFA_OK ? CFA_OK : fail(st);
+}
+
+cfa_status cfa_mlp_set_path(cfa_mlp *m, int path) {
+    if (!m || path < kGemvPathAuto || path > kGemvPathTensorCores) return fail(CFA_ERR_INVALID_ARG);
+    const cfa_status st = mlp_replan(m, m->bps_req, m->ns_req, path);
+    return st == CFA_OK ? CFA_OK : fail(st);
 }
 
 cfa_status cfa_mlp_status(cfa_mlp *m) {
@@ -432,13 +502,13 @@ cfa_status cfa_mlp_describe(const cfa_mlp *m, char *buf, int len) {
     if (!m || !buf || len < 1) return fail(CFA_ERR_INVALID_ARG);
     const GemvParams &a = m->gu.gp, &d = m->dn.gp;
     std::snprintf(buf, static_cast<size_t>(len),
-                  "{\"B\": %d, \"hidden\": %d, \"ffn\": %d, "
+                  "{\"B\": %d, \"hidden\": %d, \"ffn\": %d, \"tensor_cores\": %s, "
                   "\"gate_up\": {\"grid\": %d, \"units\": %d, \"rows_per_unit\": %d, "
                   "\"stages\": %d, \"smem_bytes\": %d}, "
                   "\"down\": {\"grid\": %d, \"units\": %d, \"rows_per_unit\": %d, "
                   "\"stages\": %d, \"smem_bytes\": %d}}",
-                  m->B, m->H, m->F, a.nblocks, a.units, a.rows, a.nstages, m->gu.smem, d.nblocks,
-                  d.units, d.rows, d.nstages, m->dn.smem);
+                  m->B, m->H, m->F, m->gu.mma ? "true" : "false", a.nblocks, a.units, a.rows, a.nstages,
+                  m->gu.smem, d.nblocks, d.units, d.rows, d.nstages, m->dn.smem);
     return CFA_OK;
 }
 
@@ -919,8 +989,8 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
         fail(CFA_ERR_CUDA);
         return nullptr;
     }
-    if (cfa::encode_bf16_2d_ex(&m->tm_aq, m->a, q_lora, B, NA, 64, B, false) != CFA_OK ||
-        cfa::encode_bf16_2d(&m->tm_v, m->v, NV, B, 64, B) != CFA_OK) {
+    if (gemv_map_x(m->gq, &m->tm_aq, m->a, q_lora, B, NA) != CFA_OK ||
+        gemv_map_x(m->go, &m->tm_v, m->v, NV, B, NV) != CFA_OK) {
         mla_free(m);
         delete m;
         fail(CFA_ERR_CUDA);
@@ -961,10 +1031,10 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
     cfa::MlaMaps maps;
     std::memset(&maps, 0, sizeof maps);
     bool enc_ok =
-        cfa::encode_bf16_2d(&tm_x, x, m->H, m->B, 64, m->B) == CFA_OK &&
-        cfa::encode_bf16_2d(&tm_wa, W_a, NA, m->H, cfa::kGemvTileCols, 64) == CFA_OK &&
-        cfa::encode_bf16_2d(&tm_wuq, W_uq, NQ, m->q_lora, cfa::kGemvTileCols, 64) == CFA_OK &&
-        cfa::encode_bf16_2d(&tm_wo, W_o, m->H, NV, cfa::kGemvTileCols, 64) == CFA_OK &&
+        gemv_map_x(m->ga, &tm_x, x, m->H, m->B, m->H) == CFA_OK &&
+        gemv_map_w(m->ga, &tm_wa, W_a, NA, m->H) == CFA_OK &&
+        gemv_map_w(m->gq, &tm_wuq, W_uq, NQ, m->q_lora) == CFA_OK &&
+        gemv_map_w(m->go, &tm_wo, W_o, m->H, NV) == CFA_OK &&
         cfa::encode_bf16_2d_ex(&tm_wkvb, W_kvb, static_cast<uint64_t>(m->nh) * 256, cfa::kMlaKv,
                                static_cast<uint64_t>(m->nh) * 256, 64, cfa::kMlaWeightRows, true) == CFA_OK;
     // one map per sequence over its cached rows only: a tile running past

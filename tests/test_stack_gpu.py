@@ -104,11 +104,13 @@ def mlp_inputs(B, H, F, seed, h_scale=2.0 ** -6):
     return h, layer["mlp_norm"], layer["W_gate"], layer["W_up"], layer["W_down"]
 
 
-def run_mlp(cfa, oracle, B, H, F, seed):
+def run_mlp(cfa, oracle, B, H, F, seed, path=None):
     h, nw, Wg, Wu, Wd = mlp_inputs(B, H, F, seed)
     dev = [t.cuda() for t in (h, nw, Wg, Wu, Wd)]
     y = torch.empty(B, H, dtype=torch.bfloat16, device="cuda")
     mlp = cfa.Mlp(B, H, F)
+    if path is not None:
+        mlp.set_path(path)
     mlp.step(*dev, y, eps=EPS)
     torch.cuda.synchronize()
     assert mlp.status() == cfa.CFA_OK
@@ -124,6 +126,35 @@ def run_mlp(cfa, oracle, B, H, F, seed):
                                    (8, 1024, 768), (16, 256, 512), (5, 4096, 1024)])
 def test_mlp_matches_oracle(cfa, oracle, B, H, F):
     run_mlp(cfa, oracle, B, H, F, seed=B + H + F)
+
+
+@pytest.mark.parametrize("path", ["cuda_cores", "tensor_cores"])
+@pytest.mark.parametrize("B,H,F", [(1, 512, 1024), (2, 1024, 768), (4, 1024, 768),
+                                   (7, 512, 1536), (16, 2048, 1024)])
+def test_mlp_paths_match_oracle(cfa, oracle, B, H, F, path):
+    """Both GEMV kernels at every batch size, the tensor-core one with the
+    batch padded to 16 rows."""
+    p = cfa.PATH_TENSOR_CORES if path == "tensor_cores" else cfa.PATH_CUDA_CORES
+    mlp, _, _ = run_mlp(cfa, oracle, B, H, F, seed=7 * B + H, path=p)
+    assert mlp.describe()["tensor_cores"] == (path == "tensor_cores")
+
+
+def test_mlp_takes_tensor_cores_from_batch_3(cfa):
+    assert not cfa.Mlp(2, 256, 512).describe()["tensor_cores"]
+    assert cfa.Mlp(3, 256, 512).describe()["tensor_cores"]
+    with pytest.raises(cfa.CfaError):
+        cfa.Mlp(3, 256, 512).set_path(2)
+
+
+def test_mlp_full_llama_shape_b16_tensor_cores(cfa, oracle):
+    """Hidden 4096, ffn 11008 at batch 16 on the tensor cores."""
+    mlp, dev, y = run_mlp(cfa, oracle, 16, 4096, 11008, seed=5)
+    assert mlp.describe()["tensor_cores"]
+    first = y.clone()
+    for _ in range(2):
+        mlp.step(*dev, y, eps=EPS)
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), y.view(torch.int16))
 
 
 def test_mlp_full_llama_shape_b1(cfa, oracle):
