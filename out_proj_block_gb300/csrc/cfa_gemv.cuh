@@ -140,60 +140,76 @@ __device__ __forceinline__ void gemv_finish_quads(const GemvParams &p, int t, in
     constexpr bool DUAL = MODE == kGemvSwiGLU;
     constexpr int NW = gemv_nw<MODE>();
     constexpr int V = 4;
+    constexpr int ITEMS = 4;  // work items per thread with their loads in flight together
     const int B = p.B;
+    const int total = B * kGemvTileCols;  // a multiple of nthr: uniform trip counts
     const long long U = p.units, P = p.nblocks;
-    for (int idx = ti; idx < B * kGemvTileCols; idx += nthr) {
-        const int sub = idx & 3, o = idx >> 2;
-        const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
-        float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    for (int idx0 = ti; idx0 < total; idx0 += ITEMS * nthr) {
+        float4 a0[ITEMS], a1[ITEMS];
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q) {
+            const int idx = idx0 + q * nthr;
+            a0[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            a1[q] = a0[q];
+            if (idx >= total) continue;
+            const int sub = idx & 3, o = idx >> 2;
+            const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
 #pragma unroll 2
-        for (int j = sub; j < n_t; j += 4) {
-            const int i = i_first + j;
-            float4 v0, v1;
-            if (i == static_cast<int>(blockIdx.x)) {
-                v0 = *reinterpret_cast<const float4 *>(tl + b * NW + c);
-                if constexpr (DUAL) v1 = *reinterpret_cast<const float4 *>(tl + b * NW + kGemvTileCols + c);
-            } else {
-                const int lt = t - unit_begin(i, U, P) / p.chunks;
-                const float *src =
-                    p.partials + ((static_cast<size_t>(i) * p.max_tiles + lt) * B + b) * NW + c;
-                v0 = __ldcg(reinterpret_cast<const float4 *>(src));
-                if constexpr (DUAL) v1 = __ldcg(reinterpret_cast<const float4 *>(src + kGemvTileCols));
+            for (int j = sub; j < n_t; j += 4) {
+                const int i = i_first + j;
+                float4 v0, v1;
+                if (i == static_cast<int>(blockIdx.x)) {
+                    v0 = *reinterpret_cast<const float4 *>(tl + b * NW + c);
+                    if constexpr (DUAL) v1 = *reinterpret_cast<const float4 *>(tl + b * NW + kGemvTileCols + c);
+                } else {
+                    const int lt = t - unit_begin(i, U, P) / p.chunks;
+                    const float *src =
+                        p.partials + ((static_cast<size_t>(i) * p.max_tiles + lt) * B + b) * NW + c;
+                    v0 = __ldcg(reinterpret_cast<const float4 *>(src));
+                    if constexpr (DUAL) v1 = __ldcg(reinterpret_cast<const float4 *>(src + kGemvTileCols));
+                }
+                a0[q].x += v0.x; a0[q].y += v0.y; a0[q].z += v0.z; a0[q].w += v0.w;
+                if constexpr (DUAL) { a1[q].x += v1.x; a1[q].y += v1.y; a1[q].z += v1.z; a1[q].w += v1.w; }
             }
-            a0.x += v0.x; a0.y += v0.y; a0.z += v0.z; a0.w += v0.w;
-            if constexpr (DUAL) { a1.x += v1.x; a1.y += v1.y; a1.z += v1.z; a1.w += v1.w; }
         }
 #pragma unroll
-        for (int off = 1; off <= 2; off <<= 1) {
-            a0.x += __shfl_xor_sync(0xffffffffu, a0.x, off);
-            a0.y += __shfl_xor_sync(0xffffffffu, a0.y, off);
-            a0.z += __shfl_xor_sync(0xffffffffu, a0.z, off);
-            a0.w += __shfl_xor_sync(0xffffffffu, a0.w, off);
+        for (int q = 0; q < ITEMS; ++q) {
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                a0[q].x += __shfl_xor_sync(0xffffffffu, a0[q].x, off);
+                a0[q].y += __shfl_xor_sync(0xffffffffu, a0[q].y, off);
+                a0[q].z += __shfl_xor_sync(0xffffffffu, a0[q].z, off);
+                a0[q].w += __shfl_xor_sync(0xffffffffu, a0[q].w, off);
+                if constexpr (DUAL) {
+                    a1[q].x += __shfl_xor_sync(0xffffffffu, a1[q].x, off);
+                    a1[q].y += __shfl_xor_sync(0xffffffffu, a1[q].y, off);
+                    a1[q].z += __shfl_xor_sync(0xffffffffu, a1[q].z, off);
+                    a1[q].w += __shfl_xor_sync(0xffffffffu, a1[q].w, off);
+                }
+            }
+            const int idx = idx0 + q * nthr;
+            const int sub = idx & 3, o = idx >> 2;
+            const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
+            // masked columns of a last half tile
+            if (idx >= total || sub != 0 || t * kGemvTileCols + c >= p.N) continue;
+            float v[V] = {a0[q].x, a0[q].y, a0[q].z, a0[q].w};
+            const size_t o2 = static_cast<size_t>(b) * p.N + static_cast<size_t>(t) * kGemvTileCols + c;
             if constexpr (DUAL) {
-                a1.x += __shfl_xor_sync(0xffffffffu, a1.x, off);
-                a1.y += __shfl_xor_sync(0xffffffffu, a1.y, off);
-                a1.z += __shfl_xor_sync(0xffffffffu, a1.z, off);
-                a1.w += __shfl_xor_sync(0xffffffffu, a1.w, off);
-            }
-        }
-        if (sub != 0 || t * kGemvTileCols + c >= p.N) continue;  // masked columns of a last half tile
-        float v[V] = {a0.x, a0.y, a0.z, a0.w};
-        const size_t o2 = static_cast<size_t>(b) * p.N + static_cast<size_t>(t) * kGemvTileCols + c;
-        if constexpr (DUAL) {
-            const float up[V] = {a1.x, a1.y, a1.z, a1.w};
+                const float up[V] = {a1[q].x, a1[q].y, a1[q].z, a1[q].w};
 #pragma unroll
-            for (int e = 0; e < V; ++e) v[e] = v[e] / (1.0f + expf(-v[e])) * up[e];  // silu(gate) * up
-        } else if constexpr (MODE == kGemvResidual) {
-            const uint2 rv = __ldcg(reinterpret_cast<const uint2 *>(p.resid + o2));
-            v[0] += bf16_lo(rv.x);
-            v[1] += bf16_hi(rv.x);
-            v[2] += bf16_lo(rv.y);
-            v[3] += bf16_hi(rv.y);
+                for (int e = 0; e < V; ++e) v[e] = v[e] / (1.0f + expf(-v[e])) * up[e];  // silu(gate) * up
+            } else if constexpr (MODE == kGemvResidual) {
+                const uint2 rv = __ldcg(reinterpret_cast<const uint2 *>(p.resid + o2));
+                v[0] += bf16_lo(rv.x);
+                v[1] += bf16_hi(rv.x);
+                v[2] += bf16_lo(rv.y);
+                v[3] += bf16_hi(rv.y);
+            }
+            uint2 packed;
+            packed.x = pack2_bf16(v[0], v[1]);
+            packed.y = pack2_bf16(v[2], v[3]);
+            *reinterpret_cast<uint2 *>(p.y + o2) = packed;
         }
-        uint2 packed;
-        packed.x = pack2_bf16(v[0], v[1]);
-        packed.y = pack2_bf16(v[2], v[3]);
-        *reinterpret_cast<uint2 *>(p.y + o2) = packed;
     }
 }
 

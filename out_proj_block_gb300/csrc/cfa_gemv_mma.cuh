@@ -15,10 +15,12 @@
 // (cfa_gemv.cuh); only the inner product moved to the tensor cores.
 //
 // Warps: 0-3 read a finished tile's accumulators out of TMEM (warp w owns
-// TMEM lanes 32w..32w+31 = output columns) and, for the RMSNorm modes, turn
-// each input box into bf16(g x / rms(x)) in place before the MMAs read it;
-// warp 4 issues the MMAs (one thread); warp 5 issues the TMA loads; warp 6
-// finishes tiles (as in the CUDA-core kernel).
+// TMEM lanes 32w..32w+31 = output columns) and finish the tile (its partial to
+// the workspace, and the fixed-order sum and epilogue if this block is the
+// last of the tile's owners). Warp 4 issues the MMAs (one thread), warp 5 the
+// TMA loads; in the RMSNorm modes warp 6 turns each input box into
+// bf16(g x / rms(x)) in place before the MMAs read it. The accumulators are
+// double-buffered, so the MMAs of the next tile run while a tile is finished.
 #pragma once
 
 #include <cuda.h>
@@ -62,12 +64,10 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
     const uint32_t bar_xready0 = bar_full0 + 16u * NS;      // input box normalized (RMSNorm modes)
     const uint32_t bar_acc_full0 = bar_full0 + 24u * NS;    // [2] a tile's accumulators are done
     const uint32_t bar_acc_free0 = bar_acc_full0 + 16u;     // [2] the readers are done with them
-    const uint32_t bar_tile_full0 = bar_acc_full0 + 32u;    // [2] a reduced tile is in smem
-    const uint32_t bar_tile_free0 = bar_acc_full0 + 48u;    // [2] the epilogue warp is done with it
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 24 * NS + 64);
+    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 24 * NS + 32);
     volatile int *timed_out = flags;
     volatile int *is_last = flags + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 24 * NS + 72);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + p.off_bars + 24 * NS + 40);
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -78,8 +78,6 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_acc_full0 + 8u * b, 1);
             mbar_init(bar_acc_free0 + 8u * b, kGemvMmaReaders);
-            mbar_init(bar_tile_full0 + 8u * b, 1);
-            mbar_init(bar_tile_free0 + 8u * b, 1);
         }
         *timed_out = 0;
         *is_last = 0;
@@ -95,7 +93,7 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
     auto tile_end = [&](int u) { return u + 1 == u1 || (u + 1) % p.chunks == 0; };
     auto tile_start = [&](int u) { return u == u0 || u % p.chunks == 0; };
 
-    float *tiles = reinterpret_cast<float *>(smem + p.off_tile);  // [2][B][NW]
+    float *tl = reinterpret_cast<float *>(smem + p.off_tile);  // [B][NW]: the tile being finished
 
     if (warp == kGemvMmaReaders + 1) {
         // ---------------------------------------------------------------- load warp
@@ -181,77 +179,71 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
     }
 
     if (warp == kGemvMmaReaders + 2) {
-        // ------------------------------------------------------------ epilogue warp
-        // Every tile of this block but the last, as in the CUDA-core kernel.
-        grid_dependency_wait();
-        const int t_last = (u1 - 1) / p.chunks;
-        for (int t = first_tile, k = 0; t < t_last; ++t, ++k) {
-            const int tb = k & 1;
-            const float *tl = tiles + tb * B * NW;
-            mbar_wait_bounded<false>(bar_tile_full0 + 8u * tb, (k >> 1) & 1, p.timeout_ns, timed_out,
-                                     p.status, kSiteStageFull);
-            int i_first, n_t;
-            gemv_tile_owners(p, t, i_first, n_t);
-            bool finish = true;
-            if (n_t > 1) {
-                float4 *slot = gemv_slot<MODE>(p, k);
-                const float4 *src = reinterpret_cast<const float4 *>(tl);
-                for (int i = lane; i < B * NW / 4; i += 32) slot[i] = src[i];
-                __syncwarp();
-                unsigned last = 0;
-                if (lane == 0) {
-                    const unsigned prev = atomic_add_acq_rel_gpu(p.counters + t, 1u);
-                    last = prev == static_cast<unsigned>(n_t - 1) ? 1u : 0u;
-                    if (last) p.counters[t] = 0u;  // ready for the next launch
+        // ------------------------------------------------------------- norm warp
+        if constexpr (NORM) {
+            float *inv_rms = reinterpret_cast<float *>(smem + p.off_misc);  // [B]
+            grid_dependency_wait();  // the input rows come from an earlier kernel
+            // 1 / sqrt(mean_k x[b, k]^2 + eps) for every row, in a fixed order
+            for (int b = 0; b < B; ++b) {
+                const uint4 *row = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(b) * p.x_stride);
+                float ss = 0.f;
+#pragma unroll 4
+                for (int i = lane; i < p.K / 8; i += 32) {
+                    float f[8];
+                    unpack8_bf16(__ldcg(row + i), f);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) ss = fmaf(f[c], f[c], ss);
                 }
-                finish = __shfl_sync(0xffffffffu, last, 0) != 0;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (lane == 0) inv_rms[b] = 1.0f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
             }
-            if (finish) gemv_finish_quads<MODE>(p, t, i_first, n_t, tl, lane, 32);
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tile_free0 + 8u * tb);
+            // Each stage's input box -> bf16(g x / rms(x)), in place: 16-byte
+            // chunk c of box row (batch row) b, c = lane % 8, b = lane / 8 + 4 i.
+            RingCursor cur;
+            for (int u = u0; u < u1; ++u) {
+                const int s = cur.stage;
+                mbar_wait_bounded<false>(bar_full0 + 8u * s, cur.phase, p.timeout_ns, timed_out, p.status,
+                                         kSiteStageFull);
+                uint8_t *xb = smem + s * SB + WBYTES;
+                const uint16_t *gw = reinterpret_cast<const uint16_t *>(xb + kGemvMmaXBytes);
+                const int pc = lane & 7;  // physical chunk
+#pragma unroll
+                for (int i = 0; i < kMmaN / 4; ++i) {
+                    const int b = (lane >> 3) + 4 * i;
+                    const int lc = pc ^ (b & 7);  // logical chunk: columns 8 lc .. 8 lc + 7
+                    if (b < B) {
+                        uint4 *q = reinterpret_cast<uint4 *>(xb + b * 128 + pc * 16);
+                        float f[8];
+                        unpack8_bf16(*q, f);
+                        const float inv = inv_rms[b];
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            o[e] = pack2_bf16(bf16_bits(gw[8 * lc + 2 * e]) * f[2 * e] * inv,
+                                              bf16_bits(gw[8 * lc + 2 * e + 1]) * f[2 * e + 1] * inv);
+                        *q = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+                fence_proxy_async_smem();  // the box is read by the tensor cores
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_xready0 + 8u * s);
+                cur.advance(NS);
+            }
         }
         return;
     }
 
     // ------------------------------------------------------------------ readers
-    float *inv_rms = reinterpret_cast<float *>(smem + p.off_misc);  // [B]
-    float *scratch = reinterpret_cast<float *>(smem + p.off_scratch);
     grid_dependency_wait();  // no dependent read or global write before this
-    if constexpr (NORM) {
-        // 1 / sqrt(mean_k x[b, k]^2 + eps) for every row, in a fixed order.
-        for (int b = 0; b < B; ++b) {
-            const uint4 *row = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(b) * p.x_stride);
-            float ss = 0.f;
-#pragma unroll 4
-            for (int i = tid; i < p.K / 8; i += kReaderThreads) {
-                float f[8];
-                unpack8_bf16(__ldcg(row + i), f);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) ss = fmaf(f[c], f[c], ss);
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            if (lane == 0) scratch[warp * kMaxBatch + b] = ss;
-        }
-        compute_bar<kReaderThreads>();
-        if (tid < B) {
-            float ss = 0.f;
-            for (int w = 0; w < kGemvMmaReaders; ++w) ss += scratch[w * kMaxBatch + tid];
-            inv_rms[tid] = 1.0f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
-        }
-        compute_bar<kReaderThreads>();
-    }
-    // Accumulators of the block's k-th tile (tile t) -> tile buffer [B][NW];
-    // the last tile is finished here, the others by the epilogue warp.
-    auto read_tile = [&](int k, int t, bool last_tile) {
+    // The block's k-th tile (tile t): accumulators -> tile buffer [B][NW],
+    // then the partial to the workspace and, by the last owner, the finish.
+    auto finish_tile = [&](int k, int t) {
         const int tb = k & 1;
-        if (k >= 2)
-            mbar_wait_bounded<false>(bar_tile_free0 + 8u * tb, ((k >> 1) - 1) & 1, p.timeout_ns,
-                                     timed_out, p.status, kSiteStageEmpty);
         mbar_wait_bounded<false>(bar_acc_full0 + 8u * tb, (k >> 1) & 1, p.timeout_ns, timed_out, p.status,
                                  kSiteStageFull);
         tcgen05_fence_after();
-        float *tl = tiles + tb * B * NW;
         const int col = 32 * warp + lane;  // this thread's TMEM lane = output column
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
@@ -265,12 +257,9 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_acc_free0 + 8u * tb);
         compute_bar<kReaderThreads>();
-        if (!last_tile) {
-            if (tid == 0) mbar_arrive(bar_tile_full0 + 8u * tb);
-            return;
-        }
         int i_first, n_t;
         gemv_tile_owners(p, t, i_first, n_t);
+        bool finish = true;
         if (n_t > 1) {
             float4 *slot = gemv_slot<MODE>(p, k);
             const float4 *src = reinterpret_cast<const float4 *>(tl);
@@ -283,44 +272,16 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
                 *is_last = last ? 1 : 0;
             }
             compute_bar<kReaderThreads>();
-            if (!*is_last) return;
+            finish = *is_last != 0;
         }
-        gemv_finish_quads<MODE>(p, t, i_first, n_t, tl, tid, kReaderThreads);
+        if (finish) gemv_finish_quads<MODE>(p, t, i_first, n_t, tl, tid, kReaderThreads);
+        compute_bar<kReaderThreads>();  // the tile buffer and the flag are free again
     };
 
-    RingCursor cur;
     int k = 0;
     int t = first_tile;
-    for (int u = u0; u < u1; ++u) {
-        if constexpr (NORM) {
-            // The input box of this stage -> bf16(g x / rms(x)), in place: thread
-            // tid takes 16-byte chunk tid % 8 of box row (batch row) tid / 8.
-            const int s = cur.stage;
-            mbar_wait_bounded<false>(bar_full0 + 8u * s, cur.phase, p.timeout_ns, timed_out, p.status,
-                                     kSiteStageFull);
-            uint8_t *xb = smem + s * SB + WBYTES;
-            const uint16_t *gw = reinterpret_cast<const uint16_t *>(xb + kGemvMmaXBytes);
-            const int b = tid >> 3, pc = tid & 7;   // box row, physical chunk
-            const int lc = pc ^ (b & 7);            // logical chunk: columns 8 lc .. 8 lc + 7
-            if (b < B) {
-                uint4 *q = reinterpret_cast<uint4 *>(xb + b * 128 + pc * 16);
-                float f[8];
-                unpack8_bf16(*q, f);
-                const float inv = inv_rms[b];
-                uint32_t o[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    o[e] = pack2_bf16(bf16_bits(gw[8 * lc + 2 * e]) * f[2 * e] * inv,
-                                      bf16_bits(gw[8 * lc + 2 * e + 1]) * f[2 * e + 1] * inv);
-                *q = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-            fence_proxy_async_smem();  // the box is read by the tensor cores
-            compute_bar<kReaderThreads>();
-            if (tid == 0) mbar_arrive(bar_xready0 + 8u * s);
-            cur.advance(NS);
-        }
-        if (tile_end(u)) read_tile(k++, t++, u + 1 == u1);
-    }
+    for (int u = u0; u < u1; ++u)
+        if (tile_end(u)) finish_tile(k++, t++);
     tcgen05_fence_before();
     compute_bar<kReaderThreads>();
     if (warp == 0) {

@@ -48,8 +48,9 @@ struct GemvParams {
 };
 
 // The tensor-core GEMV: units of 64 weight rows, read as [64 x 64] swizzled
-// boxes; the batch's input rows as one [16 x 64] box; 4 warps read TMEM, then
-// one MMA warp, one TMA warp and one epilogue warp.
+// boxes; the batch's input rows as one [16 x 64] box; 4 warps read TMEM and
+// finish tiles, then one MMA warp, one TMA warp and one warp normalizing the
+// input boxes (RMSNorm modes).
 constexpr int kGemvMmaRows = 64;
 constexpr int kGemvMmaBoxBytes = kGemvMmaRows * 128;
 constexpr int kGemvMmaXBytes = kMmaN * 128;

@@ -146,15 +146,15 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     p.x_stride = K;
     p.units = p.n_tiles * p.chunks;
     int fixed = 0, per_stage = 0, xn = 0, scratch = 0;
-    const int tile = align_up(2 * B * NW * 4, 128);  // two tile buffers
+    const int tile = align_up((mma ? 1 : 2) * B * NW * 4, 128);  // tile buffers
     const int misc = 128;
     if (mma) {
         // stage: weight boxes, the [16 x 64] input box, the norm weights
         p.xstage_bytes = align_up((dual ? 2 : 1) * 2 * cfa::kGemvMmaBoxBytes + cfa::kGemvMmaXBytes +
                                       (norm ? R * 2 : 0), 1024);
-        scratch = norm ? align_up(cfa::kGemvMmaReaders * cfa::kMaxBatch * 4, 128) : 0;
+        scratch = 0;
         per_stage = p.xstage_bytes + 24;
-        fixed = scratch + tile + misc + 96 + 1024;
+        fixed = scratch + tile + misc + 64 + 1024;
     } else {
         p.xstage_bytes = align_up(B * R * 2 + (norm ? R * 2 : 0), 128);
         // per-warp normalized input rows: 8 warps x [B][R/4] floats
@@ -201,7 +201,7 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     off += misc;
     p.off_bars = off;
     // stage barriers, tile barriers, flags (+ the TMEM address)
-    off += mma ? 24 * NS + 96 : 16 * NS + 32 + 16;
+    off += mma ? 24 * NS + 64 : 16 * NS + 32 + 16;
     if (off > dev.smem_optin) return CFA_ERR_UNSUPPORTED;
     p.nstages = NS;
     p.timeout_ns = kTimeoutNs;
