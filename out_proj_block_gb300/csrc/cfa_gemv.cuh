@@ -133,43 +133,61 @@ __device__ __forceinline__ float4 *gemv_slot(const GemvParams &p, int k) {
 // s < 4 (ascending), total = (sub_0 + sub_1) + (sub_2 + sub_3), the four
 // subs held by four adjacent lanes. This block's own partial is read from
 // its tile buffer `tl`; a tile owned by one block is just that buffer.
-// nthr threads (a multiple of 32) take the work items idx = (quad, s).
-template <int MODE>
+// nthr threads (a multiple of 32) take the work items idx = (quad, s),
+// ITEMS of them at a time with their loads in flight together (more items,
+// more registers).
+template <int MODE, int ITEMS>
 __device__ __forceinline__ void gemv_finish_quads(const GemvParams &p, int t, int i_first, int n_t,
                                                   const float *tl, int ti, int nthr) {
     constexpr bool DUAL = MODE == kGemvSwiGLU;
     constexpr int NW = gemv_nw<MODE>();
     constexpr int V = 4;
-    constexpr int ITEMS = 4;  // work items per thread with their loads in flight together
     const int B = p.B;
     const int total = B * kGemvTileCols;  // a multiple of nthr: uniform trip counts
     const long long U = p.units, P = p.nblocks;
+    // nthr is a multiple of 4, so every item of this thread has the same sub
+    // (the lane within its quad): the partials it sums are the same blocks.
+    const int sub = ti & 3;
     for (int idx0 = ti; idx0 < total; idx0 += ITEMS * nthr) {
         float4 a0[ITEMS], a1[ITEMS];
 #pragma unroll
         for (int q = 0; q < ITEMS; ++q) {
-            const int idx = idx0 + q * nthr;
             a0[q] = make_float4(0.f, 0.f, 0.f, 0.f);
             a1[q] = a0[q];
-            if (idx >= total) continue;
-            const int sub = idx & 3, o = idx >> 2;
-            const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
-#pragma unroll 2
-            for (int j = sub; j < n_t; j += 4) {
-                const int i = i_first + j;
-                float4 v0, v1;
-                if (i == static_cast<int>(blockIdx.x)) {
-                    v0 = *reinterpret_cast<const float4 *>(tl + b * NW + c);
-                    if constexpr (DUAL) v1 = *reinterpret_cast<const float4 *>(tl + b * NW + kGemvTileCols + c);
-                } else {
-                    const int lt = t - unit_begin(i, U, P) / p.chunks;
-                    const float *src =
-                        p.partials + ((static_cast<size_t>(i) * p.max_tiles + lt) * B + b) * NW + c;
-                    v0 = __ldcg(reinterpret_cast<const float4 *>(src));
-                    if constexpr (DUAL) v1 = __ldcg(reinterpret_cast<const float4 *>(src + kGemvTileCols));
+        }
+        // blocks j = sub, sub + 4, ... in ascending order; for each, the
+        // partials of all ITEMS items are requested before any is used
+        for (int j = sub; j < n_t; j += 4) {
+            const int i = i_first + j;
+            const bool own = i == static_cast<int>(blockIdx.x);
+            const float *src = own ? tl
+                                   : p.partials + (static_cast<size_t>(i) * p.max_tiles +
+                                                   (t - unit_begin(i, U, P) / p.chunks)) * B * NW;
+            float4 v0[ITEMS], v1[ITEMS];
+#pragma unroll
+            for (int q = 0; q < ITEMS; ++q) {
+                const int idx = idx0 + q * nthr;
+                const int o = idx >> 2;
+                const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
+                v0[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                v1[q] = v0[q];
+                if (idx < total) {
+                    const float *e = src + b * NW + c;
+                    if (own) {
+                        v0[q] = *reinterpret_cast<const float4 *>(e);
+                        if constexpr (DUAL) v1[q] = *reinterpret_cast<const float4 *>(e + kGemvTileCols);
+                    } else {
+                        v0[q] = __ldcg(reinterpret_cast<const float4 *>(e));
+                        if constexpr (DUAL) v1[q] = __ldcg(reinterpret_cast<const float4 *>(e + kGemvTileCols));
+                    }
                 }
-                a0[q].x += v0.x; a0[q].y += v0.y; a0[q].z += v0.z; a0[q].w += v0.w;
-                if constexpr (DUAL) { a1[q].x += v1.x; a1[q].y += v1.y; a1[q].z += v1.z; a1[q].w += v1.w; }
+            }
+#pragma unroll
+            for (int q = 0; q < ITEMS; ++q) {
+                a0[q].x += v0[q].x; a0[q].y += v0[q].y; a0[q].z += v0[q].z; a0[q].w += v0[q].w;
+                if constexpr (DUAL) {
+                    a1[q].x += v1[q].x; a1[q].y += v1[q].y; a1[q].z += v1[q].z; a1[q].w += v1[q].w;
+                }
             }
         }
 #pragma unroll
@@ -188,7 +206,7 @@ __device__ __forceinline__ void gemv_finish_quads(const GemvParams &p, int t, in
                 }
             }
             const int idx = idx0 + q * nthr;
-            const int sub = idx & 3, o = idx >> 2;
+            const int o = idx >> 2;
             const int b = o / (kGemvTileCols / V), c = V * (o % (kGemvTileCols / V));
             // masked columns of a last half tile
             if (idx >= total || sub != 0 || t * kGemvTileCols + c >= p.N) continue;
@@ -322,7 +340,7 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
     }
 
     auto finish_quads = [&](int t, int i_first, int n_t, const float *tl, int ti, int nthr) {
-        gemv_finish_quads<MODE>(p, t, i_first, n_t, tl, ti, nthr);
+        gemv_finish_quads<MODE, 1>(p, t, i_first, n_t, tl, ti, nthr);
     };
     auto tile_owners = [&](int t, int &i_first, int &n_t) { gemv_tile_owners(p, t, i_first, n_t); };
     auto slot_of = [&](int k) { return gemv_slot<MODE>(p, k); };

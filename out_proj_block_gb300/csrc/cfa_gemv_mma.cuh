@@ -274,7 +274,7 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
             compute_bar<kReaderThreads>();
             finish = *is_last != 0;
         }
-        if (finish) gemv_finish_quads<MODE>(p, t, i_first, n_t, tl, tid, kReaderThreads);
+        if (finish) gemv_finish_quads<MODE, 8>(p, t, i_first, n_t, tl, tid, kReaderThreads);
         compute_bar<kReaderThreads>();  // the tile buffer and the flag are free again
     };
 
