@@ -181,24 +181,9 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
     if (warp == kGemvMmaReaders + 2) {
         // ------------------------------------------------------------- norm warp
         if constexpr (NORM) {
-            float *inv_rms = reinterpret_cast<float *>(smem + p.off_misc);  // [B]
-            grid_dependency_wait();  // the input rows come from an earlier kernel
-            // 1 / sqrt(mean_k x[b, k]^2 + eps) for every row, in a fixed order
-            for (int b = 0; b < B; ++b) {
-                const uint4 *row = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(b) * p.x_stride);
-                float ss = 0.f;
-#pragma unroll 4
-                for (int i = lane; i < p.K / 8; i += 32) {
-                    float f[8];
-                    unpack8_bf16(__ldcg(row + i), f);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) ss = fmaf(f[c], f[c], ss);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                if (lane == 0) inv_rms[b] = 1.0f / sqrtf(ss / static_cast<float>(p.K) + p.eps);
-            }
-            __syncwarp();
+            const float *inv_rms = reinterpret_cast<const float *>(smem + p.off_misc);  // [B]
+            // the readers compute the row statistics (1 / rms) and pass them on
+            asm volatile("bar.sync 2, %0;" :: "n"(kReaderThreads + 32) : "memory");
             // Each stage's input box -> bf16(g x / rms(x)), in place: 16-byte
             // chunk c of box row (batch row) b, c = lane % 8, b = lane / 8 + 4 i.
             RingCursor cur;
@@ -237,6 +222,53 @@ gemv_mma_kernel(const __grid_constant__ CUtensorMap tm_w0,
 
     // ------------------------------------------------------------------ readers
     grid_dependency_wait();  // no dependent read or global write before this
+    if constexpr (NORM) {
+        // 1 / sqrt(mean_k x[b, k]^2 + eps) of every input row, in a fixed order
+        // (per thread, per warp, then warps in order), for the norm warp. Each
+        // thread keeps 16 loads in flight: 4 rows x 4 chunks of 8 values.
+        float *red = reinterpret_cast<float *>(smem + p.off_scratch);  // [4 warps][16 rows]
+        float *inv_rms = reinterpret_cast<float *>(smem + p.off_misc);  // [B]
+        const int KC = p.K / 8;  // 16-byte chunks of a row
+        for (int b0 = 0; b0 < B; b0 += 4) {
+            float ss[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int i0 = tid; i0 < KC; i0 += 4 * kReaderThreads) {
+                uint4 v[4][4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int i = i0 + j * kReaderThreads;
+                        v[r][j] = b0 + r < B && i < KC
+                                      ? __ldcg(reinterpret_cast<const uint4 *>(
+                                                   p.x + static_cast<size_t>(b0 + r) * p.x_stride) + i)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float f[8];
+                        unpack8_bf16(v[r][j], f);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) ss[r] = fmaf(f[c], f[c], ss[r]);
+                    }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], off);
+                if (lane == 0 && b0 + r < B) red[warp * kMaxBatch + b0 + r] = ss[r];
+            }
+        }
+        compute_bar<kReaderThreads>();
+        if (tid < B) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kGemvMmaReaders; ++w) tot += red[w * kMaxBatch + tid];
+            inv_rms[tid] = 1.0f / sqrtf(tot / static_cast<float>(p.K) + p.eps);
+        }
+        asm volatile("bar.arrive 2, %0;" :: "n"(kReaderThreads + 32) : "memory");
+    }
     // The block's k-th tile (tile t): accumulators -> tile buffer [B][NW],
     // then the partial to the workspace and, by the last owner, the finish.
     auto finish_tile = [&](int k, int t) {

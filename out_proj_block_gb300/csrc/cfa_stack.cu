@@ -152,7 +152,7 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
         // stage: weight boxes, the [16 x 64] input box, the norm weights
         p.xstage_bytes = align_up((dual ? 2 : 1) * 2 * cfa::kGemvMmaBoxBytes + cfa::kGemvMmaXBytes +
                                       (norm ? R * 2 : 0), 1024);
-        scratch = 0;
+        scratch = norm ? align_up(cfa::kGemvMmaReaders * cfa::kMaxBatch * 4, 128) : 0;
         per_stage = p.xstage_bytes + 24;
         fixed = scratch + tile + misc + 64 + 1024;
     } else {
