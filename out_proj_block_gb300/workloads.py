@@ -210,6 +210,8 @@ STACKS: Dict[str, StackWorkload] = {w.name: w for w in [
         "2 tiny layers: hidden 256, 2 heads x 128, ffn 512, ctx_len 64", max_ctx=128),
     _sw("llama7b_2l_b1_ctx1k", 2, 1, 4096, 32, 128, 11008, 1024,
         "2 Llama2-7B-shaped layers (SwiGLU MLP, ffn 11008), B=1, ctx_len 1024"),
+    _sw("llama7b_2l_b16_ctx1k", 2, 16, 4096, 32, 128, 11008, 1024,
+        "2 Llama2-7B-shaped layers (SwiGLU MLP, ffn 11008), B=16, ctx_len 1024"),
     _sw("llama7b_32l_b1_ctx1k", 32, 1, 4096, 32, 128, 11008, 1024,
         "32 Llama2-7B-shaped layers (SwiGLU MLP, ffn 11008), B=1, ctx_len 1024"),
     _sw("llama7b_32l_b16_ctx1k", 32, 16, 4096, 32, 128, 11008, 1024,
