@@ -118,7 +118,7 @@ __device__ __forceinline__ void gemv_tile_owners(const GemvParams &p, int t, int
 
 // Floats per batch row of a tile partial: one or two matrices of 128 columns.
 template <int MODE>
-constexpr int gemv_nw() { return (MODE == kGemvSwiGLU ? 2 : 1) * kGemvTileCols; }
+__host__ __device__ constexpr int gemv_nw() { return (MODE == kGemvSwiGLU ? 2 : 1) * kGemvTileCols; }
 
 // This block's workspace slot for the partial of its k-th tile.
 template <int MODE>
