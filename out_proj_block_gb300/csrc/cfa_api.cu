@@ -241,11 +241,11 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.n_qk = mma ? R / 64 : 0;
     k.n_v = mma ? R / 128 : 0;
     // TMEM: 32 columns for the projection accumulators; the out-projection
-    // keeps up to 16 tile accumulators of 16 columns. Blocks that share an SM
-    // must fit its 512 columns together.
+    // keeps up to 16 tile accumulators of 32 columns (hi and lo halves).
+    // Blocks that share an SM must fit its 512 columns together.
     unsigned cols = 32;
     if (mma) {
-        const int want = std::min(ncols / cfa::kTileCols, 16) * cfa::kMmaN;
+        const int want = std::min(ncols / cfa::kTileCols, 16) * 2 * cfa::kMmaN;
         while (static_cast<int>(cols) < want) cols <<= 1;
         const int resident = std::max(blocks_per_sm, (pl->smem_per_sm) / (off + pl->smem_reserved));
         while (cols > 32 && static_cast<int>(cols) * resident > 512) cols >>= 1;

@@ -631,29 +631,32 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         // ---- C: output projection of this block's column chunk --------------
         const size_t head_stride = static_cast<size_t>(B) * H;
         if constexpr (MMA) {
-            // attn^T as a K-major, 128-byte-swizzled [16 x D] bf16 operand, split
-            // into hi + lo halves so the product keeps ~16 mantissa bits of attn.
-            uint8_t *at_hi = smem + p.off_attn_t;
-            uint8_t *at_lo = at_hi + (D / 64) * kMmaN * 128;
+            // attn^T as a K-major, 128-byte-swizzled bf16 operand of 32 rows per
+            // 64-column atom: rows 0-15 the hi parts of the batch rows, 16-31
+            // the lo parts, so one MMA (N = 32) carries ~16 mantissa bits of attn;
+            // the two halves of each accumulator are added when read out.
+            uint8_t *at = smem + p.off_attn_t;
             for (int idx = tid; idx < kMmaN * D; idx += kComputeThreads) {
                 const int n = idx / D, k = idx % D;
                 const float a = n < B ? attn[n * D + k] : 0.f;
                 const __nv_bfloat16 hi = __float2bfloat16_rn(a);
                 const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
                 const int kk = k & 63;
-                const int off = (k >> 6) * (kMmaN * 128) + n * 128 + (((kk >> 3) ^ (n & 7)) << 4) +
-                                (kk & 7) * 2;
-                *reinterpret_cast<__nv_bfloat16 *>(at_hi + off) = hi;
-                *reinterpret_cast<__nv_bfloat16 *>(at_lo + off) = lo;
+                uint8_t *atom = at + (k >> 6) * (2 * kMmaN * 128);
+                const int in_row = (kk & 7) * 2;
+                *reinterpret_cast<__nv_bfloat16 *>(atom + n * 128 + (((kk >> 3) ^ (n & 7)) << 4) + in_row) = hi;
+                const int nl = kMmaN + n;
+                *reinterpret_cast<__nv_bfloat16 *>(atom + nl * 128 + (((kk >> 3) ^ (nl & 7)) << 4) + in_row) = lo;
             }
             fence_proxy_async_smem();
             compute_bar<kComputeThreads>();
-            const uint32_t idesc = umma_idesc_bf16(128, kMmaN, true, false);
+            const uint32_t idesc = umma_idesc_bf16(128, 2 * kMmaN, true, false);
             const uint32_t ring_a = smem_addr(smem);
-            const uint32_t hi_a = smem_addr(at_hi), lo_a = smem_addr(at_lo);
-            // One TMEM accumulator per output tile (up to kbuf of them): the MMAs
-            // of consecutive tiles are issued back to back and read out in groups.
-            const int kbuf = static_cast<int>(p.tmem_cols) / kMmaN;
+            const uint32_t at_a = smem_addr(at);
+            // One TMEM accumulator of 2 x 16 columns per output tile (up to kbuf
+            // of them): the MMAs of consecutive tiles are issued back to back and
+            // read out in groups.
+            const int kbuf = static_cast<int>(p.tmem_cols) / (2 * kMmaN);
             int group0 = 0, group_n = 0;
             uint32_t acc_phase = 0;
             auto flush = [&]() {
@@ -664,10 +667,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 tcgen05_fence_after();
                 if (warp < 2) {
                     for (int t = group0; t < group0 + group_n; ++t) {
-                        float v[16];
-                        tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) +
-                                        static_cast<uint32_t>(kMmaN * (t % kbuf)),
-                                    v);
+                        float v[16], vl[16];
+                        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * warp) << 16) +
+                                            static_cast<uint32_t>(2 * kMmaN * (t % kbuf));
+                        tmem_ld_x16(ta, v);
+                        tmem_ld_x16(ta + kMmaN, vl);
+#pragma unroll
+                        for (int b = 0; b < 16; ++b) v[b] += vl[b];
                         float *dst = p.partials + static_cast<size_t>(h) * head_stride + col0 +
                                      t * kTileCols + 32 * warp + lane;
 #pragma unroll
@@ -686,13 +692,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     if (lane == 0) {
                         tcgen05_fence_after();
                         const uint32_t a0 = ring_a + s * kStageBytes;
-                        const uint32_t d = tmem + static_cast<uint32_t>(kMmaN * (ct % kbuf));
+                        const uint32_t d = tmem + static_cast<uint32_t>(2 * kMmaN * (ct % kbuf));
 #pragma unroll
                         for (int j = 0; j < D / 16; ++j) {
                             const uint64_t da = umma_smem_desc(a0 + j * 2048, 0, 1024);
-                            const uint32_t boff = (j >> 2) * (kMmaN * 128) + (j & 3) * 32;
-                            umma_bf16(d, da, umma_smem_desc(hi_a + boff, 16, 1024), idesc, j > 0);
-                            umma_bf16(d, da, umma_smem_desc(lo_a + boff, 16, 1024), idesc, true);
+                            const uint32_t boff = (j >> 2) * (2 * kMmaN * 128) + (j & 3) * 32;
+                            umma_bf16(d, da, umma_smem_desc(at_a + boff, 16, 1024), idesc, j > 0);
                         }
                     }
                     release_after_mma(s);
@@ -734,35 +739,60 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             const int n4 = p.ncols / 4;
             // Sum n blocks of partials src[i * stride] for this chunk; fp32 to dst_f
             // (row stride H) or, when dst_f is null, bf16 to out.
+            // Items (b, 4 columns) are taken MI at a time with all their loads
+            // (up to 8 partials each) in flight; each sums its partials in
+            // ascending order.
+            constexpr int MI = MAXB >= 4 ? 2 : 1;
             auto merge = [&](const float *src0, size_t stride, int n, float *dst_f) {
-                for (int idx = tid; idx < B * n4; idx += kComputeThreads) {
-                    const int b = idx / n4;
-                    const int c = col0 + 4 * (idx % n4);
-                    const float *src = src0 + static_cast<size_t>(b) * H + c;
-                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                    for (int i = 0; i < n; ++i) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i * stride));
-                        sum.x += v.x;
-                        sum.y += v.y;
-                        sum.z += v.z;
-                        sum.w += v.w;
-                    }
-                    if (dst_f) {
-                        *reinterpret_cast<float4 *>(dst_f + static_cast<size_t>(b) * H + c) = sum;
-                    } else {
-                        if (p.resid) {  // residual stream: out = resid + attention block
-                            const uint2 rv =
-                                *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
-                            sum.x += bf16_lo(rv.x);
-                            sum.y += bf16_hi(rv.x);
-                            sum.z += bf16_lo(rv.y);
-                            sum.w += bf16_hi(rv.y);
+                for (int idx0 = tid; idx0 < B * n4; idx0 += MI * kComputeThreads) {
+                    float4 sums[MI];
+#pragma unroll
+                    for (int q = 0; q < MI; ++q) sums[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i0 = 0; i0 < n; i0 += 8) {
+                        float4 v[MI][8];
+#pragma unroll
+                        for (int q = 0; q < MI; ++q) {
+                            const int idx = idx0 + q * kComputeThreads;
+                            const float *src = src0 + static_cast<size_t>(idx / n4) * H + col0 + 4 * (idx % n4);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                v[q][i] = idx < B * n4 && i0 + i < n
+                                              ? __ldcg(reinterpret_cast<const float4 *>(src + (i0 + i) * stride))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
-                        uint2 packed;
-                        packed.x = pack2_bf16(sum.x, sum.y);
-                        packed.y = pack2_bf16(sum.z, sum.w);
-                        *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+#pragma unroll
+                        for (int q = 0; q < MI; ++q)
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                sums[q].x += v[q][i].x;
+                                sums[q].y += v[q][i].y;
+                                sums[q].z += v[q][i].z;
+                                sums[q].w += v[q][i].w;
+                            }
+                    }
+#pragma unroll
+                    for (int q = 0; q < MI; ++q) {
+                        const int idx = idx0 + q * kComputeThreads;
+                        if (idx >= B * n4) continue;
+                        const int b = idx / n4;
+                        const int c = col0 + 4 * (idx % n4);
+                        float4 sum = sums[q];
+                        if (dst_f) {
+                            *reinterpret_cast<float4 *>(dst_f + static_cast<size_t>(b) * H + c) = sum;
+                        } else {
+                            if (p.resid) {  // residual stream: out = resid + attention block
+                                const uint2 rv =
+                                    *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
+                                sum.x += bf16_lo(rv.x);
+                                sum.y += bf16_hi(rv.x);
+                                sum.z += bf16_lo(rv.y);
+                                sum.w += bf16_hi(rv.y);
+                            }
+                            uint2 packed;
+                            packed.x = pack2_bf16(sum.x, sum.y);
+                            packed.y = pack2_bf16(sum.z, sum.w);
+                            *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+                        }
                     }
                 }
             };
