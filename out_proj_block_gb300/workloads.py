@@ -326,6 +326,8 @@ MLAS: Dict[str, MlaWorkload] = {w.name: w for w in [
         "DeepSeek-V3-shaped MLA (hidden 7168, 128 heads, q_lora 1536), B=1, ctx_len 4096"),
     _mw("mla_v3_b1_ctx16k", 1, 7168, 128, 1536, 16384,
         "DeepSeek-V3-shaped MLA (hidden 7168, 128 heads, q_lora 1536), B=1, ctx_len 16384"),
+    _mw("mla_v3_b4_ctx4k", 4, 7168, 128, 1536, 4096,
+        "DeepSeek-V3-shaped MLA (hidden 7168, 128 heads, q_lora 1536), B=4, ctx_len 4096"),
 ]}
 
 
