@@ -69,15 +69,12 @@ __device__ __forceinline__ uint32_t mla_atom_off(int n, int k) {
     return static_cast<uint32_t>(n * 128 + (((k >> 3) ^ (n & 7)) << 4) + (k & 7) * 2);
 }
 
-// Bounded wait by a whole warp: lane 0 polls the barrier, the other lanes wait
-// at __syncwarp (which also passes lane 0's view of the guarded data on). 32x
-// fewer polls keep the shared memory free for the TMA engine, the tensor cores
-// and the threads still working.
+// Bounded wait of every calling thread on a barrier phase (all threads poll:
+// measured faster here than one polling lane per warp and a __syncwarp).
 template <bool CLUSTER_SCOPE>
-__device__ __forceinline__ void mla_warp_wait(uint32_t bar, uint32_t parity, const MlaParams &p,
+__device__ __forceinline__ void mla_wait(uint32_t bar, uint32_t parity, const MlaParams &p,
                                               volatile int *timed_out, unsigned site) {
-    if ((threadIdx.x & 31) == 0) mbar_wait_bounded<CLUSTER_SCOPE>(bar, parity, p.timeout_ns, timed_out, p.status, site);
-    __syncwarp();
+    mbar_wait_bounded<CLUSTER_SCOPE>(bar, parity, p.timeout_ns, timed_out, p.status, site);
 }
 
 // Rotate-half rotation of (x0, x1) = dims (k, k + 32) by pos * inv_freq, the
@@ -315,7 +312,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     // ---- A: absorbed queries of this block's heads, pushed to the cluster ----
     RingCursor cur;  // every compute thread follows the ring through phase A
     auto stage_ready = [&]() {
-        mla_warp_wait<false>(bar_full0 + 8u * cur.stage, cur.phase, p, timed_out, kSiteStageFull);
+        mla_wait<false>(bar_full0 + 8u * cur.stage, cur.phase, p, timed_out, kSiteStageFull);
         return smem + p.off_ring + cur.stage * kMlaStageBytes;
     };
     auto stage_done = [&]() {  // every compute thread has read the stage
@@ -418,7 +415,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 reinterpret_cast<uint4 *>(crow)[i] = reinterpret_cast<const uint4 *>(newrow)[i];
         }
     }
-    mla_warp_wait<true>(bar_q, 0, p, timed_out, kSiteQExchange);
+    mla_wait<true>(bar_q, 0, p, timed_out, kSiteQExchange);
 
     // Queries as the B operand of the score MMA: [32 x 64] K-major swizzled
     // atoms, rows 0-15 the bf16 hi parts of the 16 heads, rows 16-31 the lo
@@ -486,7 +483,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
 #pragma unroll
         for (int h = 0; h < kMlaMaxHG; ++h) acc[i][h] = 0.f;
     auto fold = [&](int u) {  // acc = acc alpha_u + O_u
-        mla_warp_wait<false>(bar_o0 + 8u * (u & 1), (u >> 1) & 1, p, timed_out, kSiteStageFull);
+        mla_wait<false>(bar_o0 + 8u * (u & 1), (u >> 1) & 1, p, timed_out, kSiteStageFull);
         tcgen05_fence_after();
         const float *al = alpha + kMlaMaxHG * (u & 1);
 #pragma unroll
@@ -501,7 +498,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     for (int t = 0; t < n_tiles; ++t) {
         const int nvalid = min(kMlaTileRows, cache_e - row_s - t * kMlaTileRows);
         float *rmax = red_max + 8 * kMlaMaxHG * (t & 1), *rsum = red_sum + 8 * kMlaMaxHG * (t & 1);
-        mla_warp_wait<false>(bar_s0 + 8u * (t & 1), (t >> 1) & 1, p, timed_out, kSiteStageFull);
+        mla_wait<false>(bar_s0 + 8u * (t & 1), (t >> 1) & 1, p, timed_out, kSiteStageFull);
         tcgen05_fence_after();
         // scores of tile row 32 wq + lane, heads 8 wh .. + 8 (base-2 units): hi + lo
         float sv[8], sl[8];
@@ -598,7 +595,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 make_float4(m_st[tid], l_st[tid], 0.f, 0.f);
         fence_proxy_async_smem();
         compute_bar<kComputeThreads>();
-        mla_warp_wait<true>(bar_qfree, 0, p, timed_out, kSiteSoftmaxExchange);
+        mla_wait<true>(bar_qfree, 0, p, timed_out, kSiteSoftmaxExchange);
         if (tid < HG && tid / HPB != r) {
             const int h = tid, owner = h / HPB, slot = h % HPB;
             bulk_copy_to_rank(map_to_rank(smem_addr(recv + (slot * C + r) * (kMlaKv + 4)), owner),
@@ -611,7 +608,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 reinterpret_cast<const float4 *>(stage + (r * HPB + slot) * (kMlaKv + 4))[c];
         }
         compute_bar<kComputeThreads>();  // own partials written
-        mla_warp_wait<true>(bar_red, 0, p, timed_out, kSiteSoftmaxExchange);
+        mla_wait<true>(bar_red, 0, p, timed_out, kSiteSoftmaxExchange);
         // combine in block order: o = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r,
         // the weights w_r = 2^(m_r - M) / L computed once per head
         float *wgt = scr;  // [HPB][16]
