@@ -20,25 +20,34 @@
 // Grid: B x (nh / HG) clusters of C blocks; cluster (b, g) owns heads
 // [g HG, (g+1) HG) of sequence b and block r of it owns the latent rows
 // [T r / C, T (r+1) / C) of T = L + 1 rows (the new token's row is the last).
+// C is the largest of 16, 8, 4, 2 for which every cluster of the grid is
+// resident at once; each block then finishes HPB = HG / C heads. Warps: 8
+// compute warps, a TMA warp streaming every operand through one ring of 32 KB
+// stages (W_k blocks, cache tiles, W_v blocks, in the order they are used),
+// and an MMA warp.
 //  A  Absorption [CF §3.2 deferred projection]: block r computes q~ and the
-//     rotated rope query of its HPB = HG / C heads (reading their W_k block
-//     once) and pushes them to every block of the cluster (ClusterGather over
-//     DSMEM, st.async + transaction counts), so every block holds all HG
-//     queries; they become bf16 hi + lo operands (about 16 bits together).
-//     The last block builds the new latent row (RMSNorm of the latent part,
-//     rope of the key part, bf16) on chip; one block appends it.
+//     rotated rope query of its HPB heads from their W_k blocks and sends
+//     them to every block of the cluster (ClusterGather over DSMEM: one bulk
+//     shared::cluster copy per peer, bytes counted on the peer's barrier), so
+//     every block holds all HG queries; they become one bf16 operand of hi
+//     and lo parts (about 16 bits together). The last block builds the new
+//     latent row (RMSNorm of the latent part, rope of the key part, bf16) on
+//     chip; one block appends it.
 //  B  Latent attention over the block's cached rows, 128 rows per tile, with
-//     tcgen05 and TMEM accumulators: S^T = C Q^T (M = 128 rows, N = 16 heads,
-//     K = 576; the row tile is the K-major A operand, straight from its
-//     128-byte-swizzled TMA boxes), a base-2 online softmax per head across
-//     the tile (TMEM lane = row), P written as a bf16 K-major operand, then
-//     O^T = C^T P^T (M = 4 x 128 latent dims, the same boxes read MN-major,
-//     K = 128 rows), folded into fp32 registers. The latent boxes stream
-//     through a ring of two-box stages twice per tile (scores, then values;
-//     the second pass hits L2). The new row is attended on CUDA cores.
+//     tcgen05 and TMEM accumulators: S^T = C [Qhi | Qlo]^T (M = 128 rows,
+//     N = 32, K = 576; the row tile is the K-major A operand, straight from
+//     its 128-byte-swizzled TMA boxes), a base-2 online softmax per head
+//     across the tile (TMEM lane = row), P written as a bf16 K-major operand,
+//     then O^T = C^T P^T (M = 4 x 128 latent dims, the same boxes read
+//     MN-major, K = 128 rows), folded into fp32 registers. The MMA warp
+//     issues the scores of tile t + 1 before the values of tile t, so the
+//     softmax runs under the MMAs (scores, outputs and P double-buffered).
+//     The latent boxes pass through the ring twice per tile (scores, then
+//     values; the second pass hits L2). The new row is attended on CUDA cores.
 //  C  Sparse ClusterReduce [CF §5.2]: a reduce-scatter over the cluster --
-//     block r receives, for its own HPB heads only, every block's (m, l, o)
-//     and combines them in block order (deterministic); then v_h = o_h W_v,h.
+//     block r receives, for its own HPB heads only, every block's (m, l, o),
+//     one bulk copy per head, and combines them in block order
+//     (deterministic); then v_h = o_h W_v,h.
 #pragma once
 
 #include <cuda.h>
@@ -73,7 +82,7 @@ __device__ __forceinline__ uint32_t mla_atom_off(int n, int k) {
 // measured faster here than one polling lane per warp and a __syncwarp).
 template <bool CLUSTER_SCOPE>
 __device__ __forceinline__ void mla_wait(uint32_t bar, uint32_t parity, const MlaParams &p,
-                                              volatile int *timed_out, unsigned site) {
+                                         volatile int *timed_out, unsigned site) {
     mbar_wait_bounded<CLUSTER_SCOPE>(bar, parity, p.timeout_ns, timed_out, p.status, site);
 }
 
