@@ -102,6 +102,7 @@ struct GemvPlan {
     int smem = 0;
     int threads = 0;
     bool mma = false;             // the tensor-core kernel
+    int resident = 0;             // blocks per SM the occupancy calculator allows
     size_t partial_floats = 0;
 };
 
@@ -218,6 +219,22 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
         cudaGetLastError();
         return CFA_ERR_UNSUPPORTED;
     }
+    if (mma) {
+        // The occupancy calculator answers one block per SM for the tensor-core
+        // kernels whatever their size; two of the smaller ones do fit and run
+        // together (measured: the down GEMV at B = 4 takes 57 instead of 64 µs).
+        // Count what the SM holds instead: registers, shared memory, threads.
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+            cudaGetLastError();
+            return CFA_ERR_CUDA;
+        }
+        const int warps = threads / 32;
+        const int regs_per_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+        const int by_regs = 65536 / (regs_per_warp * warps);
+        const int by_smem = dev.smem_per_sm / (off + dev.smem_reserved);
+        resident = std::max(1, std::min(by_regs, std::min(by_smem, 2048 / threads)));
+    }
     // One persistent wave; every block owns an equal share of the units.
     p.nblocks = std::min(p.units, dev.sms * std::min(resident, bps));
     const int per_block = (p.units + p.nblocks - 1) / p.nblocks;
@@ -227,6 +244,7 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     out->smem = off;
     out->threads = threads;
     out->mma = mma;
+    out->resident = resident;
     out->partial_floats = static_cast<size_t>(p.nblocks) * p.max_tiles * B * NW;
     return CFA_OK;
 }
@@ -504,11 +522,12 @@ cfa_status cfa_mlp_describe(const cfa_mlp *m, char *buf, int len) {
     std::snprintf(buf, static_cast<size_t>(len),
                   "{\"B\": %d, \"hidden\": %d, \"ffn\": %d, \"tensor_cores\": %s, "
                   "\"gate_up\": {\"grid\": %d, \"units\": %d, \"rows_per_unit\": %d, "
-                  "\"stages\": %d, \"smem_bytes\": %d}, "
+                  "\"stages\": %d, \"smem_bytes\": %d, \"resident_per_sm\": %d}, "
                   "\"down\": {\"grid\": %d, \"units\": %d, \"rows_per_unit\": %d, "
-                  "\"stages\": %d, \"smem_bytes\": %d}}",
+                  "\"stages\": %d, \"smem_bytes\": %d, \"resident_per_sm\": %d}}",
                   m->B, m->H, m->F, m->gu.mma ? "true" : "false", a.nblocks, a.units, a.rows, a.nstages,
-                  m->gu.smem, d.nblocks, d.units, d.rows, d.nstages, m->dn.smem);
+                  m->gu.smem, m->gu.resident, d.nblocks, d.units, d.rows, d.nstages, m->dn.smem,
+                  m->dn.resident);
     return CFA_OK;
 }
 
