@@ -297,7 +297,7 @@ cfa_status cfa_mlp_set_pipeline(cfa_mlp *mlp, int blocks_per_sm, int stages);
 
 /*
  * Choose the kernel of the MLP's two GEMVs: path -1 = by batch size (the
- * tcgen05 tensor-core kernel from B = 3 on, the CUDA-core kernel below), 0 =
+ * tcgen05 tensor-core kernel from B = 2 on, the CUDA-core kernel at B = 1), 0 =
  * CUDA cores, 1 = tensor cores. The result is the same to within fp32
  * summation order. Keeps the pipeline overrides of cfa_mlp_set_pipeline.
  * CFA_ERR_INVALID_ARG for another path; CFA_ERR_UNSUPPORTED if the shape does

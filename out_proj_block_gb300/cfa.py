@@ -486,7 +486,7 @@ class Mlp:
             raise CfaError(st, f"pipeline {blocks_per_sm} x {stages}")
 
     def set_path(self, path: int) -> None:
-        """PATH_AUTO (tensor cores from B = 3), PATH_CUDA_CORES or PATH_TENSOR_CORES."""
+        """PATH_AUTO (tensor cores from B = 2), PATH_CUDA_CORES or PATH_TENSOR_CORES."""
         st = cfa_mlp_set_path(self.handle, path)
         if st != CFA_OK:
             raise CfaError(st, f"path {path}")

@@ -139,11 +139,11 @@ def test_mlp_paths_match_oracle(cfa, oracle, B, H, F, path):
     assert mlp.describe()["tensor_cores"] == (path == "tensor_cores")
 
 
-def test_mlp_takes_tensor_cores_from_batch_3(cfa):
-    assert not cfa.Mlp(2, 256, 512).describe()["tensor_cores"]
-    assert cfa.Mlp(3, 256, 512).describe()["tensor_cores"]
+def test_mlp_takes_tensor_cores_from_batch_2(cfa):
+    assert not cfa.Mlp(1, 256, 512).describe()["tensor_cores"]
+    assert cfa.Mlp(2, 256, 512).describe()["tensor_cores"]
     with pytest.raises(cfa.CfaError):
-        cfa.Mlp(3, 256, 512).set_path(2)
+        cfa.Mlp(2, 256, 512).set_path(2)
 
 
 def test_mlp_full_llama_shape_b16_tensor_cores(cfa, oracle):
