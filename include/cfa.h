@@ -203,8 +203,12 @@ int cfa_plan_cluster_size(const cfa_plan *plan);
 /*
  * Write a one-line JSON description of the plan (shape, cluster size, grid,
  * block, shared memory per block, pipeline stages, stage bytes, co-resident
- * clusters) into buf (NUL-terminated, truncated to len). CFA_ERR_INVALID_ARG
- * for NULL arguments.
+ * clusters, and the form of the cross-head merge: "flat" or "two-level" --
+ * the last block of a head group sums the group's partials -- or "parallel"
+ * -- once every head is in, each block sums 1/n_heads of its column chunk;
+ * chosen when one block would otherwise read more than 256 KB and the whole
+ * grid fits on the device at once) into buf (NUL-terminated, truncated to
+ * len). CFA_ERR_INVALID_ARG for NULL arguments.
  */
 cfa_status cfa_plan_describe(const cfa_plan *plan, char *buf, int len);
 

@@ -302,6 +302,11 @@ cfa_status configure(cfa_plan *pl, int C, int stages_override) {
         return CFA_ERR_UNSUPPORTED;
     }
     if (clusters < 1) return CFA_ERR_UNSUPPORTED;
+    // Parallel merge where one block would otherwise read more than 256 KB of
+    // partials: its blocks wait for one another, so every cluster of the grid
+    // must be resident at once.
+    kp.merge_parallel =
+        (4ll * pl->nh * pl->B * kp.ncols > (256 << 10) && clusters >= pl->nh) ? 1 : 0;
     pl->C = C;
     pl->kp = kp;
     pl->smem_bytes = smem;
@@ -480,10 +485,11 @@ cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
                   "\"smem_bytes\": %d, \"stages\": %d, \"stage_bytes\": %d, "
                   "\"proj_rows_per_block\": %d, \"proj_tile_rows\": %d, "
                   "\"out_cols_per_block\": %d, \"coresident_clusters\": %d, \"num_sms\": %d, "
-                  "\"overlap\": %d}",
+                  "\"overlap\": %d, \"merge\": \"%s\"}",
                   pl->B, pl->H, pl->nh, pl->D, pl->max_ctx, pl->C, pl->nh * pl->C,
                   cfa::kThreads, pl->smem_bytes, k.nstages, cfa::kStageBytes, k.R, k.TRA,
-                  k.ncols, pl->coresident_clusters, pl->num_sms, pl->overlap ? 1 : 0);
+                  k.ncols, pl->coresident_clusters, pl->num_sms, pl->overlap ? 1 : 0,
+                  k.merge_parallel ? "parallel" : (k.merge_group < pl->nh ? "two-level" : "flat"));
     return CFA_OK;
 }
 

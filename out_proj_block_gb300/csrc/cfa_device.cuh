@@ -142,6 +142,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// Requests a 2-D tensor-map box into L2 (no shared-memory destination, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Contiguous bulk copy global -> shared (addresses 16-byte aligned, bytes a
 // multiple of 16).
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
@@ -198,6 +206,33 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *addr, unsig
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
                  : "=r"(old) : "l"(addr), "r"(v) : "memory");
     return old;
+}
+
+// Add with release semantics at GPU scope (no result).
+__device__ __forceinline__ void red_add_release_gpu(unsigned *addr, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(addr), "r"(v) : "memory");
+}
+
+// Bounded spin until *addr >= target, read with acquire semantics at GPU
+// scope. On timeout the status word records `site` and false is returned.
+__device__ __forceinline__ bool spin_until_at_least(const unsigned *addr, unsigned target,
+                                                    uint64_t timeout_ns, unsigned *status,
+                                                    unsigned site) {
+    auto load = [&]() {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+        return v;
+    };
+    if (load() >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (load() < target) {
+        __nanosleep(64);
+        if (global_timer_ns() - t0 > timeout_ns) {
+            atomicOr(status, kStatusTimeoutBit | (site << kStatusSiteShift));
+            return false;
+        }
+    }
+    return true;
 }
 
 // ------------------------------------------------------ tcgen05 (5th-gen tensor cores)

@@ -36,6 +36,7 @@ enum WaitSite : unsigned {
     kSiteQExchange = 3,
     kSiteSoftmaxExchange = 4,
     kSiteKvExchange = 5,
+    kSiteMerge = 6,
     kSiteSelftest = 15,
 };
 
@@ -65,6 +66,8 @@ struct KernelParams {
     unsigned tmem_cols;    // tensor-core path: TMEM columns per block (power of two >= 32)
     int ncols;             // output columns per block in the out-projection: H / C
     int merge_group;       // heads per first-level merge group
+    int merge_parallel;    // 1: every block sums a slice of its chunk once all heads are in
+                           // (the whole grid must be resident at once)
     int nstages;           // pipeline depth
     int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_attn_t, off_scratch,
         off_bars;

@@ -154,8 +154,10 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     }
     __syncthreads();
     // The next kernel in the stream may be scheduled now; it waits for this
-    // one to finish before touching anything this one writes.
-    grid_dependents_launch();
+    // one to finish before touching anything this one writes. (With the
+    // parallel merge, only once this block has seen every head's partials:
+    // until then the whole grid must stay resident.)
+    if (!p.merge_parallel) grid_dependents_launch();
     // Announce this block's barriers to the cluster; the matching wait comes
     // right before the first push, so loading starts without a cluster round trip.
     cluster_arrive();
@@ -796,30 +798,103 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     }
                 }
             };
-            unsigned *ctr1 = p.counters + grp * C + r;
-            unsigned *ctr2 = p.counters + ng * C + r;
-            if (tid == 0) {
-                const unsigned prev = atomic_add_acq_rel_gpu(ctr1, 1u);
-                const bool last = prev == static_cast<unsigned>(gsz - 1);
-                if (last) *ctr1 = 0u;  // ready for the next launch
-                *is_last = last ? 1 : 0;
-            }
-            compute_bar<kComputeThreads>();
-            if (*is_last) {
-                const float *grp_src = p.partials + static_cast<size_t>(grp * GS) * head_stride;
-                if (ng == 1) {
-                    merge(grp_src, head_stride, gsz, nullptr);
-                } else {
-                    merge(grp_src, head_stride, gsz, p.group_sums + static_cast<size_t>(grp) * head_stride);
-                    compute_bar<kComputeThreads>();
-                    if (tid == 0) {
-                        const unsigned prev = atomic_add_acq_rel_gpu(ctr2, 1u);
-                        const bool last = prev == static_cast<unsigned>(ng - 1);
-                        if (last) *ctr2 = 0u;
-                        *is_last = last ? 2 : 0;
+            if (p.merge_parallel) {
+                // Every head's block of chunk r announces its partials; once all
+                // nh have, block (h, r) sums items [h per, (h + 1) per) of the
+                // chunk over the heads, two threads per item (heads in two
+                // halves, each in ascending order, then half 0 + half 1).
+                unsigned *arrived = p.counters + r;
+                unsigned *done = p.counters + C + r;
+                if (tid == 0) {
+                    red_add_release_gpu(arrived, 1u);
+                    if (!spin_until_at_least(arrived, static_cast<unsigned>(p.nh), p.timeout_ns, p.status,
+                                             kSiteMerge))
+                        *timed_out = 1;
+                }
+                compute_bar<kComputeThreads>();
+                grid_dependents_launch();
+                const int items = B * n4;
+                const int per = (items + p.nh - 1) / p.nh;
+                const int i0 = h * per, i1 = min(items, i0 + per);
+                const int hh = (p.nh + 1) / 2;
+                const int half = tid & 1;
+                const int e0 = half * hh, e1 = min(p.nh, e0 + hh);
+                for (int base = i0; base < i1; base += kComputeThreads / 2) {
+                    const int idx = base + (tid >> 1);
+                    const int b = idx / n4, c = col0 + 4 * (idx % n4);
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (idx < i1) {
+                        const float *src = p.partials + static_cast<size_t>(b) * H + c;
+                        for (int e = e0; e < e1; e += 16) {
+                            float4 v[16];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                v[k] = e + k < e1 ? __ldcg(reinterpret_cast<const float4 *>(src + (e + k) * head_stride))
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                sum.x += v[k].x;
+                                sum.y += v[k].y;
+                                sum.z += v[k].z;
+                                sum.w += v[k].w;
+                            }
+                        }
                     }
-                    compute_bar<kComputeThreads>();
-                    if (*is_last == 2) merge(p.group_sums, head_stride, ng, nullptr);
+                    float4 other;
+                    other.x = __shfl_xor_sync(0xffffffffu, sum.x, 1);
+                    other.y = __shfl_xor_sync(0xffffffffu, sum.y, 1);
+                    other.z = __shfl_xor_sync(0xffffffffu, sum.z, 1);
+                    other.w = __shfl_xor_sync(0xffffffffu, sum.w, 1);
+                    if (half == 0 && idx < i1) {
+                        float4 tot = make_float4(sum.x + other.x, sum.y + other.y, sum.z + other.z,
+                                                 sum.w + other.w);
+                        if (p.resid) {
+                            const uint2 rv =
+                                *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
+                            tot.x += bf16_lo(rv.x);
+                            tot.y += bf16_hi(rv.x);
+                            tot.z += bf16_lo(rv.y);
+                            tot.w += bf16_hi(rv.y);
+                        }
+                        uint2 packed;
+                        packed.x = pack2_bf16(tot.x, tot.y);
+                        packed.y = pack2_bf16(tot.z, tot.w);
+                        *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+                    }
+                }
+                // the last block of the chunk to finish reading resets both
+                // counters for the next launch
+                compute_bar<kComputeThreads>();
+                if (tid == 0 && atomic_add_acq_rel_gpu(done, 1u) == static_cast<unsigned>(p.nh - 1)) {
+                    *arrived = 0u;
+                    *done = 0u;
+                }
+            } else {
+                unsigned *ctr1 = p.counters + grp * C + r;
+                unsigned *ctr2 = p.counters + ng * C + r;
+                if (tid == 0) {
+                    const unsigned prev = atomic_add_acq_rel_gpu(ctr1, 1u);
+                    const bool last = prev == static_cast<unsigned>(gsz - 1);
+                    if (last) *ctr1 = 0u;  // ready for the next launch
+                    *is_last = last ? 1 : 0;
+                }
+                compute_bar<kComputeThreads>();
+                if (*is_last) {
+                    const float *grp_src = p.partials + static_cast<size_t>(grp * GS) * head_stride;
+                    if (ng == 1) {
+                        merge(grp_src, head_stride, gsz, nullptr);
+                    } else {
+                        merge(grp_src, head_stride, gsz, p.group_sums + static_cast<size_t>(grp) * head_stride);
+                        compute_bar<kComputeThreads>();
+                        if (tid == 0) {
+                            const unsigned prev = atomic_add_acq_rel_gpu(ctr2, 1u);
+                            const bool last = prev == static_cast<unsigned>(ng - 1);
+                            if (last) *ctr2 = 0u;
+                            *is_last = last ? 2 : 0;
+                        }
+                        compute_bar<kComputeThreads>();
+                        if (*is_last == 2) merge(p.group_sums, head_stride, ng, nullptr);
+                    }
                 }
             }
         }

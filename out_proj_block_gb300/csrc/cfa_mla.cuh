@@ -202,11 +202,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             // does not queue in front of them.
             auto prefetch_block = [&](int col0) {
                 for (int rb = 0; rb < 2; ++rb)
-                    for (int cb = 0; cb < 2; ++cb)
-                        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                                     :: "l"(reinterpret_cast<uint64_t>(&tm_wkvb)), "r"(col0 + 64 * cb),
-                                        "r"(kMlaWeightRows * rb)
-                                     : "memory");
+                    for (int cb = 0; cb < 2; ++cb) tma_prefetch_2d(&tm_wkvb, col0 + 64 * cb, kMlaWeightRows * rb);
             };
             // weights: independent of the previous kernel. The first head's
             // W_k goes straight into the ring; the other heads' into L2 behind it.

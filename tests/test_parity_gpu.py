@@ -142,6 +142,43 @@ def test_spiky_keys_long_tile_count(cfa, oracle):
     run_and_check(cfa, oracle, wl, seed=50, C=2)
 
 
+# ------------------------------------------------- the parallel cross-head merge
+
+
+@pytest.mark.parametrize("B,H,nh,D,L", [(16, 1536, 12, 128, 150), (9, 2048, 16, 128, 77),
+                                        (16, 2048, 32, 64, 200)])
+def test_parallel_merge(cfa, oracle, B, H, nh, D, L):
+    """Shapes whose cross-head merge would read more than 256 KB through one
+    block take the parallel merge (every block sums 1/nh of its chunk once all
+    heads are in): odd items per block, a head count that is not a power of
+    two, head_dim 64. Three launches on one plan (the counters are reset by
+    the last reader of each chunk) give bit-identical outputs."""
+    wl = workloads.custom(B, H, nh, D, L, max_ctx=L + 8)
+    t = workloads.make_inputs(wl, seed=70 + B, device="cuda", poison_tail=True)
+    cpu = {k: v.cpu() for k, v in t.items()}
+    outs = []
+    with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx, cluster_size=4) as plan:
+        assert plan.describe()["merge"] == "parallel"
+        for _ in range(3):
+            out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
+            plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], L, out)
+            outs.append(out)
+        torch.cuda.synchronize()
+        assert plan.status() == cfa.CFA_OK
+    ref = oracle.decode_step(cpu["x"], cpu["W_qkv"], cpu["W_o"], cpu["k_cache"], cpu["v_cache"], L,
+                             nthreads=NTHREADS)
+    check_close("out", outs[0].float().cpu().numpy(), ref["out"])
+    assert all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16)) for o in outs[1:])
+
+
+def test_merge_forms_by_size(cfa):
+    """B = 1 keeps the last-arriver merge; the batch-16 benchmark shape merges in parallel."""
+    with cfa.Plan(1, 4096, 32, 128, 4097) as plan:
+        assert plan.describe()["merge"] == "flat"
+    with cfa.Plan(16, 4096, 32, 128, 4097) as plan:
+        assert plan.describe()["merge"] == "parallel"
+
+
 # ------------------------------------------------------ determinism and reuse
 
 
