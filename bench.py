@@ -124,7 +124,7 @@ def measured_peaks():
 
 
 # The sources the fused decode kernel and its host launch are built from.
-FUSED_SOURCES = ("cfa_api.cu", "cfa_device.cuh", "cfa_internal.h", "cfa_kernel.cuh",
+FUSED_SOURCES = ("cfa_api.cu", "cfa_device.cuh", "cfa_internal.h", "cfa_kernel.cuh", "cfa_merge.cuh",
                  "cfa_kernels_d128.cu", "cfa_kernels_d64.cu", "cfa_tile.cuh")
 
 
@@ -472,7 +472,7 @@ def run_ours(args):
         "cpu_baseline": cpu_base,
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": K,
+        "gpu_launches": K * desc.get("launches_per_step", 1),
         "parity": parity,
         "plan": desc,
     }

@@ -70,8 +70,8 @@ typedef enum cfa_status {
  * cache capacity of max_ctx positions, on the current CUDA device.
  * Chooses the cluster size (blocks per head) and the pipeline depth, sets the
  * kernel attributes, and allocates the plan's workspace (fp32 per-head
- * output-projection partials [n_heads, B, hidden] and per-head-group sums,
- * arrival counters of the cross-head merge, a status word, and device staging
+ * output-projection partials [n_heads, B, hidden], arrival counters of the
+ * cross-head merge, a status word, and device staging
  * for cfa_decode_step_host).
  * Returns NULL on failure; cfa_last_error() then says why.
  */
@@ -91,6 +91,9 @@ void cfa_plan_destroy(cfa_plan *plan);
  *   out     bf16 [B, hidden]               written
  * Re-running a step with the same ctx_len rewrites the same cache row with
  * the same value, so a step is idempotent.
+ * The step is one kernel launch, or two when the plan merges the heads'
+ * partial output projections in a separate kernel (large batches; see
+ * cfa_plan_describe).
  * Launch overlap (on by default, see cfa_plan_set_overlap): the step is
  * launched with programmatic stream serialization, so it may be scheduled
  * while the previous kernel on the stream is still running. Before that
@@ -151,18 +154,17 @@ cfa_status cfa_decode_step_host(cfa_plan *plan, const void *x_host, const void *
  * No plan is involved: the shape is passed directly, with the same meaning,
  * limits and cluster-size choice as cfa_plan_create, and the arguments after
  * it mean what they mean for cfa_decode_step. Nothing is allocated: the
- * kernel's scratch (arrival counters, status word and the fp32 per-head and
- * per-head-group output-projection partials) lives in one fixed array inside
- * the library, 8 MiB + 16.25 KiB, which every GPU that loads the library
- * keeps until the process exits. Shapes with (n_heads + G) * B * hidden > 2^21,
- * where G = ceil(n_heads / 8) for n_heads >= 16 and 1 otherwise, do not fit
- * and return CFA_ERR_UNSUPPORTED before anything is launched.
+ * kernel's scratch (arrival counters, status word and the fp32 per-head
+ * output-projection partials) lives in one fixed array inside the library,
+ * 8 MiB + 16.25 KiB, which every GPU that loads the library keeps until the
+ * process exits. Shapes with n_heads * B * hidden > 2^21 do not fit and
+ * return CFA_ERR_UNSUPPORTED before anything is launched.
  *
  * The first call on a device sets the array up (looks up its device address
  * and zeroes its counters, synchronizing that device once); make that first
  * call before any stream capture. Every call then clears the counters with an
- * asynchronous memset on `stream` and launches the kernel there, without
- * launch overlap. All calls on a device share the one array, so calls whose
+ * asynchronous memset on `stream` and launches the kernel (and the separate
+ * head merge, where the plan would use one) there, without launch overlap. All calls on a device share the one array, so calls whose
  * kernels may run at the same time on that device (other streams, other host
  * threads) race and must be serialized by the caller. Device-side wait
  * timeouts are not reported by this entry point.
@@ -203,12 +205,12 @@ int cfa_plan_cluster_size(const cfa_plan *plan);
 /*
  * Write a one-line JSON description of the plan (shape, cluster size, grid,
  * block, shared memory per block, pipeline stages, stage bytes, co-resident
- * clusters, and the form of the cross-head merge: "flat" or "two-level" --
- * the last block of a head group sums the group's partials -- or "parallel"
- * -- once every head is in, each block sums 1/n_heads of its column chunk;
- * chosen when one block would otherwise read more than 256 KB and the whole
- * grid fits on the device at once) into buf (NUL-terminated, truncated to
- * len). CFA_ERR_INVALID_ARG for NULL arguments.
+ * clusters, the form of the cross-head merge -- "flat": the last head to
+ * finish a column chunk sums every head's partials inside the fused kernel;
+ * "separate": a second kernel, launched behind it on the same stream, sums
+ * them, chosen when the flat form would read more than 256 KB through one
+ * block -- and "launches_per_step", 1 or 2) into buf (NUL-terminated,
+ * truncated to len). CFA_ERR_INVALID_ARG for NULL arguments.
  */
 cfa_status cfa_plan_describe(const cfa_plan *plan, char *buf, int len);
 

@@ -20,6 +20,7 @@ namespace cfa {
 const void *fused_kernel_d128(int maxb);
 const void *fused_kernel_d64(int maxb);
 const void *selftest_wait_kernel_ptr();
+const void *head_merge_kernel_ptr();
 }  // namespace cfa
 
 using cfa::KernelParams;
@@ -39,21 +40,6 @@ constexpr int kMinStages = 2;
 
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Heads per first-level group of the cross-head merge, and the group count.
-// One level (a flat sum by the last head) while the data the last block reads
-// is small; two levels (groups of 8 heads) once a flat merge would read more
-// than 256 KB through one SM.
-int merge_group_size(int nh, int B, int ncols) {
-    const long long flat_bytes = 4ll * nh * B * ncols;
-    return (nh >= 16 && flat_bytes > (256 << 10)) ? 8 : nh;
-}
-int merge_groups(int nh, int B, int ncols) {
-    const int gs = merge_group_size(nh, B, ncols);
-    return (nh + gs - 1) / gs;
-}
-// Upper bound over every cluster size (smaller chunks never need more groups).
-int merge_groups_max(int nh) { return nh >= 16 ? (nh + 7) / 8 : 1; }
-
 }  // namespace
 
 struct cfa_plan {
@@ -69,7 +55,6 @@ struct cfa_plan {
     // workspace
     float *partials = nullptr;    // [nh][B][H]
     unsigned *words = nullptr;    // [0, kMaxCounters) merge counters, [kMaxCounters] status
-    float *group_sums = nullptr;  // [ceil(nh / merge_group)][B][H]
     uint16_t *x_stage = nullptr;  // [B][H] for cfa_decode_step_host
     uint16_t *out_stage = nullptr;
     // cached tensor maps
@@ -252,8 +237,7 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     }
     k.tmem_cols = cols;
     k.ncols = ncols;
-    k.merge_group = merge_group_size(pl->nh, B, ncols);
-    if ((merge_groups(pl->nh, B, ncols) + 1) * C > cfa::kMaxCounters) return CFA_ERR_UNSUPPORTED;
+    if (C > cfa::kMaxCounters) return CFA_ERR_UNSUPPORTED;
     k.nstages = NS;
     k.timeout_ns = kDefaultTimeoutNs;
     k.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
@@ -302,11 +286,9 @@ cfa_status configure(cfa_plan *pl, int C, int stages_override) {
         return CFA_ERR_UNSUPPORTED;
     }
     if (clusters < 1) return CFA_ERR_UNSUPPORTED;
-    // Parallel merge where one block would otherwise read more than 256 KB of
-    // partials: its blocks wait for one another, so every cluster of the grid
-    // must be resident at once.
-    kp.merge_parallel =
-        (4ll * pl->nh * pl->B * kp.ncols > (256 << 10) && clusters >= pl->nh) ? 1 : 0;
+    // A separate merge kernel where one block would otherwise read more than
+    // 256 KB of partials at the end of the fused kernel.
+    kp.merge_separate = 4ll * pl->nh * pl->B * kp.ncols > (256 << 10) ? 1 : 0;
     pl->C = C;
     pl->kp = kp;
     pl->smem_bytes = smem;
@@ -328,12 +310,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 void free_workspace(cfa_plan *pl) {
     if (pl->partials) cudaFree(pl->partials);
     if (pl->words) cudaFree(pl->words);
-    if (pl->group_sums) cudaFree(pl->group_sums);
     if (pl->x_stage) cudaFree(pl->x_stage);
     if (pl->out_stage) cudaFree(pl->out_stage);
     pl->partials = nullptr;
     pl->words = nullptr;
-    pl->group_sums = nullptr;
     pl->x_stage = pl->out_stage = nullptr;
 }
 
@@ -411,8 +391,6 @@ cfa_plan *cfa_plan_create(int B, int hidden, int n_heads, int head_dim, int max_
     const size_t act_bytes = 2u * static_cast<size_t>(B) * hidden;
     if (cudaMalloc(&pl->partials, part_bytes) != cudaSuccess ||
         cudaMalloc(&pl->words, sizeof(unsigned) * (cfa::kMaxCounters + 16)) != cudaSuccess ||
-        cudaMalloc(&pl->group_sums, sizeof(float) * static_cast<size_t>(merge_groups_max(n_heads)) *
-                                        B * hidden) != cudaSuccess ||
         cudaMalloc(&pl->x_stage, act_bytes) != cudaSuccess ||
         cudaMalloc(&pl->out_stage, act_bytes) != cudaSuccess ||
         cudaMemset(pl->words, 0, sizeof(unsigned) * (cfa::kMaxCounters + 16)) != cudaSuccess) {
@@ -485,17 +463,39 @@ cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
                   "\"smem_bytes\": %d, \"stages\": %d, \"stage_bytes\": %d, "
                   "\"proj_rows_per_block\": %d, \"proj_tile_rows\": %d, "
                   "\"out_cols_per_block\": %d, \"coresident_clusters\": %d, \"num_sms\": %d, "
-                  "\"overlap\": %d, \"merge\": \"%s\"}",
+                  "\"overlap\": %d, \"merge\": \"%s\", \"launches_per_step\": %d}",
                   pl->B, pl->H, pl->nh, pl->D, pl->max_ctx, pl->C, pl->nh * pl->C,
                   cfa::kThreads, pl->smem_bytes, k.nstages, cfa::kStageBytes, k.R, k.TRA,
                   k.ncols, pl->coresident_clusters, pl->num_sms, pl->overlap ? 1 : 0,
-                  k.merge_parallel ? "parallel" : (k.merge_group < pl->nh ? "two-level" : "flat"));
+                  k.merge_separate ? "separate" : "flat",
+                  k.merge_separate ? 2 : 1);
     return CFA_OK;
 }
 
 }  // extern "C"
 
 namespace {
+
+// The cross-head merge kernel behind a fused launch whose plan merges
+// separately (same stream; programmatic dependent launch when `overlap`).
+cudaError_t launch_head_merge(const KernelParams &kp, bool overlap, cudaStream_t stream) {
+    const int items = kp.B * (kp.H / 4);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((items + cfa::kMergeItemsPerBlock - 1) / cfa::kMergeItemsPerBlock, 1, 1);
+    cfg.blockDim = dim3(cfa::kMergeThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    const float *partials = kp.partials;
+    int nh = kp.nh, B = kp.B, H = kp.H;
+    const uint16_t *resid = kp.resid;
+    uint16_t *out = kp.out;
+    void *args[6] = {&partials, &nh, &B, &H, &resid, &out};
+    return cudaLaunchKernelExC(&cfg, cfa::head_merge_kernel_ptr(), args);
+}
 
 // One launch of the fused kernel with the given tensor maps. lens (host,
 // one per sequence) or lens_dev (device-resident, read by the kernel) gives
@@ -514,7 +514,6 @@ cfa_status launch_fused(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensor
     kp.partials = pl->partials;
     kp.counters = pl->words;
     kp.status = pl->words + cfa::kMaxCounters;
-    kp.group_sums = pl->group_sums;
     for (int b = 0; b < pl->B; ++b) kp.ctx_lens[b] = lens ? lens[b] : 0;
     kp.rope = rope_theta > 0.0 ? 1 : 0;
     if (kp.rope)
@@ -530,7 +529,8 @@ cfa_status launch_fused(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensor
     }
     CUtensorMap m_wqkv = *tm_wqkv, m_wo = *tm_wo, m_x = *tm_x;
     void *args[4] = {&m_wqkv, &m_wo, &m_x, &kp};
-    if (cudaLaunchKernelExC(&cfg, pl->kernel, args) != cudaSuccess) {
+    if (cudaLaunchKernelExC(&cfg, pl->kernel, args) != cudaSuccess ||
+        (kp.merge_separate && launch_head_merge(kp, pl->overlap, stream) != cudaSuccess)) {
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);
     }
@@ -688,7 +688,7 @@ cfa_status cfa_selftest_wait_timeout(int limit_us, void *stream) {
 namespace {
 
 constexpr size_t kNoallocWordsBytes = (cfa::kMaxCounters + 64) * 4;  // counters + status word
-constexpr size_t kNoallocPartialFloats = size_t(1) << 21;   // (n_heads + groups) * B * hidden
+constexpr size_t kNoallocPartialFloats = size_t(1) << 21;   // n_heads * B * hidden
 constexpr size_t kNoallocBytes = kNoallocWordsBytes + kNoallocPartialFloats * sizeof(float);
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
@@ -725,8 +725,7 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     if ((head_dim != 64 && head_dim != 128) || B > 16 || hidden % 64 != 0 ||
         max_ctx > (1 << 22) || hidden > (1 << 16))
         return fail(CFA_ERR_UNSUPPORTED);
-    const size_t noalloc_floats =
-        static_cast<size_t>(n_heads + merge_groups_max(n_heads)) * B * hidden;
+    const size_t noalloc_floats = static_cast<size_t>(n_heads) * B * hidden;
     if (noalloc_floats > kNoallocPartialFloats)
         return fail(CFA_ERR_UNSUPPORTED);  // scratch array too small for this shape
     if (!x || !W_qkv || !W_o || !k_cache || !v_cache || !out) return fail(CFA_ERR_INVALID_ARG);
@@ -808,13 +807,13 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     kp.counters = reinterpret_cast<unsigned *>(scratch);
     kp.status = reinterpret_cast<unsigned *>(scratch) + cfa::kMaxCounters;
     kp.partials = reinterpret_cast<float *>(scratch + kNoallocWordsBytes);
-    kp.group_sums = kp.partials + static_cast<size_t>(n_heads) * B * hidden;
     for (int b = 0; b < B; ++b) kp.ctx_lens[b] = ctx_len;
     kp.rope = 0;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config(&pl, kp, pl.smem_bytes, s, attr);
     void *args[4] = {&tm_wqkv, &tm_wo, &tm_x, &kp};
-    if (cudaLaunchKernelExC(&cfg, pl.kernel, args) != cudaSuccess) {
+    if (cudaLaunchKernelExC(&cfg, pl.kernel, args) != cudaSuccess ||
+        (kp.merge_separate && launch_head_merge(kp, false, s) != cudaSuccess)) {
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);
     }
@@ -847,6 +846,8 @@ cfa_status plan_launch_layer(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUt
     return launch_fused(pl, tm_wqkv, tm_wo, tm_x, x, k_cache, v_cache, nullptr, lens_dev,
                         rope_theta, resid, out, stream);
 }
+
+int plan_launches_per_step(const cfa_plan *pl) { return pl->kp.merge_separate ? 2 : 1; }
 
 unsigned *plan_status_word(cfa_plan *pl) { return pl->words + kMaxCounters; }
 

@@ -208,33 +208,6 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *addr, unsig
     return old;
 }
 
-// Add with release semantics at GPU scope (no result).
-__device__ __forceinline__ void red_add_release_gpu(unsigned *addr, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(addr), "r"(v) : "memory");
-}
-
-// Bounded spin until *addr >= target, read with acquire semantics at GPU
-// scope. On timeout the status word records `site` and false is returned.
-__device__ __forceinline__ bool spin_until_at_least(const unsigned *addr, unsigned target,
-                                                    uint64_t timeout_ns, unsigned *status,
-                                                    unsigned site) {
-    auto load = [&]() {
-        unsigned v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-        return v;
-    };
-    if (load() >= target) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (load() < target) {
-        __nanosleep(64);
-        if (global_timer_ns() - t0 > timeout_ns) {
-            atomicOr(status, kStatusTimeoutBit | (site << kStatusSiteShift));
-            return false;
-        }
-    }
-    return true;
-}
-
 // ------------------------------------------------------ tcgen05 (5th-gen tensor cores)
 
 // Shared-memory matrix descriptor: start address, leading- and stride-dimension

@@ -25,6 +25,7 @@ cfa_status plan_launch_layer(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUt
                              void *v_cache, const int *lens_dev, double rope_theta,
                              const void *resid, void *out, cudaStream_t stream);
 unsigned *plan_status_word(cfa_plan *pl);
+int plan_launches_per_step(const cfa_plan *pl);  // 1, or 2 with the separate head merge
 
 // Tensor map of a row-major bf16 matrix [rows][cols] with [box_rows x
 // box_cols] boxes, no swizzle (cfa_api.cu).

@@ -21,6 +21,8 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxBatch = 16;
 constexpr int kMaxRopePairs = 64;                  // head_dim / 2
 constexpr int kMaxCounters = 4096;                 // merge counters; the status word follows
+constexpr int kMergeThreads = 256;                 // head_merge_kernel: two threads per 4 columns
+constexpr int kMergeItemsPerBlock = kMergeThreads / 2;
 constexpr int kMmaN = 16;                          // batch rows per tensor-core MMA (zero-padded)
 constexpr int kXStageMmaBytes = 2 * kMmaN * 128;   // x per stage on the tensor-core path
 
@@ -36,7 +38,6 @@ enum WaitSite : unsigned {
     kSiteQExchange = 3,
     kSiteSoftmaxExchange = 4,
     kSiteKvExchange = 5,
-    kSiteMerge = 6,
     kSiteSelftest = 15,
 };
 
@@ -49,8 +50,7 @@ struct KernelParams {
     const int *lens_dev;   // [B] device-resident ctx_lens (read after the grid dependency
                            // wait), or null to use ctx_lens below
     float *partials;       // [nh][B][H] fp32 per-head output-projection partials
-    float *group_sums;     // [ceil(nh / merge_group)][B][H] fp32 per-group sums
-    unsigned *counters;    // [groups][C] then [C]: arrivals per column chunk, two levels
+    unsigned *counters;    // [C]: arrivals per column chunk
     unsigned *status;      // device status word
     int B, H, nh, max_ctx;
     int ctx_lens[kMaxBatch];   // cached positions of each sequence before this token
@@ -65,9 +65,7 @@ struct KernelParams {
     int n_qk, n_v;         // tensor-core path: 64-row [Q|K] stages and 128-row V stages
     unsigned tmem_cols;    // tensor-core path: TMEM columns per block (power of two >= 32)
     int ncols;             // output columns per block in the out-projection: H / C
-    int merge_group;       // heads per first-level merge group
-    int merge_parallel;    // 1: every block sums a slice of its chunk once all heads are in
-                           // (the whole grid must be resident at once)
+    int merge_separate;    // 1: blocks only write their partials; head_merge_kernel sums them
     int nstages;           // pipeline depth
     int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_attn_t, off_scratch,
         off_bars;

@@ -41,9 +41,10 @@
 //     multiplies attn (head h's d rows of W_o) into fp32 partials, written to
 //     a per-head workspace row.
 //  D  Cross-head merge: instead of the page's atomicAdd merge [CF §3.2], a
-//     two-level tree of release/acquire counters: the last head of each group
-//     of heads to finish a column chunk sums that group's partials, the last
-//     group sums the group totals into bf16 out. Fixed order, deterministic.
+//     release/acquire counter per column chunk: the last head to finish the
+//     chunk sums every head's partials into bf16 out. Fixed order,
+//     deterministic. When that would read more than 256 KB through one block
+//     (large batches), head_merge_kernel does the sum after the grid instead.
 #pragma once
 
 #include <cuda.h>
@@ -154,10 +155,8 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     }
     __syncthreads();
     // The next kernel in the stream may be scheduled now; it waits for this
-    // one to finish before touching anything this one writes. (With the
-    // parallel merge, only once this block has seen every head's partials:
-    // until then the whole grid must stay resident.)
-    if (!p.merge_parallel) grid_dependents_launch();
+    // one to finish before touching anything this one writes.
+    grid_dependents_launch();
     // Announce this block's barriers to the cluster; the matching wait comes
     // right before the first push, so loading starts without a cluster round trip.
     cluster_arrive();
@@ -727,39 +726,41 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             }
         }
 
-        // ---- D: two-level deterministic cross-head merge -----------------------
-        // Heads form groups of p.merge_group. The last head of a group to finish
-        // this chunk sums the group's partials (in head order); the last group
-        // to finish sums the group totals (in group order) into bf16 out. A
-        // barrier follows each block's last store, so one thread's release
-        // covers the whole block's stores.
-        {
-            const int GS = p.merge_group;
-            const int ng = (p.nh + GS - 1) / GS;
-            const int grp = h / GS;
-            const int gsz = min(GS, p.nh - grp * GS);
+        // ---- D: deterministic cross-head merge ----------------------------------
+        // The last head to finish this column chunk sums every head's partials
+        // (in head order) into bf16 out. A barrier follows each block's last
+        // store, so one thread's release covers the whole block's stores.
+        // Plans whose merge would read more than 256 KB through one block
+        // leave it to head_merge_kernel, launched after this grid.
+        if (!p.merge_separate) {
             const int n4 = p.ncols / 4;
-            // Sum n blocks of partials src[i * stride] for this chunk; fp32 to dst_f
-            // (row stride H) or, when dst_f is null, bf16 to out.
-            // Items (b, 4 columns) are taken MI at a time with all their loads
-            // (up to 8 partials each) in flight; each sums its partials in
-            // ascending order.
-            constexpr int MI = MAXB >= 4 ? 2 : 1;
-            auto merge = [&](const float *src0, size_t stride, int n, float *dst_f) {
+            unsigned *ctr = p.counters + r;
+            if (tid == 0) {
+                const unsigned prev = atomic_add_acq_rel_gpu(ctr, 1u);
+                const bool last = prev == static_cast<unsigned>(p.nh - 1);
+                if (last) *ctr = 0u;  // ready for the next launch
+                *is_last = last ? 1 : 0;
+            }
+            compute_bar<kComputeThreads>();
+            if (*is_last) {
+                // Items (b, 4 columns) are taken MI at a time with all their
+                // loads (up to 8 heads each) in flight; each sums its heads in
+                // ascending order.
+                constexpr int MI = MAXB >= 4 ? 2 : 1;
                 for (int idx0 = tid; idx0 < B * n4; idx0 += MI * kComputeThreads) {
                     float4 sums[MI];
 #pragma unroll
                     for (int q = 0; q < MI; ++q) sums[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int i0 = 0; i0 < n; i0 += 8) {
+                    for (int i0 = 0; i0 < p.nh; i0 += 8) {
                         float4 v[MI][8];
 #pragma unroll
                         for (int q = 0; q < MI; ++q) {
                             const int idx = idx0 + q * kComputeThreads;
-                            const float *src = src0 + static_cast<size_t>(idx / n4) * H + col0 + 4 * (idx % n4);
+                            const float *src = p.partials + static_cast<size_t>(idx / n4) * H + col0 + 4 * (idx % n4);
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
-                                v[q][i] = idx < B * n4 && i0 + i < n
-                                              ? __ldcg(reinterpret_cast<const float4 *>(src + (i0 + i) * stride))
+                                v[q][i] = idx < B * n4 && i0 + i < p.nh
+                                              ? __ldcg(reinterpret_cast<const float4 *>(src + (i0 + i) * head_stride))
                                               : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
 #pragma unroll
@@ -779,121 +780,17 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                         const int b = idx / n4;
                         const int c = col0 + 4 * (idx % n4);
                         float4 sum = sums[q];
-                        if (dst_f) {
-                            *reinterpret_cast<float4 *>(dst_f + static_cast<size_t>(b) * H + c) = sum;
-                        } else {
-                            if (p.resid) {  // residual stream: out = resid + attention block
-                                const uint2 rv =
-                                    *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
-                                sum.x += bf16_lo(rv.x);
-                                sum.y += bf16_hi(rv.x);
-                                sum.z += bf16_lo(rv.y);
-                                sum.w += bf16_hi(rv.y);
-                            }
-                            uint2 packed;
-                            packed.x = pack2_bf16(sum.x, sum.y);
-                            packed.y = pack2_bf16(sum.z, sum.w);
-                            *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
-                        }
-                    }
-                }
-            };
-            if (p.merge_parallel) {
-                // Every head's block of chunk r announces its partials; once all
-                // nh have, block (h, r) sums items [h per, (h + 1) per) of the
-                // chunk over the heads, two threads per item (heads in two
-                // halves, each in ascending order, then half 0 + half 1).
-                unsigned *arrived = p.counters + r;
-                unsigned *done = p.counters + C + r;
-                if (tid == 0) {
-                    red_add_release_gpu(arrived, 1u);
-                    if (!spin_until_at_least(arrived, static_cast<unsigned>(p.nh), p.timeout_ns, p.status,
-                                             kSiteMerge))
-                        *timed_out = 1;
-                }
-                compute_bar<kComputeThreads>();
-                grid_dependents_launch();
-                const int items = B * n4;
-                const int per = (items + p.nh - 1) / p.nh;
-                const int i0 = h * per, i1 = min(items, i0 + per);
-                const int hh = (p.nh + 1) / 2;
-                const int half = tid & 1;
-                const int e0 = half * hh, e1 = min(p.nh, e0 + hh);
-                for (int base = i0; base < i1; base += kComputeThreads / 2) {
-                    const int idx = base + (tid >> 1);
-                    const int b = idx / n4, c = col0 + 4 * (idx % n4);
-                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (idx < i1) {
-                        const float *src = p.partials + static_cast<size_t>(b) * H + c;
-                        for (int e = e0; e < e1; e += 16) {
-                            float4 v[16];
-#pragma unroll
-                            for (int k = 0; k < 16; ++k)
-                                v[k] = e + k < e1 ? __ldcg(reinterpret_cast<const float4 *>(src + (e + k) * head_stride))
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                sum.x += v[k].x;
-                                sum.y += v[k].y;
-                                sum.z += v[k].z;
-                                sum.w += v[k].w;
-                            }
-                        }
-                    }
-                    float4 other;
-                    other.x = __shfl_xor_sync(0xffffffffu, sum.x, 1);
-                    other.y = __shfl_xor_sync(0xffffffffu, sum.y, 1);
-                    other.z = __shfl_xor_sync(0xffffffffu, sum.z, 1);
-                    other.w = __shfl_xor_sync(0xffffffffu, sum.w, 1);
-                    if (half == 0 && idx < i1) {
-                        float4 tot = make_float4(sum.x + other.x, sum.y + other.y, sum.z + other.z,
-                                                 sum.w + other.w);
-                        if (p.resid) {
-                            const uint2 rv =
-                                *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
-                            tot.x += bf16_lo(rv.x);
-                            tot.y += bf16_hi(rv.x);
-                            tot.z += bf16_lo(rv.y);
-                            tot.w += bf16_hi(rv.y);
+                        if (p.resid) {  // residual stream: out = resid + attention block
+                            const uint2 rv = *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
+                            sum.x += bf16_lo(rv.x);
+                            sum.y += bf16_hi(rv.x);
+                            sum.z += bf16_lo(rv.y);
+                            sum.w += bf16_hi(rv.y);
                         }
                         uint2 packed;
-                        packed.x = pack2_bf16(tot.x, tot.y);
-                        packed.y = pack2_bf16(tot.z, tot.w);
+                        packed.x = pack2_bf16(sum.x, sum.y);
+                        packed.y = pack2_bf16(sum.z, sum.w);
                         *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
-                    }
-                }
-                // the last block of the chunk to finish reading resets both
-                // counters for the next launch
-                compute_bar<kComputeThreads>();
-                if (tid == 0 && atomic_add_acq_rel_gpu(done, 1u) == static_cast<unsigned>(p.nh - 1)) {
-                    *arrived = 0u;
-                    *done = 0u;
-                }
-            } else {
-                unsigned *ctr1 = p.counters + grp * C + r;
-                unsigned *ctr2 = p.counters + ng * C + r;
-                if (tid == 0) {
-                    const unsigned prev = atomic_add_acq_rel_gpu(ctr1, 1u);
-                    const bool last = prev == static_cast<unsigned>(gsz - 1);
-                    if (last) *ctr1 = 0u;  // ready for the next launch
-                    *is_last = last ? 1 : 0;
-                }
-                compute_bar<kComputeThreads>();
-                if (*is_last) {
-                    const float *grp_src = p.partials + static_cast<size_t>(grp * GS) * head_stride;
-                    if (ng == 1) {
-                        merge(grp_src, head_stride, gsz, nullptr);
-                    } else {
-                        merge(grp_src, head_stride, gsz, p.group_sums + static_cast<size_t>(grp) * head_stride);
-                        compute_bar<kComputeThreads>();
-                        if (tid == 0) {
-                            const unsigned prev = atomic_add_acq_rel_gpu(ctr2, 1u);
-                            const bool last = prev == static_cast<unsigned>(ng - 1);
-                            if (last) *ctr2 = 0u;
-                            *is_last = last ? 2 : 0;
-                        }
-                        compute_bar<kComputeThreads>();
-                        if (*is_last == 2) merge(p.group_sums, head_stride, ng, nullptr);
                     }
                 }
             }

@@ -1,5 +1,6 @@
 // Instantiations of the fused kernel for head_dim 128.
 #include "cfa_kernel.cuh"
+#include "cfa_merge.cuh"
 
 namespace cfa {
 
@@ -13,6 +14,8 @@ const void *fused_kernel_d128(int maxb) {
         default: return nullptr;
     }
 }
+
+const void *head_merge_kernel_ptr() { return reinterpret_cast<const void *>(&head_merge_kernel); }
 
 // Exercises mbar_wait_bounded on a barrier nothing arrives on.
 __global__ void selftest_wait_kernel(unsigned *status, unsigned long long timeout_ns) {

@@ -802,7 +802,7 @@ cfa_status cfa_stack_describe(const cfa_stack *s, char *buf, int len) {
         return fail(CFA_ERR_INVALID_ARG);
     std::snprintf(buf, static_cast<size_t>(len),
                   "{\"n_layers\": %d, \"launches_per_token\": %d, \"attention\": %s, \"mlp\": %s}",
-                  s->L, 4 * s->L, a, m);
+                  s->L, (3 + cfa::plan_launches_per_step(s->attn)) * s->L, a, m);
     return CFA_OK;
 }
 

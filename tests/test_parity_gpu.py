@@ -142,23 +142,22 @@ def test_spiky_keys_long_tile_count(cfa, oracle):
     run_and_check(cfa, oracle, wl, seed=50, C=2)
 
 
-# ------------------------------------------------- the parallel cross-head merge
+# ------------------------------------------------- the separate cross-head merge
 
 
 @pytest.mark.parametrize("B,H,nh,D,L", [(16, 1536, 12, 128, 150), (9, 2048, 16, 128, 77),
                                         (16, 2048, 32, 64, 200)])
-def test_parallel_merge(cfa, oracle, B, H, nh, D, L):
+def test_separate_merge(cfa, oracle, B, H, nh, D, L):
     """Shapes whose cross-head merge would read more than 256 KB through one
-    block take the parallel merge (every block sums 1/nh of its chunk once all
-    heads are in): odd items per block, a head count that is not a power of
-    two, head_dim 64. Three launches on one plan (the counters are reset by
-    the last reader of each chunk) give bit-identical outputs."""
+    block merge in a second kernel: a head count that is not a power of two,
+    head_dim 64, a batch of 9. Three launches on one plan, each step's merge
+    overlapping the next step's start, give bit-identical outputs."""
     wl = workloads.custom(B, H, nh, D, L, max_ctx=L + 8)
     t = workloads.make_inputs(wl, seed=70 + B, device="cuda", poison_tail=True)
     cpu = {k: v.cpu() for k, v in t.items()}
     outs = []
     with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx, cluster_size=4) as plan:
-        assert plan.describe()["merge"] == "parallel"
+        assert plan.describe()["merge"] == "separate"
         for _ in range(3):
             out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
             plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], L, out)
@@ -172,11 +171,14 @@ def test_parallel_merge(cfa, oracle, B, H, nh, D, L):
 
 
 def test_merge_forms_by_size(cfa):
-    """B = 1 keeps the last-arriver merge; the batch-16 benchmark shape merges in parallel."""
+    """B = 1 merges in the fused kernel (the last head to arrive); the batch-16
+    benchmark shape merges in a second kernel."""
     with cfa.Plan(1, 4096, 32, 128, 4097) as plan:
         assert plan.describe()["merge"] == "flat"
+        assert plan.describe()["launches_per_step"] == 1
     with cfa.Plan(16, 4096, 32, 128, 4097) as plan:
-        assert plan.describe()["merge"] == "parallel"
+        assert plan.describe()["merge"] == "separate"
+        assert plan.describe()["launches_per_step"] == 2
 
 
 # ------------------------------------------------------ determinism and reuse
