@@ -666,20 +666,23 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                          kSiteStageFull);
                 acc_phase ^= 1u;
                 tcgen05_fence_after();
-                if (warp < 2) {
-                    for (int t = group0; t < group0 + group_n; ++t) {
-                        float v[16], vl[16];
-                        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * warp) << 16) +
+                // Accumulator lanes 0-63 are the tile's 64 columns: warps 0 and 1
+                // read them for even tiles, warps 4 and 5 (the same lane
+                // quarters) for odd ones; hi and lo share one load wait.
+                if ((warp & 3) < 2) {
+                    const int wq = warp & 3;
+                    for (int t = group0 + (warp >> 2); t < group0 + group_n; t += 2) {
+                        uint32_t vh[16], vl[16];
+                        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * wq) << 16) +
                                             static_cast<uint32_t>(2 * kMmaN * (t % kbuf));
-                        tmem_ld_x16(ta, v);
-                        tmem_ld_x16(ta + kMmaN, vl);
-#pragma unroll
-                        for (int b = 0; b < 16; ++b) v[b] += vl[b];
+                        tmem_ld_x16_nowait(ta, vh);
+                        tmem_ld_x16_nowait(ta + kMmaN, vl);
+                        tmem_wait_ld();
                         float *dst = p.partials + static_cast<size_t>(h) * head_stride + col0 +
-                                     t * kTileCols + 32 * warp + lane;
+                                     t * kTileCols + 32 * wq + lane;
 #pragma unroll
                         for (int b = 0; b < MAXB; ++b)
-                            if (b < B) dst[static_cast<size_t>(b) * H] = v[b];
+                            if (b < B) dst[static_cast<size_t>(b) * H] = __uint_as_float(vh[b]) + __uint_as_float(vl[b]);
                     }
                 }
                 tcgen05_fence_before();
