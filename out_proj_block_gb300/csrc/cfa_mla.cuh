@@ -30,9 +30,10 @@
 //     them to every block of the cluster (ClusterGather over DSMEM: one bulk
 //     shared::cluster copy per peer, bytes counted on the peer's barrier), so
 //     every block holds all HG queries; they become one bf16 operand of hi
-//     and lo parts (about 16 bits together). The last block builds the new
-//     latent row (RMSNorm of the latent part, rope of the key part, bf16) on
-//     chip; one block appends it.
+//     and lo parts (about 16 bits together). The last block then builds the
+//     new latent row (RMSNorm of the latent part, rope of the key part, bf16)
+//     on chip while its first tile's scores are computed; one block appends
+//     it.
 //  B  Latent attention over the block's cached rows, 128 rows per tile, with
 //     tcgen05 and TMEM accumulators: S^T = C [Qhi | Qlo]^T (M = 128 rows,
 //     N = 32, K = 576; the row tile is the K-major A operand, straight from
@@ -388,38 +389,6 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                               map_to_rank(bar_q, tid));
         }
     }
-    // The new token's latent row (last block): bf16 RMSNorm of the latent and
-    // bf16 rope of the key; one block appends it to the cache.
-    if (has_new) {
-        const uint16_t *ar = p.a + static_cast<size_t>(b) * p.a_stride + p.a_off;
-        float ss = 0.f;
-        for (int i = tid; i < kMlaKv; i += kComputeThreads) {
-            const float v = bf16_bits(ar[i]);
-            ss = fmaf(v, v, ss);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) scr[kMlaNope + warp] = ss;
-        compute_bar<kComputeThreads>();
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kComputeWarps; ++w) tot += scr[kMlaNope + w];
-        const float inv = 1.0f / sqrtf(tot / static_cast<float>(kMlaKv) + p.eps);
-        for (int i = tid; i < kMlaKv; i += kComputeThreads)
-            newrow[i] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits(p.g_kv[i]) * bf16_bits(ar[i]) * inv));
-        if (tid < kMlaRope / 2) {
-            float x0 = bf16_bits(ar[kMlaKv + tid]), x1 = bf16_bits(ar[kMlaKv + tid + kMlaRope / 2]);
-            if (p.rope) mla_rope(x0, x1, L, p.rope_inv_freq[tid]);
-            newrow[kMlaKv + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
-            newrow[kMlaKv + tid + kMlaRope / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(x1));
-        }
-        compute_bar<kComputeThreads>();
-        if (g == 0) {
-            uint16_t *crow = p.cache + (static_cast<size_t>(b) * p.max_ctx + L) * kMlaRow;
-            for (int i = tid; i < kMlaRow / 8; i += kComputeThreads)
-                reinterpret_cast<uint4 *>(crow)[i] = reinterpret_cast<const uint4 *>(newrow)[i];
-        }
-    }
     mla_wait<true>(bar_q, 0, p, timed_out, kSiteQExchange);
 
     // Queries as the B operand of the score MMA: [32 x 64] K-major swizzled
@@ -457,7 +426,42 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
         m_st[tid] = -INFINITY;
         l_st[tid] = 0.f;
     }
-    if (has_new) {  // the new row's score per head (base 2)
+    fence_proxy_async_smem();
+    compute_bar<kComputeThreads>();
+    if (tid == 0) mbar_arrive(bar_qready);
+    // The new token's latent row (last block), built while the MMA warp issues
+    // the first tile's scores: bf16 RMSNorm of the latent and bf16 rope of the
+    // key; one block appends it to the cache. Then its score per head (base
+    // 2) from the fp32 queries, which peers may overwrite only after this.
+    if (has_new) {
+        const uint16_t *ar = p.a + static_cast<size_t>(b) * p.a_stride + p.a_off;
+        float ss = 0.f;
+        for (int i = tid; i < kMlaKv; i += kComputeThreads) {
+            const float v = bf16_bits(ar[i]);
+            ss = fmaf(v, v, ss);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) scr[kMlaNope + warp] = ss;
+        compute_bar<kComputeThreads>();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kComputeWarps; ++w) tot += scr[kMlaNope + w];
+        const float inv = 1.0f / sqrtf(tot / static_cast<float>(kMlaKv) + p.eps);
+        for (int i = tid; i < kMlaKv; i += kComputeThreads)
+            newrow[i] = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits(p.g_kv[i]) * bf16_bits(ar[i]) * inv));
+        if (tid < kMlaRope / 2) {
+            float x0 = bf16_bits(ar[kMlaKv + tid]), x1 = bf16_bits(ar[kMlaKv + tid + kMlaRope / 2]);
+            if (p.rope) mla_rope(x0, x1, L, p.rope_inv_freq[tid]);
+            newrow[kMlaKv + tid] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
+            newrow[kMlaKv + tid + kMlaRope / 2] = __bfloat16_as_ushort(__float2bfloat16_rn(x1));
+        }
+        compute_bar<kComputeThreads>();
+        if (g == 0) {
+            uint16_t *crow = p.cache + (static_cast<size_t>(b) * p.max_ctx + L) * kMlaRow;
+            for (int i = tid; i < kMlaRow / 8; i += kComputeThreads)
+                reinterpret_cast<uint4 *>(crow)[i] = reinterpret_cast<const uint4 *>(newrow)[i];
+        }
         for (int h = warp; h < HG; h += kComputeWarps) {
             float s = 0.f;
             for (int k = lane; k < kMlaRow; k += 32) s = fmaf(qt[h * kMlaRow + k], bf16_bits(newrow[k]), s);
@@ -465,10 +469,8 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
             if (lane == 0) s_new[h] = s;
         }
+        compute_bar<kComputeThreads>();
     }
-    fence_proxy_async_smem();
-    compute_bar<kComputeThreads>();
-    if (tid == 0) mbar_arrive(bar_qready);
     // The fp32 queries are dead here; their space receives the peers' partials.
     if (tid == 0)
         for (int q = 0; q < C; ++q)
