@@ -394,7 +394,11 @@ cfa_status cfa_stack_describe(const cfa_stack *stack, char *buf, int len);
  * rope is the rotate-half form of cfa_decode_step_ex over the 64 rope dims
  * (rope_theta 0 disables it); rmsnorm as cfa_rmsnorm. The attention runs in
  * absorbed form (q_nope folded into W_k, values projected after the sum), one
- * thread-block cluster per (sequence, group of 16 heads).
+ * thread-block cluster per (sequence, group of 16 heads) -- or two, each over
+ * half of the latent rows ("row splits", §5.2's cache partitioned across
+ * clusters) when that grid still fits on the GPU at once; the later of the
+ * two to finish combines them in split order, so results stay bitwise
+ * reproducible.
  * ========================================================================== */
 
 typedef struct cfa_mla cfa_mla; /* opaque */
@@ -424,8 +428,18 @@ cfa_status cfa_mla_step(cfa_mla *mla, const void *x, const void *W_a, const void
 /* Synchronizes, reads and clears the plan's device status words. */
 cfa_status cfa_mla_status(cfa_mla *mla);
 
-/* One-line JSON description (cluster shape, grid, shared memory, GEMV grids). */
+/* One-line JSON description (cluster shape, row splits, grid, shared memory,
+ * GEMV grids). */
 cfa_status cfa_mla_describe(const cfa_mla *mla, char *buf, int len);
+
+/*
+ * Override the number of row splits (1 or 2 clusters per sequence and head
+ * group) chosen at creation; the cluster size becomes the largest whose grid
+ * then fits on the GPU at once. Synchronizes the device first.
+ * CFA_ERR_INVALID_ARG for other values; CFA_ERR_UNSUPPORTED if no cluster size
+ * fits.
+ */
+cfa_status cfa_mla_set_row_splits(cfa_mla *mla, int splits);
 
 #ifdef __cplusplus
 }

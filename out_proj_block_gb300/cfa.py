@@ -99,6 +99,8 @@ _lib.cfa_mla_status.restype = _i
 _lib.cfa_mla_status.argtypes = [_vp]
 _lib.cfa_mla_describe.restype = _i
 _lib.cfa_mla_describe.argtypes = [_vp, ctypes.c_char_p, _i]
+_lib.cfa_mla_set_row_splits.restype = _i
+_lib.cfa_mla_set_row_splits.argtypes = [_vp, _i]
 _lib.cfa_stack_describe.restype = _i
 _lib.cfa_stack_describe.argtypes = [_vp, ctypes.c_char_p, _i]
 
@@ -122,6 +124,7 @@ EXPORTED_SYMBOLS = (
     "cfa_mlp_describe", "cfa_stack_create", "cfa_stack_destroy", "cfa_stack_set_layer",
     "cfa_stack_step", "cfa_stack_step_graph", "cfa_stack_status", "cfa_stack_describe",
     "cfa_mla_create", "cfa_mla_destroy", "cfa_mla_step", "cfa_mla_status", "cfa_mla_describe",
+    "cfa_mla_set_row_splits",
 )
 
 
@@ -620,6 +623,10 @@ def cfa_mla_describe(mla) -> dict:
     return json.loads(buf.value.decode())
 
 
+def cfa_mla_set_row_splits(mla, splits: int) -> int:
+    return int(_lib.cfa_mla_set_row_splits(mla, int(splits)))
+
+
 class Mla:
     """Owns a cfa_mla: DeepSeek-style latent-attention decode steps."""
 
@@ -643,6 +650,13 @@ class Mla:
 
     def describe(self) -> dict:
         return cfa_mla_describe(self.handle)
+
+    def set_row_splits(self, splits: int):
+        """1 or 2 clusters per (sequence, head group), each over its share of
+        the latent rows; raises CfaError if that grid does not fit at once."""
+        st = cfa_mla_set_row_splits(self.handle, splits)
+        if st != CFA_OK:
+            raise CfaError(st, "cfa_mla_set_row_splits")
 
     def status(self) -> int:
         return cfa_mla_status(self.handle)

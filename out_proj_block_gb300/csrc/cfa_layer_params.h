@@ -71,6 +71,7 @@ constexpr int kMlaAtomBytes = kMlaMaxHG * 128;      // a [16 x 64] K-major swizz
 constexpr int kMlaWeightRows = 256;                 // a W_kvb box is [256 x 64] (one stage)
 constexpr int kMlaQAtomBytes = 2 * kMlaAtomBytes;   // a [32 x 64] atom: hi rows, then lo rows
 constexpr int kMlaThreads = kComputeThreads + 64;   // + load warp + MMA warp
+constexpr int kMlaSplitRec = kMlaV + 4;             // per-split record: v_h [128], M, L, pad
 
 struct MlaParams {
     const uint16_t *q;       // [B][nh*192] bf16: per head [q_nope | q_rope]
@@ -87,6 +88,9 @@ struct MlaParams {
     float eps;
     float qscale;            // log2(e) / sqrt(192): scores in base-2 units
     int HG, C, HPB;          // heads per cluster, blocks per cluster, heads per block
+    int S;                   // row splits: clusters per (sequence, head group)
+    float *vpart;            // S > 1: [B][nh][S][kMlaSplitRec] per-split v_h, max, sum
+    unsigned *vcount;        // S > 1: [B][nh / HG][C] arrivals of the splits
     int nstages;
     int off_ring, off_qb, off_pb, off_qt, off_newrow, off_stat, off_recv, off_ofin,
         off_scr, off_bars;

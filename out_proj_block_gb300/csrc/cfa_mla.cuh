@@ -107,12 +107,14 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
     const int C = p.C, HG = p.HG, HPB = p.HPB, NS = p.nstages;
     const int r = static_cast<int>(cluster_ctarank());
     const int cluster = blockIdx.x / C;
-    const int NG = p.nh / HG;
-    const int b = cluster / NG, g = cluster % NG;
+    const int NG = p.nh / HG, S = p.S;
+    const int b = cluster / (NG * S), g = (cluster / S) % NG, split = cluster % S;
     const int L = p.ctx_lens[b];
     const int T = L + 1;
-    const int row_s = static_cast<int>((static_cast<long long>(T) * r) / C);
-    const int row_e = static_cast<int>((static_cast<long long>(T) * (r + 1)) / C);
+    // rows of block r of split `split`: the (split C + r)-th of S C even parts
+    const long long part = static_cast<long long>(split) * C + r, parts = static_cast<long long>(S) * C;
+    const int row_s = static_cast<int>((static_cast<long long>(T) * part) / parts);
+    const int row_e = static_cast<int>((static_cast<long long>(T) * (part + 1)) / parts);
     const int cache_e = min(row_e, L);                       // rows read from the cache
     const bool has_new = row_e == T;                         // this block attends the new row
     const int n_tiles = cache_e > row_s ? (cache_e - row_s + kMlaTileRows - 1) / kMlaTileRows : 0;
@@ -619,6 +621,7 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
         // combine in block order: o = sum_r 2^(m_r - M) o_r / sum_r 2^(m_r - M) l_r,
         // the weights w_r = 2^(m_r - M) / L computed once per head
         float *wgt = scr;  // [HPB][16]
+        float *split_ml = scr + kComputeWarps * kMlaV;  // [HPB][2]: (M, L) of this split
         if (warp < (HPB * kMlaMaxHG + 31) / 32) {  // 16 lanes per head, lane q for block q
             const int i = tid / kMlaMaxHG, q = tid % kMlaMaxHG;
             const bool act = i < HPB && q < C;
@@ -633,7 +636,12 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
             float Lsum = e * lq;
 #pragma unroll
             for (int off = kMlaMaxHG / 2; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-            if (i < HPB) wgt[i * kMlaMaxHG + q] = e / Lsum;  // 0 for q >= C
+            // (a split with no rows at all has Lsum = 0 and contributes nothing)
+            if (i < HPB) wgt[i * kMlaMaxHG + q] = Lsum > 0.f ? e / Lsum : 0.f;  // 0 for q >= C
+            if (i < HPB && q == 0) {  // this split's max and sum, for the combine of splits
+                split_ml[2 * i] = M;
+                split_ml[2 * i + 1] = Lsum;
+            }
         }
         compute_bar<kComputeThreads>();
         for (int idx = tid; idx < HPB * kMlaKv; idx += kComputeThreads) {
@@ -695,10 +703,53 @@ mla_attention_kernel(const __grid_constant__ MlaMaps maps,
                 float vsum = 0.f;
 #pragma unroll
                 for (int w = 0; w < kComputeWarps; ++w) vsum += scr[w * kMlaV + tid];
-                p.v[static_cast<size_t>(b) * p.nh * kMlaV + h * kMlaV + tid] =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(vsum));
+                if (S == 1) {
+                    p.v[static_cast<size_t>(b) * p.nh * kMlaV + h * kMlaV + tid] =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(vsum));
+                } else {  // this split's v_h (normalised by its own sum) with its (M, L)
+                    float *rec = p.vpart + (static_cast<size_t>(b) * p.nh + h) * S * kMlaSplitRec +
+                                 split * kMlaSplitRec;
+                    rec[tid] = vsum;
+                    if (tid < 2) rec[kMlaV + tid] = split_ml[2 * ii + tid];
+                }
             }
             compute_bar<kComputeThreads>();
+        }
+        if (S > 1) {
+            // Combine of the row splits [CF §5.2, the cache partitioned across
+            // clusters]: block r of every split owns the same heads; the last
+            // of them to get here sums the splits in split order,
+            //   v_h = sum_s 2^(M_s - M) L_s v_s / sum_s 2^(M_s - M) L_s.
+            // (A barrier follows the block's last store, so one thread's
+            // release covers them.)
+            volatile int *last = reinterpret_cast<volatile int *>(s_new);
+            if (tid == 0) {
+                unsigned *ctr = p.vcount + (static_cast<size_t>(b) * NG + g) * C + r;
+                const bool is_last = atomic_add_acq_rel_gpu(ctr, 1u) == static_cast<unsigned>(S - 1);
+                if (is_last) *ctr = 0u;  // ready for the next launch
+                *last = is_last ? 1 : 0;
+            }
+            compute_bar<kComputeThreads>();
+            if (*last) {
+                for (int idx = tid; idx < HPB * kMlaV; idx += kComputeThreads) {
+                    const int ii = idx / kMlaV, c = idx % kMlaV;
+                    const int h = g * HG + r * HPB + ii;
+                    const float *rec = p.vpart + (static_cast<size_t>(b) * p.nh + h) * S * kMlaSplitRec;
+                    float M = -INFINITY;
+                    for (int q = 0; q < S; ++q) M = fmaxf(M, __ldcg(rec + q * kMlaSplitRec + kMlaV));
+                    float num = 0.f, den = 0.f;
+                    for (int q = 0; q < S; ++q) {
+                        const float mq = __ldcg(rec + q * kMlaSplitRec + kMlaV);
+                        const float w = mq == -INFINITY
+                                            ? 0.f
+                                            : fast_exp2(mq - M) * __ldcg(rec + q * kMlaSplitRec + kMlaV + 1);
+                        num = fmaf(w, __ldcg(rec + q * kMlaSplitRec + c), num);
+                        den += w;
+                    }
+                    p.v[static_cast<size_t>(b) * p.nh * kMlaV + h * kMlaV + c] =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(num / den));
+                }
+            }
         }
     }
     if (warp == 0) {

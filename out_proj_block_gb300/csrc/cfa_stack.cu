@@ -819,10 +819,13 @@ struct cfa_mla {
     uint16_t *v = nullptr;        // [B][nh*128]
     float *partials = nullptr;
     unsigned *words = nullptr;    // counters of the three GEMVs, GEMV status, kernel status
+    float *vpart = nullptr;       // per-split v records when the rows are split across clusters
+    unsigned *vcount = nullptr;   // their arrival counters
     CUtensorMap tm_aq, tm_v;      // inputs of the q and output GEMVs (fixed buffers)
     cfa::MlaParams mp{};
     int smem = 0;
     int coresident_clusters = 0;
+    int fit_clusters[5] = {};     // clusters of C = 2, 4, 8, 16 blocks resident at once (0: no fit)
 };
 
 namespace {
@@ -835,9 +838,44 @@ void mla_free(cfa_mla *m) {
     if (m->v) cudaFree(m->v);
     if (m->partials) cudaFree(m->partials);
     if (m->words) cudaFree(m->words);
+    if (m->vpart) cudaFree(m->vpart);
+    if (m->vcount) cudaFree(m->vcount);
     m->a = m->q = m->v = nullptr;
     m->partials = nullptr;
     m->words = nullptr;
+    m->vpart = nullptr;
+    m->vcount = nullptr;
+}
+
+constexpr int kMlaMaxSplits = 2;
+
+// Shared memory of one attention block when a cluster has C blocks (HG / C
+// heads each); sets C, HPB and the offsets in mp, returns the bytes.
+int mla_layout(cfa::MlaParams &mp, int C) {
+    const int HG = mp.HG;
+    mp.C = C;
+    mp.HPB = HG / C;
+    int off = 0;
+    mp.off_ring = off;                          // two-box stages (1024-aligned boxes)
+    off += kMlaStages * cfa::kMlaStageBytes;
+    mp.off_qb = off;                            // 9 swizzled [32 x 64] query atoms (hi, lo)
+    off += cfa::kMlaBoxes * cfa::kMlaQAtomBytes;
+    mp.off_pb = off;                            // P of two tiles: 2 x 2 atoms [16 heads x 64 rows]
+    off += 4 * cfa::kMlaAtomBytes;
+    mp.off_qt = off;                            // fp32 queries [HG][576], then
+    mp.off_recv = off;                          // partials of my heads [HPB][C][516]
+    off += align_up(std::max(HG * cfa::kMlaRow, mp.HPB * mp.C * (cfa::kMlaKv + 4)) * 4, 128);
+    mp.off_newrow = off;
+    off += align_up(cfa::kMlaRow * 2, 128);
+    mp.off_stat = off;                          // m, l, 2 alpha, 2 x two [8][16] reductions, new row
+    off += align_up(592 * 4, 128);
+    mp.off_ofin = off;                          // combined latent outputs [HPB][512]
+    off += align_up(mp.HPB * cfa::kMlaKv * 4, 128);
+    mp.off_scr = off;
+    off += align_up((cfa::kComputeWarps * cfa::kMlaV + 64) * 4, 128);
+    mp.off_bars = off;
+    off += 16 * kMlaStages + 128;
+    return off;
 }
 
 unsigned *mla_gemv_status(cfa_mla *m) {
@@ -913,32 +951,7 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
     mp.nstages = kMlaStages;
     mp.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(cfa::kMlaQk)));
     mp.timeout_ns = kTimeoutNs;
-    // Shared memory of one block when a cluster has C blocks (HG / C heads each).
-    auto layout = [&](int C) {
-        mp.C = C;
-        mp.HPB = HG / C;
-        int off = 0;
-        mp.off_ring = off;                          // two-box stages (1024-aligned boxes)
-        off += kMlaStages * cfa::kMlaStageBytes;
-        mp.off_qb = off;                            // 9 swizzled [32 x 64] query atoms (hi, lo)
-        off += cfa::kMlaBoxes * cfa::kMlaQAtomBytes;
-        mp.off_pb = off;                            // P of two tiles: 2 x 2 atoms [16 heads x 64 rows]
-        off += 4 * cfa::kMlaAtomBytes;
-        mp.off_qt = off;                            // fp32 queries [HG][576], then
-        mp.off_recv = off;                          // partials of my heads [HPB][C][516]
-        off += align_up(std::max(HG * cfa::kMlaRow, mp.HPB * mp.C * (cfa::kMlaKv + 4)) * 4, 128);
-        mp.off_newrow = off;
-        off += align_up(cfa::kMlaRow * 2, 128);
-        mp.off_stat = off;                          // m, l, 2 alpha, 2 x two [8][16] reductions, new row
-        off += align_up(592 * 4, 128);
-        mp.off_ofin = off;                          // combined latent outputs [HPB][512]
-        off += align_up(mp.HPB * cfa::kMlaKv * 4, 128);
-        mp.off_scr = off;
-        off += align_up((cfa::kComputeWarps * cfa::kMlaV + 64) * 4, 128);
-        mp.off_bars = off;
-        off += 16 * kMlaStages + 128;
-        return off;
-    };
+    auto layout = [&](int C) { return mla_layout(mp, C); };
     const void *kernel = cfa::mla_kernel_ptr(HG);
     if (!kernel ||
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin) !=
@@ -950,12 +963,15 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
         fail(CFA_ERR_UNSUPPORTED);
         return nullptr;
     }
-    // Cluster size: the largest C (blocks per head group, each finishing HG / C
-    // heads) whose clusters all fit on the GPU at once. A 16-block cluster
-    // needs 16 SMs of one GPC, and not every GPC has them.
+    // Cluster size C (blocks per head group, each finishing HG / C heads) and
+    // row splits S (clusters per head group, each taking 1/S of the latent
+    // rows): the most blocks per head group, C S, whose clusters all fit on
+    // the GPU at once, the larger C on a tie (a 16-block cluster needs 16 SMs
+    // of one GPC, and not every GPC has them). Failing that, the largest C
+    // that runs at all, unsplit.
     {
-        const int n_clusters = B * (n_heads / HG);
-        int chosen = 0, chosen_fit = 0;
+        const int n_groups = B * (n_heads / HG);
+        int chosen = 0, chosen_s = 1, chosen_fit = 0, fallback = 0, fallback_fit = 0;
         for (int C = HG; C >= 2; C /= 2) {
             if (layout(C) > dev.smem_optin) continue;
             cudaLaunchAttribute attr[1];
@@ -964,7 +980,7 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(n_clusters * C);
+            cfg.gridDim = dim3(n_groups * C);
             cfg.blockDim = dim3(cfa::kMlaThreads);
             cfg.dynamicSmemBytes = static_cast<size_t>(layout(C));
             cfg.attrs = attr;
@@ -975,15 +991,23 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
                 continue;
             }
             if (clusters < 1) continue;
-            if (!chosen) {
-                chosen = C;
-                chosen_fit = clusters;
+            m->fit_clusters[__builtin_ctz(static_cast<unsigned>(C)) - 1] = clusters;
+            if (!fallback) {
+                fallback = C;
+                fallback_fit = clusters;
             }
-            if (clusters >= n_clusters) {
-                chosen = C;
-                chosen_fit = clusters;
-                break;
-            }
+            for (int S = kMlaMaxSplits; S >= 1; --S)
+                if (clusters >= n_groups * S && C * S > chosen * chosen_s) {
+                    chosen = C;
+                    chosen_s = S;
+                    chosen_fit = clusters;
+                    break;
+                }
+        }
+        if (!chosen) {
+            chosen = fallback;
+            chosen_s = 1;
+            chosen_fit = fallback_fit;
         }
         if (!chosen) {
             delete m;
@@ -992,6 +1016,7 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
         }
         m->smem = layout(chosen);
         m->coresident_clusters = chosen_fit;
+        mp.S = chosen_s;
     }
 
     const size_t nwords = static_cast<size_t>(m->ga.gp.n_tiles + m->gq.gp.n_tiles +
@@ -1002,7 +1027,11 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
         cudaMalloc(&m->v, 2u * static_cast<size_t>(B) * NV) != cudaSuccess ||
         cudaMalloc(&m->partials, sizeof(float) * pf) != cudaSuccess ||
         cudaMalloc(&m->words, sizeof(unsigned) * nwords) != cudaSuccess ||
-        cudaMemset(m->words, 0, sizeof(unsigned) * nwords) != cudaSuccess) {
+        cudaMemset(m->words, 0, sizeof(unsigned) * nwords) != cudaSuccess ||
+        cudaMalloc(&m->vpart, sizeof(float) * static_cast<size_t>(B) * n_heads * kMlaMaxSplits *
+                                  cfa::kMlaSplitRec) != cudaSuccess ||
+        cudaMalloc(&m->vcount, sizeof(unsigned) * static_cast<size_t>(B) * n_heads) != cudaSuccess ||
+        cudaMemset(m->vcount, 0, sizeof(unsigned) * static_cast<size_t>(B) * n_heads) != cudaSuccess) {
         cudaGetLastError();
         mla_free(m);
         delete m;
@@ -1088,6 +1117,8 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
     mp.W_kvb = static_cast<const uint16_t *>(W_kvb);
     mp.cache = static_cast<uint16_t *>(cache);
     mp.v = m->v;
+    mp.vpart = m->vpart;
+    mp.vcount = m->vcount;
     mp.status = gst + 1;
     mp.eps = eps;
     for (int b = 0; b < m->B; ++b) mp.ctx_lens[b] = ctx_lens[b];
@@ -1103,7 +1134,7 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(m->B * (m->nh / mp.HG) * mp.C);
+        cfg.gridDim = dim3(m->B * (m->nh / mp.HG) * mp.S * mp.C);
         cfg.blockDim = dim3(cfa::kMlaThreads);
         cfg.dynamicSmemBytes = static_cast<size_t>(m->smem);
         cfg.stream = cs;
@@ -1121,6 +1152,20 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
     return CFA_OK;
 }
 
+cfa_status cfa_mla_set_row_splits(cfa_mla *m, int splits) {
+    if (!m || splits < 1 || splits > kMlaMaxSplits) return fail(CFA_ERR_INVALID_ARG);
+    // the largest cluster size whose split grid is resident at once
+    const int n_groups = m->B * (m->nh / m->mp.HG);
+    int C = m->mp.HG;
+    while (C >= 2 && m->fit_clusters[__builtin_ctz(static_cast<unsigned>(C)) - 1] < n_groups * splits) C /= 2;
+    if (C < 2) return fail(CFA_ERR_UNSUPPORTED);
+    cudaDeviceSynchronize();  // no launch of the old configuration may still use the counters
+    m->smem = mla_layout(m->mp, C);
+    m->coresident_clusters = m->fit_clusters[__builtin_ctz(static_cast<unsigned>(C)) - 1];
+    m->mp.S = splits;
+    return CFA_OK;
+}
+
 cfa_status cfa_mla_status(cfa_mla *m) {
     if (!m) return fail(CFA_ERR_INVALID_ARG);
     cfa_status a = read_status(mla_gemv_status(m));
@@ -1133,11 +1178,11 @@ cfa_status cfa_mla_describe(const cfa_mla *m, char *buf, int len) {
     if (!m || !buf || len < 1) return fail(CFA_ERR_INVALID_ARG);
     std::snprintf(buf, static_cast<size_t>(len),
                   "{\"B\": %d, \"hidden\": %d, \"n_heads\": %d, \"q_lora\": %d, \"max_ctx\": %d, "
-                  "\"heads_per_cluster\": %d, \"cluster_size\": %d, \"grid\": %d, "
-                  "\"smem_bytes\": %d, \"stages\": %d, \"coresident_clusters\": %d, "
+                  "\"heads_per_cluster\": %d, \"cluster_size\": %d, \"row_splits\": %d, "
+                  "\"grid\": %d, \"smem_bytes\": %d, \"stages\": %d, \"coresident_clusters\": %d, "
                   "\"gemv_grids\": [%d, %d, %d]}",
-                  m->B, m->H, m->nh, m->q_lora, m->max_ctx, m->mp.HG, m->mp.C,
-                  m->B * (m->nh / m->mp.HG) * m->mp.C, m->smem, m->mp.nstages,
+                  m->B, m->H, m->nh, m->q_lora, m->max_ctx, m->mp.HG, m->mp.C, m->mp.S,
+                  m->B * (m->nh / m->mp.HG) * m->mp.S * m->mp.C, m->smem, m->mp.nstages,
                   m->coresident_clusters, m->ga.gp.nblocks, m->gq.gp.nblocks, m->go.gp.nblocks);
     return CFA_OK;
 }

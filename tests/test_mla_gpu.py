@@ -46,7 +46,7 @@ def check_close(name, got, ref, rel=REL_L2, max_abs=MAX_ABS):
         f"{name}: rel L2 {e_rel:.3e} (<= {rel}), max abs {e_abs:.3e} (<= {max_abs})")
 
 
-def run_mla(cfa, oracle, wl, lens, seed=1, theta=THETA):
+def run_mla(cfa, oracle, wl, lens, seed=1, theta=THETA, splits=None):
     t = workloads.make_mla_inputs(wl, seed=seed, device="cpu")
     # NaN past each sequence's own position
     for b, L in enumerate(lens):
@@ -55,6 +55,8 @@ def run_mla(cfa, oracle, wl, lens, seed=1, theta=THETA):
     cache_before = dev["cache"].clone()
     out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
     mla = cfa.Mla(wl.B, wl.hidden, wl.n_heads, wl.q_lora, wl.max_ctx)
+    if splits is not None:
+        mla.set_row_splits(splits)
     mla.step(dev["x"], dev, dev["cache"], lens, out, theta, EPS)
     torch.cuda.synchronize()
     assert mla.status() == cfa.CFA_OK
@@ -93,6 +95,33 @@ def test_mla_many_heads_per_block(cfa, oracle):
     assert d["coresident_clusters"] >= d["grid"] // d["cluster_size"]
 
 
+@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("B,H,nh,ql,L", [(1, 512, 16, 128, 300), (2, 256, 4, 128, 0),
+                                         (3, 1024, 32, 256, 77), (1, 256, 2, 64, 1)])
+def test_mla_row_splits(cfa, oracle, B, H, nh, ql, L, splits):
+    """One or two clusters per (sequence, head group), each over its share of
+    the latent rows, the later of two combining them in split order: ctx 0
+    (the first split has no rows), ctx 1, ragged lengths across sequences."""
+    wl = workloads.custom_mla(B, H, nh, ql, L)
+    lens = [max(0, L - 5 * b) for b in range(B)]
+    mla, dev, out, _ = run_mla(cfa, oracle, wl, lens, seed=20 + B + L, splits=splits)
+    assert mla.describe()["row_splits"] == splits
+    first = out.clone()
+    for _ in range(2):  # the split counters are reset by the combining block
+        mla.step(dev["x"], dev, dev["cache"], lens, out, THETA, EPS)
+    torch.cuda.synchronize()
+    assert mla.status() == cfa.CFA_OK
+    assert torch.equal(first.view(torch.int16), out.view(torch.int16))
+
+
+def test_mla_rejects_bad_row_splits(cfa):
+    mla = cfa.Mla(1, 256, 4, 128, 64)
+    with pytest.raises(cfa.CfaError):
+        mla.set_row_splits(3)
+    with pytest.raises(cfa.CfaError):
+        mla.set_row_splits(0)
+
+
 def test_mla_without_rope(cfa, oracle):
     wl = workloads.custom_mla(1, 512, 16, 128, 300)
     run_mla(cfa, oracle, wl, [300], seed=9, theta=0.0)
@@ -104,6 +133,7 @@ def test_mla_v3_shape(cfa, oracle):
     wl = workloads.MLAS["mla_v3_b1_ctx4k"]
     mla, _, _, _ = run_mla(cfa, oracle, wl, list(wl.lens), seed=3)
     d = mla.describe()
+    print(d)
     assert d["heads_per_cluster"] == 16
     # every cluster of the grid is resident at once
     assert d["coresident_clusters"] >= d["grid"] // d["cluster_size"]
