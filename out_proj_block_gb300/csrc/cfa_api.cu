@@ -155,8 +155,11 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     const int sm_recv = C * B * (D + 4) * 4;
     const int qkv_full = B * (3 * D + 1) * 4;
     const int attn = B * D * 4;
-    const int scratch = std::max(mma ? 0 : cfa::kComputeWarps * B * cfa::kTileCols * 4,
-                                 (cfa::kComputeWarps * D + 2 * cfa::kComputeWarps) * 4);
+    // scratch: CUDA-core GEMV reductions; the attention warp states; on the
+    // tensor-core path also the second halves of the V accumulator [64][16]
+    const int scratch = std::max({mma ? cfa::kTileCols * cfa::kMmaN * 4 : 0,
+                                  mma ? 0 : cfa::kComputeWarps * B * cfa::kTileCols * 4,
+                                  (cfa::kComputeWarps * D + 2 * cfa::kComputeWarps) * 4});
     // Stages of x ring needed to hold attn and its hi/lo operand (tensor-core
     // path; 0 = never alias).
     const int alias_stages = mma ? (align_up(attn, 1024) + attn_t + xstage - 1) / xstage : 0;
@@ -225,15 +228,15 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.nA = R / TRA;
     k.n_qk = mma ? R / 64 : 0;
     k.n_v = mma ? R / 128 : 0;
-    // TMEM: 32 columns for the projection accumulators; the out-projection
-    // keeps up to 16 tile accumulators of 32 columns (hi and lo halves).
-    // Blocks that share an SM must fit its 512 columns together.
-    unsigned cols = 32;
+    // TMEM: 48 columns for the projection accumulators ([Q|K] 16, V 32); the
+    // out-projection keeps up to 16 tile accumulators of 32 columns (hi and lo
+    // halves). Blocks that share an SM must fit its 512 columns together.
+    unsigned cols = 64;
     if (mma) {
         const int want = std::min(ncols / cfa::kTileCols, 16) * 2 * cfa::kMmaN;
         while (static_cast<int>(cols) < want) cols <<= 1;
         const int resident = std::max(blocks_per_sm, (pl->smem_per_sm) / (off + pl->smem_reserved));
-        while (cols > 32 && static_cast<int>(cols) * resident > 512) cols >>= 1;
+        while (cols > 64 && static_cast<int>(cols) * resident > 512) cols >>= 1;
     }
     k.tmem_cols = cols;
     k.ncols = ncols;

@@ -330,11 +330,14 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         };
         if constexpr (MMA) {
             const uint32_t idesc = umma_idesc_bf16(128, kMmaN, true, false);
+            const uint32_t idesc_v = umma_idesc_bf16(128, 2 * kMmaN, true, false);
             const uint32_t ring_a = smem_addr(smem);
             const uint32_t xring_a = smem_addr(smem + p.off_xring);
             // Accumulator rows m (TMEM lanes) are weight columns: [Q | K] rows
-            // 0..63 / 64..127, V rows 0..63 (64..127 repeat them); columns are
-            // batch rows. Read back by the warps that own those lanes.
+            // 0..63 / 64..127; columns are batch rows. The V accumulator holds
+            // the stages' first halves in rows 0..63, columns 0..15 and their
+            // second halves in rows 64..127, columns 16..31. Read back by the
+            // warps that own those lanes.
             auto read_acc = [&](uint32_t col, int nwarps, int sec_of_row64) {
                 mbar_wait_bounded<false>(bar_acc_a, col == kAccQK ? 0u : 1u, p.timeout_ns, timed_out,
                                          p.status, kSiteStageFull);
@@ -364,14 +367,14 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                 umma_bf16(tmem + kAccQK, umma_smem_desc(a0 + j * 2048, kStageBytes / 2, 1024),
                                           umma_smem_desc(b0 + j * 32, 16, 1024), idesc, i > 0 || j > 0);
                         } else {
+                            // The stage's two 64-row halves of V side by side: A rows
+                            // 64..127 are the second half's rows, B rows 16..31 its
+                            // x rows (N = 32); the products of one half with the
+                            // other's x land in accumulator quadrants never read.
 #pragma unroll
-                            for (int half = 0; half < 2; ++half)
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    umma_bf16(tmem + kAccV,
-                                              umma_smem_desc(a0 + half * (kStageBytes / 2) + j * 2048, 0, 1024),
-                                              umma_smem_desc(b0 + half * (kXStageMma / 2) + j * 32, 16, 1024),
-                                              idesc, i > p.n_qk || half > 0 || j > 0);
+                            for (int j = 0; j < 4; ++j)
+                                umma_bf16(tmem + kAccV, umma_smem_desc(a0 + j * 2048, kStageBytes / 2, 1024),
+                                          umma_smem_desc(b0 + j * 32, 16, 1024), idesc_v, i > p.n_qk || j > 0);
                         }
                         if (i == p.n_qk - 1 || i == n_a - 1) umma_commit(bar_acc_a);
                     }
@@ -385,7 +388,29 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     push_sections(0, 2, bar_qk);  // the q/k exchange overlaps the V stages
                 }
             }
-            read_acc(kAccV, 2, 2);
+            {  // v = first halves + second halves (through shared memory)
+                mbar_wait_bounded<false>(bar_acc_a, 1u, p.timeout_ns, timed_out, p.status, kSiteStageFull);
+                tcgen05_fence_after();
+                float *hv = scratch;  // [64 columns][16 batch rows]
+                if (warp >= 2 && warp < 4) {
+                    float v[16];
+                    tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kAccV + kMmaN, v);
+                    const int c = 32 * (warp - 2) + lane;
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b) hv[c * kMmaN + b] = v[b];
+                }
+                compute_bar<kComputeThreads>();
+                if (warp < 2) {
+                    float v[16];
+                    tmem_ld_x16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + kAccV, v);
+                    const int c = 32 * warp + lane;
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b)
+                        if (b < B) my_qkv[(b * 3 + 2) * kTileCols + c] = v[b] + hv[c * kMmaN + b];
+                }
+                tcgen05_fence_before();
+                compute_bar<kComputeThreads>();
+            }
             push_sections(2, 1, bar_v);  // the v exchange overlaps attention
         } else {
             const uint16_t *xrows = reinterpret_cast<const uint16_t *>(smem + p.off_xring);  // [B][R]
