@@ -132,12 +132,14 @@ cfa_status cfa_decode_step_ex(cfa_plan *plan, const void *x, const void *W_qkv,
 
 /*
  * The same step for a caller whose token activations live in host memory:
- * copies x_host (bf16 [B, hidden]) to the plan's device staging buffer,
- * runs cfa_decode_step on `stream`, copies the result back to out_host
+ * moves x_host (bf16 [B, hidden]) to the plan's device staging buffer,
+ * runs cfa_decode_step on `stream`, moves the result back to out_host
  * (bf16 [B, hidden]) and synchronizes `stream` before returning. Weights and
- * caches stay device pointers. Host buffers should be pinned
- * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously;
- * pageable memory works but is slower. Errors as cfa_decode_step.
+ * caches stay device pointers. Page-locked, device-mapped host buffers
+ * (cudaHostAlloc / cudaHostRegister, 16-byte aligned) are read and written
+ * by small copy kernels launched around the step (no DMA transfer); other
+ * host memory goes through cudaMemcpyAsync and is slower. Errors as
+ * cfa_decode_step.
  */
 cfa_status cfa_decode_step_host(cfa_plan *plan, const void *x_host, const void *W_qkv,
                                 const void *W_o, void *k_cache, void *v_cache,

@@ -21,6 +21,7 @@ const void *fused_kernel_d128(int maxb);
 const void *fused_kernel_d64(int maxb);
 const void *selftest_wait_kernel_ptr();
 const void *head_merge_kernel_ptr();
+const void *copy16_kernel_ptr();
 }  // namespace cfa
 
 using cfa::KernelParams;
@@ -611,6 +612,41 @@ cfa_status cfa_decode_step_ex(cfa_plan *pl, const void *x, const void *W_qkv, co
     return launch_step(pl, x, W_qkv, W_o, k_cache, v_cache, ctx_lens, rope_theta, out, stream);
 }
 
+namespace {
+
+// Device address of page-locked host memory the GPU can access (cudaHostAlloc,
+// cudaHostRegister), or null for other host memory.
+void *mapped_host_ptr(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// copy16_kernel of `bytes` (a multiple of 16) on the stream, overlapping its
+// neighbours when the plan allows it.
+cudaError_t launch_copy16(const void *src, void *dst, size_t bytes, bool overlap, cudaStream_t s) {
+    const int n16 = static_cast<int>(bytes / 16);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min((n16 + 255) / 256, 152), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    const uint4 *in = static_cast<const uint4 *>(src);
+    uint4 *out = static_cast<uint4 *>(dst);
+    int n = n16;
+    void *args[3] = {&in, &out, &n};
+    return cudaLaunchKernelExC(&cfg, cfa::copy16_kernel_ptr(), args);
+}
+
+}  // namespace
+
 cfa_status cfa_decode_step_host(cfa_plan *pl, const void *x_host, const void *W_qkv,
                                 const void *W_o, void *k_cache, void *v_cache, int ctx_len,
                                 void *out_host, void *stream) {
@@ -618,6 +654,24 @@ cfa_status cfa_decode_step_host(cfa_plan *pl, const void *x_host, const void *W_
     if (ctx_len < 0 || ctx_len >= pl->max_ctx) return fail(CFA_ERR_INVALID_ARG);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t act = 2u * static_cast<size_t>(pl->B) * pl->H;
+    // Page-locked, device-mapped buffers: the GPU reads x and writes out itself
+    // (a copy kernel on each side of the step), with no DMA transfer to set up.
+    void *x_dev = mapped_host_ptr(x_host), *out_dev = mapped_host_ptr(out_host);
+    if (x_dev && out_dev && aligned16(x_dev) && aligned16(out_dev)) {
+        if (launch_copy16(x_dev, pl->x_stage, act, pl->overlap, s) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(CFA_ERR_CUDA);
+        }
+        const cfa_status st =
+            cfa_decode_step(pl, pl->x_stage, W_qkv, W_o, k_cache, v_cache, ctx_len, pl->out_stage, s);
+        if (st != CFA_OK) return st;
+        if (launch_copy16(pl->out_stage, out_dev, act, pl->overlap, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(CFA_ERR_CUDA);
+        }
+        return CFA_OK;
+    }
     if (cudaMemcpyAsync(pl->x_stage, x_host, act, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);

@@ -17,6 +17,20 @@ const void *fused_kernel_d128(int maxb) {
 
 const void *head_merge_kernel_ptr() { return reinterpret_cast<const void *>(&head_merge_kernel); }
 
+// Copies n16 16-byte words src -> dst: the host entry point's transfer of x
+// from, and of out to, device-mapped pinned host memory (zero-copy). Runs
+// between the fused kernel's neighbours on the stream with programmatic
+// dependent launch: it waits for the previous kernel before touching memory.
+__global__ void __launch_bounds__(256) copy16_kernel(const uint4 *__restrict__ src,
+                                                     uint4 *__restrict__ dst, int n16) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+const void *copy16_kernel_ptr() { return reinterpret_cast<const void *>(&copy16_kernel); }
+
 // Exercises mbar_wait_bounded on a barrier nothing arrives on.
 __global__ void selftest_wait_kernel(unsigned *status, unsigned long long timeout_ns) {
     __shared__ __align__(8) uint64_t bar;

@@ -214,12 +214,17 @@ def test_cluster_size_does_not_change_result_beyond_rounding(cfa):
         assert rel_l2(res[C], res[2]) < 5e-3
 
 
-def test_host_entry_point_matches_device(cfa):
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_entry_point_matches_device(cfa, pinned):
+    """Pinned host buffers take the zero-copy path (copy kernels), pageable
+    ones the cudaMemcpyAsync path; both equal the device entry point."""
     wl = workloads.custom(3, 1024, 8, 128, 200, max_ctx=256)
     t = workloads.make_inputs(wl, seed=7, device="cuda")
     out_dev = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
-    x_host = t["x"].cpu().pin_memory()
-    out_host = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16).pin_memory()
+    x_host = t["x"].cpu()
+    out_host = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16)
+    if pinned:
+        x_host, out_host = x_host.pin_memory(), out_host.pin_memory()
     with cfa.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx) as plan:
         plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"],
                          wl.ctx_len, out_dev)
