@@ -45,10 +45,12 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_plan_entry_point_twice(lib):
+@pytest.mark.parametrize("B,L", [(2, 300), (16, 100)])
+def test_noalloc_matches_plan_entry_point_twice(lib, B, L):
+    """B = 16 merges the heads in the separate merge kernel."""
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
-    wl = workloads.custom(2, 2048, 16, 128, 300, max_ctx=320)
+    wl = workloads.custom(B, 2048, 16, 128, L, max_ctx=320)
     t = workloads.make_inputs(wl, seed=70, device="cuda")
     ref_out = torch.empty(wl.B, wl.hidden, dtype=torch.bfloat16, device="cuda")
     with lib.Plan(wl.B, wl.hidden, wl.n_heads, wl.head_dim, wl.max_ctx) as plan:
