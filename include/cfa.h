@@ -396,11 +396,11 @@ cfa_status cfa_stack_describe(const cfa_stack *stack, char *buf, int len);
  * rope is the rotate-half form of cfa_decode_step_ex over the 64 rope dims
  * (rope_theta 0 disables it); rmsnorm as cfa_rmsnorm. The attention runs in
  * absorbed form (q_nope folded into W_k, values projected after the sum), one
- * thread-block cluster per (sequence, group of 16 heads) -- or two, each over
- * half of the latent rows ("row splits", §5.2's cache partitioned across
- * clusters) when that grid still fits on the GPU at once; the later of the
- * two to finish combines them in split order, so results stay bitwise
- * reproducible.
+ * thread-block cluster per (sequence, group of 16 heads) -- or two or four,
+ * each over its share of the latent rows ("row splits", §5.2's cache
+ * partitioned across clusters), chosen per step when that grid still fits on
+ * the GPU at once; the last of them to finish combines them in split order,
+ * so a given shape's results are bitwise reproducible.
  * ========================================================================== */
 
 typedef struct cfa_mla cfa_mla; /* opaque */
@@ -435,9 +435,12 @@ cfa_status cfa_mla_status(cfa_mla *mla);
 cfa_status cfa_mla_describe(const cfa_mla *mla, char *buf, int len);
 
 /*
- * Override the number of row splits (1 or 2 clusters per sequence and head
- * group) chosen at creation; the cluster size becomes the largest whose grid
- * then fits on the GPU at once. Synchronizes the device first.
+ * Fix the number of row splits (1, 2 or 4 clusters per sequence and head
+ * group, each over its share of the latent rows) for every later step; the
+ * cluster size becomes the largest whose grid then fits on the GPU at once.
+ * 0 restores the default, a choice per step: of the shapes that fit at once,
+ * the one with the least estimated attention time for the step's longest
+ * sequence (long contexts split further). Synchronizes the device first.
  * CFA_ERR_INVALID_ARG for other values; CFA_ERR_UNSUPPORTED if no cluster size
  * fits.
  */

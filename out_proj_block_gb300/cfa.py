@@ -652,8 +652,9 @@ class Mla:
         return cfa_mla_describe(self.handle)
 
     def set_row_splits(self, splits: int):
-        """1 or 2 clusters per (sequence, head group), each over its share of
-        the latent rows; raises CfaError if that grid does not fit at once."""
+        """1, 2 or 4 clusters per (sequence, head group), each over its share of
+        the latent rows (0: chosen per step); raises CfaError if that grid does
+        not fit at once."""
         st = cfa_mla_set_row_splits(self.handle, splits)
         if st != CFA_OK:
             raise CfaError(st, "cfa_mla_set_row_splits")

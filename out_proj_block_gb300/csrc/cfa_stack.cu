@@ -826,6 +826,7 @@ struct cfa_mla {
     int smem = 0;
     int coresident_clusters = 0;
     int fit_clusters[5] = {};     // clusters of C = 2, 4, 8, 16 blocks resident at once (0: no fit)
+    int forced_splits = 0;        // cfa_mla_set_row_splits; 0: chosen per step
 };
 
 namespace {
@@ -847,7 +848,8 @@ void mla_free(cfa_mla *m) {
     m->vcount = nullptr;
 }
 
-constexpr int kMlaMaxSplits = 2;
+constexpr int kMlaMaxSplits = 4;   // row splits cfa_mla_set_row_splits accepts
+constexpr int kMlaAutoSplits = 2;  // row splits the plan picks by itself
 
 // Shared memory of one attention block when a cluster has C blocks (HG / C
 // heads each); sets C, HPB and the offsets in mp, returns the bytes.
@@ -876,6 +878,40 @@ int mla_layout(cfa::MlaParams &mp, int C) {
     mp.off_bars = off;
     off += 16 * kMlaStages + 128;
     return off;
+}
+
+int mla_fit(const cfa_mla *m, int C) { return m->fit_clusters[__builtin_ctz(static_cast<unsigned>(C)) - 1]; }
+
+// Cluster size C and row splits S for a step whose longest sequence holds
+// max_len cached rows: of the shapes whose grid fits on the GPU at once, the
+// one with the least estimated attention-kernel time, 4.5 µs per head a block
+// finishes (absorption, combine, W_v projection) + 3.5 µs per 128-row tile of
+// its rows (the tile loop is bound by tensor-core instruction issue); both
+// figures measured on GB300 at the DeepSeek-V3 shape. Ties: the larger C,
+// then the fewer splits.
+void mla_choose(cfa_mla *m, int max_len) {
+    const int HG = m->mp.HG, n_groups = m->B * (m->nh / HG);
+    int best_c = 0, best_s = 1;
+    double best = 0.0;
+    for (int C = HG; C >= 2; C /= 2) {
+        if (mla_fit(m, C) < 1) continue;
+        for (int S = 1; S <= kMlaMaxSplits; S *= 2) {
+            if (mla_fit(m, C) < n_groups * S) break;
+            const double rows = std::ceil((max_len + 1.0) / (C * S));
+            const double cost = 4.5 * (HG / C) + 3.5 * std::ceil(rows / cfa::kMlaTileRows);
+            if (!best_c || cost < best - 1e-9) {
+                best = cost;
+                best_c = C;
+                best_s = S;
+            }
+        }
+    }
+    if (!best_c) return;  // keep the plan's configuration (a grid larger than one wave)
+    if (best_c != m->mp.C) {
+        m->smem = mla_layout(m->mp, best_c);
+        m->coresident_clusters = mla_fit(m, best_c);
+    }
+    m->mp.S = best_s;
 }
 
 unsigned *mla_gemv_status(cfa_mla *m) {
@@ -996,7 +1032,7 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
                 fallback = C;
                 fallback_fit = clusters;
             }
-            for (int S = kMlaMaxSplits; S >= 1; --S)
+            for (int S = kMlaAutoSplits; S >= 1; --S)
                 if (clusters >= n_groups * S && C * S > chosen * chosen_s) {
                     chosen = C;
                     chosen_s = S;
@@ -1110,6 +1146,11 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
     if ((st = launch_gemv(m->gq, pq, &tm_wuq, &tm_wuq, &m->tm_aq, cs)) != CFA_OK) return fail(st);
     ctr += m->gq.gp.n_tiles;
     // v: the latent attention core
+    if (!m->forced_splits) {
+        int max_len = 0;
+        for (int b = 0; b < m->B; ++b) max_len = std::max(max_len, ctx_lens[b]);
+        mla_choose(m, max_len);
+    }
     cfa::MlaParams mp = m->mp;
     mp.q = m->q;
     mp.a = m->a;
@@ -1153,16 +1194,22 @@ cfa_status cfa_mla_step(cfa_mla *m, const void *x, const void *W_a, const void *
 }
 
 cfa_status cfa_mla_set_row_splits(cfa_mla *m, int splits) {
-    if (!m || splits < 1 || splits > kMlaMaxSplits) return fail(CFA_ERR_INVALID_ARG);
+    if (!m || splits < 0 || splits > kMlaMaxSplits || (splits & (splits - 1)))
+        return fail(CFA_ERR_INVALID_ARG);
+    if (splits == 0) {  // back to the per-step choice
+        m->forced_splits = 0;
+        return CFA_OK;
+    }
     // the largest cluster size whose split grid is resident at once
     const int n_groups = m->B * (m->nh / m->mp.HG);
     int C = m->mp.HG;
     while (C >= 2 && m->fit_clusters[__builtin_ctz(static_cast<unsigned>(C)) - 1] < n_groups * splits) C /= 2;
     if (C < 2) return fail(CFA_ERR_UNSUPPORTED);
-    cudaDeviceSynchronize();  // no launch of the old configuration may still use the counters
+    cudaDeviceSynchronize();
     m->smem = mla_layout(m->mp, C);
-    m->coresident_clusters = m->fit_clusters[__builtin_ctz(static_cast<unsigned>(C)) - 1];
+    m->coresident_clusters = mla_fit(m, C);
     m->mp.S = splits;
+    m->forced_splits = splits;
     return CFA_OK;
 }
 

@@ -95,7 +95,7 @@ def test_mla_many_heads_per_block(cfa, oracle):
     assert d["coresident_clusters"] >= d["grid"] // d["cluster_size"]
 
 
-@pytest.mark.parametrize("splits", [1, 2])
+@pytest.mark.parametrize("splits", [1, 2, 4])
 @pytest.mark.parametrize("B,H,nh,ql,L", [(1, 512, 16, 128, 300), (2, 256, 4, 128, 0),
                                          (3, 1024, 32, 256, 77), (1, 256, 2, 64, 1)])
 def test_mla_row_splits(cfa, oracle, B, H, nh, ql, L, splits):
@@ -104,6 +104,13 @@ def test_mla_row_splits(cfa, oracle, B, H, nh, ql, L, splits):
     (the first split has no rows), ctx 1, ragged lengths across sequences."""
     wl = workloads.custom_mla(B, H, nh, ql, L)
     lens = [max(0, L - 5 * b) for b in range(B)]
+    probe = cfa.Mla(wl.B, wl.hidden, wl.n_heads, wl.q_lora, wl.max_ctx)
+    try:
+        probe.set_row_splits(splits)
+    except cfa.CfaError:
+        pytest.skip(f"{splits} row splits do not fit on this GPU for this shape")
+    finally:
+        probe.close()
     mla, dev, out, _ = run_mla(cfa, oracle, wl, lens, seed=20 + B + L, splits=splits)
     assert mla.describe()["row_splits"] == splits
     first = out.clone()
@@ -116,10 +123,31 @@ def test_mla_row_splits(cfa, oracle, B, H, nh, ql, L, splits):
 
 def test_mla_rejects_bad_row_splits(cfa):
     mla = cfa.Mla(1, 256, 4, 128, 64)
-    with pytest.raises(cfa.CfaError):
-        mla.set_row_splits(3)
-    with pytest.raises(cfa.CfaError):
-        mla.set_row_splits(0)
+    for bad in (3, 8, -1):
+        with pytest.raises(cfa.CfaError):
+            mla.set_row_splits(bad)
+    mla.set_row_splits(0)  # back to the per-step choice
+
+
+def test_mla_long_context_splits_rows(cfa):
+    """At ctx 16384 the per-step choice splits the latent rows over more
+    blocks; the result equals the unsplit one within rounding."""
+    wl = workloads.custom_mla(1, 512, 16, 128, 16384)
+    t = {k: v.cuda() for k, v in workloads.make_mla_inputs(wl, seed=31).items()}
+    outs, descs = [], []
+    for splits in (0, 1):
+        cache = t["cache"].clone()
+        out = torch.empty(1, wl.hidden, dtype=torch.bfloat16, device="cuda")
+        mla = cfa.Mla(1, wl.hidden, wl.n_heads, wl.q_lora, wl.max_ctx)
+        if splits:
+            mla.set_row_splits(splits)
+        mla.step(t["x"], t, cache, [16384], out, THETA, EPS)
+        torch.cuda.synchronize()
+        assert mla.status() == cfa.CFA_OK
+        outs.append(out.double().cpu().numpy())
+        descs.append(mla.describe())
+    assert descs[0]["row_splits"] > 1 and descs[1]["row_splits"] == 1
+    check_close("auto vs unsplit", outs[0], outs[1])
 
 
 def test_mla_without_rope(cfa, oracle):
