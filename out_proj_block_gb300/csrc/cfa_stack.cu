@@ -848,8 +848,7 @@ void mla_free(cfa_mla *m) {
     m->vcount = nullptr;
 }
 
-constexpr int kMlaMaxSplits = 4;   // row splits cfa_mla_set_row_splits accepts
-constexpr int kMlaAutoSplits = 2;  // row splits the plan picks by itself
+constexpr int kMlaMaxSplits = 4;   // row splits per head group
 
 // Shared memory of one attention block when a cluster has C blocks (HG / C
 // heads each); sets C, HPB and the offsets in mp, returns the bytes.
@@ -999,15 +998,15 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
         fail(CFA_ERR_UNSUPPORTED);
         return nullptr;
     }
-    // Cluster size C (blocks per head group, each finishing HG / C heads) and
-    // row splits S (clusters per head group, each taking 1/S of the latent
-    // rows): the most blocks per head group, C S, whose clusters all fit on
-    // the GPU at once, the larger C on a tie (a 16-block cluster needs 16 SMs
-    // of one GPC, and not every GPC has them). Failing that, the largest C
+    // How many clusters of each size C (blocks per head group, each finishing
+    // HG / C heads) fit on the GPU at once; a 16-block cluster needs 16 SMs of
+    // one GPC, and not every GPC has them. The shape of each step (C and the
+    // row splits S) is chosen from these by mla_choose; the initial one is
+    // that for a full cache, or, when no grid fits in one wave, the largest C
     // that runs at all, unsplit.
     {
         const int n_groups = B * (n_heads / HG);
-        int chosen = 0, chosen_s = 1, chosen_fit = 0, fallback = 0, fallback_fit = 0;
+        int fallback = 0;
         for (int C = HG; C >= 2; C /= 2) {
             if (layout(C) > dev.smem_optin) continue;
             cudaLaunchAttribute attr[1];
@@ -1028,31 +1027,17 @@ cfa_mla *cfa_mla_create(int B, int hidden, int n_heads, int q_lora, int max_ctx)
             }
             if (clusters < 1) continue;
             m->fit_clusters[__builtin_ctz(static_cast<unsigned>(C)) - 1] = clusters;
-            if (!fallback) {
-                fallback = C;
-                fallback_fit = clusters;
-            }
-            for (int S = kMlaAutoSplits; S >= 1; --S)
-                if (clusters >= n_groups * S && C * S > chosen * chosen_s) {
-                    chosen = C;
-                    chosen_s = S;
-                    chosen_fit = clusters;
-                    break;
-                }
+            if (!fallback) fallback = C;
         }
-        if (!chosen) {
-            chosen = fallback;
-            chosen_s = 1;
-            chosen_fit = fallback_fit;
-        }
-        if (!chosen) {
+        if (!fallback) {
             delete m;
             fail(CFA_ERR_UNSUPPORTED);
             return nullptr;
         }
-        m->smem = layout(chosen);
-        m->coresident_clusters = chosen_fit;
-        mp.S = chosen_s;
+        m->smem = layout(fallback);
+        m->coresident_clusters = mla_fit(m, fallback);
+        mp.S = 1;
+        mla_choose(m, max_ctx - 1);
     }
 
     const size_t nwords = static_cast<size_t>(m->ga.gp.n_tiles + m->gq.gp.n_tiles +
