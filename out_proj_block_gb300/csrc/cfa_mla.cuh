@@ -17,11 +17,12 @@
 // group share every latent byte, so the latent attention is a dense
 // contraction and runs on the tensor cores.
 //
-// Grid: B x (nh / HG) clusters of C blocks; cluster (b, g) owns heads
-// [g HG, (g+1) HG) of sequence b and block r of it owns the latent rows
-// [T r / C, T (r+1) / C) of T = L + 1 rows (the new token's row is the last).
-// C is the largest of 16, 8, 4, 2 for which every cluster of the grid is
-// resident at once; each block then finishes HPB = HG / C heads. Warps: 8
+// Grid: B x (nh / HG) x S clusters of C blocks; cluster (b, g, s) owns heads
+// [g HG, (g+1) HG) of sequence b and split s of the latent rows: its block r
+// attends rows [T q / (S C), T (q+1) / (S C)), q = s C + r, of T = L + 1 rows
+// (the new token's row is the last). C (16, 8, 4 or 2) and S (1, 2 or 4) are
+// chosen per step by the host among the shapes whose clusters are all
+// resident at once; each block finishes HPB = HG / C heads. Warps: 8
 // compute warps, a TMA warp streaming every operand through one ring of 32 KB
 // stages (W_k blocks, cache tiles, W_v blocks, in the order they are used),
 // and an MMA warp.
@@ -48,7 +49,10 @@
 //  C  Sparse ClusterReduce [CF §5.2]: a reduce-scatter over the cluster --
 //     block r receives, for its own HPB heads only, every block's (m, l, o),
 //     one bulk copy per head, and combines them in block order
-//     (deterministic); then v_h = o_h W_v,h.
+//     (deterministic); then v_h = o_h W_v,h. With S > 1 splits, block r of
+//     every split holds the same heads: each writes its v_h with its split's
+//     max and sum to global memory, and the last of them to arrive combines
+//     the S records in split order.
 #pragma once
 
 #include <cuda.h>
