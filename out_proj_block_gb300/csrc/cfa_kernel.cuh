@@ -737,21 +737,46 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             }
             if (group_n > 0) flush();
         } else {
-            const int rpw = D / kComputeWarps;
+            // A warp takes whole tiles (tile ct goes to warp ct % 8): all D rows
+            // of its 64 columns, summed within the warp, so no block barrier
+            // separates tiles. Every warp waits for each stage and releases it
+            // (the ring's phases stay in order); only the owner reads it.
+            const int cg = lane % GS::LPR, rq = lane / GS::LPR;
             for (int ct = 0; ct < n_out_tiles; ++ct) {
                 const int s = wait_full();
+                if (ct % kComputeWarps != warp) {
+                    release(s);
+                    continue;
+                }
                 float acc[MAXB][GS::CPL];
 #pragma unroll
                 for (int b = 0; b < MAXB; ++b)
 #pragma unroll
                     for (int c = 0; c < GS::CPL; ++c) acc[b][c] = 0.f;
-                gemv_tile<MAXB>(ring + s * kStageBytes, rpw, attn, D, B, warp, lane, acc);
+                gemv_tile<MAXB>(ring + s * kStageBytes, D, attn, D, B, 0, lane, acc);
                 release(s);
-                gemv_reduce<MAXB>(acc, B, warp, lane, tid, scratch,
-                                  p.partials + static_cast<size_t>(h) * head_stride + col0 +
-                                      ct * kTileCols,
-                                  H);
+                // the warp's row groups, in a fixed shuffle order
+#pragma unroll
+                for (int b = 0; b < MAXB; ++b)
+#pragma unroll
+                    for (int c = 0; c < GS::CPL; ++c)
+#pragma unroll
+                        for (int off = GS::LPR; off < 32; off <<= 1)
+                            acc[b][c] += __shfl_xor_sync(0xffffffffu, acc[b][c], off);
+                if (rq == 0) {
+                    float *dst = p.partials + static_cast<size_t>(h) * head_stride + col0 + ct * kTileCols +
+                                 cg * GS::CPL;
+#pragma unroll
+                    for (int b = 0; b < MAXB; ++b)
+                        if (b < B) {
+#pragma unroll
+                            for (int c = 0; c < GS::CPL; c += 4)
+                                *reinterpret_cast<float4 *>(dst + static_cast<size_t>(b) * H + c) =
+                                    make_float4(acc[b][c], acc[b][c + 1], acc[b][c + 2], acc[b][c + 3]);
+                        }
+                }
             }
+            compute_bar<kComputeThreads>();  // every tile's partials are stored
         }
 
         // ---- D: deterministic cross-head merge ----------------------------------
