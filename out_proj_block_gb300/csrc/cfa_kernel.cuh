@@ -796,55 +796,51 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             }
             compute_bar<kComputeThreads>();
             if (*is_last) {
-                // Items (b, 4 columns) are taken MI at a time with all their
-                // loads (up to 8 heads each) in flight; each sums its heads in
-                // ascending order.
-                constexpr int MI = MAXB >= 4 ? 2 : 1;
-                for (int idx0 = tid; idx0 < B * n4; idx0 += MI * kComputeThreads) {
-                    float4 sums[MI];
+                // Two threads per item (b, 4 columns): each sums half of the
+                // heads in ascending order, 8 loads in flight at a time, then
+                // half 0 + half 1.
+                const int half = tid & 1, hh = (p.nh + 1) / 2;
+                const int e0 = half * hh, e1 = min(p.nh, e0 + hh);
+                for (int base = 0; base < B * n4; base += kComputeThreads / 2) {
+                    const int idx = base + (tid >> 1);
+                    const bool valid = idx < B * n4;
+                    const int b = valid ? idx / n4 : 0;
+                    const int c = col0 + 4 * (valid ? idx % n4 : 0);
+                    const float *src = p.partials + static_cast<size_t>(b) * H + c;
+                    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i0 = e0; i0 < e1; i0 += 8) {
+                        float4 v[8];
 #pragma unroll
-                    for (int q = 0; q < MI; ++q) sums[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int i0 = 0; i0 < p.nh; i0 += 8) {
-                        float4 v[MI][8];
+                        for (int i = 0; i < 8; ++i)
+                            v[i] = valid && i0 + i < e1
+                                       ? __ldcg(reinterpret_cast<const float4 *>(src + (i0 + i) * head_stride))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                        for (int q = 0; q < MI; ++q) {
-                            const int idx = idx0 + q * kComputeThreads;
-                            const float *src = p.partials + static_cast<size_t>(idx / n4) * H + col0 + 4 * (idx % n4);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                v[q][i] = idx < B * n4 && i0 + i < p.nh
-                                              ? __ldcg(reinterpret_cast<const float4 *>(src + (i0 + i) * head_stride))
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int i = 0; i < 8; ++i) {
+                            sum.x += v[i].x;
+                            sum.y += v[i].y;
+                            sum.z += v[i].z;
+                            sum.w += v[i].w;
                         }
-#pragma unroll
-                        for (int q = 0; q < MI; ++q)
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                sums[q].x += v[q][i].x;
-                                sums[q].y += v[q][i].y;
-                                sums[q].z += v[q][i].z;
-                                sums[q].w += v[q][i].w;
-                            }
                     }
-#pragma unroll
-                    for (int q = 0; q < MI; ++q) {
-                        const int idx = idx0 + q * kComputeThreads;
-                        if (idx >= B * n4) continue;
-                        const int b = idx / n4;
-                        const int c = col0 + 4 * (idx % n4);
-                        float4 sum = sums[q];
-                        if (p.resid) {  // residual stream: out = resid + attention block
-                            const uint2 rv = *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
-                            sum.x += bf16_lo(rv.x);
-                            sum.y += bf16_hi(rv.x);
-                            sum.z += bf16_lo(rv.y);
-                            sum.w += bf16_hi(rv.y);
-                        }
-                        uint2 packed;
-                        packed.x = pack2_bf16(sum.x, sum.y);
-                        packed.y = pack2_bf16(sum.z, sum.w);
-                        *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
+                    float4 other;
+                    other.x = __shfl_xor_sync(0xffffffffu, sum.x, 1);
+                    other.y = __shfl_xor_sync(0xffffffffu, sum.y, 1);
+                    other.z = __shfl_xor_sync(0xffffffffu, sum.z, 1);
+                    other.w = __shfl_xor_sync(0xffffffffu, sum.w, 1);
+                    if (!valid || half) continue;
+                    sum = make_float4(sum.x + other.x, sum.y + other.y, sum.z + other.z, sum.w + other.w);
+                    if (p.resid) {  // residual stream: out = resid + attention block
+                        const uint2 rv = *reinterpret_cast<const uint2 *>(p.resid + static_cast<size_t>(b) * H + c);
+                        sum.x += bf16_lo(rv.x);
+                        sum.y += bf16_hi(rv.x);
+                        sum.z += bf16_lo(rv.y);
+                        sum.w += bf16_hi(rv.y);
                     }
+                    uint2 packed;
+                    packed.x = pack2_bf16(sum.x, sum.y);
+                    packed.y = pack2_bf16(sum.z, sum.w);
+                    *reinterpret_cast<uint2 *>(p.out + static_cast<size_t>(b) * H + c) = packed;
                 }
             }
         }
