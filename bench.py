@@ -14,9 +14,10 @@ value    = achieved HBM GB/s over the step's algorithmic bytes (both weights +
 e2e      = the same metric through the host-buffer C-ABI entry point
            (cfa_decode_step_host): every step copies x host->device, runs the
            kernel, copies out device->host and synchronizes.
-roofline = the fused kernel (the only kernel of a step) against the measured
+roofline = the fused kernel (the dominant kernel of a step) against the measured
            HBM copy bandwidth.
-cpu_baseline / --impl reference = the fp64 CPU oracle on the host cores.
+cpu_baseline / --impl reference = the fp64 CPU oracle on the host cores (cpu_baseline
+           at N = 1 only: under torchrun the line carries none).
 
 Inputs live in three rotating copies (each larger than the 129 MB L2), so no
 step reads what the previous step left in L2. Multi-GPU runs are independent
@@ -440,7 +441,7 @@ def run_ours(args):
             "kernel": "cfa::fused_decode_kernel"}
 
     cpu_base, parity = None, None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_inputs = {k: v.cpu() for k, v in copies[0].items()}
         cpu_base, ref = oracle_baseline(wl, cpu_inputs, args.cpu_seconds)
         step(0)  # recompute copy 0 so its output matches the oracle's inputs
@@ -664,7 +665,7 @@ def run_stack(args, wl):
             "kernel": f"whole token ({launches_per_token} kernels from one graph launch)"}
 
     cpu_base, parity = None, None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t_cpu = {"x": x.cpu(), "layers": [{k: v.cpu() for k, v in l.items()} for l in t["layers"]]}
         times, used, y_ref = stack_oracle_tokens(wl, t_cpu, args.cpu_seconds)
         tok_s = statistics.median(times)
@@ -849,7 +850,7 @@ def run_mla(args, wl):
             "kernel": "whole MLA step (4 kernels)",
             "attention_flops_per_step": wl.attention_flops}
     cpu_base, parity = None, None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t_cpu = {k: v.cpu() for k, v in t.items()}
         times, used, ref = mla_oracle_steps(wl, t_cpu, args.cpu_seconds)
         st_s = statistics.median(times)
