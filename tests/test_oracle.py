@@ -373,6 +373,70 @@ def test_rope_d2_is_a_plain_rotation(oracle, pos):
                                [x[0] * c - x[1] * s, x[1] * c + x[0] * s], rtol=0, atol=1e-15)
 
 
+# The frequency schedule of the rotate-half reading, omega_i = theta^(-2i/d),
+# fixed by angles written out in closed form (not by re-evaluating the
+# oracle's own expression): with theta = 10000 and d = 8 the frequencies are
+# exactly 10^-i, with d = 4 they are 1 and 10^-2. A schedule such as
+# theta^(-i/d), or one pairing i with d-1-i, gives other angles.
+ROPE_SCHEDULES = [
+    # (d, theta, pos, [angle of pair i])
+    (4, 10000.0, 1, [1.0, 0.01]),
+    (4, 10000.0, 250, [250.0, 2.5]),
+    (8, 10000.0, 4095, [4095.0, 409.5, 40.95, 4.095]),
+    (8, 10000.0, 1, [1.0, 0.1, 0.01, 0.001]),
+    (4, 500.0, 3, [3.0, 3.0 / math.sqrt(500.0)]),
+    (6, 1000.0, 7, [7.0, 0.7, 0.07]),
+]
+
+
+@pytest.mark.parametrize("d,theta,pos,angles", ROPE_SCHEDULES)
+def test_rope_frequency_schedule_closed_form(oracle, d, theta, pos, angles):
+    """Basis vector e_i goes to cos(a_i) e_i + sin(a_i) e_(i+d/2), and e_(i+d/2)
+    to -sin(a_i) e_i + cos(a_i) e_(i+d/2), with a_i = pos * theta^(-2i/d)."""
+    half = d // 2
+    for i, a in enumerate(angles):
+        e = np.zeros(d)
+        e[i] = 1.0
+        want = np.zeros(d)
+        want[i], want[i + half] = math.cos(a), math.sin(a)
+        np.testing.assert_allclose(oracle.rope(e, pos, theta), want, rtol=0, atol=1e-12)
+        e = np.zeros(d)
+        e[i + half] = 1.0
+        want = np.zeros(d)
+        want[i], want[i + half] = -math.sin(a), math.cos(a)
+        np.testing.assert_allclose(oracle.rope(e, pos, theta), want, rtol=0, atol=1e-12)
+
+
+def test_rope_frequency_schedule_head_dim_128(oracle):
+    """d = 128, theta = 10000: pair i turns by pos * 10^(-4i/64); pairs 16, 32
+    and 48 have the exact frequencies 10^-1, 10^-2 and 10^-3."""
+    d, pos = 128, 4095
+    for i, w in ((0, 1.0), (16, 0.1), (32, 0.01), (48, 0.001)):
+        e = np.zeros(d)
+        e[i] = 1.0
+        y = oracle.rope(e, pos, 10000.0)
+        assert y[i] == pytest.approx(math.cos(pos * w), abs=1e-11)
+        assert y[i + d // 2] == pytest.approx(math.sin(pos * w), abs=1e-11)
+
+
+def test_rope_in_the_step_rotates_by_the_closed_form_angle(oracle):
+    """Through decode_step_ex: one head, d = 4, the new key is x . W_k with
+    x = e_0 and W_k's row 0 = e_1, so k_new = R(L) e_1 = cos(0.01 L) e_1 +
+    sin(0.01 L) e_3 at theta = 10000 (pair 1's frequency is 10000^(-1/2))."""
+    B, H, nh, d, L = 1, 4, 1, 4, 37
+    t = rand_inputs(B, H, nh, d, L, 64, seed=45)
+    x = np.zeros((B, H), np.float32)
+    x[0, 0] = 1.0
+    W = np.zeros((H, 3 * H), np.float32)
+    W[0, H + 1] = 1.0
+    t["x"], t["W_qkv"] = bf16(x), bf16(W)
+    r = oracle.decode_step_ex(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], [L],
+                              rope_theta=10000.0)
+    a = 0.01 * L
+    np.testing.assert_allclose(r["k_new"][0, 0], [0.0, math.cos(a), 0.0, math.sin(a)],
+                               rtol=0, atol=1e-13)
+
+
 def test_rope_pairs_dimension_i_with_i_plus_half(oracle):
     """Rotate-half convention: basis vector e_i only mixes with e_{i+d/2}."""
     d = 16

@@ -165,3 +165,58 @@ def test_mla_brute_force_tiny(oracle):
     v = rb(o)
     want = [math.fsum(v[i] * Wo[i, j] for i in range(nh * V)) for j in range(H)]
     np.testing.assert_allclose(r["out"][0], want, rtol=1e-11, atol=1e-13)
+
+
+# The rotary frequencies of the 64 rope dims, omega_i = theta^(-2i/64), fixed
+# by closed-form angles: at theta = 10000, pairs 8, 16 and 24 have the exact
+# frequencies 10^-1, 10^-2 and 10^-3.
+MLA_ROPE_PAIRS = [(8, 0.1), (16, 0.01), (24, 0.001)]
+
+
+def _mla_zero_inputs(B, H, nh, q_lora, L, max_ctx):
+    t = mla_inputs(B, H, nh, q_lora, L, max_ctx, seed=60)
+    for k in ("x", "W_a", "W_uq", "W_kvb", "W_o", "cache"):
+        t[k] = torch.zeros_like(t[k])
+    t["g_q"] = torch.ones_like(t["g_q"])
+    t["g_kv"] = torch.ones_like(t["g_kv"])
+    return t
+
+
+@pytest.mark.parametrize("i,w", MLA_ROPE_PAIRS)
+@pytest.mark.parametrize("L", [1, 100, 4000])
+def test_mla_key_rope_turns_by_the_closed_form_angle(oracle, i, w, L):
+    """The new latent row's rope part is bf16(R(L) kr). With x = e_0 and W_a's
+    row 0 = e at rope dim i, kr = e_i, so the row holds bf16(cos(L w_i)) at
+    dim 512 + i and bf16(sin(L w_i)) at 512 + i + 32, zeros elsewhere."""
+    H, q_lora = 64, 16
+    t = _mla_zero_inputs(1, H, 1, q_lora, L, L + 1)
+    t["x"][0, 0] = 1.0
+    t["W_a"][0, q_lora + KV + i] = 1.0
+    r = run(oracle, t, [L])
+    a = L * w
+    want = np.zeros(ROW)
+    want[KV + i] = float(torch.tensor(math.cos(a)).to(torch.bfloat16))
+    want[KV + i + ROPE // 2] = float(torch.tensor(math.sin(a)).to(torch.bfloat16))
+    np.testing.assert_allclose(r["new_row"][0], want, rtol=0, atol=2.0 ** -9)
+
+
+@pytest.mark.parametrize("i,w", MLA_ROPE_PAIRS)
+def test_mla_query_rope_turns_by_the_closed_form_angle(oracle, i, w):
+    """The query's rope part is rotated at the new token's position L. Setup
+    (every other weight zero): q_rope = 8 e_i, q_nope = 0; cached row 0 holds
+    latent e_0 (its value decompresses to all ones) and rope key e_i; cached
+    rows 1..L-1 and the new row are zero. So the scores are
+    s_0 = 8 cos(L w_i) / sqrt(192) and 0 for the L others, and every value dim
+    of the head's output is e^(s_0) / (e^(s_0) + L)."""
+    H, nh, q_lora, L = 64, 1, 16, 100
+    t = _mla_zero_inputs(1, H, nh, q_lora, L, L + 1)
+    t["x"][0, 0] = 1.0
+    t["W_a"][0, 0] = 1.0          # a[0] = 1: cq = bf16(rmsnorm(e_0)) = 4 e_0 at q_lora 16
+    t["W_uq"][0, NOPE + i] = 2.0  # q_rope = bf16(4 * 2) e_i = 8 e_i
+    t["W_kvb"][0, NOPE:NOPE + V] = 1.0  # latent e_0 -> value of all ones
+    t["cache"][0, 0, 0] = 1.0
+    t["cache"][0, 0, KV + i] = 1.0
+    r = run(oracle, t, [L])
+    s0 = 8.0 * math.cos(L * w) / math.sqrt(NOPE + ROPE)
+    p0 = math.exp(s0) / (math.exp(s0) + L)
+    np.testing.assert_allclose(r["attn"][0], np.full(V, p0), rtol=1e-12)
