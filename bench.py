@@ -79,6 +79,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--preload-seconds", type=float, default=1.0,
                     help="untimed load before the timed region, for clock samples")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations timed after the default workload")
+    ap.add_argument("--config-steps", type=int, default=300,
+                    help="back-to-back steps timed for each other configuration")
     return ap.parse_args(argv)
 
 
@@ -235,11 +239,23 @@ def oracle_baseline(wl, cpu_inputs, budget_s: float, max_reps: int = 50):
         if time.perf_counter() - t_start >= budget_s:
             break
     step_s = statistics.median(times)
+    # The same oracle on one thread: three full steps, the median.
+    one = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        cfa_oracle.decode_step_ex(cpu_inputs["x"], cpu_inputs["W_qkv"], cpu_inputs["W_o"],
+                                  cpu_inputs["k_cache"], cpu_inputs["v_cache"], list(wl.lens),
+                                  rope_theta=wl.rope_theta, nthreads=1)
+        one.append(time.perf_counter() - t0)
+    one_s = statistics.median(one)
     return {"value": wl.algorithmic_bytes / step_s / 1e9, "unit": "GB/s", "cores": used,
             "kind": "oracle",
             "sample": f"{len(times)} full fp64 decode steps of {wl.name} "
                       f"(median {step_s * 1e3:.1f} ms per step)",
-            "step_ms": step_s * 1e3}, ref
+            "step_ms": step_s * 1e3,
+            "single_thread": {"value": wl.algorithmic_bytes / one_s / 1e9, "unit": "GB/s",
+                              "cores": 1, "step_ms": one_s * 1e3,
+                              "sample": "3 full fp64 decode steps on one thread, median"}}, ref
 
 
 # --------------------------------------------------------- reference arm
@@ -291,8 +307,137 @@ def run_reference(args):
 # ---------------------------------------------------------------- our arm
 
 
-def run_ours(args):
+SECONDARY_WORKLOADS = ("llama7b_b1_ctx1k", "llama7b_b16_ctx4k", "llama7b_b1_ctx16k_spiky",
+                       "hd64_b8_ctx2k")
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
+
+
+def _fused_plan_and_step(cfa, workloads, wl, dev, n_copies, cluster_size=None, stages=None):
+    """Inputs (n_copies rotating sets), a plan and a step(i, stream) callable."""
+    import torch
+    B, H = wl.B, wl.hidden
+    copies = [workloads.make_inputs(wl, seed=i, device=dev) for i in range(max(n_copies, 1))]
+    outs = [torch.empty(B, H, dtype=torch.bfloat16, device=dev) for _ in copies]
+    plan = cfa.Plan(B, H, wl.n_heads, wl.head_dim, wl.max_ctx,
+                    cluster_size=cluster_size, stages=stages)
+    uniform = wl.ctx_lens is None and wl.rope_theta == 0.0
+
+    def step(i, stream):
+        c = copies[i % len(copies)]
+        if uniform:
+            plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
+                             wl.ctx_len, outs[i % len(copies)], stream)
+        else:
+            plan.decode_step_ex(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
+                                list(wl.lens), outs[i % len(copies)], wl.rope_theta, stream)
+
+    return copies, outs, plan, step, uniform
+
+
+def _per_step_ms(step, n, stream, dev):
+    """n steps with an event recorded after each; per-step device times in ms."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    ev[0].record(stream)
+    for k in range(n):
+        step(k, stream)
+        ev[k + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    return [ev[k].elapsed_time(ev[k + 1]) for k in range(n)]
+
+
+def _back_to_back_s(step, K, stream, dev):
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for k in range(K):
+        step(k, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / 1e3
+
+
+def _kernel_only_ms(plan, step, n, stream, dev):
+    """Per-step device time with launch overlap off: each step starts only
+    after the previous kernel has finished, so an event pair brackets exactly
+    one step's kernels (the fused kernel, plus the head merge where the plan
+    uses one). Median of n samples; overlap is restored afterwards."""
+    plan.set_overlap(False)
+    try:
+        for k in range(3):
+            step(k, stream)
+        ms = _per_step_ms(step, n, stream, dev)
+    finally:
+        plan.set_overlap(True)
+    return ms
+
+
+def _parity_vs_oracle(wl, copy0, out0, step, stream, dev, nthreads):
+    """Copy 0's step recomputed on the GPU and compared with the fp64 oracle
+    (out and the appended K/V rows)."""
     import numpy as np
+    import torch
+    from oracle import cfa_oracle
+    cfa_oracle.build()
+    cpu = {k: v.cpu() for k, v in copy0.items()}
+    ref = cfa_oracle.decode_step_ex(cpu["x"], cpu["W_qkv"], cpu["W_o"], cpu["k_cache"],
+                                    cpu["v_cache"], list(wl.lens), rope_theta=wl.rope_theta,
+                                    nthreads=nthreads)
+    step(0, stream)
+    torch.cuda.synchronize(dev)
+    got = out0.double().cpu().numpy()
+    res = {"out_rel_l2": float(np.linalg.norm(got - ref["out"]) / np.linalg.norm(ref["out"])),
+           "out_max_abs": float(np.abs(got - ref["out"]).max())}
+    bidx = torch.arange(wl.B)
+    rows = torch.tensor(list(wl.lens))
+    for name, key in (("k_new", "k_cache"), ("v_new", "v_cache")):
+        g = copy0[key].cpu()[bidx, :, rows].double().numpy()
+        r = ref[name]
+        res[f"{name}_rel_l2"] = float(np.linalg.norm(g - r) / np.linalg.norm(r))
+        res[f"{name}_max_abs"] = float(np.abs(g - r).max())
+    return res
+
+
+def measure_secondary(cfa, workloads, name, dev, steps, peak, nthreads, with_parity):
+    """One more workload on the same GPU: back-to-back and kernel-only
+    per-step time, GB/s, roofline fractions and parity against the oracle."""
+    import torch
+    wl = workloads.WORKLOADS[name]
+    n_copies = max(2, -(-300_000_000 // wl.algorithmic_bytes))  # rotate > 2x the L2
+    copies, outs, plan, step, _ = _fused_plan_and_step(cfa, workloads, wl, dev, n_copies)
+    stream = torch.cuda.current_stream(dev)
+    try:
+        desc = plan.describe()
+        for k in range(10):
+            step(k, stream)
+        torch.cuda.synchronize(dev)
+        total_s = _back_to_back_s(step, steps, stream, dev)
+        kern = _kernel_only_ms(plan, step, 200, stream, dev)
+        if plan.status() != cfa.CFA_OK:
+            raise RuntimeError(f"{name}: device status after timing")
+        b2b_us = total_s / steps * 1e6
+        k_us = percentile(kern, 0.5) * 1e3
+        res = {"workload": name, "B": wl.B, "ctx_len": wl.ctx_len, "head_dim": wl.head_dim,
+               "n_heads": wl.n_heads, "cluster_size": desc["cluster_size"],
+               "stages": desc["stages"], "launches_per_step": desc["launches_per_step"],
+               "algorithmic_bytes": wl.algorithmic_bytes,
+               "us_per_step_back_to_back": b2b_us, "us_per_step_kernel_p50": k_us,
+               "gbs_back_to_back": wl.algorithmic_bytes / b2b_us / 1e3,
+               "gbs_kernel": wl.algorithmic_bytes / k_us / 1e3,
+               "frac_kernel": wl.algorithmic_bytes / k_us / 1e3 / peak,
+               "frac_pipelined": wl.algorithmic_bytes / b2b_us / 1e3 / peak,
+               "steps": steps, "kernel_samples": len(kern), "input_copies": n_copies}
+        if with_parity:
+            res["parity"] = _parity_vs_oracle(wl, copies[0], outs[0], step, stream, dev, nthreads)
+        return res
+    finally:
+        plan.close()
+        del copies, outs
+        torch.cuda.empty_cache()
+
+
+def run_ours(args):
     import torch
 
     world, rank, local = dist_env()
@@ -311,26 +456,13 @@ def run_ours(args):
 
     wl = workloads.WORKLOADS[args.workload]
     B, H = wl.B, wl.hidden
-    copies = [workloads.make_inputs(wl, seed=i, device=dev) for i in range(max(args.copies, 1))]
-    outs = [torch.empty(B, H, dtype=torch.bfloat16, device=dev) for _ in copies]
-    plan = cfa.Plan(B, H, wl.n_heads, wl.head_dim, wl.max_ctx,
-                    cluster_size=args.cluster_size, stages=args.stages)
+    copies, outs, plan, step, uniform = _fused_plan_and_step(
+        cfa, workloads, wl, dev, args.copies, args.cluster_size, args.stages)
     desc = plan.describe()
     stream = torch.cuda.current_stream(dev)
 
-    uniform = wl.ctx_lens is None and wl.rope_theta == 0.0
-
-    def step(i):
-        c = copies[i % len(copies)]
-        if uniform:
-            plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
-                             wl.ctx_len, outs[i % len(copies)], stream)
-        else:
-            plan.decode_step_ex(c["x"], c["W_qkv"], c["W_o"], c["k_cache"], c["v_cache"],
-                                list(wl.lens), outs[i % len(copies)], wl.rope_theta, stream)
-
     for i in range(max(args.warmup, 3)):
-        step(i)
+        step(i, stream)
     torch.cuda.synchronize(dev)
     st = plan.status()
     if st != cfa.CFA_OK:
@@ -341,42 +473,32 @@ def run_ours(args):
     i = 0
     while time.perf_counter() < t_end:  # untimed load so clocks settle and get sampled
         for _ in range(64):
-            step(i)
+            step(i, stream)
             i += 1
         torch.cuda.synchronize(dev)
 
     K = args.steps
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    e_start.record(stream)
-    for k in range(K):
-        step(k)
-    e_end.record(stream)
-    torch.cuda.synchronize(dev)
+    total_s = _back_to_back_s(step, K, stream, dev)
     if world > 1:
         torch.distributed.barrier()
+    # Kernel-only time (launch overlap off), at least 200 samples whatever K is.
+    n_kern = max(200, min(K, 2000))
+    kern_ms = _kernel_only_ms(plan, step, n_kern, stream, dev)
     clocks = sampler.stop()
-    total_s = e_start.elapsed_time(e_end) / 1e3
     st = plan.status()
     if st != cfa.CFA_OK:
         raise RuntimeError(f"device status after timing: {cfa.cfa_status_string(st)}")
 
-    # Per-step latency with an event between steps (steps cannot overlap here),
-    # untimed for the headline.
-    n_iso = min(K, 500)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso + 1)]
-    ev[0].record(stream)
-    for k in range(n_iso):
-        step(k)
-        ev[k + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    step_ms = [ev[k].elapsed_time(ev[k + 1]) for k in range(n_iso)]
+    # Per-step latency with overlap on and an event between steps (untimed for
+    # the headline).
+    n_iso = max(200, min(K, 500))
+    step_ms = _per_step_ms(step, n_iso, stream, dev)
     max_total_s = aggregate_max(total_s, world, dev)
     value = whole_job_gbs(wl.algorithmic_bytes, K, world, max_total_s)
     mean_step_s = total_s / K
-    achieved = wl.algorithmic_bytes / mean_step_s / 1e9
+    kernel_s = percentile(kern_ms, 0.5) / 1e3
 
     # CUDA-graph replay of the same steps (launch overhead removed)
     graph_us = None
@@ -387,15 +509,9 @@ def run_ours(args):
         with torch.cuda.stream(s2):
             with torch.cuda.graph(g, stream=s2):
                 for k in range(len(copies)):
-                    c = copies[k]
-                    if uniform:
-                        plan.decode_step(c["x"], c["W_qkv"], c["W_o"], c["k_cache"],
-                                         c["v_cache"], wl.ctx_len, outs[k], s2)
-                    else:
-                        plan.decode_step_ex(c["x"], c["W_qkv"], c["W_o"], c["k_cache"],
-                                            c["v_cache"], list(wl.lens), outs[k], wl.rope_theta, s2)
+                    step(k, s2)
         stream.wait_stream(s2)
-        reps = max(1, K // len(copies))
+        reps = max(1, max(K, 300) // len(copies))
         for _ in range(3):
             g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -434,23 +550,45 @@ def run_ours(args):
                "ms_per_step": e2e_s / K * 1e3}
 
     peak, peak_kind = measured_peaks()
+    achieved = wl.algorithmic_bytes / kernel_s / 1e9
+    achieved_pipe = wl.algorithmic_bytes / mean_step_s / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
             "traffic": recorded_traffic(wl.name, plan.cluster_size),
             "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
-            "kernel": "cfa::fused_decode_kernel"}
+            "kernel": "cfa::fused_decode_kernel",
+            "duration_us": kernel_s * 1e6,
+            "duration_source": f"median of {len(kern_ms)} single steps with launch overlap off, "
+                               "CUDA events on the launching stream"
+                               + ("; the step is this kernel plus the head-merge kernel"
+                                  if desc.get("launches_per_step", 1) > 1 else ""),
+            "achieved_pipelined": achieved_pipe, "frac_pipelined": achieved_pipe / peak,
+            "pipelined_note": "back-to-back steps whose launches overlap (programmatic "
+                              "dependent launch): the next step's prologue and first weight "
+                              "loads run under this step's tail",
+            "frac_vs_nominal": achieved / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS}
 
     cpu_base, parity = None, None
+    nthreads = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_inputs = {k: v.cpu() for k, v in copies[0].items()}
         cpu_base, ref = oracle_baseline(wl, cpu_inputs, args.cpu_seconds)
-        step(0)  # recompute copy 0 so its output matches the oracle's inputs
-        torch.cuda.synchronize(dev)
-        got = outs[0].float().cpu().numpy()
-        parity = {"out_rel_l2": float(np.linalg.norm(got - ref["out"]) / np.linalg.norm(ref["out"])),
-                  "out_max_abs": float(np.abs(got - ref["out"]).max())}
+        nthreads = cpu_base["cores"]
+        parity = _parity_vs_oracle(wl, copies[0], outs[0], step, stream, dev, nthreads)
 
     plan.close()
+    del copies, outs
+    torch.cuda.empty_cache()
+
+    # The other configurations of the block, after the headline.
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs and args.workload == DEFAULT_WORKLOAD:
+        configs = []
+        for name in SECONDARY_WORKLOADS:
+            configs.append(measure_secondary(cfa, workloads, name, dev, args.config_steps, peak,
+                                             nthreads or (os.cpu_count() or 1),
+                                             not args.no_cpu_baseline))
+
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": max_total_s / K * 1e3,
@@ -458,16 +596,22 @@ def run_ours(args):
         "data": "synthetic",
         "config": dict(wl.as_config(), cluster_size=desc["cluster_size"],
                        stages=desc["stages"], grid=desc["grid"],
-                       l2=f"{len(copies)} rotating input copies of "
+                       l2=f"{args.copies} rotating input copies of "
                           f"{wl.algorithmic_bytes / 1e6:.0f} MB each (> 129 MB L2)",
                        parallelism=f"replicas x{world}"),
         "latency_us": {"back_to_back_mean": mean_step_s * 1e6,
+                       "kernel_p10": percentile(kern_ms, 0.1) * 1e3,
+                       "kernel_p50": percentile(kern_ms, 0.5) * 1e3,
+                       "kernel_p90": percentile(kern_ms, 0.9) * 1e3,
+                       "kernel_samples": len(kern_ms),
                        "isolated_p10": percentile(step_ms, 0.1) * 1e3,
                        "isolated_p50": percentile(step_ms, 0.5) * 1e3,
                        "isolated_p90": percentile(step_ms, 0.9) * 1e3,
+                       "isolated_samples": len(step_ms),
                        "note": "back_to_back: K steps between two events (consecutive steps "
-                               "may overlap via programmatic dependent launch); isolated: an "
-                               "event recorded after every step"},
+                               "overlap via programmatic dependent launch); kernel: one step "
+                               "between two events with launch overlap off; isolated: an "
+                               "event after every step, overlap on"},
         "graph_latency_us": graph_us,
         "roofline": roof,
         "cpu_baseline": cpu_base,
@@ -475,6 +619,7 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": K * desc.get("launches_per_step", 1),
         "parity": parity,
+        "configs": configs,
         "plan": desc,
     }
     if rank == 0:

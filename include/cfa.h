@@ -164,7 +164,8 @@ cfa_status cfa_decode_step_host(cfa_plan *plan, const void *x_host, const void *
  *
  * The first call on a device sets the array up (looks up its device address
  * and zeroes its counters, synchronizing that device once); make that first
- * call before any stream capture. Every call then clears the counters with an
+ * call before any stream capture. If that set-up fails (CFA_ERR_CUDA), the
+ * device is not marked as set up and the next call tries again. Every call then clears the counters with an
  * asynchronous memset on `stream` and launches the kernel (and the separate
  * head merge, where the plan would use one) there, without launch overlap. All calls on a device share the one array, so calls whose
  * kernels may run at the same time on that device (other streams, other host

@@ -751,23 +751,27 @@ constexpr size_t kNoallocBytes = kNoallocWordsBytes + kNoallocPartialFloats * si
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
 constexpr int kNoallocMaxDevices = 64;
-std::once_flag g_noalloc_once[kNoallocMaxDevices];
-unsigned char *g_noalloc_ptr[kNoallocMaxDevices] = {};
-cudaError_t g_noalloc_setup_err[kNoallocMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+unsigned char *g_noalloc_ptr[kNoallocMaxDevices] = {};  // null until set up
 
 // Once per device, with that device current: the array's device address (the
-// host-side name is only a stand-in) and a zeroed counter/status region.
-void noalloc_setup(int dev) {
+// host-side name is only a stand-in) and a zeroed counter/status region. A
+// device counts as set up only when every step succeeded, so a call that
+// failed here (inside a stream capture, say) leaves the next call to retry.
+// Returns the address, or null.
+unsigned char *noalloc_scratch(int dev) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev]) return g_noalloc_ptr[dev];
     void *ptr = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e == cudaSuccess) e = cudaMemset(ptr, 0, kNoallocWordsBytes);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaGetLastError();
-        ptr = nullptr;
+        return nullptr;
     }
     g_noalloc_ptr[dev] = static_cast<unsigned char *>(ptr);
-    g_noalloc_setup_err[dev] = e;
+    return g_noalloc_ptr[dev];
 }
 
 }  // namespace
@@ -803,8 +807,8 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);
     }
-    std::call_once(g_noalloc_once[dev], noalloc_setup, dev);
-    if (g_noalloc_setup_err[dev] != cudaSuccess || !g_noalloc_ptr[dev]) return fail(CFA_ERR_CUDA);
+    unsigned char *scratch = noalloc_scratch(dev);
+    if (!scratch) return fail(CFA_ERR_CUDA);
 
     // A plan object on the stack: same device queries, cluster-size choice and
     // shared-memory layout as cfa_plan_create, with no workspace behind it.
@@ -815,9 +819,10 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     pl.D = head_dim;
     pl.max_ctx = max_ctx;
     pl.device = dev;
-    int major = 0, minor = 0;
+    int major = 0, minor = 0, cluster_ok = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&cluster_ok, cudaDevAttrClusterLaunch, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&pl.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&pl.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
                                dev) != cudaSuccess ||
@@ -828,7 +833,7 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
         cudaGetLastError();
         return fail(CFA_ERR_CUDA);
     }
-    if (major != 10 || minor != 3) return fail(CFA_ERR_UNSUPPORTED);
+    if (major != 10 || minor != 3 || !cluster_ok) return fail(CFA_ERR_UNSUPPORTED);
     const int candidates[5] = {1, 2, 4, 8, 16};
     bool ok = false;
     for (int C : candidates)
@@ -849,7 +854,6 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
         tm_x = tm_wqkv;  // unused by the CUDA-core path
     }
 
-    unsigned char *scratch = g_noalloc_ptr[dev];
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Counters must start at zero; the previous call may have been cut short.
     if (cudaMemsetAsync(scratch, 0, kNoallocWordsBytes, s) != cudaSuccess) {
