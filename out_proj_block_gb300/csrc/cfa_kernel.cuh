@@ -127,6 +127,11 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     };
     const int col0 = r * p.ncols;
     const int n_out_tiles = p.ncols / kTileCols;
+    // W_o tiles per ring stage: a [D x 64] tile is 16 KB at D = 128, 8 KB at
+    // D = 64, where two side by side fill a stage.
+    constexpr int TPS = kStageBytes / (D * kTileCols * 2);
+    constexpr int kTileBytes = D * kTileCols * 2;
+    const int n_out_units = (n_out_tiles + TPS - 1) / TPS;
     const int qkv_payload = B * 3 * kTileCols;   // floats one block contributes
     const int sm_payload = B * SMW;
 
@@ -258,12 +263,16 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     cur.advance(NS);
                 }
             }
-            // C: W_o tiles [D rows x 64 cols] of this block's output columns
-            for (int ct = 0; ct < n_out_tiles; ++ct) {
+            // C: W_o tiles [D rows x 64 cols] of this block's output columns,
+            // TPS per stage
+            for (int u = 0; u < n_out_units; ++u) {
                 const int s = acquire();
                 const uint32_t full = bar_full0 + 8u * s;
-                mbar_arrive_expect_tx(full, D * kTileCols * 2);
-                tma_load_2d(ring + s * kStageBytes, &tm_wo, col0 + ct * kTileCols, h * D, full);
+                const int nt = min(TPS, n_out_tiles - u * TPS);
+                mbar_arrive_expect_tx(full, static_cast<uint32_t>(nt * kTileBytes));
+                for (int k = 0; k < nt; ++k)
+                    tma_load_2d(ring + s * kStageBytes + k * kTileBytes, &tm_wo,
+                                col0 + (u * TPS + k) * kTileCols, h * D, full);
                 cur.advance(NS);
             }
             // Drain: the block may not exit with its own copies still in flight.
@@ -679,9 +688,11 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             const uint32_t idesc = umma_idesc_bf16(128, 2 * kMmaN, true, false);
             const uint32_t ring_a = smem_addr(smem);
             const uint32_t at_a = smem_addr(at);
-            // One TMEM accumulator of 2 x 16 columns per output tile (up to kbuf
-            // of them): the MMAs of consecutive tiles are issued back to back and
-            // read out in groups.
+            // One TMEM accumulator of 2 x 16 columns per stage (up to kbuf of
+            // them): the MMAs of consecutive stages are issued back to back and
+            // read out in groups. A stage's A operand is M = 128 weight columns:
+            // its two tiles side by side (D = 64), or its one tile with the
+            // second half repeated (D = 128, or a lone last tile).
             const int kbuf = static_cast<int>(p.tmem_cols) / (2 * kMmaN);
             int group0 = 0, group_n = 0;
             uint32_t acc_phase = 0;
@@ -691,20 +702,23 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                          kSiteStageFull);
                 acc_phase ^= 1u;
                 tcgen05_fence_after();
-                // Accumulator lanes 0-63 are the tile's 64 columns: warps 0 and 1
-                // read them for even tiles, warps 4 and 5 (the same lane
-                // quarters) for odd ones; hi and lo share one load wait.
-                if ((warp & 3) < 2) {
+                // Accumulator lanes 64k .. 64k+63 are the columns of the stage's
+                // tile k: the warps of lane quarters 0-3 read them for even
+                // stages, warps 4-7 (the same quarters) for odd ones; hi and lo
+                // share one load wait.
+                if (TPS == 2 || (warp & 3) < 2) {
                     const int wq = warp & 3;
-                    for (int t = group0 + (warp >> 2); t < group0 + group_n; t += 2) {
+                    for (int u = group0 + (warp >> 2); u < group0 + group_n; u += 2) {
+                        const int t = u * TPS + (wq >> 1);
+                        if (t >= n_out_tiles) continue;  // a lone last tile: quarters 2, 3 unused
                         uint32_t vh[16], vl[16];
                         const uint32_t ta = tmem + (static_cast<uint32_t>(32 * wq) << 16) +
-                                            static_cast<uint32_t>(2 * kMmaN * (t % kbuf));
+                                            static_cast<uint32_t>(2 * kMmaN * (u % kbuf));
                         tmem_ld_x16_nowait(ta, vh);
                         tmem_ld_x16_nowait(ta + kMmaN, vl);
                         tmem_wait_ld();
                         float *dst = p.partials + static_cast<size_t>(h) * head_stride + col0 +
-                                     t * kTileCols + 32 * wq + lane;
+                                     t * kTileCols + 32 * (wq & 1) + lane;
 #pragma unroll
                         for (int b = 0; b < MAXB; ++b)
                             if (b < B) dst[static_cast<size_t>(b) * H] = __uint_as_float(vh[b]) + __uint_as_float(vl[b]);
@@ -715,16 +729,17 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 group0 += group_n;
                 group_n = 0;
             };
-            for (int ct = 0; ct < n_out_tiles; ++ct) {
+            for (int u = 0; u < n_out_units; ++u) {
                 const int s = wait_full();
                 if (warp == 0) {
                     if (lane == 0) {
                         tcgen05_fence_after();
                         const uint32_t a0 = ring_a + s * kStageBytes;
-                        const uint32_t d = tmem + static_cast<uint32_t>(2 * kMmaN * (ct % kbuf));
+                        const uint32_t d = tmem + static_cast<uint32_t>(2 * kMmaN * (u % kbuf));
+                        const uint32_t half = u * TPS + 1 < n_out_tiles ? static_cast<uint32_t>(kTileBytes) : 0u;
 #pragma unroll
                         for (int j = 0; j < D / 16; ++j) {
-                            const uint64_t da = umma_smem_desc(a0 + j * 2048, 0, 1024);
+                            const uint64_t da = umma_smem_desc(a0 + j * 2048, TPS == 2 ? half : 0u, 1024);
                             const uint32_t boff = (j >> 2) * (2 * kMmaN * 128) + (j & 3) * 32;
                             umma_bf16(d, da, umma_smem_desc(at_a + boff, 16, 1024), idesc, j > 0);
                         }
@@ -740,20 +755,24 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             // A warp takes whole tiles (tile ct goes to warp ct % 8): all D rows
             // of its 64 columns, summed within the warp, so no block barrier
             // separates tiles. Every warp waits for each stage and releases it
-            // (the ring's phases stay in order); only the owner reads it.
+            // (the ring's phases stay in order); only the owners of its tiles
+            // read it.
             const int cg = lane % GS::LPR, rq = lane / GS::LPR;
-            for (int ct = 0; ct < n_out_tiles; ++ct) {
+            for (int u = 0; u < n_out_units; ++u) {
                 const int s = wait_full();
-                if (ct % kComputeWarps != warp) {
+                int k = 0;  // this warp's tile in the stage, if any (TPS <= 8 warps)
+                while (k < TPS && (u * TPS + k >= n_out_tiles || (u * TPS + k) % kComputeWarps != warp)) ++k;
+                if (k == TPS) {
                     release(s);
                     continue;
                 }
+                const int ct = u * TPS + k;
                 float acc[MAXB][GS::CPL];
 #pragma unroll
                 for (int b = 0; b < MAXB; ++b)
 #pragma unroll
                     for (int c = 0; c < GS::CPL; ++c) acc[b][c] = 0.f;
-                gemv_tile<MAXB>(ring + s * kStageBytes, D, attn, D, B, 0, lane, acc);
+                gemv_tile<MAXB>(ring + s * kStageBytes + k * kTileBytes, D, attn, D, B, 0, lane, acc);
                 release(s);
                 // the warp's row groups, in a fixed shuffle order
 #pragma unroll
