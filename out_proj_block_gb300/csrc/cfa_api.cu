@@ -110,8 +110,11 @@ cfa_status encode_w_qkv(CUtensorMap *tm, const void *W_qkv, int H, const KernelP
     const bool mma = kp.n_qk > 0;
     return encode_2d(tm, W_qkv, 3ull * H, H, cfa::kTileCols, static_cast<uint32_t>(kp.TRA), mma);
 }
+// W_o boxes: whole [D x 64] tiles on the CUDA-core path, [64 x 64] swizzled
+// K slices on the tensor-core path.
 cfa_status encode_w_o(CUtensorMap *tm, const void *W_o, int H, int D, const KernelParams &kp) {
-    return encode_2d(tm, W_o, H, H, cfa::kTileCols, static_cast<uint32_t>(D), kp.n_qk > 0);
+    const bool mma = kp.n_qk > 0;
+    return encode_2d(tm, W_o, H, H, cfa::kTileCols, static_cast<uint32_t>(mma ? 64 : D), mma);
 }
 cfa_status encode_x(CUtensorMap *tm, const void *x, int B, int H) {
     return encode_2d(tm, x, H, B, cfa::kTileCols, cfa::kMmaN, true);

@@ -127,11 +127,18 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     };
     const int col0 = r * p.ncols;
     const int n_out_tiles = p.ncols / kTileCols;
-    // W_o tiles per ring stage: a [D x 64] tile is 16 KB at D = 128, 8 KB at
-    // D = 64, where two side by side fill a stage.
-    constexpr int TPS = kStageBytes / (D * kTileCols * 2);
-    constexpr int kTileBytes = D * kTileCols * 2;
-    const int n_out_units = (n_out_tiles + TPS - 1) / TPS;
+    // W_o in the ring: boxes of KROWS rows x 64 columns, TPS of them (adjacent
+    // column tiles) side by side per stage. CUDA-core path: whole [D x 64]
+    // tiles (16 KB at D = 128; two 8 KB ones at D = 64). Tensor-core path:
+    // [64 x 64] boxes, two column tiles per stage, so the stage is one M = 128
+    // operand; at D = 128 a column pair takes two stages (KP K-passes of 64
+    // rows) accumulated into one TMEM slot.
+    constexpr int KROWS = MMA ? 64 : D;
+    constexpr int KP = D / KROWS;
+    constexpr int kTileBytes = KROWS * kTileCols * 2;
+    constexpr int TPS = kStageBytes / kTileBytes;
+    const int n_out_groups = (n_out_tiles + TPS - 1) / TPS;   // column groups of TPS tiles
+    const int n_out_units = n_out_groups * KP;                 // ring stages of phase C
     const int qkv_payload = B * 3 * kTileCols;   // floats one block contributes
     const int sm_payload = B * SMW;
 
@@ -268,11 +275,12 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             for (int u = 0; u < n_out_units; ++u) {
                 const int s = acquire();
                 const uint32_t full = bar_full0 + 8u * s;
-                const int nt = min(TPS, n_out_tiles - u * TPS);
+                const int grp = u / KP, kp = u % KP;
+                const int nt = min(TPS, n_out_tiles - grp * TPS);
                 mbar_arrive_expect_tx(full, static_cast<uint32_t>(nt * kTileBytes));
                 for (int k = 0; k < nt; ++k)
                     tma_load_2d(ring + s * kStageBytes + k * kTileBytes, &tm_wo,
-                                col0 + (u * TPS + k) * kTileCols, h * D, full);
+                                col0 + (grp * TPS + k) * kTileCols, h * D + kp * KROWS, full);
                 cur.advance(NS);
             }
             // Drain: the block may not exit with its own copies still in flight.
@@ -688,11 +696,11 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             const uint32_t idesc = umma_idesc_bf16(128, 2 * kMmaN, true, false);
             const uint32_t ring_a = smem_addr(smem);
             const uint32_t at_a = smem_addr(at);
-            // One TMEM accumulator of 2 x 16 columns per stage (up to kbuf of
-            // them): the MMAs of consecutive stages are issued back to back and
-            // read out in groups. A stage's A operand is M = 128 weight columns:
-            // its two tiles side by side (D = 64), or its one tile with the
-            // second half repeated (D = 128, or a lone last tile).
+            // One TMEM accumulator of 2 x 16 columns per column group of two
+            // tiles (up to kbuf of them): the MMAs of consecutive stages are
+            // issued back to back and read out in groups. A stage's A operand is
+            // M = 128 weight columns, its two tiles side by side (a lone last
+            // tile: its half repeated), K = 64 rows.
             const int kbuf = static_cast<int>(p.tmem_cols) / (2 * kMmaN);
             int group0 = 0, group_n = 0;
             uint32_t acc_phase = 0;
@@ -706,7 +714,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 // tile k: the warps of lane quarters 0-3 read them for even
                 // stages, warps 4-7 (the same quarters) for odd ones; hi and lo
                 // share one load wait.
-                if (TPS == 2 || (warp & 3) < 2) {
+                {
                     const int wq = warp & 3;
                     for (int u = group0 + (warp >> 2); u < group0 + group_n; u += 2) {
                         const int t = u * TPS + (wq >> 1);
@@ -729,26 +737,29 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                 group0 += group_n;
                 group_n = 0;
             };
+            static_assert(!MMA || TPS == 2, "tensor-core out-projection stages hold two tiles");
             for (int u = 0; u < n_out_units; ++u) {
                 const int s = wait_full();
+                const int grp = u / KP, kp = u % KP;
                 if (warp == 0) {
                     if (lane == 0) {
                         tcgen05_fence_after();
                         const uint32_t a0 = ring_a + s * kStageBytes;
-                        const uint32_t d = tmem + static_cast<uint32_t>(2 * kMmaN * (u % kbuf));
-                        const uint32_t half = u * TPS + 1 < n_out_tiles ? static_cast<uint32_t>(kTileBytes) : 0u;
+                        const uint32_t d = tmem + static_cast<uint32_t>(2 * kMmaN * (grp % kbuf));
+                        const uint32_t half = grp * TPS + 1 < n_out_tiles ? static_cast<uint32_t>(kTileBytes) : 0u;
 #pragma unroll
-                        for (int j = 0; j < D / 16; ++j) {
-                            const uint64_t da = umma_smem_desc(a0 + j * 2048, TPS == 2 ? half : 0u, 1024);
-                            const uint32_t boff = (j >> 2) * (2 * kMmaN * 128) + (j & 3) * 32;
-                            umma_bf16(d, da, umma_smem_desc(at_a + boff, 16, 1024), idesc, j > 0);
+                        for (int j = 0; j < KROWS / 16; ++j) {
+                            const uint64_t da = umma_smem_desc(a0 + j * 2048, half, 1024);
+                            const int k0 = kp * KROWS + 16 * j;  // attn row of this K slice
+                            const uint32_t boff = (k0 >> 6) * (2 * kMmaN * 128) + ((k0 & 63) >> 4) * 32;
+                            umma_bf16(d, da, umma_smem_desc(at_a + boff, 16, 1024), idesc, kp > 0 || j > 0);
                         }
                     }
                     release_after_mma(s);
                 } else {
                     release(s);
                 }
-                if (++group_n == kbuf) flush();
+                if (kp == KP - 1 && ++group_n == kbuf) flush();
             }
             if (group_n > 0) flush();
         } else {
@@ -758,6 +769,7 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             // (the ring's phases stay in order); only the owners of its tiles
             // read it.
             const int cg = lane % GS::LPR, rq = lane / GS::LPR;
+            static_assert(MMA || KP == 1, "CUDA-core out-projection stages hold whole tiles");
             for (int u = 0; u < n_out_units; ++u) {
                 const int s = wait_full();
                 int k = 0;  // this warp's tile in the stage, if any (TPS <= 8 warps)
