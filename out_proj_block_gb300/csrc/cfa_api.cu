@@ -527,6 +527,7 @@ cfa_status launch_fused(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensor
         for (int i = 0; i < pl->D / 2; ++i)
             kp.rope_inv_freq[i] = std::pow(rope_theta, -2.0 * i / pl->D);
 
+    kp.pdl = pl->overlap ? 1 : 0;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config(pl, kp, pl->smem_bytes, stream, attr);
     if (pl->overlap) {
@@ -873,6 +874,7 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
     kp.partials = reinterpret_cast<float *>(scratch + kNoallocWordsBytes);
     for (int b = 0; b < B; ++b) kp.ctx_lens[b] = ctx_len;
     kp.rope = 0;
+    kp.pdl = 0;  // launched without programmatic dependent launch
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config(&pl, kp, pl.smem_bytes, s, attr);
     void *args[4] = {&tm_wqkv, &tm_wo, &tm_x, &kp};

@@ -66,6 +66,8 @@ struct KernelParams {
     unsigned tmem_cols;    // tensor-core path: TMEM columns per block (power of two >= 32)
     int ncols;             // output columns per block in the out-projection: H / C
     int merge_separate;    // 1: blocks only write their partials; head_merge_kernel sums them
+    int pdl;               // 1: launched with programmatic dependent launch (may start before
+                           // the previous kernel in the stream has finished)
     int nstages;           // pipeline depth
     int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_attn_t, off_scratch,
         off_bars;

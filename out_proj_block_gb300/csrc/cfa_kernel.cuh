@@ -229,18 +229,25 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     }
                 }
             };
+            // CUDA-core path: the block's x rows [rg*R, rg*R + R) once, for all
+            // stages. Without a programmatic dependency x is ready at launch and
+            // is requested first (the first stage can then be used as soon as
+            // it lands); otherwise only after the dependency wait.
+            auto issue_x_rows = [&]() {
+                if constexpr (!MMA) {
+                    mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(B * p.R * 2));
+                    for (int b = 0; b < B; ++b)
+                        bulk_load_1d(xring + b * p.R * 2, p.x + static_cast<size_t>(b) * H + rg * p.R,
+                                     p.R * 2, bar_x);
+                }
+            };
+            if (!p.pdl) issue_x_rows();
             for (int i = 0; i < n_pre; ++i) {
                 mbar_arrive_expect_tx(bar_full0 + 8u * i, a_bytes(i));
                 issue_w(i, i);
             }
             grid_dependency_wait();
-            if constexpr (!MMA) {
-                // CUDA-core path: the block's x rows [rg*R, rg*R + R) once, for all stages
-                mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(B * p.R * 2));
-                for (int b = 0; b < B; ++b)
-                    bulk_load_1d(xring + b * p.R * 2, p.x + static_cast<size_t>(b) * H + rg * p.R,
-                                 p.R * 2, bar_x);
-            }
+            if (p.pdl) issue_x_rows();
             for (int i = 0; i < n_pre; ++i) issue_x(i, i);
             for (int i = 0; i < n_pre; ++i) cur.advance(NS);
             for (int i = n_pre; i < n_a; ++i) {
