@@ -132,14 +132,16 @@ cfa_status cfa_decode_step_ex(cfa_plan *plan, const void *x, const void *W_qkv,
 
 /*
  * The same step for a caller whose token activations live in host memory:
- * moves x_host (bf16 [B, hidden]) to the plan's device staging buffer,
- * runs cfa_decode_step on `stream`, moves the result back to out_host
+ * takes x_host (bf16 [B, hidden]) to the GPU, runs the step of
+ * cfa_decode_step on `stream`, brings the result back to out_host
  * (bf16 [B, hidden]) and synchronizes `stream` before returning. Weights and
- * caches stay device pointers. Page-locked, device-mapped host buffers
- * (cudaHostAlloc / cudaHostRegister, 16-byte aligned) are read and written
- * by small copy kernels launched around the step (no DMA transfer); other
- * host memory goes through cudaMemcpyAsync and is slower. Errors as
- * cfa_decode_step.
+ * caches stay device pointers. With page-locked, device-mapped host buffers
+ * (cudaHostAlloc / cudaHostRegister, 16-byte aligned) there is no DMA
+ * transfer: the step writes out_host itself, and reads x_host itself at
+ * B <= 2 (at B >= 3 a small copy kernel first stages x in the plan's device
+ * buffer, which the step's tensor-map loads read). Other host memory goes
+ * through cudaMemcpyAsync and the plan's staging buffers, and is slower.
+ * Errors as cfa_decode_step.
  */
 cfa_status cfa_decode_step_host(cfa_plan *plan, const void *x_host, const void *W_qkv,
                                 const void *W_o, void *k_cache, void *v_cache,

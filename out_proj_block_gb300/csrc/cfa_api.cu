@@ -510,8 +510,9 @@ cudaError_t launch_head_merge(const KernelParams &kp, bool overlap, cudaStream_t
 cfa_status launch_fused(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensorMap *tm_wo,
                         const CUtensorMap *tm_x, const void *x, void *k_cache, void *v_cache,
                         const int *lens, const int *lens_dev, double rope_theta,
-                        const void *resid, void *out, cudaStream_t stream) {
+                        const void *resid, void *out, cudaStream_t stream, bool x_direct = false) {
     KernelParams kp = pl->kp;
+    kp.x_direct = x_direct ? 1 : 0;
     kp.x = static_cast<const uint16_t *>(x);
     kp.k_cache = static_cast<uint16_t *>(k_cache);
     kp.v_cache = static_cast<uint16_t *>(v_cache);
@@ -547,9 +548,11 @@ cfa_status launch_fused(cfa_plan *pl, const CUtensorMap *tm_wqkv, const CUtensor
 
 // The launch behind cfa_decode_step and cfa_decode_step_ex: lens[b] cached
 // positions per sequence, rope_theta > 0 enables the rotary embedding.
+// x_direct: x is in host-mapped memory and read with plain loads (CUDA-core
+// path only).
 cfa_status launch_step(cfa_plan *pl, const void *x, const void *W_qkv, const void *W_o,
                        void *k_cache, void *v_cache, const int *lens, double rope_theta,
-                       void *out, void *stream) {
+                       void *out, void *stream, bool x_direct = false) {
     if (!pl || !x || !W_qkv || !W_o || !k_cache || !v_cache || !out || !lens)
         return fail(CFA_ERR_INVALID_ARG);
     for (int b = 0; b < pl->B; ++b)
@@ -594,7 +597,7 @@ cfa_status launch_step(cfa_plan *pl, const void *x, const void *W_qkv, const voi
     if (!mma) pl->tm_x = pl->tm_wqkv;  // unused by the CUDA-core path
 
     return launch_fused(pl, &pl->tm_wqkv, &pl->tm_wo, &pl->tm_x, x, k_cache, v_cache, lens,
-                        nullptr, rope_theta, nullptr, out, static_cast<cudaStream_t>(stream));
+                        nullptr, rope_theta, nullptr, out, static_cast<cudaStream_t>(stream), x_direct);
 }
 
 }  // namespace
@@ -658,19 +661,23 @@ cfa_status cfa_decode_step_host(cfa_plan *pl, const void *x_host, const void *W_
     if (ctx_len < 0 || ctx_len >= pl->max_ctx) return fail(CFA_ERR_INVALID_ARG);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t act = 2u * static_cast<size_t>(pl->B) * pl->H;
-    // Page-locked, device-mapped buffers: the GPU reads x and writes out itself
-    // (a copy kernel on each side of the step), with no DMA transfer to set up.
+    // Page-locked, device-mapped buffers: the GPU reads x and writes out
+    // itself, with no DMA transfer to set up. The step stores out straight into
+    // the host buffer; on the CUDA-core path it also reads x there (plain
+    // loads), on the tensor-core path a copy kernel stages x for its TMA loads.
     void *x_dev = mapped_host_ptr(x_host), *out_dev = mapped_host_ptr(out_host);
     if (x_dev && out_dev && aligned16(x_dev) && aligned16(out_dev)) {
-        if (launch_copy16(x_dev, pl->x_stage, act, pl->overlap, s) != cudaSuccess) {
+        const bool direct = pl->kp.n_qk == 0;
+        if (!direct && launch_copy16(x_dev, pl->x_stage, act, pl->overlap, s) != cudaSuccess) {
             cudaGetLastError();
             return fail(CFA_ERR_CUDA);
         }
-        const cfa_status st =
-            cfa_decode_step(pl, pl->x_stage, W_qkv, W_o, k_cache, v_cache, ctx_len, pl->out_stage, s);
+        int lens[cfa::kMaxBatch];
+        for (int b = 0; b < pl->B; ++b) lens[b] = ctx_len;
+        const cfa_status st = launch_step(pl, direct ? x_dev : pl->x_stage, W_qkv, W_o, k_cache,
+                                          v_cache, lens, 0.0, out_dev, s, direct);
         if (st != CFA_OK) return st;
-        if (launch_copy16(pl->out_stage, out_dev, act, pl->overlap, s) != cudaSuccess ||
-            cudaStreamSynchronize(s) != cudaSuccess) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) {
             cudaGetLastError();
             return fail(CFA_ERR_CUDA);
         }

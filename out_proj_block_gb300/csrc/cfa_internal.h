@@ -68,6 +68,8 @@ struct KernelParams {
     int merge_separate;    // 1: blocks only write their partials; head_merge_kernel sums them
     int pdl;               // 1: launched with programmatic dependent launch (may start before
                            // the previous kernel in the stream has finished)
+    int x_direct;          // 1 (CUDA-core path only): x is read by the compute warps with plain
+                           // loads (host-mapped pinned memory), not by TMA
     int nstages;           // pipeline depth
     int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_attn_t, off_scratch,
         off_bars;

@@ -241,13 +241,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                      p.R * 2, bar_x);
                 }
             };
-            if (!p.pdl) issue_x_rows();
+            if (!p.pdl && !p.x_direct) issue_x_rows();
             for (int i = 0; i < n_pre; ++i) {
                 mbar_arrive_expect_tx(bar_full0 + 8u * i, a_bytes(i));
                 issue_w(i, i);
             }
             grid_dependency_wait();
-            if (p.pdl) issue_x_rows();
+            if (p.pdl && !p.x_direct) issue_x_rows();
             for (int i = 0; i < n_pre; ++i) issue_x(i, i);
             for (int i = 0; i < n_pre; ++i) cur.advance(NS);
             for (int i = n_pre; i < n_a; ++i) {
@@ -439,7 +439,20 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         } else {
             const uint16_t *xrows = reinterpret_cast<const uint16_t *>(smem + p.off_xring);  // [B][R]
             const int rpw = p.TRA / kComputeWarps;
-            mbar_wait_bounded<false>(bar_x, 0, p.timeout_ns, timed_out, p.status, kSiteStageFull);
+            if (p.x_direct) {
+                // x in host-mapped memory: 16-byte plain loads of this block's
+                // rows (not TMA), shared by every compute warp after a barrier
+                const int n16 = p.R / 8;
+                for (int idx = tid; idx < B * n16; idx += kComputeThreads) {
+                    const int b = idx / n16, c = idx % n16;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(b) * H +
+                                                                     rg * p.R + 8 * c);
+                    *reinterpret_cast<uint4 *>(smem + p.off_xring + (static_cast<size_t>(b) * p.R + 8 * c) * 2) = v;
+                }
+                compute_bar<kComputeThreads>();
+            } else {
+                mbar_wait_bounded<false>(bar_x, 0, p.timeout_ns, timed_out, p.status, kSiteStageFull);
+            }
             for (int sec = 0; sec < 3; ++sec) {
                 float acc[MAXB][GS::CPL];
 #pragma unroll
