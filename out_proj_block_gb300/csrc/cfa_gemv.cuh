@@ -327,11 +327,17 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
                 cur.advance(NS);
             }
             // Drain: no exit with copies of this block still in flight.
+            // Each wait is bounded at kDrainTimeoutFactor times the normal
+            // limit (a copy still pending then is not going to land). If one
+            // gives up, the status word records the timeout and the block
+            // exits anyway: a block that never exits would hang the GPU,
+            // which is worse than a late copy into released shared memory.
             for (int s = 0; s < NS; ++s) {
                 if (s >= cur.stage && !cur.wrapped) break;
                 volatile int ignore = 0;
                 mbar_wait_bounded<false>(bar_full0 + 8u * s, s < cur.stage ? cur.phase : cur.phase ^ 1u,
-                                         p.timeout_ns, &ignore, p.status, kSiteStageFull);
+                                         kDrainTimeoutFactor * p.timeout_ns, &ignore, p.status,
+                                         kSiteDrain);
             }
         } else {
             grid_dependency_wait();

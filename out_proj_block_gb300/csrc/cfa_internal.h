@@ -31,6 +31,10 @@ constexpr unsigned kStatusTimeoutBit = 1u;
 constexpr unsigned kStatusBadLengthBit = 2u;  // a device-resident length was out of range
 constexpr unsigned kStatusSiteShift = 8;  // site code of the first timeout
 
+// A load warp's final wait for its own copies in flight uses this many times
+// the normal wait limit.
+constexpr unsigned long long kDrainTimeoutFactor = 4;
+
 // Site codes recorded with a timeout in the status word.
 enum WaitSite : unsigned {
     kSiteStageFull = 1,
@@ -38,6 +42,7 @@ enum WaitSite : unsigned {
     kSiteQExchange = 3,
     kSiteSoftmaxExchange = 4,
     kSiteKvExchange = 5,
+    kSiteDrain = 6,        // a load warp's final wait for its own copies
     kSiteSelftest = 15,
 };
 

@@ -293,11 +293,17 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             // Drain: the block may not exit with its own copies still in flight.
             // Stages before the cursor were last filled in the current pass,
             // the others in the previous one (if the ring ever wrapped).
+            // Each wait is bounded at kDrainTimeoutFactor times the normal
+            // limit (a copy still pending then is not going to land). If one
+            // gives up, the status word records the timeout and the block
+            // exits anyway: a block that never exits would hang the GPU,
+            // which is worse than a late copy into released shared memory.
             for (int s = 0; s < NS; ++s) {
                 if (s >= cur.stage && !cur.wrapped) break;
                 volatile int ignore = 0;
                 mbar_wait_bounded<false>(bar_full0 + 8u * s, s < cur.stage ? cur.phase : cur.phase ^ 1u,
-                                         p.timeout_ns, &ignore, p.status, kSiteStageFull);
+                                         kDrainTimeoutFactor * p.timeout_ns, &ignore, p.status,
+                                         kSiteDrain);
             }
         } else {
             grid_dependency_wait();
