@@ -123,6 +123,32 @@ def test_last_cache_row(cfa, oracle):
     run_and_check(cfa, oracle, wl, seed=20, C=4)
 
 
+def test_maximum_context(cfa, oracle):
+    """The largest cache a plan accepts, max_ctx = 2^22, with ctx_len = 2^22 - 1:
+    4,194,303 cached positions attended and the final row written, 4.3 GB of
+    K/V cache (64-bit offsets everywhere). The oracle runs on one thread here
+    (its per-head fp64 copies of K and V are 4.3 GB each)."""
+    max_ctx = 1 << 22
+    L = max_ctx - 1
+    wl = workloads.custom(1, 256, 2, 128, L, max_ctx=max_ctx)
+    t = workloads.make_inputs(wl, seed=21, device="cuda")
+    out = torch.empty(1, wl.hidden, dtype=torch.bfloat16, device="cuda")
+    k_last_before = t["k_cache"][:, :, L - 1].clone()
+    with cfa.Plan(1, wl.hidden, wl.n_heads, wl.head_dim, max_ctx) as plan:
+        plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], L, out)
+        torch.cuda.synchronize()
+        assert plan.status() == cfa.CFA_OK
+    assert torch.equal(t["k_cache"][:, :, L - 1].view(torch.int16), k_last_before.view(torch.int16))
+    cpu = {k: v.cpu() for k, v in t.items()}
+    del t
+    torch.cuda.empty_cache()
+    ref = oracle.decode_step(cpu["x"], cpu["W_qkv"], cpu["W_o"], cpu["k_cache"], cpu["v_cache"], L,
+                             nthreads=1)
+    check_close("out", out.float().cpu().numpy(), ref["out"])
+    check_close("k_new", cpu["k_cache"][:, :, L].float().numpy(), ref["k_new"])
+    check_close("v_new", cpu["v_cache"][:, :, L].float().numpy(), ref["v_new"])
+
+
 @pytest.mark.parametrize("B", [1, 2, 3, 5, 8, 9, 16])
 def test_batch_sizes(cfa, oracle, B):
     wl = workloads.custom(B, 512, 4, 128, 150, max_ctx=192)
