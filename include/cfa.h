@@ -68,8 +68,10 @@ typedef enum cfa_status {
 /*
  * Create a plan for batch B, hidden size `hidden` = n_heads * head_dim and a
  * cache capacity of max_ctx positions, on the current CUDA device.
- * Chooses the cluster size (blocks per head) and the pipeline depth, sets the
- * kernel attributes, and allocates the plan's workspace (fp32 per-head
+ * Chooses the cluster size (blocks per head) and the pipeline depth: of the
+ * sizes whose whole grid is resident on the GPU at once, the smallest whose
+ * grid gives every SM a block, else the largest; if no size is co-resident,
+ * the largest that runs. Sets the kernel attributes, and allocates the plan's workspace (fp32 per-head
  * output-projection partials [n_heads, B, hidden], arrival counters of the
  * cross-head merge, a status word, and device staging
  * for cfa_decode_step_host).

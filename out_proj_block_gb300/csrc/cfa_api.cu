@@ -285,13 +285,49 @@ cfa_status configure(cfa_plan *pl, int C, int stages_override) {
         cudaGetLastError();
         return CFA_ERR_CUDA;
     }
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config(pl, kp, smem, nullptr, attr);
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+    // Whether the grid can be resident at once. Blocks per SM come from the
+    // SM's own limits: shared memory, registers (allocated per warp in units of
+    // 256), threads. The occupancy calls report one block per SM for the
+    // tensor-core kernels at any shared memory size, though the SM holds two
+    // (a timeline of such a launch shows two blocks resident on most SMs);
+    // they do model how clusters pack into GPCs, which depends only on blocks
+    // per SM. So the cluster count is the call's answer for the CUDA-core
+    // kernel at a size that gives it the same blocks per SM, and the kernel's
+    // own answer where that does not match.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
         cudaGetLastError();
         return CFA_ERR_UNSUPPORTED;
     }
+    const int warps = cfa::kThreads / 32;
+    const int by_smem = pl->smem_per_sm / (smem + pl->smem_reserved);
+    const int by_regs = 65536 / (warps * align_up(std::max(fa.numRegs, 1) * 32, 256));
+    const int per_sm = std::min({by_smem, by_regs, 2048 / cfa::kThreads});
+    // Clusters of `dim` blocks of function `fn` that the occupancy call fits.
+    auto api_clusters = [&](const void *fn, int dim, int bytes) {
+        cudaLaunchAttribute a[1];
+        cudaLaunchConfig_t c = launch_config(pl, kp, bytes, nullptr, a);
+        c.gridDim = dim3(pl->nh * dim, 1, 1);
+        a[0].val.clusterDim.x = dim;
+        int v = 0;
+        if (cudaOccupancyMaxActiveClusters(&v, fn, &c) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        return v;
+    };
+    int clusters = api_clusters(kernel, C, smem);
+    const void *ref = kernel_for(128, 1);
+    const int ref_smem = std::min(pl->smem_optin, pl->smem_per_sm / std::max(per_sm, 1) -
+                                                      pl->smem_reserved);
+    if (clusters >= 1 && per_sm >= 1 && ref && ref != kernel &&
+        cudaFuncSetAttribute(ref, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pl->smem_optin) == cudaSuccess &&
+        cudaFuncSetAttribute(ref, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess &&
+        api_clusters(ref, 1, ref_smem) == per_sm * pl->num_sms)
+        clusters = std::max(clusters, api_clusters(ref, C, ref_smem));
+    cudaGetLastError();
     if (clusters < 1) return CFA_ERR_UNSUPPORTED;
     // A separate merge kernel where one block would otherwise read more than
     // 256 KB of partials at the end of the fused kernel.
@@ -305,6 +341,26 @@ cfa_status configure(cfa_plan *pl, int C, int stages_override) {
     pl->tm_wo_src = nullptr;
     pl->tm_x_src = nullptr;
     return CFA_OK;
+}
+
+// Default cluster size. A grid whose clusters cannot all be resident at once
+// runs in waves, each as slow as a whole step, so only sizes whose whole grid
+// fits the device at once are taken while one exists: the smallest of those
+// that gives every SM a block, else the largest of them. Failing that, the
+// largest size that runs at all. Returns the size applied, or 0.
+int choose_cluster(cfa_plan *pl) {
+    const int candidates[5] = {1, 2, 4, 8, 16};
+    int best = 0;  // largest co-resident size seen
+    for (int C : candidates) {
+        if (configure(pl, C, 0) != CFA_OK || pl->coresident_clusters < pl->nh) continue;
+        best = C;
+        if (pl->nh * C >= pl->num_sms) return C;
+    }
+    if (!best)
+        for (int i = 4; i >= 0 && !best; --i)
+            if (configure(pl, candidates[i], 0) == CFA_OK) best = candidates[i];
+    if (best && pl->C != best && configure(pl, best, 0) != CFA_OK) return 0;
+    return best;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -408,22 +464,7 @@ cfa_plan *cfa_plan_create(int B, int hidden, int n_heads, int head_dim, int max_
         return nullptr;
     }
 
-    // Default cluster size: the smallest that gives at least one block per SM,
-    // else the largest that fits this shape.
-    const int candidates[5] = {1, 2, 4, 8, 16};
-    int chosen = 0;
-    for (int C : candidates) {
-        if (n_heads * C < sms) continue;
-        if (configure(pl, C, 0) == CFA_OK) {
-            chosen = C;
-            break;
-        }
-    }
-    if (!chosen) {
-        for (int i = 4; i >= 0 && !chosen; --i)
-            if (configure(pl, candidates[i], 0) == CFA_OK) chosen = candidates[i];
-    }
-    if (!chosen) {
+    if (!choose_cluster(pl)) {
         free_workspace(pl);
         delete pl;
         fail(CFA_ERR_UNSUPPORTED);
@@ -845,15 +886,7 @@ extern "C" cfa_status cfa_decode_step_noalloc(int B, int hidden, int n_heads, in
         return fail(CFA_ERR_CUDA);
     }
     if (major != 10 || minor != 3 || !cluster_ok) return fail(CFA_ERR_UNSUPPORTED);
-    const int candidates[5] = {1, 2, 4, 8, 16};
-    bool ok = false;
-    for (int C : candidates)
-        if (n_heads * C >= pl.num_sms && configure(&pl, C, 0) == CFA_OK) {
-            ok = true;
-            break;
-        }
-    for (int i = 4; i >= 0 && !ok; --i) ok = configure(&pl, candidates[i], 0) == CFA_OK;
-    if (!ok) return fail(CFA_ERR_UNSUPPORTED);
+    if (!choose_cluster(&pl)) return fail(CFA_ERR_UNSUPPORTED);
 
     CUtensorMap tm_wqkv, tm_wo, tm_x;
     if (encode_w_qkv(&tm_wqkv, W_qkv, hidden, pl.kp) != CFA_OK ||

@@ -207,6 +207,30 @@ def test_merge_forms_by_size(cfa):
         assert plan.describe()["launches_per_step"] == 2
 
 
+@pytest.mark.parametrize("B,H,nh,D", [
+    (1, 4096, 32, 128), (16, 4096, 32, 128), (8, 4096, 64, 64),
+    (2, 2048, 16, 128),   # C = 16 fills the SMs but only 14 clusters of 16 fit at once
+    (8, 2048, 32, 64),    # C = 8 fills the SMs but only 15 clusters of 8 fit at once
+    (16, 2048, 16, 128),
+])
+def test_default_cluster_size_keeps_the_grid_resident(cfa, B, H, nh, D):
+    """The default plan never picks a cluster size whose grid would run in two
+    waves; among co-resident sizes it takes the smallest that covers the SMs."""
+    with cfa.Plan(B, H, nh, D, 320) as plan:
+        d = plan.describe()
+    C = d["cluster_size"]
+    assert d["coresident_clusters"] >= nh, d
+    if d["grid"] >= d["num_sms"]:
+        assert C == 1 or nh * (C // 2) < d["num_sms"], d
+    elif C < 16:
+        # no larger size is co-resident
+        try:
+            with cfa.Plan(B, H, nh, D, 320, cluster_size=2 * C) as plan:
+                assert plan.describe()["coresident_clusters"] < nh
+        except cfa.CfaError:
+            pass
+
+
 # ------------------------------------------------------ determinism and reuse
 
 
