@@ -560,10 +560,13 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                     const int nrows = min(TK, kv_e - kv_s - t * TK);
                     const uint4 *Kt = reinterpret_cast<const uint4 *>(ring + s * kStageBytes);
                     const uint4 *Vt = reinterpret_cast<const uint4 *>(ring + s * kStageBytes + TK * D * 2);
+                    // Scores of all the warp's rows in this tile first (the steps
+                    // are independent), then one running-max update for them all.
+                    float sc[KV_STEPS];
+                    float tmax = -INFINITY;
 #pragma unroll
                     for (int j = 0; j < KV_STEPS; ++j) {
                         const int row = (warp * KV_STEPS + j) * KV_RPS + rq;
-                        const bool valid = row < nrows;
                         uint4 kr[NV];
 #pragma unroll
                         for (int v = 0; v < NV; ++v) kr[v] = Kt[row * (D / 8) + 8 * v + li];
@@ -578,22 +581,27 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
                                 s1 = fmaf(q[8 * v + k + 1], kf[k + 1], s1);
                             }
                         }
-                        float sc = s0 + s1;
-                        sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-                        sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-                        sc += __shfl_xor_sync(0xffffffffu, sc, 4);
-                        sc = valid ? sc : -INFINITY;
-                        float tmax = fmaxf(sc, __shfl_xor_sync(0xffffffffu, sc, 8));
-                        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-                        if (tmax > m) {  // warp-uniform: rescale only when the max grows
-                            const float cf = exp2f(m - tmax);
-                            l *= cf;
+                        float x = s0 + s1;
+                        x += __shfl_xor_sync(0xffffffffu, x, 1);
+                        x += __shfl_xor_sync(0xffffffffu, x, 2);
+                        x += __shfl_xor_sync(0xffffffffu, x, 4);
+                        sc[j] = row < nrows ? x : -INFINITY;
+                        tmax = fmaxf(tmax, sc[j]);
+                    }
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+                    if (tmax > m) {  // warp-uniform: rescale only when the max grows
+                        const float cf = exp2f(m - tmax);
+                        l *= cf;
 #pragma unroll
-                            for (int k = 0; k < DPL; ++k) o[k] *= cf;
-                            m = tmax;
-                        }
-                        if (valid) {
-                            const float pw = exp2f(sc - m);
+                        for (int k = 0; k < DPL; ++k) o[k] *= cf;
+                        m = tmax;
+                    }
+#pragma unroll
+                    for (int j = 0; j < KV_STEPS; ++j) {
+                        const int row = (warp * KV_STEPS + j) * KV_RPS + rq;
+                        if (row < nrows) {
+                            const float pw = exp2f(sc[j] - m);
                             l += pw;
 #pragma unroll
                             for (int v = 0; v < NV; ++v) {
