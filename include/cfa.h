@@ -199,6 +199,22 @@ cfa_status cfa_plan_set_cluster_size(cfa_plan *plan, int cluster_size);
 cfa_status cfa_plan_set_stages(cfa_plan *plan, int stages);
 
 /*
+ * How the blocks of a head's cluster share their partial q, k and v (the
+ * ClusterGather step, CF section 3.1.2 "QKV向量共享"). mode 0: every block
+ * sends its whole partial [B][3][64] to every peer and each sums all of them
+ * (one round of pushes; the receive buffer holds C partials). mode 1:
+ * reduce-scatter then all-gather -- each block sums one slice of the columns
+ * over the blocks of its column group and sends the sum to every peer (two
+ * rounds; the receive buffer holds 2 partials whatever C, which leaves more
+ * shared memory for pipeline stages). Both sum in the same order, so the
+ * results are bit for bit the same. mode -1 (the default): mode 1 where
+ * mode 0 leaves fewer than 4 stages and mode 1 gives more, else mode 0.
+ * CFA_ERR_INVALID_ARG for another mode; CFA_ERR_UNSUPPORTED if the layout
+ * does not fit. The plan is unchanged on error.
+ */
+cfa_status cfa_plan_set_qkv_exchange(cfa_plan *plan, int mode);
+
+/*
  * Enable (1, the default) or disable (0) launch overlap for the following
  * steps. With overlap on, a step's prologue and first weight loads run under
  * the tail of the previous kernel in the stream (see cfa_decode_step); with
@@ -216,8 +232,9 @@ int cfa_plan_cluster_size(const cfa_plan *plan);
  * finish a column chunk sums every head's partials inside the fused kernel;
  * "separate": a second kernel, launched behind it on the same stream, sums
  * them, chosen when the flat form would read more than 256 KB through one
- * block -- and "launches_per_step", 1 or 2) into buf (NUL-terminated,
- * truncated to len). CFA_ERR_INVALID_ARG for NULL arguments.
+ * block -- "launches_per_step", 1 or 2, and "qkv_exchange", "gather" or
+ * "reduce_scatter") into buf (NUL-terminated, truncated to len).
+ * CFA_ERR_INVALID_ARG for NULL arguments.
  */
 cfa_status cfa_plan_describe(const cfa_plan *plan, char *buf, int len);
 

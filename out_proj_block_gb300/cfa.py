@@ -47,6 +47,8 @@ _lib.cfa_plan_set_stages.restype = _i
 _lib.cfa_plan_set_stages.argtypes = [_vp, _i]
 _lib.cfa_plan_set_overlap.restype = _i
 _lib.cfa_plan_set_overlap.argtypes = [_vp, _i]
+_lib.cfa_plan_set_qkv_exchange.restype = _i
+_lib.cfa_plan_set_qkv_exchange.argtypes = [_vp, _i]
 _lib.cfa_plan_cluster_size.restype = _i
 _lib.cfa_plan_cluster_size.argtypes = [_vp]
 _lib.cfa_plan_describe.restype = _i
@@ -116,6 +118,7 @@ EXPORTED_SYMBOLS = (
     "cfa_decode_step_host",
     "cfa_decode_step_noalloc",
     "cfa_plan_set_cluster_size", "cfa_plan_set_stages", "cfa_plan_set_overlap",
+    "cfa_plan_set_qkv_exchange",
     "cfa_plan_cluster_size",
     "cfa_plan_describe", "cfa_plan_status", "cfa_last_error", "cfa_status_string",
     "cfa_selftest_wait_timeout",
@@ -215,6 +218,10 @@ def cfa_plan_set_overlap(plan, enable: bool) -> int:
     return int(_lib.cfa_plan_set_overlap(plan, 1 if enable else 0))
 
 
+def cfa_plan_set_qkv_exchange(plan, mode: int) -> int:
+    return int(_lib.cfa_plan_set_qkv_exchange(plan, int(mode)))
+
+
 def cfa_plan_cluster_size(plan) -> int:
     return int(_lib.cfa_plan_cluster_size(plan))
 
@@ -243,13 +250,15 @@ class Plan:
 
     def __init__(self, B: int, hidden: int, n_heads: int, head_dim: int, max_ctx: int,
                  cluster_size: Optional[int] = None, stages: Optional[int] = None,
-                 overlap: Optional[bool] = None):
+                 overlap: Optional[bool] = None, qkv_exchange: Optional[int] = None):
         self.B, self.hidden, self.n_heads, self.head_dim, self.max_ctx = (
             B, hidden, n_heads, head_dim, max_ctx)
         self.handle = cfa_plan_create(B, hidden, n_heads, head_dim, max_ctx)
         try:
             if cluster_size is not None:
                 self.set_cluster_size(cluster_size)
+            if qkv_exchange is not None:
+                self.set_qkv_exchange(qkv_exchange)
             if stages is not None:
                 self.set_stages(stages)
             if overlap is not None:
@@ -288,6 +297,12 @@ class Plan:
         st = cfa_plan_set_stages(self.handle, n)
         if st != CFA_OK:
             raise CfaError(st, f"stages {n}")
+
+    def set_qkv_exchange(self, mode: int) -> None:
+        """-1 automatic, 0 gather, 1 reduce-scatter (cfa_plan_set_qkv_exchange)."""
+        st = cfa_plan_set_qkv_exchange(self.handle, mode)
+        if st != CFA_OK:
+            raise CfaError(st, f"qkv exchange {mode}")
 
     def set_overlap(self, enable: bool) -> None:
         st = cfa_plan_set_overlap(self.handle, enable)

@@ -38,6 +38,7 @@ cfa_status fail(cfa_status s) {
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxStages = 12;
 constexpr int kMinStages = 2;
+constexpr int kRsBelowStages = 4;
 
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -48,6 +49,7 @@ struct cfa_plan {
     int device = -1, num_sms = 0, smem_per_sm = 0, smem_optin = 0, smem_reserved = 0;
     int C = 0;
     int stages_override = 0;      // 0 = choose automatically
+    int exchange = -1;            // q/k/v exchange: -1 automatic, 0 gather, 1 reduce-scatter
     bool overlap = true;          // programmatic dependent launch
     KernelParams kp{};            // everything but the per-call pointers
     int smem_bytes = 0;
@@ -155,7 +157,10 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     const int xstage = mma ? cfa::kXStageMmaBytes : 0;
     const int xrows = mma ? 0 : align_up(B * R * 2, 128);
     const int attn_t = mma ? 2 * (D / 64) * cfa::kMmaN * 128 : 0;
-    const int qkv_recv = C * B * 3 * cfa::kTileCols * 4;
+    // q/k/v partials: gather mode, every rank's [B][3][64] partial; reduce-
+    // scatter mode, this block's partial plus the peers' slices of it (the
+    // same size again), whatever C.
+    auto qkv_recv_bytes = [&](int rs) { return (rs ? 2 : C) * B * 3 * cfa::kTileCols * 4; };
     const int sm_recv = C * B * (D + 4) * 4;
     const int qkv_full = B * (3 * D + 1) * 4;
     const int attn = B * D * 4;
@@ -167,25 +172,45 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     // Stages of x ring needed to hold attn and its hi/lo operand (tensor-core
     // path; 0 = never alias).
     const int alias_stages = mma ? (align_up(attn, 1024) + attn_t + xstage - 1) / xstage : 0;
-    const int fixed_common = align_up(qkv_recv, 128) + align_up(sm_recv, 128) +
-                             align_up(qkv_full, 128) + align_up(scratch, 128) + xrows +
-                             1024 /* alignment slack, barriers, flags */;
     const int attn_bytes = align_up(attn, 128) + align_up(attn_t, 1024);
     const int per_stage = cfa::kStageBytes + xstage + 16;
-
     const int grid = pl->nh * C;
-    int per_sm = (grid + pl->num_sms - 1) / std::max(pl->num_sms, 1);
-    per_sm = std::min(std::max(per_sm, 1), 4);
-    int NS = 0;
-    int blocks_per_sm = 1;
-    for (; per_sm >= 1 && NS < kMinStages; --per_sm) {
-        const int budget =
-            std::min(pl->smem_optin, pl->smem_per_sm / per_sm - pl->smem_reserved);
-        NS = std::min(kMaxStages, (budget - fixed_common) / per_stage);
-        if (!mma || NS < alias_stages)  // attn needs its own space
-            NS = std::min(kMaxStages, (budget - fixed_common - attn_bytes) / per_stage);
-        blocks_per_sm = per_sm;
+
+    // Pipeline depth and blocks per SM for an exchange mode: as many blocks
+    // per SM as the grid needs to cover the SMs (at most 4) while they get at
+    // least kMinStages stages, else fewer blocks.
+    auto depth = [&](int rs, int &ns_out, int &bps_out) {
+        const int fixed_common = align_up(qkv_recv_bytes(rs), 128) + align_up(sm_recv, 128) +
+                                 align_up(qkv_full, 128) + align_up(scratch, 128) + xrows +
+                                 1024 /* alignment slack, barriers, flags */;
+        int per_sm = (grid + pl->num_sms - 1) / std::max(pl->num_sms, 1);
+        per_sm = std::min(std::max(per_sm, 1), 4);
+        ns_out = 0;
+        bps_out = 1;
+        for (; per_sm >= 1 && ns_out < kMinStages; --per_sm) {
+            const int budget =
+                std::min(pl->smem_optin, pl->smem_per_sm / per_sm - pl->smem_reserved);
+            ns_out = std::min(kMaxStages, (budget - fixed_common) / per_stage);
+            if (!mma || ns_out < alias_stages)  // attn needs its own space
+                ns_out = std::min(kMaxStages, (budget - fixed_common - attn_bytes) / per_stage);
+            bps_out = per_sm;
+        }
+    };
+    // The reduce-scatter exchange costs one more round of pushes; it is taken
+    // automatically only where the gather mode's buffers leave fewer than
+    // kRsBelowStages stages and it gives more at the same blocks per SM.
+    int rs = pl->exchange > 0 ? 1 : 0;
+    int NS = 0, blocks_per_sm = 1;
+    depth(rs, NS, blocks_per_sm);
+    if (pl->exchange < 0 && C > 1 && NS < kRsBelowStages) {
+        int ns1 = 0, bps1 = 1;
+        depth(1, ns1, bps1);
+        if (ns1 > NS && bps1 >= blocks_per_sm) {
+            rs = 1;
+            NS = ns1;
+        }
     }
+    const int qkv_recv = qkv_recv_bytes(rs);
     if (stages_override > 0) NS = stages_override;
     if (NS < kMinStages || NS > 64) return CFA_ERR_UNSUPPORTED;
 
@@ -217,7 +242,7 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.off_scratch = off;
     off = align_up(off + scratch, 128);
     k.off_bars = off;
-    off += (2 * NS + 10) * 8;
+    off += (2 * NS + 12) * 8;
     if (off > pl->smem_optin) return CFA_ERR_UNSUPPORTED;
 
     k.B = B;
@@ -246,6 +271,7 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     k.ncols = ncols;
     if (C > cfa::kMaxCounters) return CFA_ERR_UNSUPPORTED;
     k.nstages = NS;
+    k.rs = rs;
     k.timeout_ns = kDefaultTimeoutNs;
     k.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     *kp = k;
@@ -494,6 +520,18 @@ cfa_status cfa_plan_set_stages(cfa_plan *pl, int stages) {
     return CFA_OK;
 }
 
+cfa_status cfa_plan_set_qkv_exchange(cfa_plan *pl, int mode) {
+    if (!pl || mode < -1 || mode > 1) return fail(CFA_ERR_INVALID_ARG);
+    const int old = pl->exchange;
+    pl->exchange = mode;
+    const cfa_status st = configure(pl, pl->C, pl->stages_override);
+    if (st != CFA_OK) {
+        pl->exchange = old;  // on error the plan is unchanged
+        return fail(st);
+    }
+    return CFA_OK;
+}
+
 cfa_status cfa_plan_set_overlap(cfa_plan *pl, int enable) {
     if (!pl) return fail(CFA_ERR_INVALID_ARG);
     pl->overlap = enable != 0;
@@ -511,12 +549,13 @@ cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
                   "\"smem_bytes\": %d, \"stages\": %d, \"stage_bytes\": %d, "
                   "\"proj_rows_per_block\": %d, \"proj_tile_rows\": %d, "
                   "\"out_cols_per_block\": %d, \"coresident_clusters\": %d, \"num_sms\": %d, "
-                  "\"overlap\": %d, \"merge\": \"%s\", \"launches_per_step\": %d}",
+                  "\"overlap\": %d, \"merge\": \"%s\", \"launches_per_step\": %d, "
+                  "\"qkv_exchange\": \"%s\"}",
                   pl->B, pl->H, pl->nh, pl->D, pl->max_ctx, pl->C, pl->nh * pl->C,
                   cfa::kThreads, pl->smem_bytes, k.nstages, cfa::kStageBytes, k.R, k.TRA,
                   k.ncols, pl->coresident_clusters, pl->num_sms, pl->overlap ? 1 : 0,
                   k.merge_separate ? "separate" : "flat",
-                  k.merge_separate ? 2 : 1);
+                  k.merge_separate ? 2 : 1, k.rs ? "reduce_scatter" : "gather");
     return CFA_OK;
 }
 

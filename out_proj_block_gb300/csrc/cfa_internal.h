@@ -75,6 +75,8 @@ struct KernelParams {
                            // the previous kernel in the stream has finished)
     int x_direct;          // 1 (CUDA-core path only): x is read by the compute warps with plain
                            // loads (host-mapped pinned memory), not by TMA
+    int rs;                // 1: q/k/v partials exchanged as a reduce-scatter then an all-gather
+                           // of the sums; 0: every rank's whole partial to every peer
     int nstages;           // pipeline depth
     int off_xring, off_qkv_recv, off_sm_recv, off_qkv_full, off_attn, off_attn_t, off_scratch,
         off_bars;

@@ -61,6 +61,58 @@ constexpr int kXStageMma = kXStageMmaBytes;      // x bytes per stage: two [16 x
 constexpr uint32_t kAccQK = 0;                   // TMEM columns of the [Q|K] accumulator
 constexpr uint32_t kAccV = kMmaN;                // TMEM columns of the V accumulator
 
+// Reduce-scatter exchange of the q/k/v partials (kept out of line: it runs
+// a few times per launch, and inlined it costs the kernel registers).
+// Slice prg of sections [sec0, sec0 + nsec) of this block's partial
+// `mine` [B][3][64] to the peer of row group prg in column group g, into its
+// slot rg of the peer's slice buffer [RG][B][3][64 / RG].
+static __device__ __noinline__ void rs_push_slices(const float *mine, uint32_t slices_addr,
+                                                   uint32_t bar, int sec0, int nsec, int B, int RG,
+                                                   int G, int g, int rg, int tid) {
+    const int SL = kTileCols / RG;
+    const int per_b = nsec * (SL / 4);  // 16-byte chunks per batch row
+    const int chunks = B * per_b;
+    for (int idx = tid; idx < (RG - 1) * chunks; idx += kComputeThreads) {
+        const int pi = idx / chunks, c = idx % chunks;
+        const int prg = pi < rg ? pi : pi + 1;
+        const int b = c / per_b, w = c % per_b;
+        const int sec = sec0 + w / (SL / 4), c4 = 4 * (w % (SL / 4));
+        const float4 v = *reinterpret_cast<const float4 *>(mine + (b * 3 + sec) * kTileCols + prg * SL + c4);
+        const int doff = ((rg * B + b) * 3 + sec) * SL + c4;
+        push_16B(map_to_rank(slices_addr + 4u * doff, prg * G + g), v, map_to_rank(bar, prg * G + g));
+    }
+}
+
+// Sum this block's slice of sections [sec0, sec0 + nsec) over the row groups
+// in row-group order (the order of the gather exchange's sum, so both modes
+// give the same bits) and store the raw sums into `full` [B][3][D] on every
+// rank of the cluster, this one included; bar_ag counts the peers' bytes.
+static __device__ __noinline__ void rs_reduce_gather(const float *mine, const float *slices,
+                                                     float *full, uint32_t full_addr, uint32_t bar_ag,
+                                                     int sec0, int nsec, int B, int D, int C, int RG,
+                                                     int g, int rg, int r, int tid) {
+    const int SL = kTileCols / RG;
+    const int per_b = nsec * (SL / 4);
+    for (int c = tid; c < B * per_b; c += kComputeThreads) {
+        const int b = c / per_b, w = c % per_b;
+        const int sec = sec0 + w / (SL / 4), c4 = 4 * (w % (SL / 4));
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < RG; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(
+                q == rg ? mine + (b * 3 + sec) * kTileCols + rg * SL + c4
+                        : slices + ((q * B + b) * 3 + sec) * SL + c4);
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+        }
+        const int off = (b * 3 + sec) * D + g * kTileCols + rg * SL + c4;
+        *reinterpret_cast<float4 *>(full + off) = sum;
+        for (int q = 0; q < C; ++q)
+            if (q != r) push_16B(map_to_rank(full_addr + 4u * off, q), sum, map_to_rank(bar_ag, q));
+    }
+}
+
 template <int D, int MAXB>
 __global__ void __launch_bounds__(kThreads, 2)
 fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
@@ -100,6 +152,8 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
     const uint32_t bar_acc_a = bar_qk + 24u;        // projection accumulators ready (MMA path)
     const uint32_t bar_acc_c = bar_qk + 32u;        // out-projection accumulator groups (MMA path)
     const uint32_t bar_x = bar_qk + 40u;            // the block's x rows (CUDA-core path)
+    const uint32_t bar_qk2 = bar_qk + 72u;          // reduce-scatter mode: every rank's q/k sums
+    const uint32_t bar_v2 = bar_qk + 80u;           // reduce-scatter mode: every rank's v sums
     volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_bars + 16 * NS + 56);
     volatile int *timed_out = flags;      // set by the first wait that gives up
     volatile int *is_last = flags + 1;    // this block merges its column chunk
@@ -153,12 +207,24 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         mbar_init(bar_acc_a, 1);
         mbar_init(bar_acc_c, 1);
         mbar_init(bar_x, 1);
+        mbar_init(bar_qk2, 1);
+        mbar_init(bar_v2, 1);
         *timed_out = 0;
         *is_last = 0;
         fence_mbar_init();
         // Each exchange barrier completes once every peer's bytes have landed.
-        mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>((C - 1) * B * 2 * kTileCols * 4));
-        mbar_arrive_expect_tx(bar_v, static_cast<uint32_t>((C - 1) * B * kTileCols * 4));
+        if (p.rs) {
+            // the slices of the peers of this block's column group, then every
+            // rank's summed slice (C of them cover the head's D columns)
+            const int sl = kTileCols / p.RG;
+            mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>((p.RG - 1) * B * 2 * sl * 4));
+            mbar_arrive_expect_tx(bar_v, static_cast<uint32_t>((p.RG - 1) * B * sl * 4));
+            mbar_arrive_expect_tx(bar_qk2, static_cast<uint32_t>((C - 1) * B * 2 * sl * 4));
+            mbar_arrive_expect_tx(bar_v2, static_cast<uint32_t>((C - 1) * B * sl * 4));
+        } else {
+            mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>((C - 1) * B * 2 * kTileCols * 4));
+            mbar_arrive_expect_tx(bar_v, static_cast<uint32_t>((C - 1) * B * kTileCols * 4));
+        }
         mbar_arrive_expect_tx(bar_sm, static_cast<uint32_t>((C - 1) * sm_payload * 4));
     }
     if constexpr (MMA) {
@@ -344,10 +410,24 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         };
 
         // ---- A: partial QKV projection; partials leave as soon as they exist --
-        float *my_qkv = qkv_recv + static_cast<size_t>(r) * qkv_payload;
+        // Gather mode: every rank's partial [B][3][64] lands in its own slot of
+        // qkv_recv on every peer. Reduce-scatter mode: this block's partial
+        // sits at the start of qkv_recv and, behind it, the slices
+        // [rg' SL, rg' SL + SL) that the RG - 1 peers of its column group
+        // computed for the columns this block sums ([RG][B][3][SL]).
+        float *my_qkv = p.rs ? qkv_recv : qkv_recv + static_cast<size_t>(r) * qkv_payload;
         const uint32_t my_qkv_addr = smem_addr(my_qkv);
-        // Push sections [sec0, sec0 + nsec) of every batch row to every peer.
+        float *rs_recv = qkv_recv + qkv_payload;
+        const uint32_t rs_recv_addr = smem_addr(rs_recv);
+        const uint32_t qkv_full_addr = smem_addr(qkv_full);
+        // Push sections [sec0, sec0 + nsec) of every batch row: gather mode,
+        // the whole partial to every peer; reduce-scatter mode, slice rg' to
+        // the peer of row group rg' in this block's column group.
         auto push_sections = [&](int sec0, int nsec, uint32_t bar) {
+            if (p.rs) {
+                rs_push_slices(my_qkv, rs_recv_addr, bar, sec0, nsec, B, p.RG, p.G, g, rg, tid);
+                return;
+            }
             const int per_b = nsec * (kTileCols / 4);  // 16-byte chunks per batch row
             const int chunks = B * per_b;
             for (int idx = tid; idx < (C - 1) * chunks; idx += kComputeThreads) {
@@ -503,15 +583,37 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
             }
         };
 
+        // Reduce-scatter mode: this block's slice summed into qkv_full on every rank.
+        auto reduce_gather = [&](int sec0, int nsec, uint32_t bar_ag) {
+            rs_reduce_gather(my_qkv, rs_recv, qkv_full, qkv_full_addr, bar_ag, sec0, nsec, B, D, C,
+                             p.RG, g, rg, r, tid);
+            compute_bar<kComputeThreads>();
+        };
+
         // ---- X1 (q, k): the query for attention and the new key -------------
         // With rotary embedding, dims i and i + D/2 of q and k_new are rotated
         // by ctx_lens[b] * theta^(-2i/D) (rotate-half form); the angle is taken
         // in fp64 and reduced to (-pi, pi] before the fp32 sine and cosine.
+        // The raw sums go to qkv_full first (reduce-scatter mode: by the
+        // exchange itself) and are transformed in place (each element read and
+        // written by the same thread).
         mbar_wait_bounded<true>(bar_qk, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
+        if (p.rs) {
+            reduce_gather(0, 2, bar_qk2);
+            mbar_wait_bounded<true>(bar_qk2, 0, p.timeout_ns, timed_out, p.status, kSiteQExchange);
+        } else {
+            // gather mode: the rank-order sums into qkv_full as well
+            for (int idx = tid; idx < B * 2 * D; idx += kComputeThreads) {
+                const int b = idx / (2 * D), rem = idx % (2 * D);
+                qkv_full[b * 3 * D + rem] = gathered(b, rem / D, rem % D);
+            }
+            compute_bar<kComputeThreads>();
+        }
         for (int idx = tid; idx < B * D; idx += kComputeThreads) {
             const int b = idx / D, rem = idx % D;
             const int sec = rem / (D / 2), i = rem % (D / 2);
-            float y0 = gathered(b, sec, i), y1 = gathered(b, sec, i + D / 2);
+            float y0 = qkv_full[(b * 3 + sec) * D + i];
+            float y1 = qkv_full[(b * 3 + sec) * D + i + D / 2];
             if (p.rope) {
                 const double ang = static_cast<double>(max(seq_len(b), 0)) * p.rope_inv_freq[i];
                 const double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
@@ -673,8 +775,15 @@ fused_decode_kernel(const __grid_constant__ CUtensorMap tm_wqkv,
         //      token's score; the new token is one more split of the softmax,
         //      attended from its on-chip bf16-rounded copy.
         mbar_wait_bounded<true>(bar_v, 0, p.timeout_ns, timed_out, p.status, kSiteKvExchange);
-        for (int idx = tid; idx < B * D; idx += kComputeThreads)
-            append(idx / D, 2, idx % D, gathered(idx / D, 2, idx % D));
+        if (p.rs) {
+            reduce_gather(2, 1, bar_v2);
+            mbar_wait_bounded<true>(bar_v2, 0, p.timeout_ns, timed_out, p.status, kSiteKvExchange);
+            for (int idx = tid; idx < B * D; idx += kComputeThreads)
+                append(idx / D, 2, idx % D, qkv_full[(idx / D * 3 + 2) * D + idx % D]);
+        } else {
+            for (int idx = tid; idx < B * D; idx += kComputeThreads)
+                append(idx / D, 2, idx % D, gathered(idx / D, 2, idx % D));
+        }
         float *s_new = qkv_full + static_cast<size_t>(B) * 3 * D;  // [B]
         for (int b = warp; b < B; b += kComputeWarps) {
             const float *qb = qkv_full + static_cast<size_t>(b) * 3 * D;

@@ -231,6 +231,59 @@ def test_default_cluster_size_keeps_the_grid_resident(cfa, B, H, nh, D):
             pass
 
 
+@pytest.mark.parametrize("B,H,nh,D,L,C", [
+    (1, 1024, 8, 128, 301, 8),    # two column groups, four row groups
+    (2, 1024, 8, 128, 150, 2),    # one row group: nothing to reduce, only the gather
+    (3, 1024, 8, 128, 97, 16),    # tensor-core projections, slices of 8 columns
+    (8, 2048, 32, 64, 200, 4),    # head_dim 64 on the tensor cores
+    (2, 1024, 16, 64, 77, 16),    # head_dim 64, sixteen row groups: slices of 4 columns
+    (2, 512, 8, 64, 64, 1),       # a cluster of one block
+])
+def test_qkv_exchange_modes_are_bitwise_equal(cfa, oracle, B, H, nh, D, L, C):
+    """The reduce-scatter exchange sums every slice over the row groups in the
+    same order as the gather exchange, so out and the appended rows agree bit
+    for bit; the reduce-scatter result is also held to the oracle."""
+    wl = workloads.custom(B, H, nh, D, L, max_ctx=L + 16)
+    t = workloads.make_inputs(wl, seed=80 + C, device="cuda", poison_tail=True)
+    cpu = {k: v.cpu() for k, v in t.items()}
+    res = {}
+    for mode in (0, 1):
+        out = torch.empty(B, H, dtype=torch.bfloat16, device="cuda")
+        with cfa.Plan(B, H, nh, D, wl.max_ctx, cluster_size=C, qkv_exchange=mode) as plan:
+            assert plan.describe()["qkv_exchange"] == ("reduce_scatter" if mode else "gather")
+            plan.decode_step(t["x"], t["W_qkv"], t["W_o"], t["k_cache"], t["v_cache"], L, out)
+            torch.cuda.synchronize()
+            assert plan.status() == cfa.CFA_OK
+        res[mode] = (out.view(torch.int16).clone(), t["k_cache"][:, :, L].view(torch.int16).clone(),
+                     t["v_cache"][:, :, L].view(torch.int16).clone())
+        t["k_cache"][:, :, L] = float("nan")
+        t["v_cache"][:, :, L] = float("nan")
+    for a, b, name in zip(res[0], res[1], ("out", "k_new", "v_new")):
+        assert torch.equal(a, b), f"{name} differs between the two exchange modes"
+    ref = oracle.decode_step(cpu["x"], cpu["W_qkv"], cpu["W_o"], cpu["k_cache"], cpu["v_cache"], L,
+                             nthreads=NTHREADS)
+    check_close("out", res[1][0].view(torch.bfloat16).float().cpu().numpy(), ref["out"])
+    check_close("k_new", res[1][1].view(torch.bfloat16).float().cpu().numpy(), ref["k_new"])
+    check_close("v_new", res[1][2].view(torch.bfloat16).float().cpu().numpy(), ref["v_new"])
+
+
+def test_qkv_exchange_default_choice(cfa):
+    """The reduce-scatter exchange is chosen where the gather exchange leaves
+    fewer than 4 pipeline stages (64 heads of 64 at B=8: 3 stages) and gives
+    more; elsewhere the plan keeps the gather exchange."""
+    with cfa.Plan(8, 4096, 64, 64, 2112) as plan:
+        d = plan.describe()
+        assert d["qkv_exchange"] == "reduce_scatter" and d["stages"] >= 4, d
+        plan.set_qkv_exchange(0)
+        assert plan.describe()["stages"] < d["stages"]
+    for shape in ((1, 4096, 32, 128, 4160), (16, 4096, 32, 128, 4160)):
+        with cfa.Plan(*shape) as plan:
+            assert plan.describe()["qkv_exchange"] == "gather", shape
+    with cfa.Plan(1, 512, 4, 128, 64) as plan:
+        with pytest.raises(cfa.CfaError):
+            plan.set_qkv_exchange(2)
+
+
 # ------------------------------------------------------ determinism and reuse
 
 
