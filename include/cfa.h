@@ -207,8 +207,9 @@ cfa_status cfa_plan_set_stages(cfa_plan *plan, int stages);
  * over the blocks of its column group and sends the sum to every peer (two
  * rounds; the receive buffer holds 2 partials whatever C, which leaves more
  * shared memory for pipeline stages). Both sum in the same order, so the
- * results are bit for bit the same. mode -1 (the default): mode 1 where
- * mode 0 leaves fewer than 4 stages and mode 1 gives more, else mode 0.
+ * results are bit for bit the same. mode -1 (the default): mode 1 where it
+ * gives more stages and either the batch runs its projections on the tensor
+ * cores (B >= 3) or mode 0 leaves fewer than 4 stages; else mode 0.
  * CFA_ERR_INVALID_ARG for another mode; CFA_ERR_UNSUPPORTED if the layout
  * does not fit. The plan is unchanged on error.
  */

@@ -196,13 +196,18 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
             bps_out = per_sm;
         }
     };
-    // The reduce-scatter exchange costs one more round of pushes; it is taken
-    // automatically only where the gather mode's buffers leave fewer than
-    // kRsBelowStages stages and it gives more at the same blocks per SM.
+    // The reduce-scatter exchange costs one more round of pushes between the
+    // projection and attention. With the CUDA-core projections (B <= 2) the
+    // step is short and that round costs more than deeper rings return (B=1:
+    // 41.4 -> 43.1 us alone with 6 stages instead of 5); with the tensor-core
+    // projections it pays (B=16: 238.7 -> 234.6 us with 7 stages instead of 5).
+    // So it is taken automatically on the tensor-core path, and elsewhere
+    // only where the gather mode leaves fewer than kRsBelowStages stages --
+    // in both cases only if it gives more stages at the same blocks per SM.
     int rs = pl->exchange > 0 ? 1 : 0;
     int NS = 0, blocks_per_sm = 1;
     depth(rs, NS, blocks_per_sm);
-    if (pl->exchange < 0 && C > 1 && NS < kRsBelowStages) {
+    if (pl->exchange < 0 && C > 1 && (mma || NS < kRsBelowStages)) {
         int ns1 = 0, bps1 = 1;
         depth(1, ns1, bps1);
         if (ns1 > NS && bps1 >= blocks_per_sm) {

@@ -268,17 +268,17 @@ def test_qkv_exchange_modes_are_bitwise_equal(cfa, oracle, B, H, nh, D, L, C):
 
 
 def test_qkv_exchange_default_choice(cfa):
-    """The reduce-scatter exchange is chosen where the gather exchange leaves
-    fewer than 4 pipeline stages (64 heads of 64 at B=8: 3 stages) and gives
-    more; elsewhere the plan keeps the gather exchange."""
-    with cfa.Plan(8, 4096, 64, 64, 2112) as plan:
-        d = plan.describe()
-        assert d["qkv_exchange"] == "reduce_scatter" and d["stages"] >= 4, d
-        plan.set_qkv_exchange(0)
-        assert plan.describe()["stages"] < d["stages"]
-    for shape in ((1, 4096, 32, 128, 4160), (16, 4096, 32, 128, 4160)):
+    """The reduce-scatter exchange is chosen on the tensor-core path (B >= 3)
+    where it gives more pipeline stages (64 heads of 64 at B=8: 4 instead of
+    3; B=16: 7 instead of 5); B=1 keeps the gather exchange."""
+    for shape in ((8, 4096, 64, 64, 2112), (16, 4096, 32, 128, 4160)):
         with cfa.Plan(*shape) as plan:
-            assert plan.describe()["qkv_exchange"] == "gather", shape
+            d = plan.describe()
+            assert d["qkv_exchange"] == "reduce_scatter", (shape, d)
+            plan.set_qkv_exchange(0)
+            assert plan.describe()["stages"] < d["stages"], shape
+    with cfa.Plan(1, 4096, 32, 128, 4160) as plan:
+        assert plan.describe()["qkv_exchange"] == "gather"
     with cfa.Plan(1, 512, 4, 128, 64) as plan:
         with pytest.raises(cfa.CfaError):
             plan.set_qkv_exchange(2)
