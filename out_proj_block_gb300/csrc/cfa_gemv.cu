@@ -4,14 +4,18 @@
 
 namespace cfa {
 
-const void *gemv_kernel(int mode, int maxb) {
+const void *gemv_kernel(int mode, int maxb, bool wide) {
+    // 32 KB units are built for single-row batches only (the CUDA-core GEMV's
+    // batch unless a plan forces this path for more rows).
 #define CFA_GEMV_CASES(M)                                                                   \
+    if (wide) return maxb == 1 ? reinterpret_cast<const void *>(&gemv_streamk_kernel<1, M, true>) \
+                               : nullptr;                                                   \
     switch (maxb) {                                                                         \
-        case 1: return reinterpret_cast<const void *>(&gemv_streamk_kernel<1, M>);          \
-        case 2: return reinterpret_cast<const void *>(&gemv_streamk_kernel<2, M>);          \
-        case 4: return reinterpret_cast<const void *>(&gemv_streamk_kernel<4, M>);          \
-        case 8: return reinterpret_cast<const void *>(&gemv_streamk_kernel<8, M>);          \
-        case 16: return reinterpret_cast<const void *>(&gemv_streamk_kernel<16, M>);        \
+        case 1: return reinterpret_cast<const void *>(&gemv_streamk_kernel<1, M, false>);   \
+        case 2: return reinterpret_cast<const void *>(&gemv_streamk_kernel<2, M, false>);   \
+        case 4: return reinterpret_cast<const void *>(&gemv_streamk_kernel<4, M, false>);   \
+        case 8: return reinterpret_cast<const void *>(&gemv_streamk_kernel<8, M, false>);   \
+        case 16: return reinterpret_cast<const void *>(&gemv_streamk_kernel<16, M, false>); \
         default: return nullptr;                                                            \
     }
     if (mode == kGemvSwiGLU) { CFA_GEMV_CASES(kGemvSwiGLU) }

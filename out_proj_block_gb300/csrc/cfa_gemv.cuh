@@ -10,7 +10,8 @@
 //
 // The GEMV is HBM-bound at small batch: every weight byte is read once per
 // token. Its work is cut into units of one 128-column tile x `rows` weight
-// rows (16 KB of weights), and the units, taken tile by tile, are split evenly
+// rows (16 KB of weights; 32 KB for a single batch row where K allows), and
+// the units, taken tile by tile, are split evenly
 // over a persistent grid -- so every SM streams the same number of bytes
 // whatever the matrix shape ("stream-K"). Tiles are 128 columns (256 bytes of
 // each weight row) because blocks stream different rows of the matrix at the
@@ -231,7 +232,12 @@ __device__ __forceinline__ void gemv_finish_quads(const GemvParams &p, int t, in
     }
 }
 
-template <int MAXB, int MODE>
+// WIDE: units of 32 KB (128 weight rows, 64 of each matrix in SwiGLU mode)
+// instead of 16 KB. One thread issuing copies moves more bytes per copy
+// that way: a streaming probe at this kernel's shape (304 blocks, 256-byte
+// box rows) read 5.6 TB/s with 5 stages of 16 KB and 6.3-6.7 TB/s with 2-3
+// stages of 32 KB.
+template <int MAXB, int MODE, bool WIDE>
 __global__ void __launch_bounds__(kGemvThreads, MAXB >= 16 ? 1 : 2)
 gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
                     const __grid_constant__ CUtensorMap tm_w1,
@@ -240,14 +246,15 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
     constexpr bool DUAL = MODE == kGemvSwiGLU;          // gate and up side by side
     constexpr bool NORM = DUAL || MODE == kGemvNormPlain;  // RMSNorm of the input rows
     constexpr int NW = (DUAL ? 2 : 1) * kGemvTileCols;  // partial floats per batch row
-    constexpr int BOX_BYTES = DUAL ? kStageBytes / 2 : kStageBytes;
+    constexpr int STAGE = WIDE ? 2 * kStageBytes : kStageBytes;  // weight bytes per unit
+    constexpr int BOX_BYTES = DUAL ? STAGE / 2 : STAGE;
     using GS = GemvShape<MAXB>;
     extern __shared__ __align__(1024) uint8_t smem[];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    constexpr int R = DUAL ? 32 : 64;                   // weight rows per unit (16 KB)
+    constexpr int R = (DUAL ? 32 : 64) * (WIDE ? 2 : 1);  // weight rows per unit
     constexpr int RPW = R / kWarpsPerHalf;              // weight rows per warp
     const int B = p.B;
     const int NS = p.nstages;
@@ -280,7 +287,7 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
     __syncthreads();
     grid_dependents_launch();
 
-    const uint32_t stage_tx = kStageBytes + static_cast<uint32_t>(B * R * 2 + (NORM ? R * 2 : 0));
+    const uint32_t stage_tx = STAGE + static_cast<uint32_t>(B * R * 2 + (NORM ? R * 2 : 0));
 
     if (warp == kComputeWarps) {
         // ---------------------------------------------------------------- load warp
@@ -291,7 +298,7 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
             // Weight boxes of unit u: [R x 128] of W0 (and of W1 behind it).
             auto issue_w = [&](int u, int s) {
                 const int t = u / p.chunks, k0 = (u % p.chunks) * R;
-                const uint32_t dst = ring + s * kStageBytes, bar = bar_full0 + 8u * s;
+                const uint32_t dst = ring + s * STAGE, bar = bar_full0 + 8u * s;
                 tma_load_2d(dst, &tm_w0, t * kGemvTileCols, k0, bar);
                 if constexpr (DUAL) tma_load_2d(dst + BOX_BYTES, &tm_w1, t * kGemvTileCols, k0, bar);
             };
@@ -479,7 +486,7 @@ gemv_streamk_kernel(const __grid_constant__ CUtensorMap tm_w0,
         mbar_wait_bounded<false>(bar_full0 + 8u * s, cur.phase, p.timeout_ns, timed_out, p.status,
                                  kSiteStageFull);
         const uint16_t *xs = reinterpret_cast<const uint16_t *>(xring + s * p.xstage_bytes);
-        const uint8_t *ws = ring + s * kStageBytes + half * (kTileCols * 2);
+        const uint8_t *ws = ring + s * STAGE + half * (kTileCols * 2);
         if constexpr (NORM) {
             // This warp's rows of bf16(g * x * inv_rms): the operand of the
             // projection(s), rounded as a stored bf16 tensor would be.

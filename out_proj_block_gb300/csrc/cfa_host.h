@@ -10,7 +10,7 @@
 namespace cfa {
 
 // Kernel entry points (cfa_gemv.cu).
-const void *gemv_kernel(int mode, int maxb);
+const void *gemv_kernel(int mode, int maxb, bool wide);
 const void *gemv_mma_kernel_ptr(int mode);
 const void *rmsnorm_kernel_ptr();
 const void *advance_kernel_ptr();

@@ -125,15 +125,20 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
     const bool norm = dual || mode == cfa::kGemvNormPlain;
     const bool mma = gemv_uses_mma(path, B);
     const int TW = cfa::kGemvTileCols;
-    // 16 KB of weights per unit on the CUDA cores; 64 rows of each matrix on
-    // the tensor cores (16 or 32 KB)
-    const int R = mma ? cfa::kGemvMmaRows : (dual ? 32 : 64);
+    int maxb = 1;
+    while (maxb < B) maxb <<= 1;
+    // On the CUDA cores: 32 KB of weights per unit for a single batch row when
+    // K divides into them (one issuing thread streams more with fewer,
+    // larger copies), else 16 KB; on the tensor cores, 64 rows of each matrix
+    // (16 or 32 KB).
+    const int r_narrow = dual ? 32 : 64;
+    const bool wide = !mma && maxb == 1 && K % (2 * r_narrow) == 0;
+    const int R = mma ? cfa::kGemvMmaRows : r_narrow * (wide ? 2 : 1);
+    const int unit_bytes = wide ? 2 * cfa::kStageBytes : cfa::kStageBytes;
     // N a multiple of 64: a last tile of 64 columns reads zeros past N and
     // stores nothing there.
     if (K < R || K % R || N < 64 || N % 64 || B > cfa::kMaxBatch) return CFA_ERR_UNSUPPORTED;
-    int maxb = 1;
-    while (maxb < B) maxb <<= 1;
-    const void *kernel = mma ? cfa::gemv_mma_kernel_ptr(mode) : cfa::gemv_kernel(mode, maxb);
+    const void *kernel = mma ? cfa::gemv_mma_kernel_ptr(mode) : cfa::gemv_kernel(mode, maxb, wide);
     if (!kernel) return CFA_ERR_UNSUPPORTED;
     const int threads = mma ? cfa::kGemvMmaThreads : cfa::kGemvThreads;
     const int NW = (dual ? 2 : 1) * TW;
@@ -162,16 +167,16 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
         // per-warp normalized input rows: 8 warps x [B][R/4] floats
         xn = norm ? align_up(cfa::kComputeWarps * B * (R / 4) * 4, 128) : 0;
         scratch = align_up(cfa::kComputeWarps * B * cfa::kTileCols * 4, 128);
-        per_stage = cfa::kStageBytes + p.xstage_bytes + 16;
+        per_stage = unit_bytes + p.xstage_bytes + 16;
         fixed = xn + scratch + tile + misc + 1024;  // + barriers, flags, slack
     }
-    // Two blocks per SM with at least 4 stages each (3 on the tensor cores),
-    // else one deeper block.
+    // Two blocks per SM with at least 64 KB of weight stages each (3 stages
+    // on the tensor cores), else one deeper block.
     int bps = 2, NS = 0;
     for (; bps >= 1; --bps) {
         const int budget = std::min(dev.smem_optin, dev.smem_per_sm / bps - dev.smem_reserved);
         NS = std::min(kMaxGemvStages, (budget - fixed) / per_stage);
-        if (NS >= (bps == 2 ? (mma ? 3 : 4) : 2)) break;
+        if (NS >= (bps == 2 ? (mma ? 3 : 65536 / unit_bytes) : 2)) break;
     }
     if (bps_req > 0) {
         bps = bps_req;
@@ -189,7 +194,7 @@ cfa_status make_gemv(const Device &dev, int mode, int B, int K, int N, GemvPlan 
         p.off_xring = 0;
         p.off_xn = off;
     } else {
-        off = NS * cfa::kStageBytes;
+        off = NS * unit_bytes;
         p.off_xring = off;
         off += NS * p.xstage_bytes;
         p.off_xn = off;
