@@ -208,6 +208,7 @@ cfa_status cfa_plan_set_stages(cfa_plan *plan, int stages);
  * rounds; the receive buffer holds 2 partials whatever C, which leaves more
  * shared memory for pipeline stages). Both sum in the same order, so the
  * results are bit for bit the same. mode -1 (the default): mode 1 where it
+ * fits more blocks on an SM than mode 0, or, at the same blocks per SM,
  * gives more stages and either the batch runs its projections on the tensor
  * cores (B >= 3) or mode 0 leaves fewer than 4 stages; else mode 0.
  * CFA_ERR_INVALID_ARG for another mode; CFA_ERR_UNSUPPORTED if the layout

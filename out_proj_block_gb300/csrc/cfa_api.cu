@@ -201,18 +201,25 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     // step is short and that round costs more than deeper rings return (B=1:
     // 41.4 -> 43.1 us alone with 6 stages instead of 5); with the tensor-core
     // projections it pays (B=16: 238.7 -> 234.6 us with 7 stages instead of 5).
-    // So it is taken automatically on the tensor-core path, and elsewhere
-    // only where the gather mode leaves fewer than kRsBelowStages stages --
-    // in both cases only if it gives more stages at the same blocks per SM.
+    // It is taken automatically where it fits more blocks on an SM than the
+    // gather mode (the grid can then be resident at once: 64 heads of 64 at
+    // B=16, C = 4, two blocks of 2 stages instead of one of 7, 139.7 ->
+    // 103.2 us alone), and, at the same blocks per SM, where it gives more
+    // stages on the tensor-core path or where the gather mode leaves fewer
+    // than kRsBelowStages.
     int rs = pl->exchange > 0 ? 1 : 0;
     int NS = 0, blocks_per_sm = 1;
     depth(rs, NS, blocks_per_sm);
-    if (pl->exchange < 0 && C > 1 && (mma || NS < kRsBelowStages)) {
+    if (pl->exchange < 0 && C > 1) {
         int ns1 = 0, bps1 = 1;
         depth(1, ns1, bps1);
-        if (ns1 > NS && bps1 >= blocks_per_sm) {
+        const bool more_blocks = bps1 > blocks_per_sm;
+        const bool more_stages =
+            bps1 == blocks_per_sm && ns1 > NS && (mma || NS < kRsBelowStages);
+        if (more_blocks || more_stages) {
             rs = 1;
             NS = ns1;
+            blocks_per_sm = bps1;
         }
     }
     const int qkv_recv = qkv_recv_bytes(rs);

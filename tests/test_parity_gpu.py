@@ -279,6 +279,12 @@ def test_qkv_exchange_default_choice(cfa):
             assert plan.describe()["stages"] < d["stages"], shape
     with cfa.Plan(1, 4096, 32, 128, 4160) as plan:
         assert plan.describe()["qkv_exchange"] == "gather"
+    # 64 heads of 64 at B=16: only the reduce-scatter form fits two blocks per
+    # SM at C = 4, which keeps that grid resident at once
+    with cfa.Plan(16, 4096, 64, 64, 1088) as plan:
+        d = plan.describe()
+        assert d["cluster_size"] == 4 and d["qkv_exchange"] == "reduce_scatter", d
+        assert d["coresident_clusters"] >= 64, d
     with cfa.Plan(1, 512, 4, 128, 64) as plan:
         with pytest.raises(cfa.CfaError):
             plan.set_qkv_exchange(2)
