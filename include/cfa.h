@@ -241,6 +241,30 @@ int cfa_plan_cluster_size(const cfa_plan *plan);
 cfa_status cfa_plan_describe(const cfa_plan *plan, char *buf, int len);
 
 /*
+ * The layout a plan of this shape would use with cluster size C on a device
+ * with the given limits, computed on the host with no device, no allocation
+ * and no CUDA call: the same arithmetic as cfa_plan_create and
+ * cfa_plan_set_cluster_size after they have read the device's attributes
+ * (num_sms = multiprocessor count; smem_per_sm, smem_optin, smem_reserved =
+ * shared memory per multiprocessor, the per-block opt-in maximum and the
+ * per-block reservation, in bytes). exchange and stages are as in
+ * cfa_plan_set_qkv_exchange (-1 automatic) and cfa_plan_set_stages (0
+ * automatic). C itself is the caller's: the plan's automatic choice also
+ * needs the device's answer on how many clusters of each size fit at once.
+ * Writes one JSON line into buf (len >= 256): cluster_size, grid,
+ * blocks_per_sm (the blocks an SM is sized to hold), stages, smem_bytes,
+ * qkv_exchange, tensor_cores (1: the projections run on tcgen05, B >= 3),
+ * tmem_cols, proj_rows_per_block, proj_tile_rows, out_cols_per_block and
+ * merge ("flat" or "separate"). Errors: shapes as cfa_plan_create;
+ * CFA_ERR_INVALID_ARG for out-of-range limits, exchange, stages or buffer;
+ * CFA_ERR_UNSUPPORTED when C does not divide the work or the layout does not
+ * fit the shared memory.
+ */
+cfa_status cfa_plan_layout(int B, int hidden, int n_heads, int head_dim, int max_ctx, int C,
+                           int exchange, int stages, int num_sms, int smem_per_sm,
+                           int smem_optin, int smem_reserved, char *buf, int len);
+
+/*
  * Device-side status of the plan: synchronizes the device, reads and clears
  * the status word the kernels set when a bounded wait gives up. CFA_OK when
  * nothing happened, CFA_ERR_TIMEOUT after a timed-out wait,

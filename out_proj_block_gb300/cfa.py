@@ -105,6 +105,8 @@ _lib.cfa_mla_set_row_splits.restype = _i
 _lib.cfa_mla_set_row_splits.argtypes = [_vp, _i]
 _lib.cfa_stack_describe.restype = _i
 _lib.cfa_stack_describe.argtypes = [_vp, ctypes.c_char_p, _i]
+_lib.cfa_plan_layout.restype = _i
+_lib.cfa_plan_layout.argtypes = [_i] * 12 + [ctypes.c_char_p, _i]
 
 CFA_OK = 0
 CFA_ERR_INVALID_ARG = 1
@@ -120,7 +122,8 @@ EXPORTED_SYMBOLS = (
     "cfa_plan_set_cluster_size", "cfa_plan_set_stages", "cfa_plan_set_overlap",
     "cfa_plan_set_qkv_exchange",
     "cfa_plan_cluster_size",
-    "cfa_plan_describe", "cfa_plan_status", "cfa_last_error", "cfa_status_string",
+    "cfa_plan_describe", "cfa_plan_layout", "cfa_plan_status", "cfa_last_error",
+    "cfa_status_string",
     "cfa_selftest_wait_timeout",
     "cfa_rmsnorm", "cfa_mlp_create", "cfa_mlp_destroy", "cfa_mlp_step", "cfa_mlp_status",
     "cfa_mlp_set_pipeline", "cfa_mlp_set_path",
@@ -232,6 +235,18 @@ def cfa_plan_describe(plan) -> dict:
     if st != CFA_OK:
         raise CfaError(st, "cfa_plan_describe")
     return json.loads(buf.value.decode())
+
+
+def cfa_plan_layout(B: int, hidden: int, n_heads: int, head_dim: int, max_ctx: int, C: int,
+                    exchange: int, stages: int, num_sms: int, smem_per_sm: int, smem_optin: int,
+                    smem_reserved: int):
+    """(status, layout dict or None): the layout a plan of this shape would use
+    with cluster size C on a device with these limits, computed on the host."""
+    buf = ctypes.create_string_buffer(1024)
+    st = int(_lib.cfa_plan_layout(B, hidden, n_heads, head_dim, max_ctx, C, exchange, stages,
+                                  num_sms, smem_per_sm, smem_optin, smem_reserved, buf,
+                                  len(buf)))
+    return st, (json.loads(buf.value.decode()) if st == CFA_OK else None)
 
 
 def cfa_plan_status(plan) -> int:

@@ -126,10 +126,21 @@ const void *kernel_for(int D, int maxb) {
     return D == 128 ? cfa::fused_kernel_d128(maxb) : cfa::fused_kernel_d64(maxb);
 }
 
+// The shapes a plan accepts (the limits of cfa_plan_create).
+cfa_status check_shape(int B, int hidden, int n_heads, int head_dim, int max_ctx) {
+    if (B < 1 || hidden < 1 || n_heads < 1 || head_dim < 1 || max_ctx < 1 ||
+        static_cast<long long>(n_heads) * head_dim != hidden)
+        return CFA_ERR_INVALID_ARG;
+    if ((head_dim != 64 && head_dim != 128) || B > 16 || hidden % 64 != 0 ||
+        max_ctx > (1 << 22) || hidden > (1 << 16))
+        return CFA_ERR_UNSUPPORTED;
+    return CFA_OK;
+}
+
 // Work split, shared-memory layout and pipeline depth for cluster size C.
 // Pure host arithmetic; no CUDA calls.
 cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelParams *kp,
-                       int *smem_out, int *maxb_out) {
+                       int *smem_out, int *maxb_out, int *blocks_per_sm_out = nullptr) {
     const int D = pl->D, B = pl->B, H = pl->H;
     if (C != 1 && C != 2 && C != 4 && C != 8 && C != 16) return CFA_ERR_UNSUPPORTED;
     const int G = D / cfa::kTileCols;  // 64-column groups per head block
@@ -281,6 +292,9 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     }
     k.tmem_cols = cols;
     k.ncols = ncols;
+    // A separate merge kernel where one block would otherwise read more than
+    // 256 KB of partials at the end of the fused kernel.
+    k.merge_separate = 4ll * pl->nh * B * ncols > (256 << 10) ? 1 : 0;
     if (C > cfa::kMaxCounters) return CFA_ERR_UNSUPPORTED;
     k.nstages = NS;
     k.rs = rs;
@@ -289,6 +303,7 @@ cfa_status make_layout(const cfa_plan *pl, int C, int stages_override, KernelPar
     *kp = k;
     *smem_out = off;
     *maxb_out = maxb;
+    if (blocks_per_sm_out) *blocks_per_sm_out = blocks_per_sm;
     return CFA_OK;
 }
 
@@ -367,9 +382,6 @@ cfa_status configure(cfa_plan *pl, int C, int stages_override) {
         clusters = std::max(clusters, api_clusters(ref, C, ref_smem));
     cudaGetLastError();
     if (clusters < 1) return CFA_ERR_UNSUPPORTED;
-    // A separate merge kernel where one block would otherwise read more than
-    // 256 KB of partials at the end of the fused kernel.
-    kp.merge_separate = 4ll * pl->nh * pl->B * kp.ncols > (256 << 10) ? 1 : 0;
     pl->C = C;
     pl->kp = kp;
     pl->smem_bytes = smem;
@@ -437,14 +449,9 @@ const char *cfa_status_string(cfa_status s) {
 cfa_status cfa_last_error(void) { return g_last_error; }
 
 cfa_plan *cfa_plan_create(int B, int hidden, int n_heads, int head_dim, int max_ctx) {
-    if (B < 1 || hidden < 1 || n_heads < 1 || head_dim < 1 || max_ctx < 1 ||
-        static_cast<long long>(n_heads) * head_dim != hidden) {
-        fail(CFA_ERR_INVALID_ARG);
-        return nullptr;
-    }
-    if ((head_dim != 64 && head_dim != 128) || B > 16 || hidden % 64 != 0 ||
-        max_ctx > (1 << 22) || hidden > (1 << 16)) {
-        fail(CFA_ERR_UNSUPPORTED);
+    const cfa_status shape = check_shape(B, hidden, n_heads, head_dim, max_ctx);
+    if (shape != CFA_OK) {
+        fail(shape);
         return nullptr;
     }
     int dev = -1;
@@ -568,6 +575,42 @@ cfa_status cfa_plan_describe(const cfa_plan *pl, char *buf, int len) {
                   k.ncols, pl->coresident_clusters, pl->num_sms, pl->overlap ? 1 : 0,
                   k.merge_separate ? "separate" : "flat",
                   k.merge_separate ? 2 : 1, k.rs ? "reduce_scatter" : "gather");
+    return CFA_OK;
+}
+
+cfa_status cfa_plan_layout(int B, int hidden, int n_heads, int head_dim, int max_ctx, int C,
+                           int exchange, int stages, int num_sms, int smem_per_sm,
+                           int smem_optin, int smem_reserved, char *buf, int len) {
+    if (!buf || len < 256) return fail(CFA_ERR_INVALID_ARG);
+    const cfa_status shape = check_shape(B, hidden, n_heads, head_dim, max_ctx);
+    if (shape != CFA_OK) return fail(shape);
+    if (exchange < -1 || exchange > 1 || stages < 0 || stages > 64 || num_sms < 1 ||
+        num_sms > 4096 || smem_per_sm < 1 || smem_per_sm > (1 << 20) || smem_optin < 1 ||
+        smem_optin > smem_per_sm || smem_reserved < 0 || smem_reserved >= smem_per_sm)
+        return fail(CFA_ERR_INVALID_ARG);
+    cfa_plan pl;  // the fields the layout reads; no device memory, no CUDA call
+    pl.B = B;
+    pl.H = hidden;
+    pl.nh = n_heads;
+    pl.D = head_dim;
+    pl.max_ctx = max_ctx;
+    pl.num_sms = num_sms;
+    pl.smem_per_sm = smem_per_sm;
+    pl.smem_optin = smem_optin;
+    pl.smem_reserved = smem_reserved;
+    pl.exchange = exchange;
+    KernelParams k{};
+    int smem = 0, maxb = 1, bps = 1;
+    const cfa_status st = make_layout(&pl, C, stages, &k, &smem, &maxb, &bps);
+    if (st != CFA_OK) return fail(st);
+    std::snprintf(buf, static_cast<size_t>(len),
+                  "{\"cluster_size\": %d, \"grid\": %d, \"blocks_per_sm\": %d, \"stages\": %d, "
+                  "\"smem_bytes\": %d, \"qkv_exchange\": \"%s\", \"tensor_cores\": %d, "
+                  "\"tmem_cols\": %u, \"proj_rows_per_block\": %d, \"proj_tile_rows\": %d, "
+                  "\"out_cols_per_block\": %d, \"merge\": \"%s\"}",
+                  C, n_heads * C, bps, k.nstages, smem, k.rs ? "reduce_scatter" : "gather",
+                  k.n_qk > 0 ? 1 : 0, k.n_qk > 0 ? k.tmem_cols : 0u, k.R, k.TRA, k.ncols,
+                  k.merge_separate ? "separate" : "flat");
     return CFA_OK;
 }
 
